@@ -1,0 +1,35 @@
+"""CPU oracle for FP8 (E4M3) KV-cache quantization and attention over the
+paged cache: plain, slow, float64 numpy, written from the pages' statement
+of the method.
+
+This package is TEST INFRASTRUCTURE.  Only the tests, the smoke check and
+the bench's CPU-baseline leg may import it; the library's product path never
+does, and the two share no code.
+
+Modules
+-------
+e4m3       the E4M3 codec (decode table from the format fields; saturating
+           round-to-nearest-even encode; quantize = encode(fl32(x / s))).
+kv_cache   the paged cache write (K pages [P][D], V pages [D][P]), query
+           quantization, the KV byte formulas.
+attention  paged decode (full / sliding window, FP8 / BF16 cache), the
+           log-sum-exp merge of partial results, chunked causal prefill,
+           and a planted-defect variant (reduced accumulator) used only to
+           show the long-context test is sensitive.
+
+Pins (tests/test_oracle_*.py)
+-----------------------------
+codec       worked examples of "FP8 and KV cache" (tests/golden), the format's
+            closed forms, torch's float8_e4m3fn cast on a dense bit sample and
+            on every tie, brute force over all codes, round-trip invariant.
+cache       per-element brute force, sentinel bytes, skipped / bad slots,
+            identity vs permuted block tables.
+bytes       every byte count and time the pages print for the formula.
+attention   pure-Python brute force, closed forms (constant V, zero K, one
+            token, needle), split / merge, page permutation, window, the last
+            prefill row vs decode, sensitivity to a 14-bit accumulator.
+
+Parity unpinned: the prefill's mirrored P8 codes (taken against the row's
+final maximum; a kernel with a running maximum may pick neighbouring codes).
+The prefill result itself is pinned through the unquantized-P mode.
+"""

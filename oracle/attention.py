@@ -1,0 +1,247 @@
+"""Attention over the paged FP8 (or BF16) KV cache, in float64.
+
+Test infrastructure: only the tests, the smoke check and the bench's CPU
+baseline may import this module.
+
+What is computed
+----------------
+softmax(q . K^T * sm_scale) . V over the dequantized cache, per sequence and
+query head, with query head h reading KV head h // (Hq / Hkv).
+
+Sources
+-------
+* "The state of FP8 KV-cache and attention quantization in vLLM", section
+  "Problems we found" / "Kernel and vLLM improvements", two-level
+  accumulation: the contraction dimension of softmax(score) * V is the
+  context length; partial sums must be promoted into real FP32 so that the
+  error does not grow with context.  The oracle accumulates in float64.
+* Same page, section "Performance benchmarks", single request: the FP8 FA3
+  path uses online-softmax rescaling.
+* Same page, "Skip layers": sliding-window layers attend to a fixed window
+  (e.g. 128 tokens) and keep their cache in BF16.
+* "FP8 and KV cache", section "How to enable it in the engine": with FP8
+  attention the query is also quantized to FP8 (used by prefill).
+
+Readings where the pages are silent
+-----------------------------------
+* The context length L counts the current token; decode attends to tokens
+  [0, L), or to [max(0, L - W), L) with a window W.
+* Chunked prefill: the nq new tokens of a sequence are the last nq of its L
+  cached tokens; query i sits at position L - nq + i and (causal) attends to
+  keys 0..L - nq + i.
+* The softmax scale is an input (1/sqrt(D) by default in the callers).
+* Prefill's probabilities feed an FP8 MMA: P8 = encode(fl32(p * 256)) with p
+  taken relative to the row's final maximum, and the row sum l adds the
+  unquantized p.  This mirror is approximate (a kernel with a running
+  maximum picks codes from its own maximum): parity unpinned for P8 itself.
+
+Mirrored quantization points
+----------------------------
+``mode="mirror"`` rounds exactly where the CUDA path declares it rounds:
+* decode: q is rounded to float16 (exact for bf16 values of magnitude in
+  [2^-14, 65504]); scores are taken in base-2 units,
+  s2 = (sum_d f16(q)[d] * k8[d]) * c with c = fl32(fl32(k_scale * sm_scale)
+  * log2(e)); o = s_v * sum_j 2^(s2_j - m) v8_j / sum_j 2^(s2_j - m).
+* prefill: s2 = (sum_d q8[d] * k8[d]) * c with
+  c = fl32(fl32(fl32(q_scale * k_scale) * sm_scale) * log2(e)), and P8 as
+  above.
+``mode="pure"`` uses the exact dequantized values and natural exponentials.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import e4m3
+from .kv_cache import FP8, BF16, bf16_bits_to_f32, gather_tokens
+
+LOG2E_F32 = np.float32(1.4426950408889634)
+
+
+def _f32(x):
+    return np.float32(x)
+
+
+def decode_score_coef(k_scale, sm_scale):
+    """c = fl32(fl32(k_scale * sm_scale) * log2(e)), the decode kernels'
+    declared float32 scale on q.k."""
+    return np.float32(np.float32(_f32(k_scale) * _f32(sm_scale)) * LOG2E_F32)
+
+
+def prefill_score_coef(q_scale, k_scale, sm_scale):
+    """c = fl32(fl32(fl32(q_scale * k_scale) * sm_scale) * log2(e))."""
+    a = np.float32(_f32(q_scale) * _f32(k_scale))
+    b = np.float32(a * _f32(sm_scale))
+    return np.float32(b * LOG2E_F32)
+
+
+def _softmax_row(scores_base_e):
+    """(p relative to the max, m, l) for one row of natural-log scores."""
+    m = np.max(scores_base_e)
+    p = np.exp(scores_base_e - m)
+    return p, m, p.sum()
+
+
+def decode_positions(L, window):
+    """Token positions a decode query at context length L attends to."""
+    start = 0 if window is None or window < 0 else max(0, L - window)
+    return np.arange(start, L, dtype=np.int64)
+
+
+def paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
+                 sm_scale, window=-1, cache_dtype=FP8, mode="mirror"):
+    """One decode step: every sequence's query attends to its cached tokens.
+
+    q: float32 [B][Hq][D] holding bf16 values.  k_cache / v_cache: the
+    paged cache (see kv_cache).  Returns (out float64 [B][Hq][D],
+    lse float64 [B][Hq] in natural-log units, -inf for an empty sequence).
+    An empty sequence gives an all-zero output.
+    """
+    q = np.asarray(q, dtype=np.float32)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    g = Hq // Hkv
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    lse = np.full((B, Hq), -np.inf, dtype=np.float64)
+    for b in range(B):
+        pos = decode_positions(int(seq_lens[b]), window)
+        if pos.size == 0:
+            continue
+        for kv in range(Hkv):
+            kk, vv = gather_tokens(k_cache, v_cache, block_table[b], pos, kv)
+            if cache_dtype == FP8:
+                k_codes = e4m3.decode(kk)  # [n][D]
+                v_codes = e4m3.decode(vv)
+                sk = float(np.float32(k_scale[kv]))
+                sv = float(np.float32(v_scale[kv]))
+            else:
+                k_codes = bf16_bits_to_f32(kk).astype(np.float64)
+                v_codes = bf16_bits_to_f32(vv).astype(np.float64)
+                sk = sv = 1.0
+            for h in range(kv * g, (kv + 1) * g):
+                qh = q[b, h].astype(np.float64)
+                if mode == "mirror":
+                    if cache_dtype == FP8:
+                        qe = q[b, h].astype(np.float16).astype(np.float64)
+                        c = float(decode_score_coef(k_scale[kv], sm_scale))
+                    else:
+                        qe = qh
+                        c = float(np.float32(_f32(sm_scale) * LOG2E_F32))
+                    s2 = (k_codes @ qe) * c
+                    m2 = np.max(s2)
+                    p = np.exp2(s2 - m2)
+                    l = p.sum()
+                    out[b, h] = (p @ v_codes) / l * sv
+                    lse[b, h] = (m2 + math.log2(l)) * math.log(2.0)
+                else:
+                    s = (k_codes * sk) @ qh * float(np.float32(sm_scale))
+                    p, m, l = _softmax_row(s)
+                    out[b, h] = (p @ (v_codes * sv)) / l
+                    lse[b, h] = m + math.log(l)
+    return out, lse
+
+
+def lse_merge(outs, lses):
+    """Merge attention results over disjoint key sets (the split-KV combine):
+    lse = log sum_i exp(lse_i); o = sum_i exp(lse_i - lse) o_i.  Parts with
+    lse = -inf carry no weight; if all are empty the result is (0, -inf)."""
+    outs = np.asarray(outs, dtype=np.float64)
+    lses = np.asarray(lses, dtype=np.float64)
+    m = np.max(lses)
+    if not np.isfinite(m):
+        return np.zeros(outs.shape[1:]), -np.inf
+    w = np.exp(lses - m)
+    tot = w.sum()
+    return np.tensordot(w / tot, outs, axes=1), m + math.log(tot)
+
+
+def prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
+            cu_seqlens_q, seq_lens, sm_scale, causal=True, mode="mirror",
+            rows=None):
+    """Chunked prefill over the FP8 cache (the new tokens are already cached).
+
+    q8: uint8 [Tq][Hq][D] E4M3 codes.  cu_seqlens_q: int [B+1].  seq_lens:
+    int [B], each counting the cached tokens including the new ones.
+    rows: optional iterable of (token_index, head) pairs to evaluate; other
+    rows of the result stay NaN (sampled checks at large sizes).
+    Returns out float64 [Tq][Hq][D].
+    """
+    q8 = np.asarray(q8, dtype=np.uint8)
+    Tq, Hq, D = q8.shape
+    Hkv = k_cache.shape[1]
+    g = Hq // Hkv
+    out = np.full((Tq, Hq, D), np.nan, dtype=np.float64)
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    B = len(cu) - 1
+    seq_of = np.zeros(Tq, dtype=np.int64)
+    for b in range(B):
+        seq_of[cu[b]:cu[b + 1]] = b
+    if rows is None:
+        rows = [(t, h) for t in range(Tq) for h in range(Hq)]
+    by_seq_head = {}
+    for t, h in rows:
+        by_seq_head.setdefault((int(seq_of[t]), h // g), []).append((int(t), int(h)))
+    for (b, kv), items in by_seq_head.items():
+        L = int(seq_lens[b])
+        nq = int(cu[b + 1] - cu[b])
+        kk, vv = gather_tokens(k_cache, v_cache, block_table[b], np.arange(L), kv)
+        k_codes = e4m3.decode(kk)
+        v_codes = e4m3.decode(vv)
+        sv = float(np.float32(v_scale[kv]))
+        for t, h in items:
+            i = t - int(cu[b])
+            last = L - nq + i if causal else L - 1
+            qc = e4m3.decode(q8[t, h])
+            if mode == "mirror":
+                c = float(prefill_score_coef(np.float32(q_scale), k_scale[kv], sm_scale))
+                s2 = (k_codes[: last + 1] @ qc) * c
+                m2 = np.max(s2)
+                p = np.exp2(s2 - m2)
+                l = p.sum()
+                p8 = e4m3.encode((p * 256.0).astype(np.float32))
+                num = (e4m3.decode(p8) @ v_codes[: last + 1]) / 256.0
+                out[t, h] = num / l * sv
+            else:
+                qs = float(np.float32(q_scale))
+                sk = float(np.float32(k_scale[kv]))
+                s = (k_codes[: last + 1] * sk) @ (qc * qs) * float(np.float32(sm_scale))
+                p, m, l = _softmax_row(s)
+                out[t, h] = (p @ (v_codes[: last + 1] * sv)) / l
+    return out
+
+
+def decode_reduced_accumulator(q, k_cache, v_cache, k_scale, v_scale, block_table,
+                               seq_lens, sm_scale, mantissa_bits=14):
+    """Planted-defect variant used only to show the long-context test is
+    sensitive: the P.V sum is carried in one accumulator whose value is
+    rounded to `mantissa_bits` significant bits after every addition, the
+    single-level accumulation that "FP8 and KV cache" (training section,
+    accumulation precision) reports for FP8 tensor cores (about 14 bits).
+    FP8 cache, full attention only.  Returns out float64 [B][Hq][D]."""
+    q = np.asarray(q, dtype=np.float32)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    g = Hq // Hkv
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+
+    def rnd(x):
+        mant, ex = np.frexp(x)
+        return np.ldexp(np.round(mant * 2.0 ** mantissa_bits) / 2.0 ** mantissa_bits, ex)
+
+    for b in range(B):
+        pos = decode_positions(int(seq_lens[b]), -1)
+        for kv in range(Hkv):
+            kk, vv = gather_tokens(k_cache, v_cache, block_table[b], pos, kv)
+            k_codes = e4m3.decode(kk)
+            v_codes = e4m3.decode(vv)
+            sv = float(np.float32(v_scale[kv]))
+            c = float(decode_score_coef(k_scale[kv], sm_scale))
+            heads = slice(kv * g, (kv + 1) * g)
+            s2 = (q[b, heads].astype(np.float64) @ k_codes.T) * c  # [g][n]
+            p = np.exp2(s2 - np.max(s2, axis=1, keepdims=True))
+            acc = np.zeros((g, D))
+            for j in range(p.shape[1]):
+                acc = rnd(acc + p[:, j, None] * v_codes[j][None, :])
+            out[b, heads] = acc / p.sum(axis=1, keepdims=True) * sv
+    return out
