@@ -1,0 +1,465 @@
+#!/usr/bin/env python3
+"""Benchmark: FP8 paged decode attention on the Llama-3.1-8B-shaped 128K
+workload -- KV GB/s (% of HBM peak) and us/step vs context length.
+
+One step = one decode step of a 32-layer Llama-3.1-8B-shaped model at batch
+1 and 131,072 tokens of context: for each layer, the new token's K/V is
+quantized into that layer's paged FP8 cache (kvq_reshape_and_cache), then
+paged decode attention (split-KV partial + LSE combine) reads the whole
+cache.  Each layer has its own cache (32 x 256 MiB = 8 GiB), so every step
+streams from HBM (inputs larger than L2).  Inputs are seeded synthetic
+bf16 N(0,1) with 4 outlier channels per KV head (x20) and amax/448 scales.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica on its GPU
+(independent sequences; no collective on the data path) and rank 0 prints
+the whole-job throughput over the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 paged decode attn: KV GB/s (% HBM peak) and µs/step vs context length"
+LAYERS = 32
+CONTEXT = 131072
+HQ, HKV, D, P = 32, 8, 128, 16
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=32,
+                    help="layers per step (fewer only for small profiling runs; the metric uses 32)")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def decode_bytes(context, batch=1, hq=HQ, hkv=HKV, d=D):
+    """Algorithmic bytes of one decode call: FP8 K + V of the attended
+    tokens, per-head K and V scales, q and out (bf16)."""
+    return 2 * batch * context * hkv * d + 2 * hkv * 4 + 2 * batch * hq * d * 2
+
+
+def cache_write_bytes(tokens, hkv=HKV, d=D):
+    """One token's K and V in (bf16) and out (FP8)."""
+    return tokens * hkv * d * (2 * 2 + 2 * 1)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ setup ---
+def build_workload(device, seed):
+    """32 layer caches of 131,072 cached tokens (the last one is re-written
+    by every step), per-layer q and new-token K/V, one shared block table."""
+    import torch
+
+    import fp8_kv_cache_reshape_gb300 as kvq
+    import workloads as W
+
+    g = W.generator(seed)
+    bt, num_blocks = W.paged_layout([CONTEXT], P, g)
+    bt_d = bt.to(device)
+    pos = torch.arange(CONTEXT, dtype=torch.int64)
+    slots = W.slots_for(bt, 0, pos, P).to(device)
+    layers = []
+    chunk = 16384
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    for l in range(LAYERS):
+        gl = W.generator(seed * 1000 + l, device=device)
+        k = W.randn_bf16((CONTEXT, HKV, D), gl, device=device)
+        v = W.randn_bf16((CONTEXT, HKV, D), gl, device=device)
+        ch = W.outlier_channels(HKV, D, 4, W.generator(seed * 1000 + l))
+        k = W.apply_outliers(k, ch)
+        v = W.apply_outliers(v, ch)
+        ks, vs = W.calibrate_amax(k), W.calibrate_amax(v)
+        kd, vd = kvq.alloc_kv_cache(num_blocks, HKV, D, device=device, fill=0)
+        for t0 in range(0, CONTEXT - 1, chunk):
+            t1 = min(CONTEXT - 1, t0 + chunk)
+            kvq.kvq_reshape_and_cache(k[t0:t1].contiguous(), v[t0:t1].contiguous(), slots[t0:t1].contiguous(),
+                                      kd, vd, ks, vs, dev_status=st)
+        layers.append(dict(kd=kd, vd=vd, ks=ks, vs=vs,
+                           k_new=k[CONTEXT - 1:].contiguous(), v_new=v[CONTEXT - 1:].contiguous(),
+                           q=W.randn_bf16((1, HQ, D), gl, device=device),
+                           out=torch.empty((1, HQ, D), dtype=torch.bfloat16, device=device)))
+        del k, v
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "cache fill reported a device fault"
+    ws_bytes = kvq.kvq_decode_workspace_size(1, HQ, HKV, D, bt.shape[1])
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    return dict(layers=layers, bt=bt_d, num_blocks=num_blocks, slot_new=slots[CONTEXT - 1:].contiguous(),
+                seq=torch.tensor([CONTEXT], dtype=torch.int32, device=device), ws=ws, status=st)
+
+
+def run_step(wl, seq=None, decode_only=False):
+    """One decode step over all layers (enqueued on the current stream)."""
+    import fp8_kv_cache_reshape_gb300 as kvq
+    seq = wl["seq"] if seq is None else seq
+    for ly in wl["layers"]:
+        if not decode_only:
+            kvq.kvq_reshape_and_cache(ly["k_new"], ly["v_new"], wl["slot_new"], ly["kd"], ly["vd"], ly["ks"],
+                                      ly["vs"], dev_status=wl["status"])
+        kvq.kvq_paged_decode_attention(ly["q"], ly["kd"], ly["vd"], ly["ks"], ly["vs"], wl["bt"], seq, ly["out"],
+                                       num_blocks=wl["num_blocks"], sm_scale=1.0 / math.sqrt(D),
+                                       workspace=wl["ws"], dev_status=wl["status"])
+
+
+def capture(fn):
+    """CUDA graph of everything fn() enqueues (run once eagerly first)."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, reps):
+    """Milliseconds for `reps` back-to-back replays (CUDA events on the
+    current stream, synchronized on both sides)."""
+    import torch
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record()
+    for _ in range(reps):
+        g.replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1)
+
+
+def time_eager(fn, reps):
+    import torch
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ev0.record()
+    for _ in range(reps):
+        fn()
+    ev1.record()
+    torch.cuda.synchronize()
+    return ev0.elapsed_time(ev1)
+
+
+def e2e_setup(wl):
+    """Pinned host copies of every layer's step inputs (q, new K/V) and
+    outputs, and the step with its host<->device copies."""
+    import torch
+    host_in = [dict(q=ly["q"].cpu().pin_memory(), k=ly["k_new"].cpu().pin_memory(),
+                    v=ly["v_new"].cpu().pin_memory()) for ly in wl["layers"]]
+    host_out = [torch.empty(ly["out"].shape, dtype=ly["out"].dtype).pin_memory() for ly in wl["layers"]]
+    h2d = sum(h["q"].numel() * 2 + h["k"].numel() * 2 + h["v"].numel() * 2 for h in host_in)
+    d2h = sum(o.numel() * 2 for o in host_out)
+
+    def one():
+        for i, ly in enumerate(wl["layers"]):
+            ly["q"].copy_(host_in[i]["q"], non_blocking=True)
+            ly["k_new"].copy_(host_in[i]["k"], non_blocking=True)
+            ly["v_new"].copy_(host_in[i]["v"], non_blocking=True)
+        run_step(wl)
+        for i, ly in enumerate(wl["layers"]):
+            host_out[i].copy_(ly["out"], non_blocking=True)
+
+    return one, h2d, d2h
+
+
+def context_sweep(wl, g_dec, reps=10):
+    """us per layer of the decode call at shorter contexts over the same
+    caches (seq_len = L attends to the first L cached tokens)."""
+    rows = []
+    for L in (4096, 8192, 16384, 32768, 65536, 131072):
+        wl["seq"].fill_(L)
+        g_dec.replay()
+        us = time_graph(g_dec, reps) * 1e3 / (reps * LAYERS)
+        rows.append({"context": L, "us_per_layer_decode": round(us, 3),
+                     "kv_gbs": round(decode_bytes(L) / (us * 1e-6) / 1e9, 1)})
+    wl["seq"].fill_(CONTEXT)
+    xs = [r["context"] for r in rows]
+    ys = [r["us_per_layer_decode"] for r in rows]
+    n = len(xs)
+    mx, my = sum(xs) / n, sum(ys) / n
+    slope = sum((x - mx) * (y - my) for x, y in zip(xs, ys)) / sum((x - mx) ** 2 for x in xs)
+    icpt = my - slope * mx
+    return {"points": rows, "fit_us_per_token": slope, "fit_intercept_us": round(icpt, 3),
+            "slope_kv_gbs": round(2 * HKV * D / (slope * 1e-6) / 1e9, 1)}
+
+
+# ---------------------------------------------------------- CPU baseline ---
+CPU_SAMPLE_CONTEXT = 131072
+CPU_SAMPLE_HEADS = 2
+
+
+def _oracle_sample():
+    """One layer of the workload cut to 2 of its 8 KV heads (8 query heads),
+    full 131,072-token context, cached by the oracle (not timed)."""
+    import numpy as np
+    import torch
+    import workloads as W
+    from oracle import kv_cache
+    g = W.generator(4242)
+    H, L = CPU_SAMPLE_HEADS, CPU_SAMPLE_CONTEXT
+    bt, nb = W.paged_layout([L], P, g)
+    slots = W.slots_for(bt, 0, torch.arange(L), P).numpy()
+    k = W.randn_bf16((L, H, D), g).float().numpy()
+    v = W.randn_bf16((L, H, D), g).float().numpy()
+    q = W.randn_bf16((1, H * (HQ // HKV), D), g).float().numpy()
+    ks = (np.abs(k).max(axis=(0, 2)) / 448).astype(np.float32)
+    vs = (np.abs(v).max(axis=(0, 2)) / 448).astype(np.float32)
+    kc = np.zeros((nb, H, P, D), np.uint8)
+    vc = np.zeros((nb, H, D, P), np.uint8)
+    kv_cache.reshape_and_cache(k, v, slots, kc, vc, ks, vs)
+    return dict(q=q, kc=kc, vc=vc, ks=ks, vs=vs, bt=bt.numpy(), L=L, H=H)
+
+
+def cpu_baseline_run(steps, warmup, min_seconds=0.0):
+    """Time the oracle's decode (float64 numpy, one host thread) on the
+    bounded sample: `warmup` untimed calls, then `steps` timed calls (more
+    until `min_seconds` have passed)."""
+    import numpy as np
+    from oracle import attention
+    smp = _oracle_sample()
+
+    def call():
+        attention.paged_decode(smp["q"], smp["kc"], smp["vc"], smp["ks"], smp["vs"], smp["bt"],
+                               np.array([smp["L"]]), 1 / math.sqrt(D))
+
+    for _ in range(warmup):
+        call()
+    t0 = time.perf_counter()
+    reps = 0
+    while reps < steps or time.perf_counter() - t0 < min_seconds:
+        call()
+        reps += 1
+    dt = (time.perf_counter() - t0) / reps
+    H = smp["H"]
+    byts = decode_bytes(smp["L"], hq=H * HQ // HKV, hkv=H)
+    return {"value": round(byts / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"decode call over one layer cut to {H} of {HKV} KV heads ({H * HQ // HKV} query heads), "
+                      f"context {smp['L']}; {reps} timed calls; float64 numpy, 1 host thread",
+            "seconds_per_call": round(dt, 4), "bytes_per_call": byts, "reps": reps}
+
+
+def cpu_baseline(steps=1, warmup=0, min_seconds=10.0):
+    """Run the CPU baseline in a child process pinned to one BLAS thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_cpu-baseline-child", str(steps), str(warmup),
+                        str(min_seconds)], env=env, capture_output=True, text=True, timeout=1800)
+    for line in r.stdout.splitlines()[::-1]:
+        if line.startswith("{"):
+            return json.loads(line)
+    return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+
+
+# ----------------------------------------------------------------- arms ---
+def reference_arm(args, rank, world):
+    """The oracle (the reference implementation of this build) timed on the
+    host cores, on the same metric, unit and workload shape; each step is
+    one oracle decode call over the bounded sample."""
+    if rank != 0:
+        return
+    cb = cpu_baseline(steps=args.steps, warmup=args.warmup, min_seconds=0.0)
+    sec = cb.get("seconds_per_call")
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None if sec is None else round(sec * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "llama31_8b_decode_128k", "layers": LAYERS, "batch": 1, "context": CONTEXT,
+                       "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "page": P,
+                       "step": f"one oracle decode call over {CPU_SAMPLE_HEADS} of {HKV} KV heads of one layer"},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def ours_arm(args, rank, world, local_rank):
+    import torch
+    device = f"cuda:{local_rank}"
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(device))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    wl = build_workload(device, seed=7 + rank)
+    g_step = capture(lambda: run_step(wl))
+    g_dec = capture(lambda: run_step(wl, decode_only=True))
+    for _ in range(max(3, args.warmup)):
+        g_step.replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        total_ms = time_graph(g_step, args.steps)
+        # the dominant kernel pair alone: 32 decode calls per replay
+        dec_reps = max(10, args.steps)
+        dec_ms = time_graph(g_dec, dec_reps)
+    barrier()
+    torch.cuda.synchronize()
+    elapsed = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
+    total_ms = float(elapsed.item())
+    st = int(wl["status"].item())
+    assert st == 0, f"device status {st:#x}"
+
+    step_bytes = LAYERS * (decode_bytes(CONTEXT) + cache_write_bytes(1))
+    ms_per_step = total_ms / args.steps
+    value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    peaks, src = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    call_ms = dec_ms / (dec_reps * LAYERS)
+    achieved = decode_bytes(CONTEXT) / (call_ms * 1e-3) / 1e9
+    traffic = None
+    tf = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if os.path.exists(tf):
+        try:
+            traffic = json.load(open(tf)).get("traffic_bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+    sweep = None if args.no_sweep else context_sweep(wl, g_dec)
+    e2e_fn, h2d, d2h = e2e_setup(wl)
+    g_e2e = capture(e2e_fn)
+    e2e_reps = max(3, args.steps)
+    e2e_ms = time_graph(g_e2e, e2e_reps) / e2e_reps
+    eager_ms = time_eager(e2e_fn, 3) / 3
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8_e4m3 storage, f16/f32 MMA, f32 accumulate", "data": "synthetic",
+        "config": {"workload": "llama31_8b_decode_128k", "layers": LAYERS, "batch": 1, "context": CONTEXT,
+                   "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "page": P, "block_table": "permuted",
+                   "scales": "per-KV-head amax/448, 4 outlier channels x20",
+                   "l2": "inputs larger than L2: 32 distinct 256 MiB layer caches per step",
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "us_per_layer": round(ms_per_step * 1e3 / LAYERS, 3)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": traffic,
+                     "kernel": "paged decode attention call (split-KV partial + LSE combine), per layer",
+                     "peak_source": f"{src} hbm_gbs",
+                     "avg_call_us": round(call_ms * 1e3, 3), "bytes_per_call": decode_bytes(CONTEXT),
+                     "timing": f"{dec_reps} replays of a CUDA graph of {LAYERS} decode calls"},
+        "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "how": "public API calls (host->device copies from pinned memory, step, device->host copies) "
+                       "captured once in a CUDA graph and replayed",
+                "eager_python_ms_per_step": round(eager_ms, 4),
+                "eager_python_value": round(step_bytes / (eager_ms * 1e-3) / 1e9, 1)},
+        "gpu_launches": args.steps * LAYERS * 3,
+        "timing": "CUDA graph of one step (32 x [cache write + decode partial + combine]) replayed",
+        "clocks": clk.summary(),
+        "sweep": sweep,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    if len(sys.argv) == 5 and sys.argv[1] == "--_cpu-baseline-child":
+        print(json.dumps(cpu_baseline_run(int(sys.argv[2]), int(sys.argv[3]), float(sys.argv[4]))), flush=True)
+        return
+    args = parse()
+    global LAYERS
+    LAYERS = args.layers
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    ours_arm(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

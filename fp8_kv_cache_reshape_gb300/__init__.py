@@ -1,0 +1,199 @@
+"""Python binding of libkvq (include/kvq.h): FP8 E4M3 KV-cache quantization
+and attention over a paged FP8 / BF16 KV cache on GB300 (sm_103a).
+
+The functions below carry the C ABI's names and only marshal arguments:
+shapes and device pointers are read from torch tensors, the current CUDA
+stream is passed through, and a non-zero status raises KvqError with the
+library's message.  Every step runs in the library's CUDA kernels; there is
+no fallback.  PyTorch provides device memory and streams.
+
+Build the library first (``python -c "import __graft_entry__ as g; g.build()"``
+or ``python fp8_kv_cache_reshape_gb300/_build.py``); importing this module
+without it raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+
+KVQ_OK = 0
+KVQ_ERR_INVALID_ARG = 1
+KVQ_ERR_UNSUPPORTED = 2
+KVQ_ERR_CUDA = 3
+KVQ_ERR_DEVICE_FAULT = 4
+
+KVQ_DTYPE_FP8_E4M3 = 0
+KVQ_DTYPE_BF16 = 1
+
+KVQ_DEV_BAD_SLOT = 0x1
+KVQ_DEV_BAD_BLOCK = 0x2
+KVQ_DEV_BAD_SEQLEN = 0x4
+KVQ_DEV_TIMEOUT = 0x8
+KVQ_DEV_BAD_QROWS = 0x10
+
+PAGE = 16
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libkvq.so is not built ({LIB_PATH}); run fp8_kv_cache_reshape_gb300/_build.py")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+
+lib.kvq_version.restype = _i
+lib.kvq_version.argtypes = []
+lib.kvq_last_error_string.restype = ctypes.c_char_p
+lib.kvq_last_error_string.argtypes = []
+lib.kvq_reshape_and_cache.restype = _i
+lib.kvq_reshape_and_cache.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i64, _i, _p, _p]
+lib.kvq_quantize_query.restype = _i
+lib.kvq_quantize_query.argtypes = [_p, _p, _p, _i64, _p]
+lib.kvq_decode_num_splits.restype = _i
+lib.kvq_decode_num_splits.argtypes = [_i, _i, _i, _i, _i, _i]
+lib.kvq_decode_workspace_size.restype = _sz
+lib.kvq_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i]
+lib.kvq_paged_decode_attention.restype = _i
+lib.kvq_paged_decode_attention.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _f,
+                                           _i, _i, _i, _p, _sz, _p, _p]
+lib.kvq_prefill_attention.restype = _i
+lib.kvq_prefill_attention.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
+                                      _f, _i, _p, _p]
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = lib.kvq_last_error_string().decode(errors="replace")
+        super().__init__(f"{where}: status {status}: {msg}")
+        self.status = status
+
+
+def _check(status: int, where: str):
+    if status != KVQ_OK:
+        raise KvqError(status, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libkvq takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libkvq takes contiguous tensors only")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(cache_dtype: str) -> int:
+    if cache_dtype in ("fp8", "fp8_e4m3", KVQ_DTYPE_FP8_E4M3):
+        return KVQ_DTYPE_FP8_E4M3
+    if cache_dtype in ("bf16", "bfloat16", KVQ_DTYPE_BF16):
+        return KVQ_DTYPE_BF16
+    raise ValueError(f"unknown cache dtype {cache_dtype!r}")
+
+
+def version() -> int:
+    return lib.kvq_version()
+
+
+def alloc_kv_cache(num_blocks: int, kv_heads: int, head_dim: int, cache_dtype="fp8_e4m3",
+                   device="cuda", fill=None):
+    """Allocate (k_cache, v_cache) as uint8 tensors in the library's paged
+    format ([num_blocks][Hkv][P][D] and [num_blocks][Hkv][D][P] elements)."""
+    esz = 1 if _dtype_code(cache_dtype) == KVQ_DTYPE_FP8_E4M3 else 2
+    shape = (num_blocks, kv_heads, PAGE * head_dim * esz)
+    if fill is None:
+        return (torch.empty(shape, dtype=torch.uint8, device=device),
+                torch.empty(shape, dtype=torch.uint8, device=device))
+    return (torch.full(shape, fill, dtype=torch.uint8, device=device),
+            torch.full(shape, fill, dtype=torch.uint8, device=device))
+
+
+def kvq_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None,
+                          cache_dtype="fp8_e4m3", dev_status=None, stream=None):
+    """Quantize (or copy) new tokens k, v (bf16 [T][Hkv][D]) into the cache."""
+    T, Hkv, D = k.shape
+    dt = _dtype_code(cache_dtype)
+    esz = 1 if dt == KVQ_DTYPE_FP8_E4M3 else 2
+    num_blocks = k_cache.numel() // (Hkv * PAGE * D * esz)
+    _check(lib.kvq_reshape_and_cache(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(k_scale), _ptr(v_scale), T, Hkv, D, PAGE, num_blocks, dt,
+                                     _ptr(dev_status), _stream(stream)), "kvq_reshape_and_cache")
+
+
+def kvq_quantize_query(q, q8, q_scale, stream=None):
+    """q8 = E4M3(q / q_scale), per tensor."""
+    _check(lib.kvq_quantize_query(_ptr(q), _ptr(q8), _ptr(q_scale), q.numel(), _stream(stream)),
+           "kvq_quantize_query")
+
+
+def kvq_decode_num_splits(B, Hkv, max_blocks, window=-1, num_splits=0):
+    return lib.kvq_decode_num_splits(B, Hkv, PAGE, max_blocks, window, num_splits)
+
+
+def kvq_decode_workspace_size(B, Hq, Hkv, D, max_blocks, window=-1, num_splits=0):
+    return lib.kvq_decode_workspace_size(B, Hq, Hkv, D, PAGE, max_blocks, window, num_splits)
+
+
+def kvq_paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out,
+                               num_blocks=None, sm_scale=None, window=-1, cache_dtype="fp8_e4m3",
+                               num_splits=0, workspace=None, dev_status=None, stream=None):
+    """One decode step over the paged cache; writes out (bf16 [B][Hq][D]).
+
+    workspace: a uint8 CUDA tensor of at least kvq_decode_workspace_size()
+    bytes (allocated here when omitted)."""
+    B, Hq, D = q.shape
+    max_blocks = block_table.shape[1]
+    dt = _dtype_code(cache_dtype)
+    esz = 1 if dt == KVQ_DTYPE_FP8_E4M3 else 2
+    Hkv = k_cache.shape[1] if k_cache.dim() >= 3 else None
+    if Hkv is None:
+        raise ValueError("k_cache must be [num_blocks][Hkv][...]")
+    if num_blocks is None:
+        num_blocks = k_cache.shape[0]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    need = kvq_decode_workspace_size(B, Hq, Hkv, D, max_blocks, window, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib.kvq_paged_decode_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                          _ptr(block_table), _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, PAGE,
+                                          max_blocks, num_blocks, float(sm_scale), window, dt, num_splits,
+                                          _ptr(workspace), workspace.numel(), _ptr(dev_status),
+                                          _stream(stream)), "kvq_paged_decode_attention")
+    return out
+
+
+def kvq_prefill_attention(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q,
+                          seq_lens, out, max_q_tokens, num_blocks=None, sm_scale=None, causal=True,
+                          dev_status=None, stream=None):
+    """Chunked causal prefill over the FP8 cache; writes out (bf16 [Tq][Hq][D])."""
+    Tq, Hq, D = q8.shape
+    B = cu_seqlens_q.numel() - 1
+    Hkv = k_cache.shape[1]
+    if num_blocks is None:
+        num_blocks = k_cache.shape[0]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    _check(lib.kvq_prefill_attention(_ptr(q8), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                     _ptr(v_scale), _ptr(block_table), _ptr(cu_seqlens_q), _ptr(seq_lens),
+                                     _ptr(out), B, Hq, Hkv, D, PAGE, block_table.shape[1], num_blocks,
+                                     int(max_q_tokens), float(sm_scale), 1 if causal else 0,
+                                     _ptr(dev_status), _stream(stream)), "kvq_prefill_attention")
+    return out

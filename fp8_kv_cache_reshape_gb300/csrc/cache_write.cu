@@ -1,0 +1,238 @@
+// kvq_reshape_and_cache and kvq_quantize_query.
+//
+// Quantization follows "FP8 quantization and long-context inference"
+// (section 1.1: q = round(x / scale)) and "FP8 and KV cache" ("Dynamic or
+// static scale": values whose quotient exceeds 448 saturate to 448): one IEEE
+// float32 division, then one saturating round-to-nearest-even conversion.
+// Per-KV-head scales follow "The state of FP8 KV-cache and attention
+// quantization in vLLM" ("Kernel and vLLM improvements", per-head scales: the
+// cache-write kernel takes an array of scales instead of a scalar).
+//
+// One CTA handles a group of 16 consecutive tokens of one KV head.  When the
+// group's slots fill exactly one page (the common case: prefill chunks and
+// cache fills) the V page is transposed in shared memory and written as full
+// 16-byte rows; otherwise every token is scattered on its own.
+#include "kvq_device.cuh"
+#include "kvq_host.h"
+
+namespace kvq {
+
+namespace {
+
+// 16 bf16 (two 16-byte loads) -> 16 floats.
+KVQ_DEVINL void load16_bf16(const __nv_bfloat16* src, float (&x)[16]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4 a = __ldg(s), b = __ldg(s + 1);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+KVQ_DEVINL uint4 quant16(const float (&x)[16], float s) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t b0 = f32_to_e4m3(__fdiv_rn(x[4 * i + 0], s));
+    uint32_t b1 = f32_to_e4m3(__fdiv_rn(x[4 * i + 1], s));
+    uint32_t b2 = f32_to_e4m3(__fdiv_rn(x[4 * i + 2], s));
+    uint32_t b3 = f32_to_e4m3(__fdiv_rn(x[4 * i + 3], s));
+    w[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// FP8 cache write.  grid = (ceil(T / 16), Hkv), block = 128.
+template <int D>
+__global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
+    const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+    const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+    const float* __restrict__ k_scale, const float* __restrict__ v_scale, int T, int Hkv, int64_t num_slots,
+    int* dev_status) {
+  constexpr int CH = D / 16;          // 16-byte chunks per row
+  constexpr int PAGE_BYTES = kPage * D;
+  __shared__ __align__(16) uint8_t vt[D * kPage];  // transposed V page
+  __shared__ int64_t slots[kPage];
+  __shared__ int fast;
+
+  const int g0 = blockIdx.x * kPage;
+  const int h = blockIdx.y;
+  const int tid = threadIdx.x;
+  if (tid < kPage) {
+    int t = g0 + tid;
+    slots[tid] = (t < T) ? slot_mapping[t] : -1;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int64_t s0 = slots[0];
+    bool ok = (g0 + kPage <= T) && s0 >= 0 && (s0 % kPage) == 0 && s0 + kPage <= num_slots;
+    for (int i = 1; ok && i < kPage; ++i) ok = (slots[i] == s0 + i);
+    fast = ok ? 1 : 0;
+    for (int i = 0; i < kPage; ++i)
+      if (slots[i] >= num_slots) set_status(dev_status, KVQ_DEV_BAD_SLOT);
+  }
+  __syncthreads();
+  const float sk = k_scale[h], sv = v_scale[h];
+
+  for (int u = tid; u < kPage * CH; u += blockDim.x) {
+    const int t = u / CH, j = u % CH;
+    const int64_t slot = slots[t];
+    if (slot < 0 || slot >= num_slots) continue;
+    const int64_t blk = slot / kPage;
+    const int off = static_cast<int>(slot % kPage);
+    const size_t src = (static_cast<size_t>(g0 + t) * Hkv + h) * D + j * 16;
+    const size_t page = (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
+    float x[16];
+    load16_bf16(k + src, x);
+    *reinterpret_cast<uint4*>(k_cache + page + k_chunk_offset(off, j, D)) = quant16(x, sk);
+    load16_bf16(v + src, x);
+    uint4 qv = quant16(x, sv);
+    const uint8_t* qb = reinterpret_cast<const uint8_t*>(&qv);
+    const int slot_in_row = fp8_v_slot(off);
+    if (fast) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) vt[(j * 16 + i) * kPage + slot_in_row] = qb[i];
+    } else {
+      uint8_t* vp = v_cache + page + slot_in_row;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) vp[(j * 16 + i) * kPage] = qb[i];
+    }
+  }
+  if (fast) {
+    __syncthreads();
+    const int64_t blk = slots[0] / kPage;
+    uint8_t* vp = v_cache + (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
+    for (int d = tid; d < D; d += blockDim.x)
+      *reinterpret_cast<uint4*>(vp + d * kPage) = *reinterpret_cast<const uint4*>(vt + d * kPage);
+  }
+}
+
+// BF16 cache write (bit copy into the BF16 page format).
+template <int D>
+__global__ void __launch_bounds__(128) reshape_and_cache_bf16_kernel(
+    const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int64_t* __restrict__ slot_mapping,
+    uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, int T, int Hkv, int64_t num_slots,
+    int* dev_status) {
+  constexpr int ROWB = D * 2;
+  constexpr int CH = ROWB / 16;  // 8 bf16 per chunk
+  constexpr int PAGE_BYTES = kPage * ROWB;
+  const int g0 = blockIdx.x * kPage;
+  const int h = blockIdx.y;
+  for (int u = threadIdx.x; u < kPage * CH; u += blockDim.x) {
+    const int t = u / CH, j = u % CH;
+    if (g0 + t >= T) continue;
+    const int64_t slot = slot_mapping[g0 + t];
+    if (slot < 0) continue;
+    if (slot >= num_slots) {
+      if (j == 0) set_status(dev_status, KVQ_DEV_BAD_SLOT);
+      continue;
+    }
+    const int64_t blk = slot / kPage;
+    const int off = static_cast<int>(slot % kPage);
+    const size_t src = (static_cast<size_t>(g0 + t) * Hkv + h) * D + j * 8;
+    uint8_t* page_k = k_cache + (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
+    uint8_t* page_v = v_cache + (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
+    *reinterpret_cast<uint4*>(page_k + k_chunk_offset(off, j, ROWB)) =
+        __ldg(reinterpret_cast<const uint4*>(k + src));
+    uint4 vv = __ldg(reinterpret_cast<const uint4*>(v + src));
+    const uint16_t* ve = reinterpret_cast<const uint16_t*>(&vv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int d = j * 8 + i;
+      *reinterpret_cast<uint16_t*>(page_v + bf16_v_offset(d, off)) = ve[i];
+    }
+  }
+}
+
+// Query quantization: 16 elements per thread, scalar tail.
+__global__ void __launch_bounds__(256) quantize_query_kernel(const __nv_bfloat16* __restrict__ q,
+                                                             uint8_t* __restrict__ q8,
+                                                             const float* __restrict__ q_scale, int64_t n) {
+  const float s = *q_scale;
+  const int64_t nvec = n / 16;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nvec;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float x[16];
+    load16_bf16(q + i * 16, x);
+    *reinterpret_cast<uint4*>(q8 + i * 16) = quant16(x, s);
+  }
+  if (blockIdx.x == 0) {
+    for (int64_t i = nvec * 16 + threadIdx.x; i < n; i += blockDim.x)
+      q8[i] = f32_to_e4m3(__fdiv_rn(__bfloat162float(q[i]), s));
+  }
+}
+
+}  // namespace
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping,
+                                              void* k_cache, void* v_cache, const float* k_scale,
+                                              const float* v_scale, int T, int Hkv, int D, int P,
+                                              int64_t num_blocks, kvq_dtype_t cache_dtype, int* dev_status,
+                                              kvq_stream_t stream) {
+  clear_error();
+  if (T < 0 || Hkv < 1 || num_blocks < 1) return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: bad sizes");
+  if (P != kPage) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache: page size %d (only 16)", P);
+  if (D != 64 && D != 128) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache: head_dim %d", D);
+  if (cache_dtype != KVQ_DTYPE_FP8_E4M3 && cache_dtype != KVQ_DTYPE_BF16)
+    return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: bad cache dtype");
+  if (T == 0) return KVQ_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+    return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: null pointer");
+  if (cache_dtype == KVQ_DTYPE_FP8_E4M3 && (!k_scale || !v_scale))
+    return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: FP8 needs k_scale and v_scale");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8))
+    return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: pointers must be 16-byte aligned");
+  if (Hkv > 65535) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache: too many KV heads");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dim3 grid((T + kPage - 1) / kPage, Hkv);
+  const int64_t num_slots = num_blocks * kPage;
+  if (cache_dtype == KVQ_DTYPE_FP8_E4M3) {
+    auto kb = static_cast<const __nv_bfloat16*>(k);
+    auto vb = static_cast<const __nv_bfloat16*>(v);
+    auto kc = static_cast<uint8_t*>(k_cache);
+    auto vc = static_cast<uint8_t*>(v_cache);
+    if (D == 128)
+      reshape_and_cache_fp8_kernel<128><<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, k_scale, v_scale, T, Hkv,
+                                                             num_slots, dev_status);
+    else
+      reshape_and_cache_fp8_kernel<64><<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, k_scale, v_scale, T, Hkv,
+                                                            num_slots, dev_status);
+  } else {
+    auto kb = static_cast<const uint16_t*>(k);
+    auto vb = static_cast<const uint16_t*>(v);
+    auto kc = static_cast<uint8_t*>(k_cache);
+    auto vc = static_cast<uint8_t*>(v_cache);
+    if (D == 128)
+      reshape_and_cache_bf16_kernel<128><<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, T, Hkv, num_slots,
+                                                              dev_status);
+    else
+      reshape_and_cache_bf16_kernel<64><<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, T, Hkv, num_slots,
+                                                             dev_status);
+  }
+  return cuda_status(cudaGetLastError(), "reshape_and_cache launch");
+}
+
+extern "C" kvq_status_t kvq_quantize_query(const void* q, uint8_t* q8, const float* q_scale, int64_t n,
+                                           kvq_stream_t stream) {
+  clear_error();
+  if (n < 0) return fail(KVQ_ERR_INVALID_ARG, "quantize_query: n < 0");
+  if (n == 0) return KVQ_OK;
+  if (!q || !q8 || !q_scale) return fail(KVQ_ERR_INVALID_ARG, "quantize_query: null pointer");
+  if (!aligned(q, 16) || !aligned(q8, 16))
+    return fail(KVQ_ERR_INVALID_ARG, "quantize_query: pointers must be 16-byte aligned");
+  const int64_t nvec = n / 16;
+  int64_t blocks = (nvec + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  quantize_query_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(q), q8, q_scale, n);
+  return cuda_status(cudaGetLastError(), "quantize_query launch");
+}

@@ -1,0 +1,240 @@
+/*
+ * kvq.h -- C ABI of libkvq: FP8 (E4M3) KV-cache quantization and attention
+ * over a paged FP8 (or BF16) KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the statement of the method on these pages:
+ *  [vLLM]   "The state of FP8 KV-cache and attention quantization in vLLM"
+ *           (vLLM blog, 2026-04-22): sections "Problems we found",
+ *           "Kernel and vLLM improvements" (two-level accumulation, skip
+ *           layers, per-head scales, query quantization fusion),
+ *           "Performance benchmarks".
+ *  [FP8KV]  "FP8 and KV cache" (cooking-agi tutorial): sections "Dynamic or
+ *           static scale", "KV cache", "How to enable it in the engine".
+ *  [GTNT]   "FP8 quantization and long-context inference" (gtnt.cn),
+ *           section 1.1 (scale = max_abs / 448, q = round(x / scale)) and
+ *           section 6 (PagedAttention).
+ *
+ * Conventions for every call
+ *  - All tensor arguments are DEVICE pointers owned by the caller; the
+ *    library never allocates, frees or keeps them.  Scales are device
+ *    pointers too, so calls can be captured in a CUDA graph.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and runs asynchronously; a KVQ_OK return means "validated and
+ *    launched".
+ *  - Host-side validation (null pointers, sizes, alignment, unsupported
+ *    shapes) happens before any launch; on failure nothing is launched, a
+ *    status is returned and kvq_last_error_string() describes it.
+ *  - Faults only the device can see (a block id outside [0, num_blocks), a
+ *    cache slot beyond the cache, a sequence longer than its block table, a
+ *    pipeline wait that timed out) OR a KVQ_DEV_* bit into *dev_status
+ *    (a device int the caller zeroes and reads back) and skip the offending
+ *    work; kernels never trap.  dev_status may be NULL to ignore them.
+ *  - bf16 tensors are passed as raw 16-bit storage (void*).
+ *
+ * Cache format (both caches have num_blocks blocks of Hkv pages each; one
+ * page holds P = 16 tokens of one KV head; token slot s is block s / P,
+ * offset t = s % P, following PagedAttention):
+ *  - K cache, element [block][h][t][d]: a page is P rows of D elements; the
+ *    16-byte chunks of row t are stored XOR-swizzled so that the page can be
+ *    copied to shared memory as one contiguous block and read without bank
+ *    conflicts: with 128-byte rows chunk j sits at chunk j ^ (t % 8); with
+ *    64-byte rows at j ^ ((t / 2) % 4); with 256-byte rows (BF16, D = 128)
+ *    each 128-byte half is swizzled as a 128-byte row.  Row bytes = D * esize.
+ *  - V cache, element [block][h][d][slot]: the page transposed, one row of P
+ *    token slots per dimension d.  FP8: token t occupies slot rho(t) with
+ *    rho = {0,1,4,5,8,9,12,13,2,3,6,7,10,11,14,15} (tokens 2c,2c+1,2c+8,2c+9
+ *    share the 4-byte word c).  BF16: slot = t, and the two 16-byte halves of
+ *    row d are swapped when (d / 4) is odd.
+ *  - FP8 elements are E4M3 ("OCP FN": bias 7, max 448, min subnormal 2^-9,
+ *    0x7F/0xFF NaN, no infinity).  Page bytes = P * D * esize.
+ *
+ * Quantization (kvq_reshape_and_cache, kvq_quantize_query):
+ *    code = e4m3_rne_satfinite( fl32(x / scale) )
+ *  one IEEE float32 division, then one round-to-nearest-even conversion that
+ *  saturates to +-448 ([FP8KV] "Dynamic or static scale": 180 / s = 672
+ *  saturates to 448).  Dequantized value = decode(code) * scale.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+  KVQ_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim, page size, GQA ratio) */
+  KVQ_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute query) */
+  KVQ_ERR_DEVICE_FAULT = 4   /* reserved for callers that fold *dev_status into a status */
+} kvq_status_t;
+
+typedef enum kvq_dtype {
+  KVQ_DTYPE_FP8_E4M3 = 0,    /* 1-byte E4M3 codes with per-KV-head scales */
+  KVQ_DTYPE_BF16 = 1         /* unquantized bfloat16 ("skip layers") */
+} kvq_dtype_t;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define KVQ_DEV_BAD_SLOT     0x1  /* slot_mapping[t] >= num_blocks * P: token skipped */
+#define KVQ_DEV_BAD_BLOCK    0x2  /* block id outside [0, num_blocks): page masked out */
+#define KVQ_DEV_BAD_SEQLEN   0x4  /* seq_len < 0 or > max_blocks * P: clamped */
+#define KVQ_DEV_TIMEOUT      0x8  /* a pipeline wait exceeded its bound: work abandoned */
+#define KVQ_DEV_BAD_QROWS    0x10 /* prefill: new tokens exceed seq_len: rows skipped */
+
+typedef void* kvq_stream_t;   /* cudaStream_t */
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int kvq_version(void);
+
+/* Text of the last host-side error on the calling thread ("" if none). */
+const char* kvq_last_error_string(void);
+
+/*
+ * kvq_reshape_and_cache -- quantize new K/V tokens into the paged cache.
+ * [vLLM] "Kernel and vLLM improvements", per-head scales: the cache-write
+ * kernel takes an array of scales, one per KV head.  [FP8KV] "How to enable
+ * it in the engine": scales per tensor or per head; uncalibrated = 1.0.
+ *
+ *  k, v          bf16 [T][Hkv][D], row-major, contiguous.
+ *  slot_mapping  int64 [T]: cache slot of each token; a negative slot skips
+ *                the token; a slot >= num_blocks * P sets KVQ_DEV_BAD_SLOT.
+ *  k_cache       [num_blocks][Hkv][P][D] in the format above (written).
+ *  v_cache       [num_blocks][Hkv][D][P] in the format above (written).
+ *  k_scale,      float32 [Hkv] per-KV-head scales (FP8 only; may be NULL for
+ *  v_scale       BF16).  Must be finite and > 0.
+ *  T >= 0 (T == 0 launches nothing), Hkv >= 1, D in {64, 128}, P == 16,
+ *  num_blocks >= 1.  For BF16 the values are copied bit for bit.
+ *  Only the bytes of the given slots are written; everything else in the
+ *  caches is left as it was.  Slots must be distinct within one call.
+ */
+kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping,
+                                   void* k_cache, void* v_cache,
+                                   const float* k_scale, const float* v_scale,
+                                   int T, int Hkv, int D, int P, int64_t num_blocks,
+                                   kvq_dtype_t cache_dtype, int* dev_status, kvq_stream_t stream);
+
+/*
+ * kvq_quantize_query -- per-tensor query quantization to E4M3.
+ * [vLLM] "Kernel and vLLM improvements", query quantization fusion;
+ * [FP8KV] "How to enable it in the engine": with FP8 attention the query is
+ * quantized to FP8 too; one scale per tensor for Q.
+ *
+ *  q        bf16 [n] (any shape, contiguous).
+ *  q8       uint8 [n] E4M3 codes (written).
+ *  q_scale  float32 [1], finite and > 0.
+ *  n >= 0; pointers 16-byte aligned when n > 0.
+ */
+kvq_status_t kvq_quantize_query(const void* q, uint8_t* q8, const float* q_scale, int64_t n,
+                                kvq_stream_t stream);
+
+/*
+ * Split-KV plan for kvq_paged_decode_attention.  num_splits = 0 asks for the
+ * library's choice for this GPU; the function returns the number of splits
+ * that a call with the same arguments will use (>= 1), or 0 on bad input.
+ */
+int kvq_decode_num_splits(int B, int Hkv, int P, int max_blocks, int window, int num_splits);
+
+/* Workspace bytes a decode call with these arguments needs (float32
+ * partial outputs [B][Hq][S][D] and log-sum-exps [B][Hq][S]). */
+size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P, int max_blocks,
+                                 int window, int num_splits);
+
+/*
+ * kvq_paged_decode_attention -- one decode step of softmax(q K^T * sm_scale) V
+ * over the paged cache, read directly in FP8 (or BF16).
+ * [vLLM] "Performance benchmarks" (the decode cost is the per-token KV read,
+ * the ITL slope), "Problems we found" / "Kernel and vLLM improvements"
+ * (two-level FP32 accumulation: the P.V contraction runs over the context;
+ * partial sums are promoted into real FP32 registers), "Skip layers"
+ * (sliding-window layers keep a BF16 cache).
+ *
+ * Split-KV: each (sequence, KV head) is cut into num_splits ranges of pages;
+ * a partial kernel writes per range a normalized output and a log-sum-exp to
+ * the workspace, and a combine kernel merges them:
+ *   lse = log sum_i exp(lse_i),  out = sum_i exp(lse_i - lse) out_i.
+ * Accumulation: scores and P.V products are accumulated by tensor-core MMAs
+ * into fresh FP32 registers per page of 16 tokens, then added into a running
+ * FP32 sum (first level), and ranges are merged in FP32 (second level).
+ *
+ *  q            bf16 [B][Hq][D].  Query head h reads KV head h / (Hq / Hkv).
+ *  k_cache,     the caches written by kvq_reshape_and_cache.
+ *  v_cache
+ *  k_scale,     float32 [Hkv] (FP8; ignored for BF16, may be NULL).
+ *  v_scale
+ *  block_table  int32 [B][max_blocks]: block id of each page of a sequence.
+ *  seq_lens     int32 [B]: tokens in each sequence's cache (including the
+ *               current token); 0 gives an all-zero output.
+ *  out          bf16 [B][Hq][D] (written).
+ *  window       -1 = full attention; W > 0 = the last W tokens
+ *               [max(0, L - W), L) only (sliding-window layers).
+ *  num_splits   0 = automatic, else the number of page ranges (>= 1).
+ *  workspace    device buffer of kvq_decode_workspace_size(...) bytes,
+ *               16-byte aligned, owned by the caller; contents on entry are
+ *               ignored; calls sharing a workspace must not overlap.
+ *  Supported: D in {64, 128}, P == 16, Hq % Hkv == 0, Hq / Hkv <= 8.
+ *  Declared rounding: FP8 -- q is rounded to float16 (exact for bf16 values
+ *  of magnitude in [2^-14, 65504]), K and V codes are used exactly, scores
+ *  are s2 = fl32(sum_d f16(q)[d] k8[d]) * c with c = fl32(fl32(k_scale *
+ *  sm_scale) * log2(e)); probabilities 2^(s2 - m) are fed to the P.V MMA as
+ *  the sum of two float16 terms (hi + lo, about 22 significant bits); the
+ *  result is multiplied by v_scale.  BF16 -- scores use
+ *  q and k exactly, c = fl32(sm_scale * log2(e)); probabilities are fed to
+ *  the P.V MMA as the sum of two bfloat16 terms.  The output is rounded to
+ *  bf16 once, at the end.
+ */
+kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                        const float* k_scale, const float* v_scale,
+                                        const int32_t* block_table, const int32_t* seq_lens,
+                                        void* out, int B, int Hq, int Hkv, int D, int P,
+                                        int max_blocks, int64_t num_blocks, float sm_scale,
+                                        int window, kvq_dtype_t cache_dtype, int num_splits,
+                                        void* workspace, size_t workspace_bytes,
+                                        int* dev_status, kvq_stream_t stream);
+
+/*
+ * kvq_prefill_attention -- chunked causal prefill over the FP8 cache on FP8
+ * tensor cores.  [vLLM] "Kernel and vLLM improvements" (two-level
+ * accumulation, prefill tile configurations), "Large head dimension
+ * limitations" (two-level accumulation's cost in prefill); [FP8KV] "How to
+ * enable it in the engine" (QK and score.V in FP8, query quantized to FP8).
+ *
+ * The new tokens must already be in the cache (kvq_reshape_and_cache).
+ * Sequence b has nq_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] new tokens, the
+ * last nq_b of its L_b = seq_lens[b] cached tokens; query i of b sits at
+ * position L_b - nq_b + i and attends to keys 0 .. L_b - nq_b + i (causal)
+ * or to all L_b keys (causal = 0).
+ *
+ *  q8            uint8 [Tq][Hq][D] E4M3 codes (kvq_quantize_query), Tq =
+ *                cu_seqlens_q[B].
+ *  q_scale       float32 [1].
+ *  k_cache, v_cache, k_scale, v_scale, block_table  as for decode (FP8 only).
+ *  cu_seqlens_q  int32 [B+1], non-decreasing, cu_seqlens_q[0] = 0.
+ *  seq_lens      int32 [B].
+ *  out           bf16 [Tq][Hq][D] (written).
+ *  max_q_tokens  an upper bound of max_b nq_b (sizes the launch).
+ *  Supported: D == 128, P == 16, Hq % Hkv == 0.
+ *  Declared rounding: S = sum_d q8[d] k8[d] (exact products, FP32 sums),
+ *  s2 = S * c with c = fl32(fl32(fl32(q_scale * k_scale) * sm_scale) *
+ *  log2(e)); P8 = e4m3_rne_sat(fl32(2^(s2 - m) * 256)) against the running
+ *  row maximum m; each KV tile's P8.V8 product goes into a fresh FP32
+ *  tensor-memory accumulator that is then added in FP32 into the running
+ *  output (two-level accumulation); out = O * v_scale / (256 * l), l the
+ *  FP32 sum of the unquantized probabilities.
+ */
+kvq_status_t kvq_prefill_attention(const uint8_t* q8, const float* q_scale,
+                                   const void* k_cache, const void* v_cache,
+                                   const float* k_scale, const float* v_scale,
+                                   const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                   const int32_t* seq_lens, void* out,
+                                   int B, int Hq, int Hkv, int D, int P, int max_blocks,
+                                   int64_t num_blocks, int max_q_tokens, float sm_scale,
+                                   int causal, int* dev_status, kvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

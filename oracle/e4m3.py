@@ -131,3 +131,18 @@ def quantize(x, scale) -> np.ndarray:
 def dequantize(codes, scale) -> np.ndarray:
     """x_hat = decode(q) * scale, in float64."""
     return decode(codes) * np.asarray(scale, dtype=np.float32).astype(np.float64)
+
+
+_ALL_BF16 = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+
+
+def quantize_bf16_table(scale) -> np.ndarray:
+    """quantize() evaluated once for every bfloat16 input: uint8 [65536],
+    indexed by the bf16 bit pattern.  The same function as quantize() on a
+    finite domain, used to keep large test cases fast."""
+    return quantize(_ALL_BF16, np.float32(scale))
+
+
+def quantize_bf16_bits(bits, scale) -> np.ndarray:
+    """quantize() of bfloat16 inputs given as uint16 bit patterns."""
+    return quantize_bf16_table(scale)[np.asarray(bits, dtype=np.uint16)]

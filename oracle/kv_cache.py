@@ -56,6 +56,14 @@ def f32_to_bf16_bits_exact(x) -> np.ndarray:
     return (u >> 16).astype(np.uint16)
 
 
+def _bf16_bits_or_none(x):
+    """uint16 bit patterns if every value of x is a bfloat16, else None."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    if np.any(u & 0xFFFF):
+        return None
+    return (u >> 16).astype(np.uint16)
+
+
 # -------------------------------------------------------------- cache write ---
 def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
                       cache_dtype=FP8):
@@ -76,23 +84,27 @@ def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
     T, Hkv, D = k.shape
     num_blocks, _, P, _ = k_cache.shape
     slots = np.asarray(slot_mapping, dtype=np.int64)
-    bad = False
     if cache_dtype == FP8:
-        kq = e4m3.quantize(k, np.asarray(k_scale, np.float32)[None, :, None])
-        vq = e4m3.quantize(v, np.asarray(v_scale, np.float32)[None, :, None])
+        ks = np.asarray(k_scale, np.float32)
+        vs = np.asarray(v_scale, np.float32)
+        kb, vb = _bf16_bits_or_none(k), _bf16_bits_or_none(v)
+        if kb is not None and vb is not None:
+            kq = np.empty(k.shape, np.uint8)
+            vq = np.empty(v.shape, np.uint8)
+            for h in range(Hkv):  # one table per head: encode(fl32(x / s[h])) for every bf16 x
+                kq[:, h] = e4m3.quantize_bf16_bits(kb[:, h], ks[h])
+                vq[:, h] = e4m3.quantize_bf16_bits(vb[:, h], vs[h])
+        else:
+            kq = e4m3.quantize(k, ks[None, :, None])
+            vq = e4m3.quantize(v, vs[None, :, None])
     else:
         kq = f32_to_bf16_bits_exact(k)
         vq = f32_to_bf16_bits_exact(v)
-    for t in range(T):
-        s = int(slots[t])
-        if s < 0:
-            continue
-        if s >= num_blocks * P:
-            bad = True
-            continue
-        blk, off = divmod(s, P)
-        k_cache[blk, :, off, :] = kq[t]
-        v_cache[blk, :, :, off] = vq[t]
+    bad = bool(np.any(slots >= num_blocks * P))
+    keep = (slots >= 0) & (slots < num_blocks * P)
+    blk, off = slots[keep] // P, slots[keep] % P
+    k_cache[blk, :, off, :] = kq[keep]
+    v_cache[blk, :, :, off] = vq[keep]
     return k_cache, v_cache, bad
 
 

@@ -1,0 +1,70 @@
+"""Helpers shared by the tests: build caches with the oracle, move them to
+the device in the library's page format, and measure errors.  Inputs come
+from workloads/; expected values come only from oracle/."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import attention, kv_cache, layout
+from oracle.kv_cache import FP8, BF16
+
+SENTINEL = 0xA5
+
+# Attention tolerance for unit-variance inputs: max-abs 1e-2, mean-abs 1e-3.
+# The output is bfloat16, whose round-to-nearest adds up to 2^-9 |o| to an
+# element of magnitude |o|; outputs far from unit scale (the x20 outlier
+# channels) get that rounding on top of the absolute budget.
+MAX_ABS = 1e-2
+MEAN_ABS = 1e-3
+BF16_HALF_ULP_REL = 2.0 ** -9
+
+
+def f32(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy()
+
+
+def oracle_cache(case, sentinel=SENTINEL):
+    """Logical oracle caches holding every token of the case."""
+    cfg = case.cfg
+    D, H = cfg.head_dim, cfg.kv_heads
+    dt = np.uint8 if case.cache_dtype == FP8 else np.uint16
+    fill = sentinel if dt == np.uint8 else (sentinel << 8) | sentinel
+    kc = np.full((case.num_blocks, H, 16, D), fill, dt)
+    vc = np.full((case.num_blocks, H, D, 16), fill, dt)
+    kv_cache.reshape_and_cache(f32(case.k), f32(case.v), case.slot_mapping.numpy(), kc, vc,
+                               case.k_scale.numpy(), case.v_scale.numpy(), case.cache_dtype)
+    return kc, vc
+
+
+def to_device_cache(kc, vc, device="cuda"):
+    kd, vd = layout.to_device_format(kc, vc)
+    return torch.from_numpy(kd).to(device), torch.from_numpy(vd).to(device)
+
+
+def oracle_decode(case, kc, vc, mode="mirror", window=None):
+    return attention.paged_decode(f32(case.q), kc, vc, case.k_scale.numpy(), case.v_scale.numpy(),
+                                  case.block_table.numpy(), case.seq_lens.numpy(), case.sm_scale,
+                                  window=case.window if window is None else window,
+                                  cache_dtype=case.cache_dtype, mode=mode)
+
+
+def errors(got: np.ndarray, ref: np.ndarray):
+    d = np.abs(np.asarray(got, np.float64) - np.asarray(ref, np.float64))
+    return float(d.max()), float(d.mean())
+
+
+def assert_close(got, ref, max_abs=MAX_ABS, mean_abs=MEAN_ABS, what=""):
+    """Elementwise |got - ref| <= max_abs + 2^-9 |ref| and mean |got - ref| <=
+    mean_abs.  Returns (max-abs, mean-abs)."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    mx, mn = errors(got, ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    bound = max_abs + BF16_HALF_ULP_REL * np.abs(ref)
+    excess = np.abs(got - ref) - bound
+    worst = np.unravel_index(np.argmax(excess), excess.shape)
+    assert np.all(excess <= 0), (f"{what}: |err| {abs(got[worst] - ref[worst]):.3e} > bound {bound[worst]:.3e} "
+                                 f"at {worst} (ref {ref[worst]:.4f}); max-abs {mx:.3e}")
+    assert mn <= mean_abs, f"{what}: mean-abs {mn:.3e}"
+    return mx, mn

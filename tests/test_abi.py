@@ -1,0 +1,64 @@
+"""The C-ABI library loads and exports every symbol include/kvq.h declares
+(no compute calls: this runs without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+LIB = os.path.join(ROOT, "fp8_kv_cache_reshape_gb300", "libkvq.so")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        import __graft_entry__
+        __graft_entry__.build()
+    return ctypes.CDLL(LIB)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("kvq_reshape_and_cache", "kvq_quantize_query", "kvq_paged_decode_attention",
+              "kvq_decode_workspace_size", "kvq_decode_num_splits", "kvq_prefill_attention",
+              "kvq_last_error_string", "kvq_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_host_only_calls(lib):
+    lib.kvq_version.restype = ctypes.c_int
+    assert lib.kvq_version() >= 10000
+    lib.kvq_last_error_string.restype = ctypes.c_char_p
+    assert isinstance(lib.kvq_last_error_string(), bytes)
+
+
+def test_host_validation_without_gpu(lib):
+    """Argument checks run before any CUDA call and return their status."""
+    f = lib.kvq_reshape_and_cache
+    f.restype = ctypes.c_int
+    p = ctypes.c_void_p
+    f.argtypes = [p, p, p, p, p, p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int64, ctypes.c_int, p, p]
+    assert f(None, None, None, None, None, None, None, 4, 1, 96, 16, 8, 0, None, None) == 2  # head_dim 96
+    assert f(None, None, None, None, None, None, None, 4, 1, 128, 32, 8, 0, None, None) == 2  # page 32
+    assert f(None, None, None, None, None, None, None, 4, 1, 128, 16, 8, 0, None, None) == 1  # null pointers
+    assert f(None, None, None, None, None, None, None, 0, 1, 128, 16, 8, 0, None, None) == 0  # nothing to do
+    lib.kvq_last_error_string.restype = ctypes.c_char_p
+    q = lib.kvq_quantize_query
+    q.restype = ctypes.c_int
+    q.argtypes = [p, p, p, ctypes.c_int64, p]
+    assert q(None, None, None, -1, None) == 1
+    assert q(None, None, None, 0, None) == 0

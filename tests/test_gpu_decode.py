@@ -1,0 +1,239 @@
+"""GPU parity of kvq_paged_decode_attention (split-KV partial + LSE combine)
+against the float64 oracle, on caches the oracle builds.
+
+Tolerance (unit-variance inputs): max-abs 1e-2, mean-abs 1e-3 against both
+the mirrored and the pure oracle.  Properties with one exact answer are
+checked exactly: page-permutation invariance, empty sequences, device-side
+fault reporting."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention
+from oracle.kv_cache import FP8, BF16
+from tests.kvq_testlib import assert_close, errors, f32, oracle_cache, oracle_decode, to_device_cache
+
+pytestmark = pytest.mark.gpu
+
+
+def _k():
+    import fp8_kv_cache_reshape_gb300 as k
+    return k
+
+
+def gpu_decode(case, kd, vd, num_splits=0, window=None, block_table=None, seq_lens=None, status=False):
+    k = _k()
+    B, Hq, D = case.q.shape
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bt = (case.block_table if block_table is None else block_table).cuda()
+    sl = (case.seq_lens if seq_lens is None else seq_lens).cuda()
+    k.kvq_paged_decode_attention(case.q.cuda(), kd, vd, case.k_scale.cuda(), case.v_scale.cuda(), bt, sl,
+                                 out, num_blocks=case.num_blocks, sm_scale=case.sm_scale,
+                                 window=case.window if window is None else window,
+                                 cache_dtype=case.cache_dtype, num_splits=num_splits, dev_status=st)
+    torch.cuda.synchronize()
+    if status:
+        return f32(out), int(st.item())
+    assert int(st.item()) == 0, f"device status {int(st.item()):#x}"
+    return f32(out)
+
+
+def run_case(case, num_splits=0):
+    kc, vc = oracle_cache(case)
+    kd, vd = to_device_cache(kc, vc)
+    got = gpu_decode(case, kd, vd, num_splits=num_splits)
+    ref, _ = oracle_decode(case, kc, vc, mode="mirror")
+    pure, _ = oracle_decode(case, kc, vc, mode="pure")
+    m1 = assert_close(got, ref, what="vs mirrored oracle")
+    m2 = assert_close(got, pure, what="vs pure oracle")
+    return got, ref, m1, m2
+
+
+CASES = {
+    # name: (config kwargs, lengths, dtype, window)
+    "tiny_512": (dict(batch=1, q_heads=4, kv_heads=1, head_dim=64, context=512, calibrated=False), [512], FP8, -1),
+    "llama_small": (dict(batch=2, q_heads=32, kv_heads=8, head_dim=128, context=1000, outliers=4), [1000, 333], FP8, -1),
+    "ragged_g4": (dict(batch=5, q_heads=8, kv_heads=2, head_dim=128, context=2049), [1, 16, 17, 250, 2049], FP8, -1),
+    "gptoss_full": (dict(batch=2, q_heads=64, kv_heads=8, head_dim=64, context=1500), [700, 1500], FP8, -1),
+    "g1_d64": (dict(batch=2, q_heads=3, kv_heads=3, head_dim=64, context=300), [300, 31], FP8, -1),
+    "g2_d128": (dict(batch=1, q_heads=4, kv_heads=2, head_dim=128, context=77), [77], FP8, -1),
+    "window_fp8": (dict(batch=4, q_heads=64, kv_heads=8, head_dim=64, context=1000), [50, 128, 129, 1000], FP8, 128),
+    "window_bf16": (dict(batch=4, q_heads=64, kv_heads=8, head_dim=64, context=1000), [50, 128, 129, 1000], BF16, 128),
+    "window_bf16_d128": (dict(batch=2, q_heads=32, kv_heads=8, head_dim=128, context=700), [700, 99], BF16, 128),
+    "bf16_full_d128": (dict(batch=2, q_heads=32, kv_heads=8, head_dim=128, context=1300), [1300, 64], BF16, -1),
+    "bf16_full_d64": (dict(batch=1, q_heads=16, kv_heads=2, head_dim=64, context=900), [900], BF16, -1),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_decode_parity(name):
+    kw, lengths, dtype, window = CASES[name]
+    cfg = W.DecodeConfig(name, **kw)
+    case = W.decode_case(cfg, lengths=lengths, cache_dtype=dtype, window=window)
+    run_case(case)
+
+
+def test_tiny_config_exact_shape():
+    """The tiny decode configuration: 1 sequence, 4/1 heads, head_dim 64,
+    context 512, scales 1.0."""
+    case = W.decode_case(W.TINY)
+    got, ref, (mx, mn), _ = run_case(case)
+    assert mx < 5e-3
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 64])
+def test_split_count_invariance(splits):
+    cfg = W.DecodeConfig("s", batch=2, q_heads=32, kv_heads=8, head_dim=128, context=3000)
+    case = W.decode_case(cfg, lengths=[3000, 1234])
+    kc, vc = oracle_cache(case)
+    kd, vd = to_device_cache(kc, vc)
+    auto = gpu_decode(case, kd, vd, num_splits=0)
+    fixed = gpu_decode(case, kd, vd, num_splits=splits)
+    # identical up to FP32 summation order, then one bf16 rounding
+    assert np.max(np.abs(auto - fixed)) <= 2 ** -7 * np.max(np.abs(auto)) + 1e-6
+
+
+def test_page_permutation_invariance_bit_exact():
+    """The same logical tokens through an identity and a shuffled block table
+    give bit-identical outputs with the same split plan."""
+    cfg = W.DecodeConfig("perm", batch=1, q_heads=8, kv_heads=2, head_dim=128, context=800)
+    case = W.decode_case(cfg, lengths=[800])
+    kc, vc = oracle_cache(case)
+    kd, vd = to_device_cache(kc, vc)
+    a = gpu_decode(case, kd, vd, num_splits=5)
+    # move every page to a new block: new_block = perm(old_block)
+    nb = case.num_blocks
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(3))
+    kd2 = torch.empty_like(kd)
+    vd2 = torch.empty_like(vd)
+    kd2[perm.cuda()] = kd
+    vd2[perm.cuda()] = vd
+    bt2 = perm[case.block_table.long()].to(torch.int32)
+    b = gpu_decode(case, kd2, vd2, num_splits=5, block_table=bt2)
+    assert np.array_equal(a, b)
+
+
+def test_empty_and_single_token_sequences():
+    cfg = W.DecodeConfig("e", batch=3, q_heads=8, kv_heads=2, head_dim=64, context=40)
+    case = W.decode_case(cfg, lengths=[40, 1, 5])
+    kc, vc = oracle_cache(case)
+    kd, vd = to_device_cache(kc, vc)
+    sl = torch.tensor([40, 0, 1], dtype=torch.int32)
+    case.seq_lens = sl
+    got = gpu_decode(case, kd, vd)
+    ref, _ = oracle_decode(case, kc, vc)
+    assert np.all(got[1] == 0)
+    assert_close(got, ref)
+
+
+def test_nan_poisoned_tails_and_spare_pages_are_never_read():
+    """Every byte outside the cached tokens is an E4M3 NaN (0x7F); the
+    output stays finite and matches the oracle (which reads only valid
+    tokens)."""
+    cfg = W.DecodeConfig("p", batch=3, q_heads=16, kv_heads=4, head_dim=128, context=500)
+    case = W.decode_case(cfg, lengths=[500, 17, 250])
+    kc, vc = oracle_cache(case, sentinel=0x7F)
+    kd, vd = to_device_cache(kc, vc)
+    got = gpu_decode(case, kd, vd, num_splits=3)
+    ref, _ = oracle_decode(case, kc, vc)
+    assert_close(got, ref)
+
+
+def test_window_pages_only_poisoned_outside_window():
+    """Sliding-window layer: only the window's tokens exist in the cache;
+    everything else is NaN-poisoned (BF16 0xA5A5 / FP8 0x7F)."""
+    for dtype, sentinel in ((BF16, 0xFF), (FP8, 0x7F)):
+        cfg = W.DecodeConfig("w", batch=2, q_heads=64, kv_heads=8, head_dim=64, context=5000)
+        case = W.decode_case(cfg, lengths=[5000, 300], cache_dtype=dtype, window=128, only_window_tokens=True)
+        kc, vc = oracle_cache(case, sentinel=sentinel)
+        kd, vd = to_device_cache(kc, vc)
+        got = gpu_decode(case, kd, vd)
+        ref, _ = oracle_decode(case, kc, vc)
+        assert_close(got, ref, what=dtype)
+
+
+def test_device_faults_are_reported_not_trapped():
+    cfg = W.DecodeConfig("f", batch=2, q_heads=8, kv_heads=2, head_dim=128, context=100)
+    case = W.decode_case(cfg, lengths=[100, 60])
+    kc, vc = oracle_cache(case)
+    kd, vd = to_device_cache(kc, vc)
+    bt = case.block_table.clone()
+    bt[0, 2] = case.num_blocks + 7
+    _, st = gpu_decode(case, kd, vd, block_table=bt, status=True)
+    assert st & 0x2
+    sl = torch.tensor([100, 10 ** 6], dtype=torch.int32)
+    out, st = gpu_decode(case, kd, vd, seq_lens=sl, status=True)
+    assert st & 0x4 and np.all(np.isfinite(out))
+    # the context stays usable after reported faults
+    got = gpu_decode(case, kd, vd)
+    ref, _ = oracle_decode(case, kc, vc)
+    assert_close(got, ref)
+
+
+def test_host_validation_errors():
+    k = _k()
+    q = torch.zeros((1, 8, 96), dtype=torch.bfloat16, device="cuda")
+    kd = torch.zeros((4, 2, 16 * 96), dtype=torch.uint8, device="cuda")
+    bt = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
+    sl = torch.ones(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    sc = torch.ones(2, device="cuda")
+    with pytest.raises(k.KvqError) as e:
+        k.kvq_paged_decode_attention(q, kd, kd, sc, sc, bt, sl, out)
+    assert e.value.status == k.KVQ_ERR_UNSUPPORTED
+    q = torch.zeros((1, 8, 128), dtype=torch.bfloat16, device="cuda")
+    kd = torch.zeros((4, 3, 16 * 128), dtype=torch.uint8, device="cuda")
+    with pytest.raises(k.KvqError) as e:  # 8 % 3 != 0
+        k.kvq_paged_decode_attention(q, kd, kd, torch.ones(3, device="cuda"), torch.ones(3, device="cuda"), bt, sl,
+                                     torch.empty_like(q))
+    assert e.value.status == k.KVQ_ERR_INVALID_ARG
+    kd = torch.zeros((4, 2, 16 * 128), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(8, dtype=torch.uint8, device="cuda")
+    with pytest.raises(k.KvqError) as e:
+        k.kvq_paged_decode_attention(q, kd, kd, sc, sc, bt, sl, torch.empty_like(q), workspace=ws)
+    assert e.value.status == k.KVQ_ERR_INVALID_ARG
+
+
+def test_long_context_error_does_not_grow():
+    """Error against the oracle at 4K .. 131,072 tokens stays within the
+    tolerance and does not trend upward (V has a nonzero mean so the output
+    does not shrink with context; the planted 14-bit accumulator in the
+    oracle tests fails this at 64K)."""
+    errs = {}
+    for L in (4096, 16384, 65536, 131072):
+        cfg = W.DecodeConfig("lc", batch=1, q_heads=4, kv_heads=1, head_dim=128, context=L)
+        case = W.decode_case(cfg, lengths=[L])
+        case.v = (case.v.float() + 0.5).bfloat16()
+        case.v_scale = W.calibrate_amax(case.v)
+        kc, vc = oracle_cache(case)
+        kd, vd = to_device_cache(kc, vc)
+        got = gpu_decode(case, kd, vd)
+        ref, _ = oracle_decode(case, kc, vc)
+        errs[L] = assert_close(got, ref, what=f"L={L}")[0]
+    assert errs[131072] <= 2 * errs[4096] + 2 ** -9
+
+
+def test_full_size_llama_128k_layer():
+    """The Llama-3.1-8B-shaped decode layer: 32/8 heads, head_dim 128, one
+    sequence of 131,072 tokens, permuted pages, outliers, amax/448 scales."""
+    case = W.decode_case(W.LLAMA_128K, layer=0)
+    run_case(case)
+
+
+def test_full_size_concurrency_8():
+    """Batch 8, lengths uniform in [16384, 24576], shuffled pages."""
+    case = W.decode_case(W.CONC8)
+    run_case(case)
+
+
+def test_full_size_hybrid_stack_layers():
+    """One full-attention FP8 layer and one sliding-window-128 BF16 layer of
+    the gpt-oss-20b-shaped stack (batch 8, context 32,768)."""
+    full = W.decode_case(W.HYBRID, layer=1, window=-1)
+    run_case(full)
+    sw = W.decode_case(W.HYBRID, layer=0, window=128, cache_dtype=BF16, only_window_tokens=True)
+    run_case(sw)

@@ -135,3 +135,32 @@ def test_byte_formulas_against_pages():
     for r in cap["rows"]:
         per = kv_cache.kv_values_per_token(cap["layers"], cap["kv_heads"], cap["head_dim"]) * cap["tokens"] * r["kv_bits"] / 8
         assert int((cap["hbm_gb"] - cap["reserve_gb"] - r["weights_gb"]) * 1e9 // per) == r["seqs"]
+
+
+def test_device_format_is_a_bijection_with_documented_positions():
+    from oracle import layout
+    rng = np.random.default_rng(0)
+    for D, dt in ((128, np.uint8), (64, np.uint8), (64, np.uint16), (128, np.uint16)):
+        info = np.iinfo(dt)
+        kc = rng.integers(0, info.max + 1, (3, 2, 16, D), dtype=dt)
+        vc = rng.integers(0, info.max + 1, (3, 2, D, 16), dtype=dt)
+        kd, vd = layout.to_device_format(kc, vc)
+        k2, v2 = layout.from_device_format(kd, vd, D, np.dtype(dt).itemsize)
+        assert np.array_equal(k2, kc) and np.array_equal(v2, vc)
+        es = np.dtype(dt).itemsize
+        rb = D * es
+        # spot positions by the documented rule, element by element
+        kb = kc.view(np.uint8).reshape(3, 2, 16, rb)
+        for t in (0, 3, 9, 15):
+            for j in range(rb // 16):
+                pj = {128: j ^ (t % 8), 64: j ^ ((t // 2) % 4), 256: (j & 8) | ((j ^ t) & 7)}[rb]
+                assert np.array_equal(kd[1, 1, t * rb + pj * 16: t * rb + pj * 16 + 16], kb[1, 1, t, j * 16: j * 16 + 16])
+        for d in (0, 5, D - 1):
+            for t in range(16):
+                if es == 1:
+                    slot = [0, 1, 4, 5, 8, 9, 12, 13, 2, 3, 6, 7, 10, 11, 14, 15][t]
+                    assert vd[2, 0, d * 16 + slot] == vc[2, 0, d, t]
+                else:
+                    half = (t // 8) ^ ((d // 4) % 2)
+                    off = d * 32 + half * 16 + (t % 8) * 2
+                    assert vd[2, 0, off: off + 2].view(np.uint16)[0] == vc[2, 0, d, t]

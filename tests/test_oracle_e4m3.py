@@ -137,3 +137,12 @@ def test_quantize_divides_in_float32():
     q = e4m3.quantize(x, s)
     ref = _torch_reference((x / s).astype(np.float32))
     assert np.array_equal(q, ref)
+
+
+def test_bf16_table_equals_quantize():
+    bits = np.arange(65536, dtype=np.uint32)
+    x = (bits << 16).view(np.float32)
+    for s in (1.0, 0.0123, 3.2 / 448, 120 / 448, 1e-3):
+        t = e4m3.quantize_bf16_table(s)
+        fin = ~np.isnan(x)
+        assert np.array_equal(t[fin], e4m3.quantize(x[fin], np.float32(s)))

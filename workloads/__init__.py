@@ -23,6 +23,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import zlib
 from typing import Optional
 
 import torch
@@ -73,6 +74,12 @@ HYBRID = DecodeConfig("gpt_oss_20b_hybrid_decode_32k", batch=8, q_heads=64, kv_h
                       window=128)
 
 CONFIGS = {c.name: c for c in (TINY, LLAMA_128K, CONC8, PREFILL, HYBRID)}
+
+
+def config_seed(name: str) -> int:
+    """1..5 for the named configurations, a stable hash for others."""
+    names = list(CONFIGS)
+    return 1 + names.index(name) if name in names else 100 + zlib.crc32(name.encode()) % 100000
 
 
 def generator(seed: int, device="cpu") -> torch.Generator:
@@ -166,7 +173,7 @@ def decode_case(cfg: DecodeConfig, layer: int = 0, seed_base: int = 0, lengths=N
     Every position 0..L-1 of every sequence is a cached token (the last one
     being the step's own token).  With only_window_tokens, only the last
     `window` positions are produced (what a sliding-window layer reads)."""
-    gen = generator(seed_base + 1000 * (1 + list(CONFIGS).index(cfg.name)) + layer)
+    gen = generator(seed_base + 1000 * config_seed(cfg.name) + layer)
     lens = list(lengths) if lengths is not None else context_lengths(cfg, gen)
     win = cfg.window if window is None else window
     bt, num_blocks = paged_layout(lens, cfg.page, gen)
