@@ -5,22 +5,25 @@
 //  - "Performance benchmarks": decode cost is the per-token KV read (the ITL
 //    slope), so the kernel streams pages at HBM speed and reads FP8 directly;
 //  - "Problems we found" / "Kernel and vLLM improvements", two-level
-//    accumulation: the P.V contraction runs over the whole context; here every
-//    page's MMA result lands in fresh FP32 registers and is then added into a
-//    running FP32 sum, and page ranges are merged in FP32 by the combine;
+//    accumulation: the P.V contraction runs over the whole context; here each
+//    pair of pages' MMA result lands in fresh FP32 registers and is then added
+//    into a running FP32 sum, and page ranges are merged in FP32;
 //  - "Skip layers": sliding-window layers read only the window's pages and
 //    may keep a BF16 cache.
 //
 // Partial kernel (persistent): work item = (sequence, KV head, page range).
-// Warp NW is the producer: it reads block ids and streams each page (K page +
-// V page, one contiguous bulk copy each) into a ring of NST shared-memory
-// stages guarded by mbarriers.  Warps 0..NW-1 consume pages round-robin.  Per
-// page a consumer computes S^T = K Q^T (16 tokens x 8 query heads, M = tokens)
-// with mma.m16n8k16 (f16 inputs: E4M3 converts to f16 exactly), updates an
-// online softmax in base 2, transposes P in registers with movmatrix, and
-// computes O^T += V^T P^T (M = dims) into fresh FP32 fragments.  At the end of
-// an item the NW warp states are merged through shared memory and one
-// normalized partial output + log2-sum-exp is written per query head.
+// Warp NW is the producer: it reads block ids and streams pages (one
+// contiguous bulk copy per K page and per V page, two pages per stage) into a
+// ring of NST shared-memory stages guarded by mbarriers.  Warps 0..NW-1
+// consume stages round-robin.  Per page a consumer computes S^T = K Q^T
+// (16 tokens x 8 query heads, M = tokens) with mma.m16n8k16 (f16 inputs:
+// E4M3 converts to f16 exactly); one online-softmax update (base 2) covers
+// the stage's 32 tokens; P is transposed in registers with movmatrix, and
+// O^T = V^T P^T (M = dims) goes into fresh FP32 fragments that are then
+// added into the running output.  At the end of an item the NW warp states
+// are merged through shared memory and one normalized partial output plus
+// its log2-sum-exp is written per query head.  A combine kernel, launched as
+// a programmatic dependent of the partial kernel, merges the page ranges.
 #include <cfloat>
 #include <cmath>
 
@@ -32,6 +35,7 @@ namespace kvq {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int PPS = 2;  // pages per pipeline stage
 
 struct DecodeParams {
   const void* q;
@@ -48,7 +52,6 @@ struct DecodeParams {
   float sm_scale;
   int window;
   int num_splits;
-  int pages_per_split;
   int num_items;
   int* dev_status;
 };
@@ -58,10 +61,15 @@ struct Geo {
   static constexpr int ESZ = FP8 ? 1 : 2;
   static constexpr int ROWB = D * ESZ;        // bytes of one K row
   static constexpr int PAGE = kPage * ROWB;   // bytes of one K page (= one V page)
-  static constexpr int STAGE = 2 * PAGE;
+  static constexpr int STAGE = 2 * PPS * PAGE;
   static constexpr int MT = D / 16;           // 16-row tiles of O^T
   static constexpr int KS = D / 16;           // 16-dim k-steps of QK
 };
+
+template <int D, bool FP8>
+constexpr int stages_for() {  // about 80 KiB of pages in flight per CTA
+  return (81920 / Geo<D, FP8>::STAGE) > 32 ? 32 : (81920 / Geo<D, FP8>::STAGE);
+}
 
 template <int D, bool FP8, int NW, int NST>
 constexpr size_t decode_smem_bytes() {
@@ -92,12 +100,19 @@ KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
   r.lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
   const int first = r.lo / kPage;
   const int last = (L + kPage - 1) / kPage;
-  r.pg0 = first + r.split * p.pages_per_split;
-  int pg1 = r.pg0 + p.pages_per_split;
+  // this sequence's pages are cut into S near-equal ranges, so shorter
+  // sequences still spread over all splits
+  const int pps = (last - first + S - 1) / S;
+  r.pg0 = first + r.split * pps;
+  int pg1 = r.pg0 + pps;
   if (pg1 > last) pg1 = last;
   r.n = pg1 > r.pg0 ? pg1 - r.pg0 : 0;
   return r;
 }
+
+// Stage info word written by the producer: bit 0/1 = page 0/1 present,
+// bit 2/3 = page 0/1 had an invalid block id (fully masked).
+constexpr int kPresent0 = 1, kPresent1 = 2, kBad0 = 4, kBad1 = 8;
 
 template <int D, bool FP8, int NW, int NST>
 __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __grid_constant__ DecodeParams p) {
@@ -106,10 +121,10 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(NST) * G::STAGE);
   uint64_t* empty = full + NST;
-  int* stage_bad = reinterpret_cast<int*>(empty + NST);
-  float* mbuf = reinterpret_cast<float*>(stage_bad + NST);  // [NW][8]
-  float* lbuf = mbuf + NW * 8;                              // [NW][8]
-  float* obuf = lbuf + NW * 8;                              // [NW][8][D]
+  int* stage_info = reinterpret_cast<int*>(empty + NST);
+  float* mbuf = reinterpret_cast<float*>(stage_info + NST);  // [NW][8]
+  float* lbuf = mbuf + NW * 8;                               // [NW][8]
+  float* obuf = lbuf + NW * 8;                               // [NW][8][D]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(obuf + NW * 8 * D);
 
   const int warp = threadIdx.x >> 5;
@@ -123,14 +138,15 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
     fence_barrier_init();
   }
   __syncthreads();
+  grid_launch_dependents();
 
   if (warp == NW) {
     // ------------------------------------------------------------ producer --
     const uint64_t pol = policy_evict_first();
-    uint32_t it = 0;
+    uint32_t it = 0;  // stage counter
     bool aborted = false;
     for (int item = blockIdx.x; item < p.num_items && !aborted; item += gridDim.x) {
-      const ItemRange r = item_range(p, item, lane == 0 && threadIdx.x == NW * 32);
+      const ItemRange r = item_range(p, item, lane == 0);
       const int32_t* bt = p.block_table + static_cast<size_t>(r.b) * p.max_blocks + r.pg0;
       for (int base = 0; base < r.n && !aborted; base += 32) {
         const int cnt = min(32, r.n - base);
@@ -143,22 +159,31 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
             set_status(p.dev_status, KVQ_DEV_BAD_BLOCK);
           }
         }
-        for (int j = 0; j < cnt; ++j, ++it) {
-          const int bj = __shfl_sync(0xffffffffu, blk, j);
-          const int badj = __shfl_sync(0xffffffffu, bad, j);
+        for (int j = 0; j < cnt; j += PPS, ++it) {
+          const int b0 = __shfl_sync(0xffffffffu, blk, j);
+          const int d0 = __shfl_sync(0xffffffffu, bad, j);
+          const int b1 = __shfl_sync(0xffffffffu, blk, (j + 1) & 31);
+          const int d1 = __shfl_sync(0xffffffffu, bad, (j + 1) & 31);
+          const bool two = j + 1 < cnt;
           int ok = 1;
           if (lane == 0) {
             const int st = it % NST;
-            const uint32_t ph = (it / NST) & 1;
-            if (*abort_flag || !mbar_wait(&empty[st], ph ^ 1, abort_flag)) {
+            if (*abort_flag || !mbar_wait(&empty[st], ((it / NST) & 1) ^ 1, abort_flag)) {
               ok = 0;
             } else {
-              stage_bad[st] = badj;
-              mbar_arrive_expect_tx(&full[st], G::STAGE);
-              const size_t page = (static_cast<size_t>(bj) * p.Hkv + r.kvh) * G::PAGE;
-              uint8_t* sk = stages + size_t(st) * G::STAGE;
-              bulk_g2s(sk, p.k_cache + page, G::PAGE, &full[st], pol);
-              bulk_g2s(sk + G::PAGE, p.v_cache + page, G::PAGE, &full[st], pol);
+              int info = kPresent0 | (d0 ? kBad0 : 0);
+              if (two) info |= kPresent1 | (d1 ? kBad1 : 0);
+              stage_info[st] = info;
+              mbar_arrive_expect_tx(&full[st], (two ? 2u : 1u) * 2u * G::PAGE);
+              uint8_t* sk = stages + size_t(st) * G::STAGE;  // [K0][K1][V0][V1]
+              const size_t pg0 = (static_cast<size_t>(b0) * p.Hkv + r.kvh) * G::PAGE;
+              bulk_g2s(sk, p.k_cache + pg0, G::PAGE, &full[st], pol);
+              bulk_g2s(sk + 2 * G::PAGE, p.v_cache + pg0, G::PAGE, &full[st], pol);
+              if (two) {
+                const size_t pg1 = (static_cast<size_t>(b1) * p.Hkv + r.kvh) * G::PAGE;
+                bulk_g2s(sk + G::PAGE, p.k_cache + pg1, G::PAGE, &full[st], pol);
+                bulk_g2s(sk + 3 * G::PAGE, p.v_cache + pg1, G::PAGE, &full[st], pol);
+              }
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -183,15 +208,12 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
   const int r = lane >> 2;   // fragment row group
   const int c = lane & 3;    // fragment column pair
   const float NEG_INF = -INFINITY;
-  // per-lane ldmatrix offsets for the K page (constant per page)
-  int koff[G::KS / (FP8 ? 2 : 1)];
+  // per-lane ldmatrix byte offsets inside a K page and a V page
+  int koff[FP8 ? G::KS / 2 : G::KS];
   {
     const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-    for (int i = 0; i < G::KS / (FP8 ? 2 : 1); ++i) {
-      const int ch = FP8 ? (2 * i + (lane >> 4)) : (2 * i + (lane >> 4));
-      koff[i] = k_chunk_offset(tok, ch, G::ROWB);
-    }
+    for (int i = 0; i < (FP8 ? G::KS / 2 : G::KS); ++i) koff[i] = k_chunk_offset(tok, 2 * i + (lane >> 4), G::ROWB);
   }
   int voff[FP8 ? (G::MT / 2) : G::MT];
   if constexpr (FP8) {
@@ -201,10 +223,38 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
 #pragma unroll
     for (int i = 0; i < G::MT; ++i) {
       const int row = 16 * i + (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int half = lane >> 4;
-      voff[i] = row * 32 + 16 * (half ^ ((row >> 2) & 1));
+      voff[i] = row * 32 + 16 * ((lane >> 4) ^ ((row >> 2) & 1));
     }
   }
+
+  // S^T fragment of one page: s[0..1] = token r, heads 2c, 2c+1; s[2..3] = token r + 8
+  auto qk_page = [&](uint32_t kb, const uint32_t (&qf)[G::KS][2], float (&s)[4]) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};  // two independent chains
+    if constexpr (FP8) {
+#pragma unroll
+      for (int kk = 0; kk < G::KS; kk += 2) {
+        uint32_t x0, x1, x2, x3, l0, h0, l1, h1, l2, h2, l3, h3;
+        ldsm_x4(kb + koff[kk / 2], x0, x1, x2, x3);
+        e4m3x4_to_f16x2x2(x0, l0, h0);
+        e4m3x4_to_f16x2x2(x1, l1, h1);
+        e4m3x4_to_f16x2x2(x2, l2, h2);
+        e4m3x4_to_f16x2x2(x3, l3, h3);
+        mma_f16(a, l0, l1, h0, h1, qf[kk][0], qf[kk][1], a);
+        mma_f16(b, l2, l3, h2, h3, qf[kk + 1][0], qf[kk + 1][1], b);
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < G::KS; kk += 2) {
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+        ldsm_x4(kb + koff[kk], x0, x1, x2, x3);
+        ldsm_x4(kb + koff[kk + 1], y0, y1, y2, y3);
+        mma_bf16(a, x0, x1, x2, x3, qf[kk][0], qf[kk][1], a);
+        mma_bf16(b, y0, y1, y2, y3, qf[kk + 1][0], qf[kk + 1][1], b);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[e] = a[e] + b[e];
+  };
 
   uint32_t it0 = 0;
   for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
@@ -218,11 +268,11 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
 #pragma unroll
       for (int kk = 0; kk < G::KS; ++kk) {
         if constexpr (FP8) {
+          // dims 4c .. 4c+3 of the 16-dim chunk: (4c, 4c+1) pair with K's low
+          // bytes, (4c+2, 4c+3) with its high bytes
           const uint2 w = live ? __ldg(reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * c)) : make_uint2(0, 0);
-          const float x0 = __uint_as_float(w.x << 16), x1 = __uint_as_float(w.x & 0xFFFF0000u);
-          const float x2 = __uint_as_float(w.y << 16), x3 = __uint_as_float(w.y & 0xFFFF0000u);
-          qf[kk][0] = pack_f16x2(x0, x1);
-          qf[kk][1] = pack_f16x2(x2, x3);
+          qf[kk][0] = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+          qf[kk][1] = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
         } else {
           qf[kk][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * c)) : 0u;
           qf[kk][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * c)) : 0u;
@@ -239,9 +289,10 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
 #pragma unroll
     for (int i = 0; i < G::MT; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
 
+    const int nst_item = (rg.n + PPS - 1) / PPS;  // stages of this item
     int i = (warp - static_cast<int>(it0 % NW) + NW) % NW;
-    if (*abort_flag) i = rg.n;  // abandoned: skip the pages, keep the barriers in step
-    for (; i < rg.n; i += NW) {
+    if (*abort_flag) i = nst_item;  // abandoned: skip the pages, keep the barriers in step
+    for (; i < nst_item; i += NW) {
       const uint32_t itg = it0 + i;
       const int st = itg % NST;
       if (!mbar_wait(&full[st], (itg / NST) & 1, abort_flag)) {
@@ -251,55 +302,56 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
         }
         break;
       }
-      const uint8_t* sk = stages + size_t(st) * G::STAGE;
-      const uint32_t kb = smem_u32(sk);
-      const uint32_t vb = kb + G::PAGE;
-      const int tok0 = (rg.pg0 + i) * kPage;
-      const bool edge = stage_bad[st] || tok0 < rg.lo || tok0 + kPage > rg.hi;
+      const uint32_t kb = smem_u32(stages + size_t(st) * G::STAGE);
+      const uint32_t vb = kb + 2 * G::PAGE;
+      const int info = stage_info[st];
+      const bool two = (info & kPresent1) != 0;
+      const int tok0 = (rg.pg0 + i * PPS) * kPage;  // first token of page 0
+      const int tok_end = tok0 + (two ? 2 : 1) * kPage;
+      const bool edge = (info & (kBad0 | kBad1)) || tok0 < rg.lo || tok_end > rg.hi;
 
-      // ---- S^T = K Q^T : 16 tokens x 8 heads ----
-      float s[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (FP8) {
+      // ---- scores: page 0 -> s0, page 1 -> s1 ----
+      float s0[4], s1[4];
+      qk_page(kb, qf, s0);
+      if (two) qk_page(kb + G::PAGE, qf, s1);
+      else s1[0] = s1[1] = s1[2] = s1[3] = NEG_INF;
 #pragma unroll
-        for (int kk = 0; kk < G::KS; kk += 2) {
-          uint32_t x0, x1, x2, x3;
-          ldsm_x4(kb + koff[kk / 2], x0, x1, x2, x3);
-          mma_f16(s, e4m3x2_to_f16x2(x0 & 0xFFFF), e4m3x2_to_f16x2(x1 & 0xFFFF), e4m3x2_to_f16x2(x0 >> 16),
-                  e4m3x2_to_f16x2(x1 >> 16), qf[kk][0], qf[kk][1], s);
-          mma_f16(s, e4m3x2_to_f16x2(x2 & 0xFFFF), e4m3x2_to_f16x2(x3 & 0xFFFF), e4m3x2_to_f16x2(x2 >> 16),
-                  e4m3x2_to_f16x2(x3 >> 16), qf[kk + 1][0], qf[kk + 1][1], s);
-        }
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < G::KS; ++kk) {
-          uint32_t x0, x1, x2, x3;
-          ldsm_x4(kb + koff[kk], x0, x1, x2, x3);
-          mma_bf16(s, x0, x1, x2, x3, qf[kk][0], qf[kk][1], s);
-        }
+      for (int e = 0; e < 4; ++e) {
+        s0[e] *= coef;
+        s1[e] *= coef;
       }
-      // ---- scale, mask, online softmax (base 2) ----
-      bool ok0 = true, ok1 = true;  // tokens r and r + 8 of this page
-      uint32_t vmask_lo = 0xFFFFFFFFu, vmask_hi = 0xFFFFFFFFu;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) s[e] *= coef;
+      // masks (edge stages only): scores of dead tokens -> -inf, their V codes -> 0
+      uint32_t vm0_lo = 0xFFFFFFFFu, vm0_hi = 0xFFFFFFFFu, vm1_lo = 0xFFFFFFFFu, vm1_hi = 0xFFFFFFFFu;
       if (edge) {
-        const bool bad = stage_bad[st] != 0;
-        auto live = [&](int t) { return !bad && tok0 + t >= rg.lo && tok0 + t < rg.hi; };
-        ok0 = live(r);
-        ok1 = live(r + 8);
-        if (!ok0) s[0] = s[1] = NEG_INF;
-        if (!ok1) s[2] = s[3] = NEG_INF;
-        // V fragment lanes hold tokens 2c, 2c+1 (low) and 2c+8, 2c+9 (high)
-        const bool t0 = live(2 * c), t1 = live(2 * c + 1), t8 = live(2 * c + 8), t9 = live(2 * c + 9);
-        if constexpr (FP8) {
-          vmask_lo = (t0 ? 0x000000FFu : 0u) | (t1 ? 0x0000FF00u : 0u) | (t8 ? 0x00FF0000u : 0u) |
-                     (t9 ? 0xFF000000u : 0u);
-        } else {
-          vmask_lo = (t0 ? 0x0000FFFFu : 0u) | (t1 ? 0xFFFF0000u : 0u);
-          vmask_hi = (t8 ? 0x0000FFFFu : 0u) | (t9 ? 0xFFFF0000u : 0u);
-        }
+        auto live = [&](int pg, int t) {
+          const int tok = tok0 + pg * kPage + t;
+          const bool badp = pg == 0 ? (info & kBad0) : (info & kBad1);
+          const bool present = pg == 0 || two;
+          return present && !badp && tok >= rg.lo && tok < rg.hi;
+        };
+        if (!live(0, r)) s0[0] = s0[1] = NEG_INF;
+        if (!live(0, r + 8)) s0[2] = s0[3] = NEG_INF;
+        if (!live(1, r)) s1[0] = s1[1] = NEG_INF;
+        if (!live(1, r + 8)) s1[2] = s1[3] = NEG_INF;
+        // V fragments hold tokens 2c, 2c+1 (low pair) and 2c+8, 2c+9 (high pair)
+        auto vmask = [&](int pg, uint32_t& lo, uint32_t& hi) {
+          const bool t0 = live(pg, 2 * c), t1 = live(pg, 2 * c + 1), t8 = live(pg, 2 * c + 8),
+                     t9 = live(pg, 2 * c + 9);
+          if constexpr (FP8) {
+            lo = (t0 ? 0x000000FFu : 0u) | (t1 ? 0x0000FF00u : 0u) | (t8 ? 0x00FF0000u : 0u) |
+                 (t9 ? 0xFF000000u : 0u);
+            hi = lo;
+          } else {
+            lo = (t0 ? 0x0000FFFFu : 0u) | (t1 ? 0xFFFF0000u : 0u);
+            hi = (t8 ? 0x0000FFFFu : 0u) | (t9 ? 0xFFFF0000u : 0u);
+          }
+        };
+        vmask(0, vm0_lo, vm0_hi);
+        vmask(1, vm1_lo, vm1_hi);
       }
-      float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+      // ---- online softmax over the stage's 32 tokens (base 2) ----
+      float mx0 = fmaxf(fmaxf(s0[0], s0[2]), fmaxf(s1[0], s1[2]));
+      float mx1 = fmaxf(fmaxf(s0[1], s0[3]), fmaxf(s1[1], s1[3]));
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
@@ -311,65 +363,87 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
       const float al0 = ex2(m[0] - base0), al1 = ex2(m[1] - base1);  // rescale of the running sums
       m[0] = mn0;
       m[1] = mn1;
-      const float p0 = ex2(s[0] - base0), p1 = ex2(s[1] - base1), p2 = ex2(s[2] - base0), p3 = ex2(s[3] - base1);
-      l[0] = l[0] * al0 + (p0 + p2);
-      l[1] = l[1] * al1 + (p1 + p3);
+      const float p00 = ex2(s0[0] - base0), p01 = ex2(s0[1] - base1), p02 = ex2(s0[2] - base0),
+                  p03 = ex2(s0[3] - base1);
+      const float p10 = ex2(s1[0] - base0), p11 = ex2(s1[1] - base1), p12 = ex2(s1[2] - base0),
+                  p13 = ex2(s1[3] - base1);
+      l[0] = l[0] * al0 + ((p00 + p02) + (p10 + p12));
+      l[1] = l[1] * al1 + ((p01 + p03) + (p11 + p13));
 
-      // ---- O^T += V^T P^T : dims x 8 heads, fresh FP32 per page ----
+      // ---- O^T += V^T P^T over both pages, fresh FP32 per stage ----
       if constexpr (FP8) {
-        // P as the sum of two f16 terms (hi + lo): ~22 significant bits
-        const uint32_t h0 = pack_f16x2(p0, p1), h1 = pack_f16x2(p2, p3);
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
-        const uint32_t pb0 = movmatrix_t(h0);  // tokens 2c, 2c+1 of head r
-        const uint32_t pb1 = movmatrix_t(h1);  // tokens 2c+8, 2c+9 of head r
-        const uint32_t pl0 = movmatrix_t(pack_f16x2(p0 - f0.x, p1 - f0.y));
-        const uint32_t pl1 = movmatrix_t(pack_f16x2(p2 - f1.x, p3 - f1.y));
+        const uint32_t pa0 = movmatrix_t(pack_f16x2(p00, p01));  // page 0: tokens 2c, 2c+1 of head r
+        const uint32_t pa1 = movmatrix_t(pack_f16x2(p02, p03));  //         tokens 2c+8, 2c+9
+        const uint32_t pb0 = movmatrix_t(pack_f16x2(p10, p11));  // page 1
+        const uint32_t pb1 = movmatrix_t(pack_f16x2(p12, p13));
 #pragma unroll
         for (int mt = 0; mt < G::MT; mt += 2) {
-          uint32_t y0, y1, y2, y3;
-          ldsm_x4(vb + voff[mt / 2], y0, y1, y2, y3);
-          y0 &= vmask_lo;
-          y1 &= vmask_lo;
-          y2 &= vmask_lo;
-          y3 &= vmask_lo;
-          float t[4] = {0.f, 0.f, 0.f, 0.f};
-          const uint32_t va0 = e4m3x2_to_f16x2(y0 & 0xFFFF), va1 = e4m3x2_to_f16x2(y1 & 0xFFFF);
-          const uint32_t va2 = e4m3x2_to_f16x2(y0 >> 16), va3 = e4m3x2_to_f16x2(y1 >> 16);
-          mma_f16(t, va0, va1, va2, va3, pb0, pb1, t);
-          mma_f16(t, va0, va1, va2, va3, pl0, pl1, t);
+          float t[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            uint32_t y0, y1, y2, y3, a0, b0, a1, b1, a2, b2, a3, b3;
+            ldsm_x4(vb + voff[mt / 2], y0, y1, y2, y3);
+            e4m3x4_to_f16x2x2(y0 & vm0_lo, a0, b0);
+            e4m3x4_to_f16x2x2(y1 & vm0_lo, a1, b1);
+            e4m3x4_to_f16x2x2(y2 & vm0_lo, a2, b2);
+            e4m3x4_to_f16x2x2(y3 & vm0_lo, a3, b3);
+            mma_f16(t, a0, a1, b0, b1, pa0, pa1, t);
+            mma_f16(u, a2, a3, b2, b3, pa0, pa1, u);
+          }
+          if (two) {
+            uint32_t y0, y1, y2, y3, a0, b0, a1, b1, a2, b2, a3, b3;
+            ldsm_x4(vb + G::PAGE + voff[mt / 2], y0, y1, y2, y3);
+            e4m3x4_to_f16x2x2(y0 & vm1_lo, a0, b0);
+            e4m3x4_to_f16x2x2(y1 & vm1_lo, a1, b1);
+            e4m3x4_to_f16x2x2(y2 & vm1_lo, a2, b2);
+            e4m3x4_to_f16x2x2(y3 & vm1_lo, a3, b3);
+            mma_f16(t, a0, a1, b0, b1, pb0, pb1, t);
+            mma_f16(u, a2, a3, b2, b3, pb0, pb1, u);
+          }
           O[mt][0] = fmaf(O[mt][0], al0, t[0]);
           O[mt][1] = fmaf(O[mt][1], al1, t[1]);
           O[mt][2] = fmaf(O[mt][2], al0, t[2]);
           O[mt][3] = fmaf(O[mt][3], al1, t[3]);
-          float u[4] = {0.f, 0.f, 0.f, 0.f};
-          const uint32_t vb0 = e4m3x2_to_f16x2(y2 & 0xFFFF), vb1 = e4m3x2_to_f16x2(y3 & 0xFFFF);
-          const uint32_t vb2 = e4m3x2_to_f16x2(y2 >> 16), vb3 = e4m3x2_to_f16x2(y3 >> 16);
-          mma_f16(u, vb0, vb1, vb2, vb3, pb0, pb1, u);
-          mma_f16(u, vb0, vb1, vb2, vb3, pl0, pl1, u);
           O[mt + 1][0] = fmaf(O[mt + 1][0], al0, u[0]);
           O[mt + 1][1] = fmaf(O[mt + 1][1], al1, u[1]);
           O[mt + 1][2] = fmaf(O[mt + 1][2], al0, u[2]);
           O[mt + 1][3] = fmaf(O[mt + 1][3], al1, u[3]);
         }
       } else {
-        // P as the sum of two bf16 terms (hi + lo) keeps ~16 significant bits
-        const uint32_t h0 = pack_bf16x2(p0, p1), h1 = pack_bf16x2(p2, p3);
-        const float r0 = p0 - __uint_as_float(h0 << 16), r1 = p1 - __uint_as_float(h0 & 0xFFFF0000u);
-        const float r2 = p2 - __uint_as_float(h1 << 16), r3 = p3 - __uint_as_float(h1 & 0xFFFF0000u);
-        const uint32_t ph0 = movmatrix_t(h0), ph1 = movmatrix_t(h1);
-        const uint32_t pl0 = movmatrix_t(pack_bf16x2(r0, r1)), pl1 = movmatrix_t(pack_bf16x2(r2, r3));
+        // BF16 cache: P as the sum of two bf16 terms (hi + lo), ~16 significant bits
+        auto split = [&](float x, float y, uint32_t& hi, uint32_t& lo) {
+          hi = pack_bf16x2(x, y);
+          lo = pack_bf16x2(x - __uint_as_float(hi << 16), y - __uint_as_float(hi & 0xFFFF0000u));
+          hi = movmatrix_t(hi);
+          lo = movmatrix_t(lo);
+        };
+        uint32_t ha0, la0, ha1, la1, hb0, lb0, hb1, lb1;
+        split(p00, p01, ha0, la0);
+        split(p02, p03, ha1, la1);
+        split(p10, p11, hb0, lb0);
+        split(p12, p13, hb1, lb1);
 #pragma unroll
         for (int mt = 0; mt < G::MT; ++mt) {
-          uint32_t y0, y1, y2, y3;
-          ldsm_x4(vb + voff[mt], y0, y1, y2, y3);
-          y0 &= vmask_lo;
-          y1 &= vmask_lo;
-          y2 &= vmask_hi;
-          y3 &= vmask_hi;
           float t[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_bf16(t, y0, y1, y2, y3, ph0, ph1, t);
-          mma_bf16(t, y0, y1, y2, y3, pl0, pl1, t);
+          {
+            uint32_t y0, y1, y2, y3;
+            ldsm_x4(vb + voff[mt], y0, y1, y2, y3);
+            y0 &= vm0_lo;
+            y1 &= vm0_lo;
+            y2 &= vm0_hi;
+            y3 &= vm0_hi;
+            mma_bf16(t, y0, y1, y2, y3, ha0, ha1, t);
+            mma_bf16(t, y0, y1, y2, y3, la0, la1, t);
+          }
+          if (two) {
+            uint32_t y0, y1, y2, y3;
+            ldsm_x4(vb + G::PAGE + voff[mt], y0, y1, y2, y3);
+            y0 &= vm1_lo;
+            y1 &= vm1_lo;
+            y2 &= vm1_hi;
+            y3 &= vm1_hi;
+            mma_bf16(t, y0, y1, y2, y3, hb0, hb1, t);
+            mma_bf16(t, y0, y1, y2, y3, lb0, lb1, t);
+          }
           O[mt][0] = fmaf(O[mt][0], al0, t[0]);
           O[mt][1] = fmaf(O[mt][1], al1, t[1]);
           O[mt][2] = fmaf(O[mt][2], al0, t[2]);
@@ -379,7 +453,7 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
-    it0 += rg.n;
+    it0 += nst_item;
 
     // ---- merge the NW warp states of this item ----
 #pragma unroll
@@ -431,35 +505,64 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
 }
 
 // out[row][d] = sum_s 2^(lse_s - M) o_s[d] / sum_s 2^(lse_s - M), row = (b, hq).
+// One CTA of 256 threads per row: the weights are formed once in shared
+// memory, then D columns x (256 / D) split groups accumulate in parallel.
 template <int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restrict__ o_part,
-                                                           const float* __restrict__ lse_part,
-                                                           __nv_bfloat16* __restrict__ out, int S) {
+__global__ void __launch_bounds__(256) decode_combine_kernel(const float* __restrict__ o_part,
+                                                             const float* __restrict__ lse_part,
+                                                             __nv_bfloat16* __restrict__ out, int S) {
+  constexpr int GROUPS = 256 / D;
+  __shared__ float red[8];
+  __shared__ float part[GROUPS][D];
+  __shared__ float wsum_s;
+  extern __shared__ float w[];  // [S]
+  grid_dependency_wait();      // the partial kernel's writes are visible past this point
   const int row = blockIdx.x;
-  const int d = threadIdx.x;
+  const int tid = threadIdx.x;
   const float* lp = lse_part + static_cast<size_t>(row) * S;
-  float M = -INFINITY;
-  for (int s = 0; s < S; ++s) M = fmaxf(M, lp[s]);
-  float acc = 0.f, den = 0.f;
-  if (M != -INFINITY) {
-    const float* op = o_part + static_cast<size_t>(row) * S * D + d;
-    for (int s = 0; s < S; ++s) {
-      const float w = ex2(lp[s] - M);
-      den += w;
-      acc = fmaf(w, op[static_cast<size_t>(s) * D], acc);
-    }
-    acc = acc / den;
+  float mx = -INFINITY;
+  for (int s = tid; s < S; s += 256) mx = fmaxf(mx, lp[s]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) M = fmaxf(M, red[i]);
+  __syncthreads();
+  float ws = 0.f;
+  for (int s = tid; s < S; s += 256) {
+    const float e = (M == -INFINITY) ? 0.f : ex2(lp[s] - M);
+    w[s] = e;
+    ws += e;
   }
-  out[static_cast<size_t>(row) * D + d] = __float2bfloat16_rn(acc);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+  if ((tid & 31) == 0) red[tid >> 5] = ws;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.f;
+    for (int i = 0; i < 8; ++i) t += red[i];
+    wsum_s = t;
+  }
+  const int d = tid % D, gi = tid / D;
+  const float* op = o_part + static_cast<size_t>(row) * S * D + d;
+  float acc = 0.f;
+#pragma unroll 4
+  for (int s = gi; s < S; s += GROUPS) acc = fmaf(w[s], op[static_cast<size_t>(s) * D], acc);
+  part[gi][d] = acc;
+  __syncthreads();
+  if (gi == 0) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < GROUPS; ++k) t += part[k][d];
+    const float den = wsum_s;
+    out[static_cast<size_t>(row) * D + d] = __float2bfloat16_rn(den > 0.f ? t / den : 0.f);
+  }
 }
 
 constexpr int kNW = 4;     // consumer warps per CTA
 constexpr int kCtasPerSm = 2;
-
-template <int D, bool FP8>
-constexpr int stages_for() {  // about 64 KiB of pages in flight per CTA
-  return (65536 / Geo<D, FP8>::STAGE) > 32 ? 32 : (65536 / Geo<D, FP8>::STAGE);
-}
 
 int decode_pages(int P, int max_blocks, int window) {
   int pages = max_blocks;
@@ -476,10 +579,10 @@ void split_plan(int B, int Hkv, int P, int max_blocks, int window, int num_split
   if (num_splits > 0) {
     S = num_splits;
   } else {
-    const long target = 4L * kCtasPerSm * sm_count();
+    const long target = 2L * kCtasPerSm * sm_count();  // about two items per CTA
     const long pairs = static_cast<long>(B) * Hkv;
     S = static_cast<int>((target + pairs - 1) / pairs);
-    const int max_s = (pages + 15) / 16;
+    const int max_s = (pages + 31) / 32;  // at least 32 pages per split
     if (S > max_s) S = max_s;
   }
   if (S > pages) S = pages;
@@ -508,8 +611,20 @@ kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream
   kern<<<grid, (kNW + 1) * 32, smem, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e, "decode partial launch");
-  decode_combine_kernel<D><<<p.B * p.Hq, D, 0, s>>>(p.o_part, p.lse_part, out, p.num_splits);
-  return cuda_status(cudaGetLastError(), "decode combine launch");
+  // combine: programmatic dependent launch (its launch overlaps the partial's tail)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.B * p.Hq);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = static_cast<size_t>(p.num_splits) * sizeof(float);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, static_cast<const float*>(p.o_part),
+                         static_cast<const float*>(p.lse_part), out, p.num_splits);
+  return cuda_status(e, "decode combine launch");
 }
 
 }  // namespace
@@ -566,7 +681,7 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
   if (workspace_bytes < need)
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: workspace %zu bytes < %zu needed", workspace_bytes, need);
   const long items = static_cast<long>(B) * Hkv * S;
-  if (items > 0x7FFFFFFFL || static_cast<long>(B) * Hq > 0x7FFFFFFFL)
+  if (items > 0x7FFFFFFFL || static_cast<long>(B) * Hq > 0x7FFFFFFFL || S > 12000)
     return fail(KVQ_ERR_UNSUPPORTED, "paged_decode: problem too large");
 
   DecodeParams prm;
@@ -589,7 +704,6 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
   prm.sm_scale = sm_scale;
   prm.window = window;
   prm.num_splits = S;
-  prm.pages_per_split = pps;
   prm.num_items = static_cast<int>(items);
   prm.dev_status = dev_status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -112,6 +112,12 @@ KVQ_DEVINL uint64_t policy_evict_first() {
   return p;
 }
 
+// Programmatic dependent launch: wait until the preceding grid's memory is visible.
+KVQ_DEVINL void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the programmatic dependent grid to be scheduled (it still waits for
+// this grid's completion in grid_dependency_wait()).
+KVQ_DEVINL void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 KVQ_DEVINL void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -149,6 +155,14 @@ KVQ_DEVINL void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, u
 KVQ_DEVINL uint32_t e4m3x2_to_f16x2(uint16_t two) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+// Four E4M3 codes in one register -> two f16x2 registers (bytes 0,1 -> lo;
+// bytes 2,3 -> hi); exact.
+KVQ_DEVINL void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
 }
 KVQ_DEVINL uint32_t pack_f16x2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);

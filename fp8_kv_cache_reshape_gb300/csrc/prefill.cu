@@ -1,6 +1,483 @@
-// kvq_prefill_attention: chunked causal prefill on FP8 tensor cores.
+// kvq_prefill_attention: chunked causal prefill over the paged FP8 cache on
+// FP8 tensor cores (tcgen05.mma kind::f8f6f4, accumulators in tensor memory).
+//
+// Method: "The state of FP8 KV-cache and attention quantization in vLLM"
+//  - "Kernel and vLLM improvements": QK^T and score.V both run in FP8 (e4m3);
+//    two-level accumulation: partial P.V sums are promoted into real FP32;
+//  - "Large head dimension limitations": the cost of the second level in
+//    prefill (register pressure / extra passes);
+// "FP8 and KV cache", "How to enable it in the engine": the query is
+// quantized to FP8 too (kvq_quantize_query).
+//
+// One CTA = 128 query rows of one sequence x one query head.  Keys come in
+// tiles of 128 (8 pages).  Warp roles:
+//  warp 0     producer: block ids -> one bulk copy per K page and V page into
+//             a 3-stage ring (pages of unknown / out-of-range blocks are zero
+//             filled and masked);
+//  warp 1     TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
+//             score buffers, then O_j = P_j V_j into one of two fresh TMEM
+//             accumulators (first level);
+//  warps 2-5  one query row per thread: online softmax in base 2 over S_j,
+//             P_j = e4m3(2^(s - m) * 256) into swizzled shared memory, and
+//             O_run = O_run * alpha + O_j in FP32 registers (second level).
+// Shared-memory operands use the UMMA canonical K-major layouts: Q, K and P
+// with the 128-byte swizzle (K pages are stored pre-swizzled by the cache
+// format), V pages ([d][16 token slots]) without swizzle.
+#include <cfloat>
+#include <cmath>
+
 #include "kvq_device.cuh"
 #include "kvq_host.h"
+
+namespace kvq {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int TQ = 128;           // query rows per CTA
+constexpr int TK = 128;           // keys per tile (8 pages)
+constexpr int HD = 128;           // head dim
+constexpr int NKV = 3;            // K/V stages
+constexpr int PAGE_B = kPage * HD;             // 2048 bytes per page (K or V)
+constexpr int TILE_B = TK * HD;                // 16 KB per K tile (= V tile)
+constexpr int OFF_Q = 0;
+constexpr int OFF_KV = OFF_Q + TQ * HD;        // 16 KB
+constexpr int STAGE_B = 2 * TILE_B;            // K tile + V tile
+constexpr int OFF_P = OFF_KV + NKV * STAGE_B;  // 2 P buffers of 16 KB
+constexpr int OFF_BAR = OFF_P + 2 * TQ * TK;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers, + alignment slack
+constexpr int NTHREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;            // S0 | S1 | O0 | O1, 128 columns each
+
+struct PrefillParams {
+  const uint8_t* q8;
+  const float* q_scale;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* block_table;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seq_lens;
+  __nv_bfloat16* out;
+  int B, Hq, Hkv, g, max_blocks;
+  int64_t num_blocks;
+  float sm_scale;
+  int causal;
+  int* dev_status;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t kv_full[NKV];
+  uint64_t kv_empty[NKV];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t o_free[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  uint32_t stage_bad[NKV];  // bit i: page i of the stage was zero-filled (bad block id)
+};
+
+// ------------------------------------------------------------ tcgen05 PTX ---
+KVQ_DEVINL uint64_t desc_sw128(uint32_t saddr) {  // K-major, 128B swizzle, 8-row groups 1024 B apart
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>(1) << 16;                 // leading offset (unused for swizzled K-major)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;         // stride offset
+  d |= static_cast<uint64_t>(1) << 46;                 // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                 // SWIZZLE_128B
+  return d;
+}
+KVQ_DEVINL uint64_t desc_interleave(uint32_t saddr, uint32_t lbo, uint32_t sbo) {  // K-major, no swizzle
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFF);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+// kind::f8f6f4 instruction descriptor: D f32, A/B e4m3, both K-major, M x N.
+constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+KVQ_DEVINL void umma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+KVQ_DEVINL void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+KVQ_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+KVQ_DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+KVQ_DEVINL void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct Job {
+  int b, h, kvh, q0, nq, L, first_q;  // first_q: absolute position of the sequence's first new token
+  int nkv;                             // key tiles this CTA visits
+  bool valid;
+};
+
+KVQ_DEVINL Job make_job(const PrefillParams& p) {
+  Job j;
+  j.b = blockIdx.z;
+  j.h = blockIdx.y;
+  j.kvh = j.h / p.g;
+  j.q0 = blockIdx.x * TQ;
+  const int c0 = p.cu_seqlens_q[j.b];
+  const int c1 = p.cu_seqlens_q[j.b + 1];
+  j.nq = c1 - c0;
+  int L = p.seq_lens[j.b];
+  const int cap = p.max_blocks * kPage;
+  j.valid = j.q0 < j.nq;
+  if (L < 0 || L > cap) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) set_status(p.dev_status, KVQ_DEV_BAD_SEQLEN);
+    L = L < 0 ? 0 : cap;
+  }
+  if (j.nq > L) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) set_status(p.dev_status, KVQ_DEV_BAD_QROWS);
+    j.valid = false;
+  }
+  j.L = L;
+  j.first_q = L - j.nq;
+  const int last_row = min(j.q0 + TQ, j.nq) - 1;
+  const int kend = p.causal ? (j.first_q + last_row + 1) : L;  // keys [0, kend)
+  j.nkv = j.valid ? (kend + TK - 1) / TK : 0;
+  return j;
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(smem);
+  Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  volatile int* abort_flag = &bars->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const Job job = make_job(p);
+  if (!job.valid) return;  // uniform across the CTA
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, TQ);
+    for (int i = 0; i < NKV; ++i) {
+      mbar_init(&bars->kv_full[i], 1);
+      mbar_init(&bars->kv_empty[i], 1);
+      bars->stage_bad[i] = 0;
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], TQ);
+      mbar_init(&bars->o_full[i], 1);
+      mbar_init(&bars->o_free[i], TQ);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&bars->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int nkv = job.nkv;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    const int n_pages = (job.L + kPage - 1) / kPage;
+    const int32_t* bt = p.block_table + static_cast<size_t>(job.b) * p.max_blocks;
+    int j = 0;
+    for (; j < nkv; ++j) {
+      const int st = j % NKV;
+      int ok = 1;
+      if (lane == 0) ok = (!*abort_flag && mbar_wait(&bars->kv_empty[st], ((j / NKV) & 1) ^ 1, abort_flag)) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      uint8_t* ks = smem + OFF_KV + st * STAGE_B;
+      uint8_t* vs = ks + TILE_B;
+      // lanes 0..7: one page each
+      int blk = -1;
+      uint32_t bad = 0;
+      const int page = j * (TK / kPage) + lane;
+      if (lane < TK / kPage && page < n_pages) {
+        blk = __ldg(bt + page);
+        if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
+          set_status(p.dev_status, KVQ_DEV_BAD_BLOCK);
+          blk = -1;
+          bad = 1;
+        }
+      }
+      const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad != 0);
+      const uint32_t load_mask = __ballot_sync(0xffffffffu, blk >= 0) & 0xFFu;
+      // zero-fill pages that are not loaded (past the end, or bad block ids)
+      for (int pg = 0; pg < TK / kPage; ++pg) {
+        if (load_mask & (1u << pg)) continue;
+        uint4* kz = reinterpret_cast<uint4*>(ks + pg * PAGE_B);
+        uint4* vz = reinterpret_cast<uint4*>(vs + pg * PAGE_B);
+        for (int i = lane; i < PAGE_B / 16; i += 32) {
+          kz[i] = make_uint4(0, 0, 0, 0);
+          vz[i] = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        bars->stage_bad[st] = bad_mask & 0xFFu;
+        mbar_arrive_expect_tx(&bars->kv_full[st], 2u * PAGE_B * __popc(load_mask));
+      }
+      __syncwarp();
+      if (lane < TK / kPage && blk >= 0) {
+        const size_t off = (static_cast<size_t>(blk) * p.Hkv + job.kvh) * PAGE_B;
+        bulk_g2s(ks + lane * PAGE_B, p.k_cache + off, PAGE_B, &bars->kv_full[st], policy_evict_first());
+        bulk_g2s(vs + lane * PAGE_B, p.v_cache + off, PAGE_B, &bars->kv_full[st], policy_evict_first());
+      }
+    }
+    if (j < nkv && lane == 0) {  // abandoned: let issued copies land
+      set_status(p.dev_status, KVQ_DEV_TIMEOUT);
+      *abort_flag = 1;
+      for (int k = j - NKV > 0 ? j - NKV : 0; k < j; ++k) mbar_wait(&bars->kv_full[k % NKV], (k / NKV) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer --
+    constexpr uint32_t IDESC = idesc_e4m3(TQ, TK);
+    const uint32_t q_s = sbase + OFF_Q;
+    bool ok = true;
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      if (ok && !mbar_wait(bar, parity, abort_flag)) {
+        ok = false;
+        if (lane == 0) {
+          set_status(p.dev_status, KVQ_DEV_TIMEOUT);
+          *abort_flag = 1;
+        }
+      }
+      return ok;
+    };
+    auto issue_s = [&](int j) {  // S[j%2] = Q K_j^T
+      const int st = j % NKV;
+      if (!wait(&bars->kv_full[st], (j / NKV) & 1)) return;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t k_s = sbase + OFF_KV + st * STAGE_B;
+        const uint32_t d = tmem + (j & 1) * TK;
+#pragma unroll
+        for (int kk = 0; kk < HD / 32; ++kk)
+          umma_f8(d, desc_sw128(q_s + kk * 32), desc_sw128(k_s + kk * 32), IDESC, kk > 0 ? 1u : 0u);
+        umma_commit(&bars->s_full[j & 1]);
+      }
+      __syncwarp();
+    };
+    if (wait(&bars->q_full, 0) && nkv > 0) issue_s(0);
+    for (int j = 0; j < nkv && ok; ++j) {
+      if (j + 1 < nkv) issue_s(j + 1);
+      if (!ok) break;
+      if (!wait(&bars->p_full[j & 1], (j >> 1) & 1)) break;
+      if (j >= 2 && !wait(&bars->o_free[j & 1], ((j >> 1) & 1) ^ 1)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const int st = j % NKV;
+        const uint32_t p_s = sbase + OFF_P + (j & 1) * (TQ * TK);
+        const uint32_t v_s = sbase + OFF_KV + st * STAGE_B + TILE_B;
+        const uint32_t d = tmem + 2 * TK + (j & 1) * HD;
+#pragma unroll
+        for (int kk = 0; kk < TK / 32; ++kk)  // 32 keys = 2 V pages per MMA
+          umma_f8(d, desc_sw128(p_s + kk * 32), desc_interleave(v_s + kk * 2 * PAGE_B, PAGE_B, 128), IDESC,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(&bars->o_full[j & 1]);
+        umma_commit(&bars->kv_empty[st]);
+      }
+      __syncwarp();
+    }
+    // every MMA this thread issued has completed before TMEM is released
+    if (lane == 0) umma_commit(&bars->mma_done);
+    __syncwarp();
+    mbar_wait(&bars->mma_done, 0);
+  } else {
+    // ------------------------------------------------------ softmax warps --
+    const int r = threadIdx.x - 64;        // query row of this thread, 0..127
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+    const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+    const int row = quarter * 32 + lane;   // TMEM lane == query row
+    (void)r;
+    const bool live_row = job.q0 + row < job.nq;
+    const int qpos = job.first_q + job.q0 + row;  // absolute position of this query
+    const int kend = (p.causal && qpos + 1 < job.L) ? qpos + 1 : job.L;  // this row attends to keys [0, kend)
+    const size_t out_row = (static_cast<size_t>(p.cu_seqlens_q[job.b]) + job.q0 + row) * p.Hq + job.h;
+
+    // Q row -> shared memory, 128-byte swizzled
+    {
+      uint8_t* qs = smem + OFF_Q + row * HD;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q8 + out_row * HD);
+#pragma unroll
+      for (int c = 0; c < HD / 16; ++c) {
+        const uint4 v = live_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qs + ((c ^ (row & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->q_full);
+    }
+    const float coef = __fmul_rn(__fmul_rn(__fmul_rn(*p.q_scale, p.k_scale[job.kvh]), p.sm_scale), kLog2e);
+    const int tail = job.L % kPage;          // valid tokens in the last page (0 = full)
+    const int last_page = (job.L - 1) / kPage;
+
+    float O[HD];
+#pragma unroll
+    for (int i = 0; i < HD; ++i) O[i] = 0.f;
+    float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+    bool ok = true;
+
+    auto accumulate = [&](int jt, float alpha) {  // O = O * alpha + O_tile[jt]
+      if (!ok) return;
+      if (!mbar_wait(&bars->o_full[jt & 1], (jt >> 1) & 1, abort_flag)) {
+        ok = false;
+        set_status(p.dev_status, KVQ_DEV_TIMEOUT);
+        *abort_flag = 1;
+        return;
+      }
+      tc_fence_after();
+      const uint32_t base = tmem + t_lane + 2 * TK + (jt & 1) * HD;
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(base + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) O[c * 32 + i] = fmaf(O[c * 32 + i], alpha, __uint_as_float(v[i]));
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[jt & 1]);
+    };
+
+    for (int j = 0; j < nkv && ok; ++j) {
+      if (!mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort_flag)) {
+        ok = false;
+        set_status(p.dev_status, KVQ_DEV_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int st = j % NKV;
+      const int key0 = j * TK;
+      // the stage's page flags and, for the last page, zeroing of its unused V slots
+      mbar_wait(&bars->kv_full[st], (j / NKV) & 1, abort_flag);
+      const uint32_t bad = bars->stage_bad[st];
+      if (tail != 0 && last_page / (TK / kPage) == j) {
+        uint8_t* vrow = smem + OFF_KV + st * STAGE_B + TILE_B + (last_page % (TK / kPage)) * PAGE_B + row * kPage;
+        for (int t = tail; t < kPage; ++t) vrow[fp8_v_slot(t)] = 0;
+      }
+      const bool need_mask = (key0 + TK > kend) || bad != 0;
+      const uint32_t sbuf = tmem + t_lane + (j & 1) * TK;
+      auto masked = [&](float s, int k) {
+        const int key = key0 + k;
+        return (key >= kend || ((bad >> (k / kPage)) & 1)) ? -INFINITY : s;
+      };
+      // pass 1: row maximum of this tile
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < TK / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(sbuf + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float s = __uint_as_float(v[i]) * coef;
+          if (need_mask) s = masked(s, c * 32 + i);
+          mx = fmaxf(mx, s);
+        }
+      }
+      const float m_new = fmaxf(m, mx);
+      const float base = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2(m - base);
+      // pass 2: probabilities, FP8 P tile, row sum
+      float rs = 0.f;
+      uint8_t* prow = smem + OFF_P + (j & 1) * (TQ * TK) + row * TK;
+#pragma unroll
+      for (int c = 0; c < TK / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(sbuf + c * 32, v);
+        float pr[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float s = __uint_as_float(v[i]) * coef;
+          if (need_mask) s = masked(s, c * 32 + i);
+          pr[i] = ex2(s - base);
+          rs += pr[i];
+        }
+        // two pages of 16 keys; word w of a page holds keys 2w, 2w+1, 2w+8, 2w+9
+#pragma unroll
+        for (int hpg = 0; hpg < 2; ++hpg) {
+          const float* q = pr + 16 * hpg;
+          uint32_t w[4];
+#pragma unroll
+          for (int ww = 0; ww < 4; ++ww) {
+            const __nv_fp8x2_storage_t lo =
+                __nv_cvt_float2_to_fp8x2(make_float2(q[2 * ww] * 256.f, q[2 * ww + 1] * 256.f), __NV_SATFINITE,
+                                         __NV_E4M3);
+            const __nv_fp8x2_storage_t hi =
+                __nv_cvt_float2_to_fp8x2(make_float2(q[2 * ww + 8] * 256.f, q[2 * ww + 9] * 256.f),
+                                         __NV_SATFINITE, __NV_E4M3);
+            w[ww] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+          }
+          const int chunk = 2 * c + hpg;  // page index within the tile
+          *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      l = l * alpha + rs;
+      m = m_new;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[j & 1]);
+      if (j >= 1) accumulate(j - 1, alpha_prev);
+      alpha_prev = alpha;
+    }
+    if (ok && nkv >= 1) accumulate(nkv - 1, alpha_prev);
+
+    // epilogue: out = O * v_scale / (256 * l)
+    if (live_row && ok) {
+      const float f = (l > 0.f) ? p.v_scale[job.kvh] / (256.f * l) : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD);
+#pragma unroll
+      for (int c = 0; c < HD / 8; ++c) {
+        uint4 w;
+        w.x = pack_bf16x2(O[8 * c + 0] * f, O[8 * c + 1] * f);
+        w.y = pack_bf16x2(O[8 * c + 2] * f, O[8 * c + 3] * f);
+        w.z = pack_bf16x2(O[8 * c + 4] * f, O[8 * c + 5] * f);
+        w.w = pack_bf16x2(O[8 * c + 6] * f, O[8 * c + 7] * f);
+        dst[c] = w;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+}  // namespace
+
+}  // namespace kvq
 
 using namespace kvq;
 
@@ -11,5 +488,48 @@ extern "C" kvq_status_t kvq_prefill_attention(const uint8_t* q8, const float* q_
                                               int P, int max_blocks, int64_t num_blocks, int max_q_tokens,
                                               float sm_scale, int causal, int* dev_status, kvq_stream_t stream) {
   clear_error();
-  return fail(KVQ_ERR_UNSUPPORTED, "prefill_attention: not built yet");
+  if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || max_q_tokens < 0)
+    return fail(KVQ_ERR_INVALID_ARG, "prefill: bad sizes");
+  if (Hq % Hkv != 0) return fail(KVQ_ERR_INVALID_ARG, "prefill: Hq %% Hkv != 0");
+  if (!(sm_scale > 0.f) || !(sm_scale < FLT_MAX)) return fail(KVQ_ERR_INVALID_ARG, "prefill: bad sm_scale");
+  if (P != kPage) return fail(KVQ_ERR_UNSUPPORTED, "prefill: page size %d (only 16)", P);
+  if (D != HD) return fail(KVQ_ERR_UNSUPPORTED, "prefill: head_dim %d (only 128)", D);
+  if (max_q_tokens == 0) return KVQ_OK;
+  if (!q8 || !q_scale || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !cu_seqlens_q ||
+      !seq_lens || !out)
+    return fail(KVQ_ERR_INVALID_ARG, "prefill: null pointer");
+  if (!aligned(q8, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return fail(KVQ_ERR_INVALID_ARG, "prefill: pointers must be 16-byte aligned");
+  if (B > 65535 || Hq > 65535) return fail(KVQ_ERR_UNSUPPORTED, "prefill: grid too large");
+  PrefillParams prm;
+  prm.q8 = q8;
+  prm.q_scale = q_scale;
+  prm.k_cache = static_cast<const uint8_t*>(k_cache);
+  prm.v_cache = static_cast<const uint8_t*>(v_cache);
+  prm.k_scale = k_scale;
+  prm.v_scale = v_scale;
+  prm.block_table = block_table;
+  prm.cu_seqlens_q = cu_seqlens_q;
+  prm.seq_lens = seq_lens;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.g = Hq / Hkv;
+  prm.max_blocks = max_blocks;
+  prm.num_blocks = num_blocks;
+  prm.sm_scale = sm_scale;
+  prm.causal = causal ? 1 : 0;
+  prm.dev_status = dev_status;
+  static int configured_mask = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!(configured_mask & (1 << (dev & 31)))) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_status(e, "prefill: set shared memory size");
+    configured_mask |= 1 << (dev & 31);
+  }
+  dim3 grid((max_q_tokens + TQ - 1) / TQ, Hq, B);
+  prefill_kernel<<<grid, NTHREADS, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(prm);
+  return cuda_status(cudaGetLastError(), "prefill launch");
 }

@@ -30,10 +30,14 @@ Readings where the pages are silent
   cached tokens; query i sits at position L - nq + i and (causal) attends to
   keys 0..L - nq + i.
 * The softmax scale is an input (1/sqrt(D) by default in the callers).
-* Prefill's probabilities feed an FP8 MMA: P8 = encode(fl32(p * 256)) with p
-  taken relative to the row's final maximum, and the row sum l adds the
-  unquantized p.  This mirror is approximate (a kernel with a running
-  maximum picks codes from its own maximum): parity unpinned for P8 itself.
+* Prefill's probabilities feed an FP8 MMA: P8 = encode(fl32(p * 256)).  The
+  online softmax the vLLM page names for its FP8 attention kernel rescales
+  as it walks the keys, so p is taken relative to the running row maximum:
+  keys are visited in tiles of 128 in key order, the maximum is updated per
+  tile, and earlier tiles' sums are rescaled by 2^(m_old - m_new).  The row
+  sum l adds the unquantized p.  The P8 codes themselves are parity
+  unpinned (the kernel's float32 exponentials can land on the other side of
+  a rounding midpoint); the result is pinned through the unquantized mode.
 
 Mirrored quantization points
 ----------------------------
@@ -44,7 +48,7 @@ Mirrored quantization points
   * log2(e)); o = s_v * sum_j 2^(s2_j - m) v8_j / sum_j 2^(s2_j - m).
 * prefill: s2 = (sum_d q8[d] * k8[d]) * c with
   c = fl32(fl32(fl32(q_scale * k_scale) * sm_scale) * log2(e)), and P8 as
-  above.
+  above (running maximum over 128-key tiles).
 ``mode="pure"`` uses the exact dequantized values and natural exponentials.
 """
 from __future__ import annotations
@@ -158,13 +162,14 @@ def lse_merge(outs, lses):
 
 def prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
             cu_seqlens_q, seq_lens, sm_scale, causal=True, mode="mirror",
-            rows=None):
+            rows=None, tile=128):
     """Chunked prefill over the FP8 cache (the new tokens are already cached).
 
     q8: uint8 [Tq][Hq][D] E4M3 codes.  cu_seqlens_q: int [B+1].  seq_lens:
     int [B], each counting the cached tokens including the new ones.
     rows: optional iterable of (token_index, head) pairs to evaluate; other
     rows of the result stay NaN (sampled checks at large sizes).
+    tile: keys per online-softmax step of the mirrored P8 quantization.
     Returns out float64 [Tq][Hq][D].
     """
     q8 = np.asarray(q8, dtype=np.uint8)
@@ -196,11 +201,16 @@ def prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
             if mode == "mirror":
                 c = float(prefill_score_coef(np.float32(q_scale), k_scale[kv], sm_scale))
                 s2 = (k_codes[: last + 1] @ qc) * c
-                m2 = np.max(s2)
-                p = np.exp2(s2 - m2)
-                l = p.sum()
-                p8 = e4m3.encode((p * 256.0).astype(np.float32))
-                num = (e4m3.decode(p8) @ v_codes[: last + 1]) / 256.0
+                m_run, l, num = -np.inf, 0.0, np.zeros(D)
+                for t0 in range(0, last + 1, tile):  # online softmax over key tiles
+                    seg = s2[t0:t0 + tile]
+                    m_new = max(m_run, float(np.max(seg)))
+                    a = math.exp2(m_run - m_new) if np.isfinite(m_run) else 0.0
+                    p = np.exp2(seg - m_new)
+                    p8 = e4m3.encode((p * 256.0).astype(np.float32))
+                    num = num * a + (e4m3.decode(p8) @ v_codes[t0:t0 + seg.size]) / 256.0
+                    l = l * a + p.sum()
+                    m_run = m_new
                 out[t, h] = num / l * sv
             else:
                 qs = float(np.float32(q_scale))

@@ -12,12 +12,13 @@ from oracle.kv_cache import FP8, BF16
 SENTINEL = 0xA5
 
 # Attention tolerance for unit-variance inputs: max-abs 1e-2, mean-abs 1e-3.
-# The output is bfloat16, whose round-to-nearest adds up to 2^-9 |o| to an
-# element of magnitude |o|; outputs far from unit scale (the x20 outlier
-# channels) get that rounding on top of the absolute budget.
+# The output is bfloat16 (8 significant bits): round-to-nearest moves an
+# element o in [2^e, 2^(e+1)) by at most half an ulp, 2^(e-8) <= 2^-8 |o|.
+# Outputs far from unit scale (the x20 outlier channels) get that rounding
+# on top of the absolute budget.
 MAX_ABS = 1e-2
 MEAN_ABS = 1e-3
-BF16_HALF_ULP_REL = 2.0 ** -9
+BF16_HALF_ULP_REL = 2.0 ** -8
 
 
 def f32(t: torch.Tensor) -> np.ndarray:
@@ -55,7 +56,7 @@ def errors(got: np.ndarray, ref: np.ndarray):
 
 
 def assert_close(got, ref, max_abs=MAX_ABS, mean_abs=MEAN_ABS, what=""):
-    """Elementwise |got - ref| <= max_abs + 2^-9 |ref| and mean |got - ref| <=
+    """Elementwise |got - ref| <= max_abs + 2^-8 |ref| and mean |got - ref| <=
     mean_abs.  Returns (max-abs, mean-abs)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
