@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--layers", type=int, default=32,
                     help="layers per step (fewer only for small profiling runs; the metric uses 32)")
     return ap.parse_args()
@@ -268,6 +269,62 @@ def context_sweep(wl, g_dec, reps=10):
             "slope_kv_gbs": round(2 * HKV * D / (slope * 1e-6) / 1e9, 1)}
 
 
+# -------------------------------------------------------------- prefill ---
+PF_NEW, PF_CACHED = 4096, 28672
+
+
+def prefill_flops(new=PF_NEW, cached=PF_CACHED, hq=HQ, d=D):
+    """4 * D FLOPs (QK^T and P.V, 2 each) per attended (query, key) pair;
+    query i attends to cached + i + 1 keys."""
+    pairs = new * cached + new * (new + 1) // 2
+    return pairs * hq * 4 * d
+
+
+def prefill_leg(device, reps=10):
+    """Chunked causal prefill of 4,096 new tokens on 28,672 cached FP8
+    tokens (32/8 heads, head_dim 128): TFLOP/s of kvq_prefill_attention."""
+    import torch
+    import fp8_kv_cache_reshape_gb300 as kvq
+    import workloads as W
+    g = W.generator(77)
+    L = PF_NEW + PF_CACHED
+    bt, nb = W.paged_layout([L], P, g)
+    slots = W.slots_for(bt, 0, torch.arange(L), P).to(device)
+    gd = W.generator(78, device=device)
+    k = W.randn_bf16((L, HKV, D), gd, device=device)
+    v = W.randn_bf16((L, HKV, D), gd, device=device)
+    q = W.randn_bf16((PF_NEW, HQ, D), gd, device=device)
+    ks, vs = W.calibrate_amax(k), W.calibrate_amax(v)
+    qs = (q.float().abs().amax() / 448.0).reshape(1).to(torch.float32)
+    kd, vd = kvq.alloc_kv_cache(nb, HKV, D, device=device, fill=0)
+    kvq.kvq_reshape_and_cache(k, v, slots, kd, vd, ks, vs)
+    q8 = torch.empty(q.shape, dtype=torch.uint8, device=device)
+    kvq.kvq_quantize_query(q, q8, qs)
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=device)
+    btd = bt.to(device)
+    cu = torch.tensor([0, PF_NEW], dtype=torch.int32, device=device)
+    sl = torch.tensor([L], dtype=torch.int32, device=device)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def call():
+        kvq.kvq_prefill_attention(q8, qs, kd, vd, ks, vs, btd, cu, sl, out, max_q_tokens=PF_NEW,
+                                  sm_scale=1.0 / math.sqrt(D), dev_status=st)
+
+    for _ in range(3):
+        call()
+    ms = time_eager(call, reps) / reps
+    assert int(st.item()) == 0, "prefill reported a device fault"
+    peaks, src = measured_peaks()
+    bf16 = float(peaks.get("bf16_tflops", 1900.0))
+    fp8_peak = 2.0 * bf16  # nominal FP8:BF16 dense ratio 4.5 : 2.25
+    tf = prefill_flops() / (ms * 1e-3) / 1e12
+    return {"workload": "llama31_8b_chunked_prefill_4k_on_28k", "ms": round(ms, 4), "flops": prefill_flops(),
+            "bound": "tensor", "achieved": round(tf, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+            "frac": round(tf / fp8_peak, 4),
+            "peak_source": f"{src} bf16_tflops x 2 (nominal FP8:BF16 dense ratio)",
+            "exps": PF_NEW * PF_CACHED * HQ + PF_NEW * (PF_NEW + 1) // 2 * HQ}
+
+
 # ---------------------------------------------------------- CPU baseline ---
 CPU_SAMPLE_CONTEXT = 131072
 CPU_SAMPLE_HEADS = 2
@@ -406,6 +463,7 @@ def ours_arm(args, rank, world, local_rank):
         except (OSError, ValueError):
             traffic = None
     sweep = None if args.no_sweep else context_sweep(wl, g_dec)
+    pf = None if args.no_prefill else prefill_leg(device)
     e2e_fn, h2d, d2h = e2e_setup(wl)
     g_e2e = capture(e2e_fn)
     e2e_reps = max(3, args.steps)
@@ -437,6 +495,7 @@ def ours_arm(args, rank, world, local_rank):
         "timing": "CUDA graph of one step (32 x [cache write + decode partial + combine]) replayed",
         "clocks": clk.summary(),
         "sweep": sweep,
+        "prefill": pf,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

@@ -66,9 +66,19 @@ struct Geo {
   static constexpr int KS = D / 16;           // 16-dim k-steps of QK
 };
 
+constexpr int kNW = 4;     // consumer warps per CTA
+constexpr int kCtasPerSm = 2;
+
+// About 80 KiB of pages in flight per CTA, in a multiple of kNW stages: the
+// consumers take stages round-robin, so with NST % NW == 0 every ring slot
+// is always consumed by the same warp, which waits on the slot's phases in
+// order.  (If two warps shared a slot, a warp could test a slot whose
+// previous fill has not landed yet, and a parity wait would then see the
+// phase before it as complete.)
 template <int D, bool FP8>
-constexpr int stages_for() {  // about 80 KiB of pages in flight per CTA
-  return (81920 / Geo<D, FP8>::STAGE) > 32 ? 32 : (81920 / Geo<D, FP8>::STAGE);
+constexpr int stages_for() {
+  constexpr int n = (81920 / Geo<D, FP8>::STAGE) > 32 ? 32 : (81920 / Geo<D, FP8>::STAGE);
+  return (n / kNW) * kNW < kNW ? kNW : (n / kNW) * kNW;
 }
 
 template <int D, bool FP8, int NW, int NST>
@@ -117,6 +127,7 @@ constexpr int kPresent0 = 1, kPresent1 = 2, kBad0 = 4, kBad1 = 8;
 template <int D, bool FP8, int NW, int NST>
 __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __grid_constant__ DecodeParams p) {
   using G = Geo<D, FP8>;
+  static_assert(NST % NW == 0 && NST >= NW, "each ring slot must belong to one consumer warp");
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(NST) * G::STAGE);
@@ -561,9 +572,6 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float* __rest
   }
 }
 
-constexpr int kNW = 4;     // consumer warps per CTA
-constexpr int kCtasPerSm = 2;
-
 int decode_pages(int P, int max_blocks, int window) {
   int pages = max_blocks;
   if (window > 0) {
@@ -712,3 +720,4 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
   if (D == 128) return fp8 ? launch_decode<128, true>(prm, o, s) : launch_decode<128, false>(prm, o, s);
   return fp8 ? launch_decode<64, true>(prm, o, s) : launch_decode<64, false>(prm, o, s);
 }
+
