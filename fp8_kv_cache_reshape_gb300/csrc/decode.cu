@@ -15,12 +15,15 @@
 // Warp NW is the producer: it reads block ids and streams pages (one
 // contiguous bulk copy per K page and per V page, two pages per stage) into a
 // ring of NST shared-memory stages guarded by mbarriers.  Warps 0..NW-1
-// consume stages round-robin.  Per page a consumer computes S^T = K Q^T
-// (16 tokens x 8 query heads, M = tokens) with mma.m16n8k16 (f16 inputs:
-// E4M3 converts to f16 exactly); one online-softmax update (base 2) covers
-// the stage's 32 tokens; P is transposed in registers with movmatrix, and
-// O^T = V^T P^T (M = dims) goes into fresh FP32 fragments that are then
-// added into the running output.  At the end of an item the NW warp states
+// consume stages round-robin; each ring slot belongs to one warp.  FP8
+// cache: a consumer copies its whole stage into registers with ldmatrix and
+// releases the slot at once; S^T = K Q^T (16 tokens x 8 query heads, M =
+// tokens) runs on mma.m16n8k32 with E4M3 operands straight from the cache
+// bytes, q entering as two exact E4M3 terms; one online-softmax update (base
+// 2) covers the stage's 32 tokens; P is transposed in registers (movmatrix)
+// and split into two E4M3 terms, and O^T = V^T P^T (M = dims, K = the 32
+// token slots of both pages) goes into fresh FP32 fragments that are then
+// added into the running output.  BF16 cache: the same flow on bf16 MMAs.  At the end of an item the NW warp states
 // are merged through shared memory and one normalized partial output plus
 // its log2-sum-exp is written per query head.  A combine kernel, launched as
 // a programmatic dependent of the partial kernel, merges the page ranges.
@@ -226,10 +229,12 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
 #pragma unroll
     for (int i = 0; i < (FP8 ? G::KS / 2 : G::KS); ++i) koff[i] = k_chunk_offset(tok, 2 * i + (lane >> 4), G::ROWB);
   }
-  int voff[FP8 ? (G::MT / 2) : G::MT];
+  // V offsets.  FP8: matrix 0/1 = page 0 rows (16 mt + 0..7 / 8..15), matrix
+  // 2/3 = the same rows of page 1.  BF16: one m-tile of one page per x4.
+  int voff[G::MT];
   if constexpr (FP8) {
 #pragma unroll
-    for (int i = 0; i < G::MT / 2; ++i) voff[i] = (32 * i + lane) * kPage;
+    for (int i = 0; i < G::MT; ++i) voff[i] = (lane >> 4) * G::PAGE + (16 * i + (lane & 15)) * kPage;
   } else {
 #pragma unroll
     for (int i = 0; i < G::MT; ++i) {
@@ -238,61 +243,65 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
     }
   }
 
-  // S^T fragment of one page: s[0..1] = token r, heads 2c, 2c+1; s[2..3] = token r + 8
-  auto qk_page = [&](uint32_t kb, const uint32_t (&qf)[G::KS][2], float (&s)[4]) {
-    float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};  // two independent chains
-    if constexpr (FP8) {
-#pragma unroll
-      for (int kk = 0; kk < G::KS; kk += 2) {
-        uint32_t x0, x1, x2, x3, l0, h0, l1, h1, l2, h2, l3, h3;
-        ldsm_x4(kb + koff[kk / 2], x0, x1, x2, x3);
-        e4m3x4_to_f16x2x2(x0, l0, h0);
-        e4m3x4_to_f16x2x2(x1, l1, h1);
-        e4m3x4_to_f16x2x2(x2, l2, h2);
-        e4m3x4_to_f16x2x2(x3, l3, h3);
-        mma_f16(a, l0, l1, h0, h1, qf[kk][0], qf[kk][1], a);
-        mma_f16(b, l2, l3, h2, h3, qf[kk + 1][0], qf[kk + 1][1], b);
-      }
-    } else {
-#pragma unroll
-      for (int kk = 0; kk < G::KS; kk += 2) {
-        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
-        ldsm_x4(kb + koff[kk], x0, x1, x2, x3);
-        ldsm_x4(kb + koff[kk + 1], y0, y1, y2, y3);
-        mma_bf16(a, x0, x1, x2, x3, qf[kk][0], qf[kk][1], a);
-        mma_bf16(b, y0, y1, y2, y3, qf[kk + 1][0], qf[kk + 1][1], b);
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) s[e] = a[e] + b[e];
-  };
-
   uint32_t it0 = 0;
   for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
     const ItemRange rg = item_range(p, item, false);
-    // query fragments of head (kvh * g + r); heads >= g are zero padding
-    uint32_t qf[G::KS][2];
+    // ---- query fragments of head (kvh * g + r); heads >= g are zero padding ----
+    // FP8: q * sigma = hi + lo, two E4M3 terms (sigma = 2^(7 - floor(log2 max|q|))
+    // per head) feed the E4M3 MMA; lanes c hold dims 32kk + 4c..4c+3 (b0) and
+    // 32kk + 16 + 4c..4c+3 (b1).  BF16: q as stored.
+    constexpr int QW = FP8 ? (D / 32) * 2 : G::KS * 2;  // 32-bit words per term
+    uint32_t qh[QW], ql[FP8 ? QW : 1];
+    float coef0, coef1;  // score coefficient of heads 2c and 2c + 1
     {
       const bool live = r < p.g;
       const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
                              (static_cast<size_t>(rg.b) * p.Hq + rg.kvh * p.g + (live ? r : 0)) * D;
+      if constexpr (FP8) {
+        float x[QW][4];
+        float mx = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < G::KS; ++kk) {
-        if constexpr (FP8) {
-          // dims 4c .. 4c+3 of the 16-dim chunk: (4c, 4c+1) pair with K's low
-          // bytes, (4c+2, 4c+3) with its high bytes
-          const uint2 w = live ? __ldg(reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * c)) : make_uint2(0, 0);
-          qf[kk][0] = pack_f16x2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
-          qf[kk][1] = pack_f16x2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
-        } else {
-          qf[kk][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * c)) : 0u;
-          qf[kk][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * c)) : 0u;
+        for (int w = 0; w < QW; ++w) {
+          const int dim = (w >> 1) * 32 + (w & 1) * 16 + 4 * c;
+          const uint2 u = live ? __ldg(reinterpret_cast<const uint2*>(qrow + dim)) : make_uint2(0, 0);
+          x[w][0] = __uint_as_float(u.x << 16);
+          x[w][1] = __uint_as_float(u.x & 0xFFFF0000u);
+          x[w][2] = __uint_as_float(u.y << 16);
+          x[w][3] = __uint_as_float(u.y & 0xFFFF0000u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fabsf(x[w][e]));
         }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        int e2 = mx > 0.f ? static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127 : 0;
+        e2 = e2 < -100 ? -100 : e2;
+        const float sigma = __uint_as_float(static_cast<uint32_t>(127 + 7 - e2) << 23);   // 2^(7 - e2)
+        const float inv_sigma = __uint_as_float(static_cast<uint32_t>(127 - 7 + e2) << 23);
+#pragma unroll
+        for (int w = 0; w < QW; ++w) {
+          const float y0 = x[w][0] * sigma, y1 = x[w][1] * sigma, y2 = x[w][2] * sigma, y3 = x[w][3] * sigma;
+          const uint32_t h01 = f32x2_to_e4m3x2(y0, y1), h23 = f32x2_to_e4m3x2(y2, y3);
+          const uint32_t f01 = e4m3x2_to_f16x2(static_cast<uint16_t>(h01));
+          const uint32_t f23 = e4m3x2_to_f16x2(static_cast<uint16_t>(h23));
+          const float2 d01 = __half22float2(*reinterpret_cast<const __half2*>(&f01));
+          const float2 d23 = __half22float2(*reinterpret_cast<const __half2*>(&f23));
+          qh[w] = h01 | (h23 << 16);
+          ql[w] = f32x2_to_e4m3x2(y0 - d01.x, y1 - d01.y) | (f32x2_to_e4m3x2(y2 - d23.x, y3 - d23.y) << 16);
+        }
+        const float cf = __fmul_rn(__fmul_rn(p.k_scale[rg.kvh], p.sm_scale), kLog2e);
+        // 1/sigma of heads 2c and 2c + 1 lives in lanes 8c and 8c + 4
+        coef0 = cf * __shfl_sync(0xffffffffu, inv_sigma, 8 * c);
+        coef1 = cf * __shfl_sync(0xffffffffu, inv_sigma, 8 * c + 4);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < G::KS; ++kk) {
+          qh[2 * kk] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * c)) : 0u;
+          qh[2 * kk + 1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * c)) : 0u;
+        }
+        ql[0] = 0u;
+        coef0 = coef1 = __fmul_rn(p.sm_scale, kLog2e);
       }
     }
-    float coef;
-    if constexpr (FP8) coef = __fmul_rn(__fmul_rn(p.k_scale[rg.kvh], p.sm_scale), kLog2e);
-    else coef = __fmul_rn(p.sm_scale, kLog2e);
 
     float m[2] = {NEG_INF, NEG_INF};
     float l[2] = {0.f, 0.f};
@@ -320,107 +329,155 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
       const int tok0 = (rg.pg0 + i * PPS) * kPage;  // first token of page 0
       const int tok_end = tok0 + (two ? 2 : 1) * kPage;
       const bool edge = (info & (kBad0 | kBad1)) || tok0 < rg.lo || tok_end > rg.hi;
+      // token liveness (edge stages): inside [lo, hi), present, valid block id
+      auto live = [&](int pg, int t) {
+        const int tok = tok0 + pg * kPage + t;
+        const bool badp = pg == 0 ? (info & kBad0) : (info & kBad1);
+        const bool present = pg == 0 || two;
+        return present && !badp && tok >= rg.lo && tok < rg.hi;
+      };
 
-      // ---- scores: page 0 -> s0, page 1 -> s1 ----
       float s0[4], s1[4];
-      qk_page(kb, qf, s0);
-      if (two) qk_page(kb + G::PAGE, qf, s1);
-      else s1[0] = s1[1] = s1[2] = s1[3] = NEG_INF;
+      float p00, p01, p02, p03, p10, p11, p12, p13, al0, al1;
+      auto softmax = [&]() {  // online softmax over the stage's 32 tokens (base 2)
+        float mx0 = fmaxf(fmaxf(s0[0], s0[2]), fmaxf(s1[0], s1[2]));
+        float mx1 = fmaxf(fmaxf(s0[1], s0[3]), fmaxf(s1[1], s1[3]));
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        s0[e] *= coef;
-        s1[e] *= coef;
-      }
-      // masks (edge stages only): scores of dead tokens -> -inf, their V codes -> 0
-      uint32_t vm0_lo = 0xFFFFFFFFu, vm0_hi = 0xFFFFFFFFu, vm1_lo = 0xFFFFFFFFu, vm1_hi = 0xFFFFFFFFu;
-      if (edge) {
-        auto live = [&](int pg, int t) {
-          const int tok = tok0 + pg * kPage + t;
-          const bool badp = pg == 0 ? (info & kBad0) : (info & kBad1);
-          const bool present = pg == 0 || two;
-          return present && !badp && tok >= rg.lo && tok < rg.hi;
-        };
-        if (!live(0, r)) s0[0] = s0[1] = NEG_INF;
-        if (!live(0, r + 8)) s0[2] = s0[3] = NEG_INF;
-        if (!live(1, r)) s1[0] = s1[1] = NEG_INF;
-        if (!live(1, r + 8)) s1[2] = s1[3] = NEG_INF;
-        // V fragments hold tokens 2c, 2c+1 (low pair) and 2c+8, 2c+9 (high pair)
-        auto vmask = [&](int pg, uint32_t& lo, uint32_t& hi) {
-          const bool t0 = live(pg, 2 * c), t1 = live(pg, 2 * c + 1), t8 = live(pg, 2 * c + 8),
-                     t9 = live(pg, 2 * c + 9);
-          if constexpr (FP8) {
-            lo = (t0 ? 0x000000FFu : 0u) | (t1 ? 0x0000FF00u : 0u) | (t8 ? 0x00FF0000u : 0u) |
-                 (t9 ? 0xFF000000u : 0u);
-            hi = lo;
-          } else {
-            lo = (t0 ? 0x0000FFFFu : 0u) | (t1 ? 0xFFFF0000u : 0u);
-            hi = (t8 ? 0x0000FFFFu : 0u) | (t9 ? 0xFFFF0000u : 0u);
-          }
-        };
-        vmask(0, vm0_lo, vm0_hi);
-        vmask(1, vm1_lo, vm1_hi);
-      }
-      // ---- online softmax over the stage's 32 tokens (base 2) ----
-      float mx0 = fmaxf(fmaxf(s0[0], s0[2]), fmaxf(s1[0], s1[2]));
-      float mx1 = fmaxf(fmaxf(s0[1], s0[3]), fmaxf(s1[1], s1[3]));
-#pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-      }
-      const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-      const float base0 = (mn0 == NEG_INF) ? 0.f : mn0;
-      const float base1 = (mn1 == NEG_INF) ? 0.f : mn1;
-      const float al0 = ex2(m[0] - base0), al1 = ex2(m[1] - base1);  // rescale of the running sums
-      m[0] = mn0;
-      m[1] = mn1;
-      const float p00 = ex2(s0[0] - base0), p01 = ex2(s0[1] - base1), p02 = ex2(s0[2] - base0),
-                  p03 = ex2(s0[3] - base1);
-      const float p10 = ex2(s1[0] - base0), p11 = ex2(s1[1] - base1), p12 = ex2(s1[2] - base0),
-                  p13 = ex2(s1[3] - base1);
-      l[0] = l[0] * al0 + ((p00 + p02) + (p10 + p12));
-      l[1] = l[1] * al1 + ((p01 + p03) + (p11 + p13));
+        for (int o = 4; o < 32; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        // probabilities come out scaled by 2^8 (exact): P fills the E4M3 range
+        const float base0 = ((mn0 == NEG_INF) ? 0.f : mn0) - 8.f;
+        const float base1 = ((mn1 == NEG_INF) ? 0.f : mn1) - 8.f;
+        al0 = ex2(m[0] - base0 - 8.f);  // rescale of the running sums
+        al1 = ex2(m[1] - base1 - 8.f);
+        m[0] = mn0;
+        m[1] = mn1;
+        p00 = ex2(s0[0] - base0); p01 = ex2(s0[1] - base1); p02 = ex2(s0[2] - base0); p03 = ex2(s0[3] - base1);
+        p10 = ex2(s1[0] - base0); p11 = ex2(s1[1] - base1); p12 = ex2(s1[2] - base0); p13 = ex2(s1[3] - base1);
+        l[0] = l[0] * al0 + ((p00 + p02) + (p10 + p12));
+        l[1] = l[1] * al1 + ((p01 + p03) + (p11 + p13));
+      };
 
-      // ---- O^T += V^T P^T over both pages, fresh FP32 per stage ----
       if constexpr (FP8) {
-        const uint32_t pa0 = movmatrix_t(pack_f16x2(p00, p01));  // page 0: tokens 2c, 2c+1 of head r
-        const uint32_t pa1 = movmatrix_t(pack_f16x2(p02, p03));  //         tokens 2c+8, 2c+9
-        const uint32_t pb0 = movmatrix_t(pack_f16x2(p10, p11));  // page 1
-        const uint32_t pb1 = movmatrix_t(pack_f16x2(p12, p13));
+        // ---- copy the whole stage to registers, then release the ring slot ----
+        uint32_t ka[2][D / 32][4];
+        uint32_t va[G::MT][4];
 #pragma unroll
-        for (int mt = 0; mt < G::MT; mt += 2) {
-          float t[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
-          {
-            uint32_t y0, y1, y2, y3, a0, b0, a1, b1, a2, b2, a3, b3;
-            ldsm_x4(vb + voff[mt / 2], y0, y1, y2, y3);
-            e4m3x4_to_f16x2x2(y0 & vm0_lo, a0, b0);
-            e4m3x4_to_f16x2x2(y1 & vm0_lo, a1, b1);
-            e4m3x4_to_f16x2x2(y2 & vm0_lo, a2, b2);
-            e4m3x4_to_f16x2x2(y3 & vm0_lo, a3, b3);
-            mma_f16(t, a0, a1, b0, b1, pa0, pa1, t);
-            mma_f16(u, a2, a3, b2, b3, pa0, pa1, u);
+        for (int kk = 0; kk < D / 32; ++kk) ldsm_x4(kb + koff[kk], ka[0][kk][0], ka[0][kk][1], ka[0][kk][2], ka[0][kk][3]);
+        if (two) {
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk)
+            ldsm_x4(kb + G::PAGE + koff[kk], ka[1][kk][0], ka[1][kk][1], ka[1][kk][2], ka[1][kk][3]);
+        }
+#pragma unroll
+        for (int mt = 0; mt < G::MT; ++mt) ldsm_x4(vb + voff[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+
+        // ---- S^T = K Q^T, E4M3 MMA, q as hi + lo (two independent chains) ----
+        auto qk = [&](const uint32_t (&kp)[D / 32][4], float (&s)[4]) {
+          float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < D / 32; ++kk) {
+            mma_e4m3(a, kp[kk][0], kp[kk][1], kp[kk][2], kp[kk][3], qh[2 * kk], qh[2 * kk + 1], a);
+            mma_e4m3(b, kp[kk][0], kp[kk][1], kp[kk][2], kp[kk][3], ql[2 * kk], ql[2 * kk + 1], b);
           }
-          if (two) {
-            uint32_t y0, y1, y2, y3, a0, b0, a1, b1, a2, b2, a3, b3;
-            ldsm_x4(vb + G::PAGE + voff[mt / 2], y0, y1, y2, y3);
-            e4m3x4_to_f16x2x2(y0 & vm1_lo, a0, b0);
-            e4m3x4_to_f16x2x2(y1 & vm1_lo, a1, b1);
-            e4m3x4_to_f16x2x2(y2 & vm1_lo, a2, b2);
-            e4m3x4_to_f16x2x2(y3 & vm1_lo, a3, b3);
-            mma_f16(t, a0, a1, b0, b1, pb0, pb1, t);
-            mma_f16(u, a2, a3, b2, b3, pb0, pb1, u);
+          s[0] = (a[0] + b[0]) * coef0;
+          s[1] = (a[1] + b[1]) * coef1;
+          s[2] = (a[2] + b[2]) * coef0;
+          s[3] = (a[3] + b[3]) * coef1;
+        };
+        qk(ka[0], s0);
+        if (two) qk(ka[1], s1);
+        else s1[0] = s1[1] = s1[2] = s1[3] = NEG_INF;
+        // masks (edge stages only): scores of dead tokens -> -inf, their V codes -> 0
+        if (edge) {
+          if (!live(0, r)) s0[0] = s0[1] = NEG_INF;
+          if (!live(0, r + 8)) s0[2] = s0[3] = NEG_INF;
+          if (!live(1, r)) s1[0] = s1[1] = NEG_INF;
+          if (!live(1, r + 8)) s1[2] = s1[3] = NEG_INF;
+          // lane word c of a V row holds tokens 2c, 2c+1, 2c+8, 2c+9
+          auto vmask = [&](int pg) {
+            return (live(pg, 2 * c) ? 0x000000FFu : 0u) | (live(pg, 2 * c + 1) ? 0x0000FF00u : 0u) |
+                   (live(pg, 2 * c + 8) ? 0x00FF0000u : 0u) | (live(pg, 2 * c + 9) ? 0xFF000000u : 0u);
+          };
+          const uint32_t m0 = vmask(0), m1 = vmask(1);
+#pragma unroll
+          for (int mt = 0; mt < G::MT; ++mt) {
+            va[mt][0] &= m0;
+            va[mt][1] &= m0;
+            va[mt][2] &= m1;
+            va[mt][3] &= m1;
           }
+        } else if (!two) {
+#pragma unroll
+          for (int mt = 0; mt < G::MT; ++mt) va[mt][2] = va[mt][3] = 0u;
+        }
+        softmax();
+        // ---- P^T fragments: transpose f16 pairs, then two E4M3 terms ----
+        auto pterms = [&](float x0, float x1, float x2, float x3, uint32_t& hi, uint32_t& lo) {
+          const uint32_t t0 = movmatrix_t(pack_f16x2(x0, x1));  // tokens 2c, 2c+1 of head r
+          const uint32_t t1 = movmatrix_t(pack_f16x2(x2, x3));  // tokens 2c+8, 2c+9
+          const uint32_t h0 = f16x2_to_e4m3x2(t0), h1 = f16x2_to_e4m3x2(t1);
+          hi = h0 | (h1 << 16);
+          const uint32_t d0 = e4m3x2_to_f16x2(static_cast<uint16_t>(h0));
+          const uint32_t d1 = e4m3x2_to_f16x2(static_cast<uint16_t>(h1));
+          const __half2 r0 = __hsub2(*reinterpret_cast<const __half2*>(&t0), *reinterpret_cast<const __half2*>(&d0));
+          const __half2 r1 = __hsub2(*reinterpret_cast<const __half2*>(&t1), *reinterpret_cast<const __half2*>(&d1));
+          lo = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&r0)) |
+               (f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&r1)) << 16);
+        };
+        uint32_t ph0, pl0, ph1 = 0u, pl1 = 0u;
+        pterms(p00, p01, p02, p03, ph0, pl0);
+        pterms(p10, p11, p12, p13, ph1, pl1);
+        // ---- O^T += V^T P^T (32 token slots per MMA), fresh FP32 per stage ----
+#pragma unroll
+        for (int mt = 0; mt < G::MT; ++mt) {
+          float t[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_e4m3(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], ph0, ph1, t);
+          mma_e4m3(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], pl0, pl1, t);
           O[mt][0] = fmaf(O[mt][0], al0, t[0]);
           O[mt][1] = fmaf(O[mt][1], al1, t[1]);
           O[mt][2] = fmaf(O[mt][2], al0, t[2]);
           O[mt][3] = fmaf(O[mt][3], al1, t[3]);
-          O[mt + 1][0] = fmaf(O[mt + 1][0], al0, u[0]);
-          O[mt + 1][1] = fmaf(O[mt + 1][1], al1, u[1]);
-          O[mt + 1][2] = fmaf(O[mt + 1][2], al0, u[2]);
-          O[mt + 1][3] = fmaf(O[mt + 1][3], al1, u[3]);
         }
       } else {
-        // BF16 cache: P as the sum of two bf16 terms (hi + lo), ~16 significant bits
+        // ---- BF16 cache: S^T via bf16 MMA straight from shared memory ----
+        auto qk = [&](uint32_t kp, float (&s)[4]) {
+          float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < G::KS; kk += 2) {
+            uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+            ldsm_x4(kp + koff[kk], x0, x1, x2, x3);
+            ldsm_x4(kp + koff[kk + 1], y0, y1, y2, y3);
+            mma_bf16(a, x0, x1, x2, x3, qh[2 * kk], qh[2 * kk + 1], a);
+            mma_bf16(b, y0, y1, y2, y3, qh[2 * kk + 2], qh[2 * kk + 3], b);
+          }
+          s[0] = (a[0] + b[0]) * coef0;
+          s[1] = (a[1] + b[1]) * coef1;
+          s[2] = (a[2] + b[2]) * coef0;
+          s[3] = (a[3] + b[3]) * coef1;
+        };
+        qk(kb, s0);
+        if (two) qk(kb + G::PAGE, s1);
+        else s1[0] = s1[1] = s1[2] = s1[3] = NEG_INF;
+        uint32_t vm0_lo = 0xFFFFFFFFu, vm0_hi = 0xFFFFFFFFu, vm1_lo = 0xFFFFFFFFu, vm1_hi = 0xFFFFFFFFu;
+        if (edge) {
+          if (!live(0, r)) s0[0] = s0[1] = NEG_INF;
+          if (!live(0, r + 8)) s0[2] = s0[3] = NEG_INF;
+          if (!live(1, r)) s1[0] = s1[1] = NEG_INF;
+          if (!live(1, r + 8)) s1[2] = s1[3] = NEG_INF;
+          // V fragments hold tokens 2c, 2c+1 (low pair) and 2c+8, 2c+9 (high pair)
+          vm0_lo = (live(0, 2 * c) ? 0x0000FFFFu : 0u) | (live(0, 2 * c + 1) ? 0xFFFF0000u : 0u);
+          vm0_hi = (live(0, 2 * c + 8) ? 0x0000FFFFu : 0u) | (live(0, 2 * c + 9) ? 0xFFFF0000u : 0u);
+          vm1_lo = (live(1, 2 * c) ? 0x0000FFFFu : 0u) | (live(1, 2 * c + 1) ? 0xFFFF0000u : 0u);
+          vm1_hi = (live(1, 2 * c + 8) ? 0x0000FFFFu : 0u) | (live(1, 2 * c + 9) ? 0xFFFF0000u : 0u);
+        }
+        softmax();
+        // P as the sum of two bf16 terms (hi + lo), ~16 significant bits
         auto split = [&](float x, float y, uint32_t& hi, uint32_t& lo) {
           hi = pack_bf16x2(x, y);
           lo = pack_bf16x2(x - __uint_as_float(hi << 16), y - __uint_as_float(hi & 0xFFFF0000u));
@@ -460,9 +517,9 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
           O[mt][2] = fmaf(O[mt][2], al0, t[2]);
           O[mt][3] = fmaf(O[mt][3], al1, t[3]);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
     }
     it0 += nst_item;
 
@@ -505,7 +562,7 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
           num += f * obuf[(w * 8 + h) * D + d];
         }
         o = num / den * vs;
-        lse = M + __log2f(den);
+        lse = M + __log2f(den) - 8.f;  // den is in units of 2^8 p
       }
       const size_t idx = (row0 + h) * p.num_splits + rg.split;
       p.o_part[idx * D + d] = o;

@@ -175,12 +175,14 @@ size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P, int max_b
  *               16-byte aligned, owned by the caller; contents on entry are
  *               ignored; calls sharing a workspace must not overlap.
  *  Supported: D in {64, 128}, P == 16, Hq % Hkv == 0, Hq / Hkv <= 8.
- *  Declared rounding: FP8 -- q is rounded to float16 (exact for bf16 values
- *  of magnitude in [2^-14, 65504]), K and V codes are used exactly, scores
- *  are s2 = fl32(sum_d f16(q)[d] k8[d]) * c with c = fl32(fl32(k_scale *
- *  sm_scale) * log2(e)); probabilities 2^(s2 - m) are fed to the P.V MMA as
- *  the sum of two float16 terms (hi + lo, about 22 significant bits); the
- *  result is multiplied by v_scale.  BF16 -- scores use
+ *  Declared rounding: FP8 -- per query head, sigma = 2^(7 - floor(log2
+ *  max_d |q_d|)) and q * sigma = hi + lo with hi = e4m3(q * sigma), lo =
+ *  e4m3(q * sigma - hi) (float32, RNE, saturating): exact except for
+ *  elements below 2^-9 of the head's maximum; K and V codes are used
+ *  exactly; scores s2 = fl32(sum_d (hi + lo)_d k8_d) * c / sigma with c =
+ *  fl32(fl32(k_scale * sm_scale) * log2(e)); probabilities 2^(s2 - m) * 2^8
+ *  are rounded to float16 and fed to the P.V MMA as two E4M3 terms (hi + lo,
+ *  about 8 significant bits); the result is multiplied by v_scale.  BF16 -- scores use
  *  q and k exactly, c = fl32(sm_scale * log2(e)); probabilities are fed to
  *  the P.V MMA as the sum of two bfloat16 terms.  The output is rounded to
  *  bf16 once, at the end.

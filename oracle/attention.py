@@ -42,10 +42,14 @@ Readings where the pages are silent
 Mirrored quantization points
 ----------------------------
 ``mode="mirror"`` rounds exactly where the CUDA path declares it rounds:
-* decode: q is rounded to float16 (exact for bf16 values of magnitude in
-  [2^-14, 65504]); scores are taken in base-2 units,
-  s2 = (sum_d f16(q)[d] * k8[d]) * c with c = fl32(fl32(k_scale * sm_scale)
-  * log2(e)); o = s_v * sum_j 2^(s2_j - m) v8_j / sum_j 2^(s2_j - m).
+* decode: per query head, sigma = 2^(7 - floor(log2 max_d |q_d|)) (a power
+  of two) and q * sigma = hi + lo, hi = e4m3(q * sigma), lo = e4m3(q * sigma
+  - hi) -- two E4M3 terms that feed an FP8 MMA; scores are taken in base-2
+  units, s2 = (sum_d (hi + lo)[d] * k8[d]) / sigma * c with
+  c = fl32(fl32(k_scale * sm_scale) * log2(e));
+  o = s_v * sum_j 2^(s2_j - m) v8_j / sum_j 2^(s2_j - m).  The kernel's
+  rounding of P into two E4M3 terms is not mirrored (it depends on the
+  running maximum); the tolerance covers it.
 * prefill: s2 = (sum_d q8[d] * k8[d]) * c with
   c = fl32(fl32(fl32(q_scale * k_scale) * sm_scale) * log2(e)), and P8 as
   above (running maximum over 128-key tiles).
@@ -85,6 +89,24 @@ def _softmax_row(scores_base_e):
     m = np.max(scores_base_e)
     p = np.exp(scores_base_e - m)
     return p, m, p.sum()
+
+
+def split_query_e4m3(q_row):
+    """The decode kernels' declared rounding of one query head: returns
+    (hi + lo) / sigma in float64, with sigma = 2^(7 - floor(log2 max|q|))
+    (exponent clamped at -100), hi = e4m3(fl32(q * sigma)) and
+    lo = e4m3(fl32(q * sigma - hi))."""
+    q = np.asarray(q_row, dtype=np.float32)
+    mx = float(np.max(np.abs(q))) if q.size else 0.0
+    if mx == 0.0:
+        return np.zeros(q.shape, dtype=np.float64)
+    e = max(int(np.frexp(np.float32(mx))[1]) - 1, -100)
+    sigma = np.float32(2.0 ** (7 - e))
+    y = (q * sigma).astype(np.float32)
+    hi = e4m3.decode(e4m3.encode(y))
+    res = (y.astype(np.float64) - hi).astype(np.float32)
+    lo = e4m3.decode(e4m3.encode(res))
+    return (hi + lo) / float(sigma)
 
 
 def decode_positions(L, window):
@@ -127,7 +149,7 @@ def paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                 qh = q[b, h].astype(np.float64)
                 if mode == "mirror":
                     if cache_dtype == FP8:
-                        qe = q[b, h].astype(np.float16).astype(np.float64)
+                        qe = split_query_e4m3(q[b, h])
                         c = float(decode_score_coef(k_scale[kv], sm_scale))
                     else:
                         qe = qh
