@@ -65,6 +65,11 @@ lib.kvq_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i]
 lib.kvq_paged_decode_attention.restype = _i
 lib.kvq_paged_decode_attention.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _f,
                                            _i, _i, _i, _p, _sz, _p, _p]
+lib.kvq_decode_static_scratch_bytes.restype = _sz
+lib.kvq_decode_static_scratch_bytes.argtypes = []
+lib.kvq_paged_decode_attention_static_scratch.restype = _i
+lib.kvq_paged_decode_attention_static_scratch.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
+                                                          _i64, _f, _i, _i, _i, _p, _p]
 lib.kvq_prefill_attention.restype = _i
 lib.kvq_prefill_attention.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
                                       _f, _i, _p, _p]

@@ -29,6 +29,7 @@
 // a programmatic dependent of the partial kernel, merges the page ranges.
 #include <cfloat>
 #include <cmath>
+#include <mutex>
 
 #include "kvq_device.cuh"
 #include "kvq_host.h"
@@ -778,3 +779,60 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
   return fp8 ? launch_decode<64, true>(prm, o, s) : launch_decode<64, false>(prm, o, s);
 }
 
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they run
+// decode: code inside a region that must not call cudaMalloc (a memory-pool
+// policy, a real-time loop, a plugin that has no access to its host engine's
+// allocator).  For them the split-KV partials live in one fixed array that is
+// part of this library's device image.  Every GPU that loads the library
+// holds the array until the process exits.
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {nullptr};  // device address of the array, per device
+
+}  // namespace
+
+extern "C" size_t kvq_decode_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
+extern "C" kvq_status_t kvq_paged_decode_attention_static_scratch(
+    const void* q, const void* k_cache, const void* v_cache, const float* k_scale, const float* v_scale,
+    const int32_t* block_table, const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int D, int P,
+    int max_blocks, int64_t num_blocks, float sm_scale, int window, kvq_dtype_t cache_dtype, int num_splits,
+    int* dev_status, kvq_stream_t stream) {
+  clear_error();
+  if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || P < 1 || max_blocks < 1 || num_splits < 0)
+    return fail(KVQ_ERR_INVALID_ARG, "paged_decode_static_scratch: bad sizes");
+  const size_t need = kvq_decode_workspace_size(B, Hq, Hkv, D, P, max_blocks, window, num_splits);
+  if (need > kStaticScratchBytes)
+    return fail(KVQ_ERR_UNSUPPORTED,
+                "paged_decode_static_scratch: needs %zu bytes of scratch, the static array holds %zu "
+                "(use kvq_paged_decode_attention with a workspace, or fewer splits)",
+                need, kStaticScratchBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "paged_decode_static_scratch: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(KVQ_ERR_UNSUPPORTED, "paged_decode_static_scratch: device %d", dev);
+  void* ptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
+      // first call on this device: host code must use the array's device address
+      e = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_decode_scratch);
+      if (e != cudaSuccess) {
+        g_scratch_ptr[dev] = nullptr;
+        return cuda_status(e, "paged_decode_static_scratch: cudaGetSymbolAddress");
+      }
+    }
+    ptr = g_scratch_ptr[dev];
+  }
+  return kvq_paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, B, Hq, Hkv,
+                                    D, P, max_blocks, num_blocks, sm_scale, window, cache_dtype, num_splits, ptr,
+                                    kStaticScratchBytes, dev_status, stream);
+}

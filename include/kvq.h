@@ -197,6 +197,38 @@ kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_cache, cons
                                         int* dev_status, kvq_stream_t stream);
 
 /*
+ * kvq_paged_decode_attention_static_scratch -- kvq_paged_decode_attention
+ * for callers that cannot allocate device memory where they run decode (a
+ * memory-pool policy that forbids new allocations, a real-time loop, a plugin
+ * without access to its host engine's allocator).  The pages have no
+ * counterpart: this entry point is about memory ownership only; the
+ * computation, arguments and results are those of kvq_paged_decode_attention.
+ *
+ *  - The split-KV scratch lives in a fixed array of
+ *    kvq_decode_static_scratch_bytes() bytes (4 MiB) inside the library's
+ *    device image; every GPU that loads the library holds it until the
+ *    process exits.  Nothing is allocated or freed by this call.
+ *  - A call whose kvq_decode_workspace_size(...) exceeds the array returns
+ *    KVQ_ERR_UNSUPPORTED and launches nothing.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress with that device current); make that first call
+ *    before any stream capture on that device.
+ *  - All calls on a device share the one array and it keeps the last call's
+ *    contents.  Nothing in it needs to start at zero (each call writes every
+ *    partial result before reading it), but calls that overlap on the GPU
+ *    (different streams, or different host threads without ordering) race on
+ *    it: order them on one stream.
+ */
+size_t kvq_decode_static_scratch_bytes(void);
+kvq_status_t kvq_paged_decode_attention_static_scratch(const void* q, const void* k_cache, const void* v_cache,
+                                                       const float* k_scale, const float* v_scale,
+                                                       const int32_t* block_table, const int32_t* seq_lens,
+                                                       void* out, int B, int Hq, int Hkv, int D, int P,
+                                                       int max_blocks, int64_t num_blocks, float sm_scale,
+                                                       int window, kvq_dtype_t cache_dtype, int num_splits,
+                                                       int* dev_status, kvq_stream_t stream);
+
+/*
  * kvq_prefill_attention -- chunked causal prefill over the FP8 cache on FP8
  * tensor cores.  [vLLM] "Kernel and vLLM improvements" (two-level
  * accumulation, prefill tile configurations), "Large head dimension
