@@ -71,7 +71,7 @@ struct Geo {
 };
 
 constexpr int kNW = 4;     // consumer warps per CTA
-constexpr int kCtasPerSm = 2;
+constexpr int kCtasPerSm = 3;
 
 // About 80 KiB of pages in flight per CTA, in a multiple of kNW stages: the
 // consumers take stages round-robin, so with NST % NW == 0 every ring slot
@@ -85,10 +85,9 @@ constexpr int stages_for() {
   return (n / kNW) * kNW < kNW ? kNW : (n / kNW) * kNW;
 }
 
-template <int D, bool FP8, int NW, int NST>
+template <int D, bool FP8, int NST>
 constexpr size_t decode_smem_bytes() {
-  return size_t(NST) * Geo<D, FP8>::STAGE + 2 * NST * sizeof(uint64_t) + NST * sizeof(int) +
-         (2 * NW * 8 + NW * 8 * D) * sizeof(float) + 16;
+  return size_t(NST) * Geo<D, FP8>::STAGE + 2 * NST * sizeof(uint64_t) + NST * sizeof(int) + 16;
 }
 
 struct ItemRange {
@@ -129,7 +128,7 @@ KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
 constexpr int kPresent0 = 1, kPresent1 = 2, kBad0 = 4, kBad1 = 8;
 
 template <int D, bool FP8, int NW, int NST>
-__global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const __grid_constant__ DecodeParams p) {
   using G = Geo<D, FP8>;
   static_assert(NST % NW == 0 && NST >= NW, "each ring slot must belong to one consumer warp");
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -137,10 +136,7 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(NST) * G::STAGE);
   uint64_t* empty = full + NST;
   int* stage_info = reinterpret_cast<int*>(empty + NST);
-  float* mbuf = reinterpret_cast<float*>(stage_info + NST);  // [NW][8]
-  float* lbuf = mbuf + NW * 8;                               // [NW][8]
-  float* obuf = lbuf + NW * 8;                               // [NW][8][D]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(obuf + NW * 8 * D);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(stage_info + NST);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -232,10 +228,10 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
   }
   // V offsets.  FP8: matrix 0/1 = page 0 rows (16 mt + 0..7 / 8..15), matrix
   // 2/3 = the same rows of page 1.  BF16: one m-tile of one page per x4.
-  int voff[G::MT];
+  const int vofs = (lane >> 4) * G::PAGE + (lane & 15) * kPage;  // FP8: + 256 per m-tile
+  int voff[FP8 ? 1 : G::MT];
   if constexpr (FP8) {
-#pragma unroll
-    for (int i = 0; i < G::MT; ++i) voff[i] = (lane >> 4) * G::PAGE + (16 * i + (lane & 15)) * kPage;
+    voff[0] = vofs;
   } else {
 #pragma unroll
     for (int i = 0; i < G::MT; ++i) {
@@ -363,37 +359,30 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
       };
 
       if constexpr (FP8) {
-        // ---- copy the whole stage to registers, then release the ring slot ----
-        uint32_t ka[2][D / 32][4];
-        uint32_t va[G::MT][4];
-#pragma unroll
-        for (int kk = 0; kk < D / 32; ++kk) ldsm_x4(kb + koff[kk], ka[0][kk][0], ka[0][kk][1], ka[0][kk][2], ka[0][kk][3]);
-        if (two) {
-#pragma unroll
-          for (int kk = 0; kk < D / 32; ++kk)
-            ldsm_x4(kb + G::PAGE + koff[kk], ka[1][kk][0], ka[1][kk][1], ka[1][kk][2], ka[1][kk][3]);
-        }
-#pragma unroll
-        for (int mt = 0; mt < G::MT; ++mt) ldsm_x4(vb + voff[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-
         // ---- S^T = K Q^T, E4M3 MMA, q as hi + lo (two independent chains) ----
-        auto qk = [&](const uint32_t (&kp)[D / 32][4], float (&s)[4]) {
+        auto qk = [&](uint32_t kp, float (&s)[4]) {
           float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk) {
-            mma_e4m3(a, kp[kk][0], kp[kk][1], kp[kk][2], kp[kk][3], qh[2 * kk], qh[2 * kk + 1], a);
-            mma_e4m3(b, kp[kk][0], kp[kk][1], kp[kk][2], kp[kk][3], ql[2 * kk], ql[2 * kk + 1], b);
+            uint32_t x0, x1, x2, x3;
+            ldsm_x4(kp + koff[kk], x0, x1, x2, x3);
+            mma_e4m3(a, x0, x1, x2, x3, qh[2 * kk], qh[2 * kk + 1], a);
+            mma_e4m3(b, x0, x1, x2, x3, ql[2 * kk], ql[2 * kk + 1], b);
           }
           s[0] = (a[0] + b[0]) * coef0;
           s[1] = (a[1] + b[1]) * coef1;
           s[2] = (a[2] + b[2]) * coef0;
           s[3] = (a[3] + b[3]) * coef1;
         };
-        qk(ka[0], s0);
-        if (two) qk(ka[1], s1);
+        qk(kb, s0);
+        if (two) qk(kb + G::PAGE, s1);
         else s1[0] = s1[1] = s1[2] = s1[3] = NEG_INF;
+        // ---- V fragments to registers, then release the ring slot ----
+        uint32_t va[G::MT][4];
+#pragma unroll
+        for (int mt = 0; mt < G::MT; ++mt) ldsm_x4(vb + vofs + mt * 256, va[mt][0], va[mt][1], va[mt][2], va[mt][3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
         // masks (edge stages only): scores of dead tokens -> -inf, their V codes -> 0
         if (edge) {
           if (!live(0, r)) s0[0] = s0[1] = NEG_INF;
@@ -524,109 +513,84 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_partial_kernel(const __g
     }
     it0 += nst_item;
 
-    // ---- merge the NW warp states of this item ----
+    // ---- this warp's partial result for the item (no cross-warp merge) ----
+    // partial row ((b * Hq + head) * S + split) * NW + warp; l and O are in
+    // units of 2^8 p, the log-sum-exp in units of p
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
       l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
     }
-    if (r == 0) {
-      mbuf[warp * 8 + 2 * c] = m[0];
-      mbuf[warp * 8 + 2 * c + 1] = m[1];
-      lbuf[warp * 8 + 2 * c] = l[0];
-      lbuf[warp * 8 + 2 * c + 1] = l[1];
-    }
-    float* ow = obuf + warp * 8 * D;
+    {
+      const float vs = FP8 ? p.v_scale[rg.kvh] : 1.f;
+      const size_t row0 = static_cast<size_t>(rg.b) * p.Hq + rg.kvh * p.g;
 #pragma unroll
-    for (int mt = 0; mt < G::MT; ++mt) {
-      const int d = mt * 16 + r;
-      ow[(2 * c) * D + d] = O[mt][0];
-      ow[(2 * c + 1) * D + d] = O[mt][1];
-      ow[(2 * c) * D + d + 8] = O[mt][2];
-      ow[(2 * c + 1) * D + d + 8] = O[mt][3];
-    }
-    named_bar_sync(1, NW * 32);
-    const float vs = FP8 ? p.v_scale[rg.kvh] : 1.f;
-    const size_t row0 = static_cast<size_t>(rg.b) * p.Hq + rg.kvh * p.g;
-    for (int e = warp * 32 + lane; e < p.g * D; e += NW * 32) {
-      const int h = e / D, d = e - h * D;
-      float M = NEG_INF;
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = 2 * c + hh;
+        if (h < p.g) {
+          const bool any = l[hh] > 0.f;
+          const float f = any ? vs / l[hh] : 0.f;
+          const size_t idx = ((row0 + h) * p.num_splits + rg.split) * NW + warp;
+          float* dst = p.o_part + idx * D;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, mbuf[w * 8 + h]);
-      float o = 0.f, lse = NEG_INF;
-      if (M != NEG_INF) {
-        float den = 0.f, num = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-          const float f = ex2(mbuf[w * 8 + h] - M);
-          den += f * lbuf[w * 8 + h];
-          num += f * obuf[(w * 8 + h) * D + d];
+          for (int mt = 0; mt < G::MT; ++mt) {
+            dst[mt * 16 + r] = O[mt][hh] * f;
+            dst[mt * 16 + r + 8] = O[mt][hh + 2] * f;
+          }
+          if (r == 0) p.lse_part[idx] = any ? m[hh] + __log2f(l[hh]) - 8.f : -INFINITY;
         }
-        o = num / den * vs;
-        lse = M + __log2f(den) - 8.f;  // den is in units of 2^8 p
       }
-      const size_t idx = (row0 + h) * p.num_splits + rg.split;
-      p.o_part[idx * D + d] = o;
-      if (d == 0) p.lse_part[idx] = lse;
     }
-    named_bar_sync(1, NW * 32);
   }
 }
 
-// out[row][d] = sum_s 2^(lse_s - M) o_s[d] / sum_s 2^(lse_s - M), row = (b, hq).
-// One CTA of 256 threads per row: the weights are formed once in shared
-// memory, then D columns x (256 / D) split groups accumulate in parallel.
-template <int D>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const float* __restrict__ o_part,
-                                                             const float* __restrict__ lse_part,
-                                                             __nv_bfloat16* __restrict__ out, int S) {
-  constexpr int GROUPS = 256 / D;
-  __shared__ float red[8];
-  __shared__ float part[GROUPS][D];
-  __shared__ float wsum_s;
-  extern __shared__ float w[];  // [S]
-  grid_dependency_wait();      // the partial kernel's writes are visible past this point
+// out[row][d] = sum_s 2^(lse_s - M) o_s[d] / sum_s 2^(lse_s - M) over the
+// S' partials of row = (b, hq).  Grid (rows, D / 32); 32 warps split the
+// partials (lane = dimension), so each thread issues a handful of
+// independent loads.
+constexpr int kCombineWarps = 32;
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const float* __restrict__ o_part,
+                                                                            const float* __restrict__ lse_part,
+                                                                            __nv_bfloat16* __restrict__ out, int S,
+                                                                            int D) {
+  __shared__ float red[kCombineWarps];
+  __shared__ float acc_s[kCombineWarps][33];
+  __shared__ float den_s[kCombineWarps];
+  grid_dependency_wait();  // the partial kernel's writes are visible past this point
   const int row = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int d = blockIdx.y * 32 + lane;
   const float* lp = lse_part + static_cast<size_t>(row) * S;
   float mx = -INFINITY;
-  for (int s = tid; s < S; s += 256) mx = fmaxf(mx, lp[s]);
+  for (int s = tid; s < S; s += kCombineWarps * 32) mx = fmaxf(mx, lp[s]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  if (lane == 0) red[wid] = mx;
   __syncthreads();
-  float M = red[0];
+  float M = red[lane];
 #pragma unroll
-  for (int i = 1; i < 8; ++i) M = fmaxf(M, red[i]);
-  __syncthreads();
-  float ws = 0.f;
-  for (int s = tid; s < S; s += 256) {
-    const float e = (M == -INFINITY) ? 0.f : ex2(lp[s] - M);
-    w[s] = e;
-    ws += e;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-  if ((tid & 31) == 0) red[tid >> 5] = ws;
-  __syncthreads();
-  if (tid == 0) {
-    float t = 0.f;
-    for (int i = 0; i < 8; ++i) t += red[i];
-    wsum_s = t;
-  }
-  const int d = tid % D, gi = tid / D;
-  const float* op = o_part + static_cast<size_t>(row) * S * D + d;
-  float acc = 0.f;
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float acc = 0.f, den = 0.f;
+  if (M != -INFINITY) {
+    const float* op = o_part + static_cast<size_t>(row) * S * D + d;
 #pragma unroll 4
-  for (int s = gi; s < S; s += GROUPS) acc = fmaf(w[s], op[static_cast<size_t>(s) * D], acc);
-  part[gi][d] = acc;
+    for (int s = wid; s < S; s += kCombineWarps) {
+      const float w = ex2(lp[s] - M);
+      den += w;
+      acc = fmaf(w, op[static_cast<size_t>(s) * D], acc);
+    }
+  }
+  acc_s[wid][lane] = acc;
+  if (lane == 0) den_s[wid] = den;
   __syncthreads();
-  if (gi == 0) {
+  if (wid == 0) {
     float t = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < kCombineWarps; ++k) t += acc_s[k][lane];
+    float dd = den_s[lane];
 #pragma unroll
-    for (int k = 0; k < GROUPS; ++k) t += part[k][d];
-    const float den = wsum_s;
-    out[static_cast<size_t>(row) * D + d] = __float2bfloat16_rn(den > 0.f ? t / den : 0.f);
+    for (int o = 16; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    out[static_cast<size_t>(row) * D + d] = __float2bfloat16_rn(dd > 0.f ? t / dd : 0.f);
   }
 }
 
@@ -645,10 +609,10 @@ void split_plan(int B, int Hkv, int P, int max_blocks, int window, int num_split
   if (num_splits > 0) {
     S = num_splits;
   } else {
-    const long target = 2L * kCtasPerSm * sm_count();  // about two items per CTA
+    const long target = static_cast<long>(kCtasPerSm) * sm_count();  // about one item per CTA
     const long pairs = static_cast<long>(B) * Hkv;
     S = static_cast<int>((target + pairs - 1) / pairs);
-    const int max_s = (pages + 31) / 32;  // at least 32 pages per split
+    const int max_s = (pages + 15) / 16;  // at least 16 pages per split
     if (S > max_s) S = max_s;
   }
   if (S > pages) S = pages;
@@ -662,7 +626,7 @@ void split_plan(int B, int Hkv, int P, int max_blocks, int window, int num_split
 template <int D, bool FP8>
 kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream_t s) {
   constexpr int NST = stages_for<D, FP8>();
-  constexpr size_t smem = decode_smem_bytes<D, FP8, kNW, NST>();
+  constexpr size_t smem = decode_smem_bytes<D, FP8, NST>();
   auto kern = decode_partial_kernel<D, FP8, kNW, NST>;
   static int configured_mask = 0;  // devices whose attribute is set
   int dev = 0;
@@ -679,17 +643,17 @@ kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream
   if (e != cudaSuccess) return cuda_status(e, "decode partial launch");
   // combine: programmatic dependent launch (its launch overlaps the partial's tail)
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.B * p.Hq);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = static_cast<size_t>(p.num_splits) * sizeof(float);
+  cfg.gridDim = dim3(p.B * p.Hq, D / 32);
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<D>, static_cast<const float*>(p.o_part),
-                         static_cast<const float*>(p.lse_part), out, p.num_splits);
+  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel, static_cast<const float*>(p.o_part),
+                         static_cast<const float*>(p.lse_part), out, p.num_splits * kNW, D);
   return cuda_status(e, "decode combine launch");
 }
 
@@ -711,7 +675,7 @@ extern "C" size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P
   if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || P < 1 || max_blocks < 1 || num_splits < 0) return 0;
   int S, pps;
   split_plan(B, Hkv, P, max_blocks, window, num_splits, &S, &pps);
-  const size_t rows = static_cast<size_t>(B) * Hq * S;
+  const size_t rows = static_cast<size_t>(B) * Hq * S * kNW;  // one partial per consumer warp
   const size_t o_bytes = rows * D * sizeof(float);
   return o_bytes + ((rows * sizeof(float) + 15) / 16) * 16;
 }
@@ -747,7 +711,7 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
   if (workspace_bytes < need)
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: workspace %zu bytes < %zu needed", workspace_bytes, need);
   const long items = static_cast<long>(B) * Hkv * S;
-  if (items > 0x7FFFFFFFL || static_cast<long>(B) * Hq > 0x7FFFFFFFL || S > 12000)
+  if (items > 0x7FFFFFFFL || static_cast<long>(B) * Hq > 0x7FFFFFFFL || S > 65535)
     return fail(KVQ_ERR_UNSUPPORTED, "paged_decode: problem too large");
 
   DecodeParams prm;
@@ -760,7 +724,7 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
   prm.seq_lens = seq_lens;
   prm.o_part = static_cast<float*>(workspace);
   prm.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                          static_cast<size_t>(B) * Hq * S * D * sizeof(float));
+                                          static_cast<size_t>(B) * Hq * S * kNW * D * sizeof(float));
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
