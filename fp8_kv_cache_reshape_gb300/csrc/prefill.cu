@@ -17,9 +17,12 @@
 //  warp 1     TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
 //             score buffers, then O_j = P_j V_j into one of two fresh TMEM
 //             accumulators (first level);
-//  warps 2-5  one query row per thread: online softmax in base 2 over S_j,
-//             P_j = e4m3(2^(s - m) * 256) into swizzled shared memory, and
-//             O_run = O_run * alpha + O_j in FP32 registers (second level).
+//  warps 2-9  two threads per query row (warps w and w + 4 share TMEM lane
+//             quarter w % 4), each owning 64 of the 128 columns of S_j and of
+//             O_j: online softmax in base 2 (the two halves exchange their
+//             tile maxima through shared memory), P_j = e4m3(2^(s - m) * 256)
+//             into swizzled shared memory, and O_run = O_run * alpha + O_j in
+//             FP32 registers (second level).
 // Shared-memory operands use the UMMA canonical K-major layouts: Q, K and P
 // with the 128-byte swizzle (K pages are stored pre-swizzled by the cache
 // format), V pages ([d][16 token slots]) without swizzle.
@@ -45,8 +48,10 @@ constexpr int OFF_KV = OFF_Q + TQ * HD;        // 16 KB
 constexpr int STAGE_B = 2 * TILE_B;            // K tile + V tile
 constexpr int OFF_P = OFF_KV + NKV * STAGE_B;  // 2 P buffers of 16 KB
 constexpr int OFF_BAR = OFF_P + 2 * TQ * TK;
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // + barriers, + alignment slack
-constexpr int NTHREADS = 192;
+constexpr int OFF_XCH = OFF_BAR + 512;             // row max / row sum exchange between column halves
+constexpr int SMEM_BYTES = OFF_XCH + 3 * 2 * TQ * 4 + 1024;  // + alignment slack
+constexpr int NSOFT = 8;                           // softmax warps: two per TMEM lane quarter
+constexpr int NTHREADS = 64 + NSOFT * 32;
 constexpr uint32_t TMEM_COLS = 512;            // S0 | S1 | O0 | O1, 128 columns each
 
 struct PrefillParams {
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
   if (!job.valid) return;  // uniform across the CTA
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, TQ);
+    mbar_init(&bars->q_full, NSOFT * 32);
     for (int i = 0; i < NKV; ++i) {
       mbar_init(&bars->kv_full[i], 1);
       mbar_init(&bars->kv_empty[i], 1);
@@ -183,9 +188,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->p_full[i], TQ);
+      mbar_init(&bars->p_full[i], NSOFT * 32);
       mbar_init(&bars->o_full[i], 1);
-      mbar_init(&bars->o_free[i], TQ);
+      mbar_init(&bars->o_free[i], NSOFT * 32);
     }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -315,22 +320,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     mbar_wait(&bars->mma_done, 0);
   } else {
     // ------------------------------------------------------ softmax warps --
-    const int r = threadIdx.x - 64;        // query row of this thread, 0..127
+    const int half = (warp - 2) >> 2;      // columns half*64 .. +63 of S and of O
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     const int row = quarter * 32 + lane;   // TMEM lane == query row
-    (void)r;
+    constexpr int HC = TK / 2;             // columns per thread
+    float* xmax = reinterpret_cast<float*>(smem + OFF_XCH);   // [2 tiles][2 halves][TQ]
+    float* xsum = xmax + 2 * 2 * TQ;                           // [2 halves][TQ]
     const bool live_row = job.q0 + row < job.nq;
     const int qpos = job.first_q + job.q0 + row;  // absolute position of this query
     const int kend = (p.causal && qpos + 1 < job.L) ? qpos + 1 : job.L;  // this row attends to keys [0, kend)
     const size_t out_row = (static_cast<size_t>(p.cu_seqlens_q[job.b]) + job.q0 + row) * p.Hq + job.h;
 
-    // Q row -> shared memory, 128-byte swizzled
+    // Q row (this thread's half) -> shared memory, 128-byte swizzled
     {
       uint8_t* qs = smem + OFF_Q + row * HD;
       const uint4* src = reinterpret_cast<const uint4*>(p.q8 + out_row * HD);
 #pragma unroll
-      for (int c = 0; c < HD / 16; ++c) {
+      for (int cc = 0; cc < HD / 32; ++cc) {
+        const int c = half * (HD / 32) + cc;
         const uint4 v = live_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(qs + ((c ^ (row & 7)) << 4)) = v;
       }
@@ -341,24 +349,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const int tail = job.L % kPage;          // valid tokens in the last page (0 = full)
     const int last_page = (job.L - 1) / kPage;
 
-    float O[HD];
+    float O[HC];
 #pragma unroll
-    for (int i = 0; i < HD; ++i) O[i] = 0.f;
+    for (int i = 0; i < HC; ++i) O[i] = 0.f;
     float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
     bool ok = true;
+    auto fail_wait = [&]() {
+      ok = false;
+      set_status(p.dev_status, KVQ_DEV_TIMEOUT);
+      *abort_flag = 1;
+    };
 
-    auto accumulate = [&](int jt, float alpha) {  // O = O * alpha + O_tile[jt]
+    auto accumulate = [&](int jt, float alpha) {  // O = O * alpha + O_tile[jt] (this half's dims)
       if (!ok) return;
       if (!mbar_wait(&bars->o_full[jt & 1], (jt >> 1) & 1, abort_flag)) {
-        ok = false;
-        set_status(p.dev_status, KVQ_DEV_TIMEOUT);
-        *abort_flag = 1;
+        fail_wait();
         return;
       }
       tc_fence_after();
-      const uint32_t base = tmem + t_lane + 2 * TK + (jt & 1) * HD;
+      const uint32_t base = tmem + t_lane + 2 * TK + (jt & 1) * HD + half * HC;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < HC / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(base + c * 32, v);
 #pragma unroll
@@ -368,95 +379,87 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       mbar_arrive(&bars->o_free[jt & 1]);
     };
 
-    for (int j = 0; j < nkv && ok; ++j) {
-      if (!mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort_flag)) {
-        ok = false;
-        set_status(p.dev_status, KVQ_DEV_TIMEOUT);
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
+    // every softmax thread runs every tile's named barrier, also after a
+    // failed wait, so no warp is left behind at bar.sync
+    for (int j = 0; j < nkv; ++j) {
       const int st = j % NKV;
-      const int key0 = j * TK;
-      // the stage's page flags and, for the last page, zeroing of its unused V slots
-      mbar_wait(&bars->kv_full[st], (j / NKV) & 1, abort_flag);
-      const uint32_t bad = bars->stage_bad[st];
-      if (tail != 0 && last_page / (TK / kPage) == j) {
-        uint8_t* vrow = smem + OFF_KV + st * STAGE_B + TILE_B + (last_page % (TK / kPage)) * PAGE_B + row * kPage;
-        for (int t = tail; t < kPage; ++t) vrow[fp8_v_slot(t)] = 0;
-      }
-      const bool need_mask = (key0 + TK > kend) || bad != 0;
-      const uint32_t sbuf = tmem + t_lane + (j & 1) * TK;
-      auto masked = [&](float s, int k) {
-        const int key = key0 + k;
-        return (key >= kend || ((bad >> (k / kPage)) & 1)) ? -INFINITY : s;
-      };
-      // pass 1: row maximum of this tile
+      const int key0 = j * TK + half * HC;
+      float sv[HC];
       float mx = -INFINITY;
+      uint32_t bad = 0;
+      if (ok && !mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort_flag)) fail_wait();
+      if (ok) {
+        tc_fence_after();
+        // the stage's page flags and, for the last page, zeroing of its unused V slots
+        if (!mbar_wait(&bars->kv_full[st], (j / NKV) & 1, abort_flag)) fail_wait();
+        bad = bars->stage_bad[st];
+        if (half == 0 && tail != 0 && last_page / (TK / kPage) == j) {
+          uint8_t* vrow = smem + OFF_KV + st * STAGE_B + TILE_B + (last_page % (TK / kPage)) * PAGE_B + row * kPage;
+          for (int t = tail; t < kPage; ++t) vrow[fp8_v_slot(t)] = 0;
+        }
+        const bool need_mask = (key0 + HC > kend) || bad != 0;
+        const uint32_t sbuf = tmem + t_lane + (j & 1) * TK + half * HC;
 #pragma unroll
-      for (int c = 0; c < TK / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(sbuf + c * 32, v);
+        for (int c = 0; c < HC / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(sbuf + c * 32, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float s = __uint_as_float(v[i]) * coef;
-          if (need_mask) s = masked(s, c * 32 + i);
-          mx = fmaxf(mx, s);
+          for (int i = 0; i < 32; ++i) {
+            float x = __uint_as_float(v[i]) * coef;
+            if (need_mask) {
+              const int k = c * 32 + i;  // column within this half
+              if (key0 + k >= kend || ((bad >> ((half * HC + k) / kPage)) & 1)) x = -INFINITY;
+            }
+            sv[c * 32 + i] = x;
+            mx = fmaxf(mx, x);
+          }
         }
       }
-      const float m_new = fmaxf(m, mx);
-      const float base = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m - base);
-      // pass 2: probabilities, FP8 P tile, row sum
-      float rs = 0.f;
-      uint8_t* prow = smem + OFF_P + (j & 1) * (TQ * TK) + row * TK;
+      xmax[((j & 1) * 2 + half) * TQ + row] = mx;
+      named_bar_sync(1, NSOFT * 32);
+      if (ok) {
+        const float m_new = fmaxf(m, fmaxf(mx, xmax[((j & 1) * 2 + (half ^ 1)) * TQ + row]));
+        const float base = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ex2(m - base);
+        float rs = 0.f;
+        uint8_t* prow = smem + OFF_P + (j & 1) * (TQ * TK) + row * TK;
 #pragma unroll
-      for (int c = 0; c < TK / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(sbuf + c * 32, v);
-        float pr[32];
+        for (int pg = 0; pg < HC / kPage; ++pg) {  // 4 pages of 16 keys
+          float q[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float s = __uint_as_float(v[i]) * coef;
-          if (need_mask) s = masked(s, c * 32 + i);
-          pr[i] = ex2(s - base);
-          rs += pr[i];
-        }
-        // two pages of 16 keys; word w of a page holds keys 2w, 2w+1, 2w+8, 2w+9
-#pragma unroll
-        for (int hpg = 0; hpg < 2; ++hpg) {
-          const float* q = pr + 16 * hpg;
+          for (int t = 0; t < 16; ++t) {
+            q[t] = ex2(sv[pg * 16 + t] - base);
+            rs += q[t];
+          }
+          // word w of a page holds keys 2w, 2w+1, 2w+8, 2w+9 (the V slot order)
           uint32_t w[4];
 #pragma unroll
-          for (int ww = 0; ww < 4; ++ww) {
-            const __nv_fp8x2_storage_t lo =
-                __nv_cvt_float2_to_fp8x2(make_float2(q[2 * ww] * 256.f, q[2 * ww + 1] * 256.f), __NV_SATFINITE,
-                                         __NV_E4M3);
-            const __nv_fp8x2_storage_t hi =
-                __nv_cvt_float2_to_fp8x2(make_float2(q[2 * ww + 8] * 256.f, q[2 * ww + 9] * 256.f),
-                                         __NV_SATFINITE, __NV_E4M3);
-            w[ww] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-          }
-          const int chunk = 2 * c + hpg;  // page index within the tile
+          for (int ww = 0; ww < 4; ++ww)
+            w[ww] = f32x2_to_e4m3x2(q[2 * ww] * 256.f, q[2 * ww + 1] * 256.f) |
+                    (f32x2_to_e4m3x2(q[2 * ww + 8] * 256.f, q[2 * ww + 9] * 256.f) << 16);
+          const int chunk = half * (HC / kPage) + pg;  // page index within the tile
           *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
+        l = l * alpha + rs;
+        m = m_new;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[j & 1]);
+        if (j >= 1) accumulate(j - 1, alpha_prev);
+        alpha_prev = alpha;
       }
-      l = l * alpha + rs;
-      m = m_new;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full[j & 1]);
-      if (j >= 1) accumulate(j - 1, alpha_prev);
-      alpha_prev = alpha;
     }
     if (ok && nkv >= 1) accumulate(nkv - 1, alpha_prev);
 
-    // epilogue: out = O * v_scale / (256 * l)
+    // epilogue: out = O * v_scale / (256 * l), l summed over both halves
+    xsum[half * TQ + row] = l;
+    named_bar_sync(1, NSOFT * 32);
+    const float lt = l + xsum[(half ^ 1) * TQ + row];
     if (live_row && ok) {
-      const float f = (l > 0.f) ? p.v_scale[job.kvh] / (256.f * l) : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD);
+      const float f = (lt > 0.f) ? p.v_scale[job.kvh] / (256.f * lt) : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD + half * HC);
 #pragma unroll
-      for (int c = 0; c < HD / 8; ++c) {
+      for (int c = 0; c < HC / 8; ++c) {
         uint4 w;
         w.x = pack_bf16x2(O[8 * c + 0] * f, O[8 * c + 1] * f);
         w.y = pack_bf16x2(O[8 * c + 2] * f, O[8 * c + 3] * f);
