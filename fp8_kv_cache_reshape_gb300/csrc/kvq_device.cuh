@@ -8,6 +8,7 @@
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
+#include <cstring>
 
 #include "../../include/kvq.h"
 
@@ -192,6 +193,17 @@ KVQ_DEVINL uint32_t pack_f16x2(float lo, float hi) {
 KVQ_DEVINL uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+// Two float32 FMAs in one instruction: (a.x*b.x + c.x, a.y*b.y + c.y).
+KVQ_DEVINL float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long ra, rb, rc, rd;
+  memcpy(&ra, &a, 8);
+  memcpy(&rb, &b, 8);
+  memcpy(&rc, &c, 8);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+  float2 d;
+  memcpy(&d, &rd, 8);
+  return d;
 }
 KVQ_DEVINL float ex2(float x) {
   float y;

@@ -368,12 +368,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       }
       tc_fence_after();
       const uint32_t base = tmem + t_lane + 2 * TK + (jt & 1) * HD + half * HC;
+      const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
       for (int c = 0; c < HC / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(base + c * 32, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) O[c * 32 + i] = fmaf(O[c * 32 + i], alpha, __uint_as_float(v[i]));
+        for (int i = 0; i < 32; i += 2) {
+          const float2 r = ffma2(make_float2(O[c * 32 + i], O[c * 32 + i + 1]), a2,
+                                 make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])));
+          O[c * 32 + i] = r.x;
+          O[c * 32 + i + 1] = r.y;
+        }
       }
       tc_fence_before();
       mbar_arrive(&bars->o_free[jt & 1]);
@@ -399,44 +405,46 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         }
         const bool need_mask = (key0 + HC > kend) || bad != 0;
         const uint32_t sbuf = tmem + t_lane + (j & 1) * TK + half * HC;
+        // raw scores (the positive scale is applied in the exponent below)
 #pragma unroll
         for (int c = 0; c < HC / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(sbuf + c * 32, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float x = __uint_as_float(v[i]) * coef;
-            if (need_mask) {
-              const int k = c * 32 + i;  // column within this half
-              if (key0 + k >= kend || ((bad >> ((half * HC + k) / kPage)) & 1)) x = -INFINITY;
-            }
-            sv[c * 32 + i] = x;
-            mx = fmaxf(mx, x);
-          }
+          for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(v[i]);
         }
+        if (need_mask) {  // last tiles only; static indices keep sv in registers
+          const int lim = kend - key0;  // columns k < lim are causally visible
+          const uint32_t badh = bad >> (half * (HC / kPage));
+#pragma unroll
+          for (int k = 0; k < HC; ++k)
+            sv[k] = (k >= lim || ((badh >> (k / kPage)) & 1)) ? -INFINITY : sv[k];
+        }
+#pragma unroll
+        for (int k = 0; k < HC; ++k) mx = fmaxf(mx, sv[k]);
       }
       xmax[((j & 1) * 2 + half) * TQ + row] = mx;
       named_bar_sync(1, NSOFT * 32);
       if (ok) {
+        // m and the maxima are raw scores; 2^(s - m) * 256 = 2^(raw * coef - (m * coef - 8))
         const float m_new = fmaxf(m, fmaxf(mx, xmax[((j & 1) * 2 + (half ^ 1)) * TQ + row]));
-        const float base = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ex2(m - base);
-        float rs = 0.f;
+        const float nb = (m_new == -INFINITY) ? 0.f : 8.f - m_new * coef;
+        const float alpha = (m == -INFINITY) ? 0.f : ex2((m - m_new) * coef);
+        float rs = 0.f;  // in units of 2^8 p
         uint8_t* prow = smem + OFF_P + (j & 1) * (TQ * TK) + row * TK;
 #pragma unroll
         for (int pg = 0; pg < HC / kPage; ++pg) {  // 4 pages of 16 keys
           float q[16];
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
-            q[t] = ex2(sv[pg * 16 + t] - base);
+            q[t] = ex2(fmaf(sv[pg * 16 + t], coef, nb));
             rs += q[t];
           }
           // word w of a page holds keys 2w, 2w+1, 2w+8, 2w+9 (the V slot order)
           uint32_t w[4];
 #pragma unroll
           for (int ww = 0; ww < 4; ++ww)
-            w[ww] = f32x2_to_e4m3x2(q[2 * ww] * 256.f, q[2 * ww + 1] * 256.f) |
-                    (f32x2_to_e4m3x2(q[2 * ww + 8] * 256.f, q[2 * ww + 9] * 256.f) << 16);
+            w[ww] = f32x2_to_e4m3x2(q[2 * ww], q[2 * ww + 1]) | (f32x2_to_e4m3x2(q[2 * ww + 8], q[2 * ww + 9]) << 16);
           const int chunk = half * (HC / kPage) + pg;  // page index within the tile
           *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
@@ -451,12 +459,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     }
     if (ok && nkv >= 1) accumulate(nkv - 1, alpha_prev);
 
-    // epilogue: out = O * v_scale / (256 * l), l summed over both halves
+    // epilogue: out = O * v_scale / l (O and l both in units of 2^8 p), l summed over both halves
     xsum[half * TQ + row] = l;
     named_bar_sync(1, NSOFT * 32);
     const float lt = l + xsum[(half ^ 1) * TQ + row];
     if (live_row && ok) {
-      const float f = (lt > 0.f) ? p.v_scale[job.kvh] / (256.f * lt) : 0.f;
+      const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD + half * HC);
 #pragma unroll
       for (int c = 0; c < HC / 8; ++c) {
