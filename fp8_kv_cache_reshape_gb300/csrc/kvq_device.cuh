@@ -205,6 +205,16 @@ KVQ_DEVINL float2 ffma2(float2 a, float2 b, float2 c) {
   memcpy(&d, &rd, 8);
   return d;
 }
+// Two float32 additions in one instruction.
+KVQ_DEVINL float2 fadd2(float2 a, float2 b) {
+  unsigned long long ra, rb, rd;
+  memcpy(&ra, &a, 8);
+  memcpy(&rb, &b, 8);
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  float2 d;
+  memcpy(&d, &rd, 8);
+  return d;
+}
 KVQ_DEVINL float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -430,15 +430,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         const float m_new = fmaxf(m, fmaxf(mx, xmax[((j & 1) * 2 + (half ^ 1)) * TQ + row]));
         const float nb = (m_new == -INFINITY) ? 0.f : 8.f - m_new * coef;
         const float alpha = (m == -INFINITY) ? 0.f : ex2((m - m_new) * coef);
-        float rs = 0.f;  // in units of 2^8 p
+        float2 rs2 = make_float2(0.f, 0.f);  // in units of 2^8 p
+        const float2 coef2 = make_float2(coef, coef), nb2 = make_float2(nb, nb);
         uint8_t* prow = smem + OFF_P + (j & 1) * (TQ * TK) + row * TK;
 #pragma unroll
         for (int pg = 0; pg < HC / kPage; ++pg) {  // 4 pages of 16 keys
           float q[16];
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            q[t] = ex2(fmaf(sv[pg * 16 + t], coef, nb));
-            rs += q[t];
+          for (int t = 0; t < 16; t += 2) {
+            const float2 e = ffma2(make_float2(sv[pg * 16 + t], sv[pg * 16 + t + 1]), coef2, nb2);
+            q[t] = ex2(e.x);
+            q[t + 1] = ex2(e.y);
+            rs2 = fadd2(rs2, make_float2(q[t], q[t + 1]));
           }
           // word w of a page holds keys 2w, 2w+1, 2w+8, 2w+9 (the V slot order)
           uint32_t w[4];
@@ -448,7 +451,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
           const int chunk = half * (HC / kPage) + pg;  // page index within the tile
           *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        l = l * alpha + rs;
+        l = l * alpha + (rs2.x + rs2.y);
         m = m_new;
         fence_proxy_async_smem();
         tc_fence_before();
