@@ -41,12 +41,13 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--layers", type=int, default=32,
                     help="layers per step (fewer only for small profiling runs; the metric uses 32)")
     return ap.parse_args()
@@ -63,6 +64,21 @@ def measured_peaks():
             return json.load(f), "measured"
     except OSError:
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def decode_traffic():
+    """DRAM bytes per partial-kernel launch from the committed ncu record,
+    or None when the kernel source changed since the counters were taken."""
+    import hashlib
+    tf = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        rec = json.load(open(tf))
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+    except (OSError, ValueError, KeyError):
+        return None
+    if hashlib.sha256(src).hexdigest() != rec.get("source_sha256"):
+        return None
+    return rec.get("traffic_bytes_per_launch")
 
 
 def decode_bytes(context, batch=1, hq=HQ, hkv=HKV, d=D):
@@ -92,7 +108,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -269,6 +285,64 @@ def context_sweep(wl, g_dec, reps=10):
             "slope_kv_gbs": round(2 * HKV * D / (slope * 1e-6) / 1e9, 1)}
 
 
+# ------------------------------------------------- BF16 cache comparison ---
+BF16_LAYERS = 8
+
+
+def bf16_compare(fp8_sweep, device, reps=20):
+    """The same decode on a BF16 cache (the "skip layers" format) over 8
+    distinct 128K layer caches (4.8 GB): us per layer vs context, the
+    linear fit, and the FP8 / BF16 slope ratio and break-even context
+    (the vLLM blog's ITL-slope comparison, here at kernel level)."""
+    import torch
+    import fp8_kv_cache_reshape_gb300 as kvq
+    import workloads as W
+    g = W.generator(501)
+    bt, nb = W.paged_layout([CONTEXT], P, g)
+    slots = W.slots_for(bt, 0, torch.arange(CONTEXT, dtype=torch.int64), P).to(device)
+    layers = []
+    for l in range(BF16_LAYERS):
+        gl = W.generator(502 * 1000 + l, device=device)
+        kd, vd = kvq.alloc_kv_cache(nb, HKV, D, cache_dtype="bf16", device=device, fill=0)
+        for t0 in range(0, CONTEXT, 16384):
+            k = W.randn_bf16((16384, HKV, D), gl, device=device)
+            v = W.randn_bf16((16384, HKV, D), gl, device=device)
+            kvq.kvq_reshape_and_cache(k, v, slots[t0:t0 + 16384].contiguous(), kd, vd, cache_dtype="bf16")
+        layers.append(dict(kd=kd, vd=vd, q=W.randn_bf16((1, HQ, D), gl, device=device),
+                           out=torch.empty((1, HQ, D), dtype=torch.bfloat16, device=device)))
+    btd = bt.to(device)
+    seq = torch.tensor([CONTEXT], dtype=torch.int32, device=device)
+    ws = torch.empty(kvq.kvq_decode_workspace_size(1, HQ, HKV, D, bt.shape[1]), dtype=torch.uint8, device=device)
+
+    def run():
+        for ly in layers:
+            kvq.kvq_paged_decode_attention(ly["q"], ly["kd"], ly["vd"], None, None, btd, seq, ly["out"],
+                                           num_blocks=nb, sm_scale=1.0 / math.sqrt(D), cache_dtype="bf16",
+                                           workspace=ws)
+
+    gr = capture(run)
+    rows = []
+    for L in (4096, 8192, 16384, 32768, 65536, 131072):
+        seq.fill_(L)
+        gr.replay()
+        us = time_graph(gr, reps) * 1e3 / (reps * BF16_LAYERS)
+        kvb = 2 * L * HKV * D * 2
+        rows.append({"context": L, "us_per_layer_decode": round(us, 3), "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1)})
+    xs = [r["context"] for r in rows]
+    ys = [r["us_per_layer_decode"] for r in rows]
+    n = len(xs)
+    mx, my = sum(xs) / n, sum(ys) / n
+    slope = sum((x - mx) * (y - my) for x, y in zip(xs, ys)) / sum((x - mx) ** 2 for x in xs)
+    icpt = my - slope * mx
+    out = {"points": rows, "fit_us_per_token": slope, "fit_intercept_us": round(icpt, 3),
+           "slope_kv_gbs": round(2 * HKV * D * 2 / (slope * 1e-6) / 1e9, 1)}
+    if fp8_sweep:
+        s8, i8 = fp8_sweep["fit_us_per_token"], fp8_sweep["fit_intercept_us"]
+        out["slope_ratio_fp8_over_bf16"] = round(s8 / slope, 4)
+        out["break_even_tokens"] = round((i8 - icpt) / (slope - s8)) if slope > s8 else None
+    return out
+
+
 # -------------------------------------------------------------- prefill ---
 PF_NEW, PF_CACHED = 4096, 28672
 
@@ -437,7 +511,7 @@ def ours_arm(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         total_ms = time_graph(g_step, args.steps)
         # the dominant kernel pair alone: 32 decode calls per replay
-        dec_reps = max(10, args.steps)
+        dec_reps = max(200, args.steps)
         dec_ms = time_graph(g_dec, dec_reps)
     barrier()
     torch.cuda.synchronize()
@@ -455,15 +529,10 @@ def ours_arm(args, rank, world, local_rank):
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     call_ms = dec_ms / (dec_reps * LAYERS)
     achieved = decode_bytes(CONTEXT) / (call_ms * 1e-3) / 1e9
-    traffic = None
-    tf = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    if os.path.exists(tf):
-        try:
-            traffic = json.load(open(tf)).get("traffic_bytes_per_launch")
-        except (OSError, ValueError):
-            traffic = None
+    traffic = decode_traffic()
     sweep = None if args.no_sweep else context_sweep(wl, g_dec)
     pf = None if args.no_prefill else prefill_leg(device)
+    bf = None if (args.no_sweep or args.no_bf16) else bf16_compare(sweep, device)
     e2e_fn, h2d, d2h = e2e_setup(wl)
     g_e2e = capture(e2e_fn)
     e2e_reps = max(3, args.steps)
@@ -496,6 +565,7 @@ def ours_arm(args, rank, world, local_rank):
         "clocks": clk.summary(),
         "sweep": sweep,
         "prefill": pf,
+        "bf16_compare": bf,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
