@@ -11,18 +11,23 @@
 //
 // One CTA = 128 query rows of one sequence x one query head.  Keys come in
 // tiles of 128 (8 pages).  Warp roles:
-//  warp 0     producer: block ids -> one bulk copy per K page and V page into
-//             a 3-stage ring (pages of unknown / out-of-range blocks are zero
-//             filled and masked);
+//  warps 0, 10  producers of the even / odd key tiles: block ids (read a
+//             group of 4 tiles ahead) -> one bulk copy per K page and V page
+//             into a 4-stage ring, each producer owning two of the stages
+//             (pages of unknown / out-of-range blocks are zero filled and
+//             masked).  Two issuing warps, because a page-sized bulk copy
+//             costs the issuing warp tens of cycles;
 //  warp 1     TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
-//             score buffers, then O_j = P_j V_j into one of two fresh TMEM
-//             accumulators (first level);
+//             score buffers, then O_j = P_j V_j into a fresh TMEM accumulator
+//             (first level);
 //  warps 2-9  two threads per query row (warps w and w + 4 share TMEM lane
 //             quarter w % 4), each owning 64 of the 128 columns of S_j and of
 //             O_j: online softmax in base 2 (the two halves exchange their
 //             tile maxima through shared memory), P_j = e4m3(2^(s - m) * 256)
 //             into swizzled shared memory, and O_run = O_run * alpha + O_j in
-//             FP32 registers (second level).
+//             FP32 (second level; O_run lives in its own TMEM columns and is
+//             updated through registers, which keeps the softmax warps free
+//             of spills).
 // Shared-memory operands use the UMMA canonical K-major layouts: Q, K and P
 // with the 128-byte swizzle (K pages are stored pre-swizzled by the cache
 // format), V pages ([d][16 token slots]) without swizzle.
@@ -40,7 +45,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int TQ = 128;           // query rows per CTA
 constexpr int TK = 128;           // keys per tile (8 pages)
 constexpr int HD = 128;           // head dim
-constexpr int NKV = 3;            // K/V stages
+constexpr int NKV = 4;            // K/V stages
+constexpr int NPROD = 2;          // producer warps; tile j comes from producer j % NPROD
+static_assert(NKV % NPROD == 0, "each stage belongs to one producer, which refills it in tile order");
 constexpr int PAGE_B = kPage * HD;             // 2048 bytes per page (K or V)
 constexpr int TILE_B = TK * HD;                // 16 KB per K tile (= V tile)
 constexpr int OFF_Q = 0;
@@ -51,8 +58,8 @@ constexpr int OFF_BAR = OFF_P + 2 * TQ * TK;
 constexpr int OFF_XCH = OFF_BAR + 512;             // row max / row sum exchange between column halves
 constexpr int SMEM_BYTES = OFF_XCH + 3 * 2 * TQ * 4 + 1024;  // + alignment slack
 constexpr int NSOFT = 8;                           // softmax warps: two per TMEM lane quarter
-constexpr int NTHREADS = 64 + NSOFT * 32;
-constexpr uint32_t TMEM_COLS = 512;            // S0 | S1 | O0 | O1, 128 columns each
+constexpr int NTHREADS = (NPROD + 1 + NSOFT) * 32;  // producer 0, MMA, softmax warps, producer 1
+constexpr uint32_t TMEM_COLS = 512;            // S0 | S1 | O_tile | O_run, 128 columns each
 
 struct PrefillParams {
   const uint8_t* q8;
@@ -78,8 +85,8 @@ struct Bars {
   uint64_t kv_empty[NKV];
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t o_full[2];
-  uint64_t o_free[2];
+  uint64_t o_full;  // P.V of the current tile is in O_tile
+  uint64_t o_free;  // O_tile has been read
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -120,6 +127,22 @@ KVQ_DEVINL void umma_commit(uint64_t* bar) {
 }
 KVQ_DEVINL void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 KVQ_DEVINL void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+KVQ_DEVINL void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+KVQ_DEVINL void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+KVQ_DEVINL void tmem_ld16_async(uint32_t taddr, uint32_t (&v)[16]) {  // complete after tmem_wait_ld()
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+KVQ_DEVINL void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::
+                   "r"(taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+               "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+               : "memory");
+}
 KVQ_DEVINL void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
@@ -129,7 +152,7 @@ KVQ_DEVINL void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
         "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tmem_wait_ld();
 }
 
 struct Job {
@@ -189,9 +212,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->p_full[i], NSOFT * 32);
-      mbar_init(&bars->o_full[i], 1);
-      mbar_init(&bars->o_free[i], NSOFT * 32);
     }
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_free, NSOFT * 32);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -209,12 +232,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
   const uint32_t tmem = bars->tmem_base;
   const int nkv = job.nkv;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer --
+  if (warp == 0 || warp >= 2 + NSOFT) {
+    // ----------------------------------------------------------- producers --
     const int n_pages = (job.L + kPage - 1) / kPage;
     const int32_t* bt = p.block_table + static_cast<size_t>(job.b) * p.max_blocks;
-    int j = 0;
-    for (; j < nkv; ++j) {
+    // Block ids come one warp-wide load per group of 4 tiles (32 pages), issued
+    // a group ahead so that its latency hides behind the copies; lane
+    // (j % 4) * 8 + i of `ids` holds the block of page i of tile j.
+    auto load_ids = [&](int grp) {
+      const int page = grp * 32 + lane;
+      return page < n_pages ? __ldg(bt + page) : -1;
+    };
+    int ids = load_ids(0);
+    int ids_next = load_ids(1);
+    int cur_grp = 0;
+    int j = (warp == 0) ? 0 : warp - (1 + NSOFT);  // this producer's first tile
+    for (; j < nkv; j += NPROD) {
+      if ((j >> 2) != cur_grp) {  // steps of NPROD < 4 tiles: at most one group ahead
+        cur_grp = j >> 2;
+        ids = ids_next;
+        ids_next = load_ids(cur_grp + 1);
+      }
       const int st = j % NKV;
       int ok = 1;
       if (lane == 0) ok = (!*abort_flag && mbar_wait(&bars->kv_empty[st], ((j / NKV) & 1) ^ 1, abort_flag)) ? 1 : 0;
@@ -223,30 +261,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       uint8_t* ks = smem + OFF_KV + st * STAGE_B;
       uint8_t* vs = ks + TILE_B;
       // lanes 0..7: one page each
-      int blk = -1;
+      int blk = __shfl_sync(0xffffffffu, ids, ((j & 3) << 3) | (lane & 7));
       uint32_t bad = 0;
       const int page = j * (TK / kPage) + lane;
-      if (lane < TK / kPage && page < n_pages) {
-        blk = __ldg(bt + page);
-        if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
-          set_status(p.dev_status, KVQ_DEV_BAD_BLOCK);
-          blk = -1;
-          bad = 1;
-        }
+      if (lane >= TK / kPage || page >= n_pages) {
+        blk = -1;
+      } else if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
+        set_status(p.dev_status, KVQ_DEV_BAD_BLOCK);
+        blk = -1;
+        bad = 1;
       }
       const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad != 0);
       const uint32_t load_mask = __ballot_sync(0xffffffffu, blk >= 0) & 0xFFu;
       // zero-fill pages that are not loaded (past the end, or bad block ids)
-      for (int pg = 0; pg < TK / kPage; ++pg) {
-        if (load_mask & (1u << pg)) continue;
-        uint4* kz = reinterpret_cast<uint4*>(ks + pg * PAGE_B);
-        uint4* vz = reinterpret_cast<uint4*>(vs + pg * PAGE_B);
-        for (int i = lane; i < PAGE_B / 16; i += 32) {
-          kz[i] = make_uint4(0, 0, 0, 0);
-          vz[i] = make_uint4(0, 0, 0, 0);
+      if (load_mask != 0xFFu) {
+        for (int pg = 0; pg < TK / kPage; ++pg) {
+          if (load_mask & (1u << pg)) continue;
+          uint4* kz = reinterpret_cast<uint4*>(ks + pg * PAGE_B);
+          uint4* vz = reinterpret_cast<uint4*>(vs + pg * PAGE_B);
+          for (int i = lane; i < PAGE_B / 16; i += 32) {
+            kz[i] = make_uint4(0, 0, 0, 0);
+            vz[i] = make_uint4(0, 0, 0, 0);
+          }
         }
+        fence_proxy_async_smem();  // the zeros, before the tensor cores read the stage
       }
-      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         bars->stage_bad[st] = bad_mask & 0xFFu;
@@ -259,10 +298,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         bulk_g2s(vs + lane * PAGE_B, p.v_cache + off, PAGE_B, &bars->kv_full[st], policy_evict_first());
       }
     }
-    if (j < nkv && lane == 0) {  // abandoned: let issued copies land
+    if (j < nkv && lane == 0) {  // abandoned: let this producer's issued copies land
       set_status(p.dev_status, KVQ_DEV_TIMEOUT);
       *abort_flag = 1;
-      for (int k = j - NKV > 0 ? j - NKV : 0; k < j; ++k) mbar_wait(&bars->kv_full[k % NKV], (k / NKV) & 1);
+      for (int k = j - NPROD; k >= 0 && k >= j - NKV; k -= NPROD) mbar_wait(&bars->kv_full[k % NKV], (k / NKV) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer --
@@ -298,18 +337,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       if (j + 1 < nkv) issue_s(j + 1);
       if (!ok) break;
       if (!wait(&bars->p_full[j & 1], (j >> 1) & 1)) break;
-      if (j >= 2 && !wait(&bars->o_free[j & 1], ((j >> 1) & 1) ^ 1)) break;
+      if (j >= 1 && !wait(&bars->o_free, (j - 1) & 1)) break;  // O_tile of tile j - 1 has been read
       tc_fence_after();
       if (lane == 0) {
         const int st = j % NKV;
         const uint32_t p_s = sbase + OFF_P + (j & 1) * (TQ * TK);
         const uint32_t v_s = sbase + OFF_KV + st * STAGE_B + TILE_B;
-        const uint32_t d = tmem + 2 * TK + (j & 1) * HD;
+        const uint32_t d = tmem + 2 * TK;  // O_tile
 #pragma unroll
         for (int kk = 0; kk < TK / 32; ++kk)  // 32 keys = 2 V pages per MMA
           umma_f8(d, desc_sw128(p_s + kk * 32), desc_interleave(v_s + kk * 2 * PAGE_B, PAGE_B, 128), IDESC,
                   kk > 0 ? 1u : 0u);
-        umma_commit(&bars->o_full[j & 1]);
+        umma_commit(&bars->o_full);
         umma_commit(&bars->kv_empty[st]);
       }
       __syncwarp();
@@ -349,40 +388,52 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const int tail = job.L % kPage;          // valid tokens in the last page (0 = full)
     const int last_page = (job.L - 1) / kPage;
 
-    float O[HC];
+    const uint32_t o_tile = tmem + t_lane + 2 * TK + half * HC;  // this half's columns of O_tile
+    const uint32_t o_run = o_tile + HD;                           // ... and of O_run
+    {  // O_run = 0
+      uint32_t z[16];
 #pragma unroll
-    for (int i = 0; i < HC; ++i) O[i] = 0.f;
+      for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+      for (int c = 0; c < HC / 16; ++c) tmem_st16(o_run + 16 * c, z);
+    }
     float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
-    bool ok = true;
-    auto fail_wait = [&]() {
-      ok = false;
-      set_status(p.dev_status, KVQ_DEV_TIMEOUT);
-      *abort_flag = 1;
+    bool ok = true;  // warp-uniform, since tcgen05.ld / st need every lane of the warp
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      if (!ok) return false;
+      const bool got = mbar_wait(bar, parity, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        set_status(p.dev_status, KVQ_DEV_TIMEOUT);
+        *abort_flag = 1;
+      }
+      return ok;
     };
 
-    auto accumulate = [&](int jt, float alpha) {  // O = O * alpha + O_tile[jt] (this half's dims)
-      if (!ok) return;
-      if (!mbar_wait(&bars->o_full[jt & 1], (jt >> 1) & 1, abort_flag)) {
-        fail_wait();
-        return;
-      }
+    auto accumulate = [&](int jt, float alpha) {  // O_run = O_run * alpha + O_tile (this half's dims)
+      if (!wait_all(&bars->o_full, jt & 1)) return;
       tc_fence_after();
-      const uint32_t base = tmem + t_lane + 2 * TK + (jt & 1) * HD + half * HC;
+      tmem_wait_st();  // the previous update of O_run
       const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-      for (int c = 0; c < HC / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(base + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 r = ffma2(make_float2(O[c * 32 + i], O[c * 32 + i + 1]), a2,
-                                 make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])));
-          O[c * 32 + i] = r.x;
-          O[c * 32 + i + 1] = r.y;
+      for (int c = 0; c < HC / 16; ++c) {  // 16 columns at a time
+        uint32_t t[16], o[16];
+        tmem_ld16_async(o_tile + 16 * c, t);
+        tmem_ld16_async(o_run + 16 * c, o);
+        tmem_wait_ld();
+        if (c == HC / 16 - 1) {  // the whole tile has been read: the next P.V may overwrite it
+          tc_fence_before();
+          mbar_arrive(&bars->o_free);
         }
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const float2 r = ffma2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2,
+                                 make_float2(__uint_as_float(t[i]), __uint_as_float(t[i + 1])));
+          o[i] = __float_as_uint(r.x);
+          o[i + 1] = __float_as_uint(r.y);
+        }
+        tmem_st16(o_run + 16 * c, o);
       }
-      tc_fence_before();
-      mbar_arrive(&bars->o_free[jt & 1]);
     };
 
     // every softmax thread runs every tile's named barrier, also after a
@@ -393,11 +444,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       float sv[HC];
       float mx = -INFINITY;
       uint32_t bad = 0;
-      if (ok && !mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort_flag)) fail_wait();
-      if (ok) {
+      // S_j, then the stage's page flags and, for the last page, zeroing of its unused V slots
+      if (wait_all(&bars->s_full[j & 1], (j >> 1) & 1) && wait_all(&bars->kv_full[st], (j / NKV) & 1)) {
         tc_fence_after();
-        // the stage's page flags and, for the last page, zeroing of its unused V slots
-        if (!mbar_wait(&bars->kv_full[st], (j / NKV) & 1, abort_flag)) fail_wait();
         bad = bars->stage_bad[st];
         if (half == 0 && tail != 0 && last_page / (TK / kPage) == j) {
           uint8_t* vrow = smem + OFF_KV + st * STAGE_B + TILE_B + (last_page % (TK / kPage)) * PAGE_B + row * kPage;
@@ -466,17 +515,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     xsum[half * TQ + row] = l;
     named_bar_sync(1, NSOFT * 32);
     const float lt = l + xsum[(half ^ 1) * TQ + row];
-    if (live_row && ok) {
-      const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD + half * HC);
+    if (ok) {
+      float O[HC];
+      tmem_wait_st();
 #pragma unroll
-      for (int c = 0; c < HC / 8; ++c) {
-        uint4 w;
-        w.x = pack_bf16x2(O[8 * c + 0] * f, O[8 * c + 1] * f);
-        w.y = pack_bf16x2(O[8 * c + 2] * f, O[8 * c + 3] * f);
-        w.z = pack_bf16x2(O[8 * c + 4] * f, O[8 * c + 5] * f);
-        w.w = pack_bf16x2(O[8 * c + 6] * f, O[8 * c + 7] * f);
-        dst[c] = w;
+      for (int c = 0; c < HC / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(o_run + 32 * c, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) O[32 * c + i] = __uint_as_float(o[i]);
+      }
+      if (live_row) {
+        const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD + half * HC);
+#pragma unroll
+        for (int c = 0; c < HC / 8; ++c) {
+          uint4 w;
+          w.x = pack_bf16x2(O[8 * c + 0] * f, O[8 * c + 1] * f);
+          w.y = pack_bf16x2(O[8 * c + 2] * f, O[8 * c + 3] * f);
+          w.z = pack_bf16x2(O[8 * c + 4] * f, O[8 * c + 5] * f);
+          w.w = pack_bf16x2(O[8 * c + 6] * f, O[8 * c + 7] * f);
+          dst[c] = w;
+        }
       }
     }
   }
