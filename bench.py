@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
+    ap.add_argument("--no-e5m2", action="store_true")
     ap.add_argument("--layers", type=int, default=32,
                     help="layers per step (fewer only for small profiling runs; the metric uses 32)")
     return ap.parse_args()
@@ -289,26 +290,34 @@ def context_sweep(wl, g_dec, reps=10):
 BF16_LAYERS = 8
 
 
-def bf16_compare(fp8_sweep, device, reps=20):
-    """The same decode on a BF16 cache (the "skip layers" format) over 8
-    distinct 128K layer caches (4.8 GB): us per layer vs context, the
-    linear fit, and the FP8 / BF16 slope ratio and break-even context
-    (the vLLM blog's ITL-slope comparison, here at kernel level)."""
+def format_compare(fp8_sweep, device, cache_dtype, reps=20):
+    """The same decode on another cache format over 8 distinct 128K layer
+    caches: us per layer vs context, the linear fit, and the slope ratio and
+    break-even context against the FP8 E4M3 sweep.  For the BF16 cache (the
+    "skip layers" format) this is the vLLM blog's ITL-slope comparison at
+    kernel level; the E5M2 cache reads the same bytes as E4M3."""
     import torch
     import fp8_kv_cache_reshape_gb300 as kvq
     import workloads as W
+    esz = 2 if cache_dtype == "bf16" else 1
     g = W.generator(501)
     bt, nb = W.paged_layout([CONTEXT], P, g)
     slots = W.slots_for(bt, 0, torch.arange(CONTEXT, dtype=torch.int64), P).to(device)
     layers = []
     for l in range(BF16_LAYERS):
         gl = W.generator(502 * 1000 + l, device=device)
-        kd, vd = kvq.alloc_kv_cache(nb, HKV, D, cache_dtype="bf16", device=device, fill=0)
+        kd, vd = kvq.alloc_kv_cache(nb, HKV, D, cache_dtype=cache_dtype, device=device, fill=0)
+        ks = vs = None
+        if esz == 1:  # unit-variance data: per-head scale amax / 57344 taken from one chunk
+            probe = W.randn_bf16((16384, HKV, D), gl, device=device)
+            ks = W.calibrate_amax(probe, W.E5M2_MAX).to(device)
+            vs = ks.clone()
         for t0 in range(0, CONTEXT, 16384):
             k = W.randn_bf16((16384, HKV, D), gl, device=device)
             v = W.randn_bf16((16384, HKV, D), gl, device=device)
-            kvq.kvq_reshape_and_cache(k, v, slots[t0:t0 + 16384].contiguous(), kd, vd, cache_dtype="bf16")
-        layers.append(dict(kd=kd, vd=vd, q=W.randn_bf16((1, HQ, D), gl, device=device),
+            kvq.kvq_reshape_and_cache(k, v, slots[t0:t0 + 16384].contiguous(), kd, vd, ks, vs,
+                                      cache_dtype=cache_dtype)
+        layers.append(dict(kd=kd, vd=vd, ks=ks, vs=vs, q=W.randn_bf16((1, HQ, D), gl, device=device),
                            out=torch.empty((1, HQ, D), dtype=torch.bfloat16, device=device)))
     btd = bt.to(device)
     seq = torch.tensor([CONTEXT], dtype=torch.int32, device=device)
@@ -316,8 +325,8 @@ def bf16_compare(fp8_sweep, device, reps=20):
 
     def run():
         for ly in layers:
-            kvq.kvq_paged_decode_attention(ly["q"], ly["kd"], ly["vd"], None, None, btd, seq, ly["out"],
-                                           num_blocks=nb, sm_scale=1.0 / math.sqrt(D), cache_dtype="bf16",
+            kvq.kvq_paged_decode_attention(ly["q"], ly["kd"], ly["vd"], ly["ks"], ly["vs"], btd, seq, ly["out"],
+                                           num_blocks=nb, sm_scale=1.0 / math.sqrt(D), cache_dtype=cache_dtype,
                                            workspace=ws)
 
     gr = capture(run)
@@ -326,7 +335,7 @@ def bf16_compare(fp8_sweep, device, reps=20):
         seq.fill_(L)
         gr.replay()
         us = time_graph(gr, reps) * 1e3 / (reps * BF16_LAYERS)
-        kvb = 2 * L * HKV * D * 2
+        kvb = 2 * L * HKV * D * esz
         rows.append({"context": L, "us_per_layer_decode": round(us, 3), "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1)})
     xs = [r["context"] for r in rows]
     ys = [r["us_per_layer_decode"] for r in rows]
@@ -334,11 +343,11 @@ def bf16_compare(fp8_sweep, device, reps=20):
     mx, my = sum(xs) / n, sum(ys) / n
     slope = sum((x - mx) * (y - my) for x, y in zip(xs, ys)) / sum((x - mx) ** 2 for x in xs)
     icpt = my - slope * mx
-    out = {"points": rows, "fit_us_per_token": slope, "fit_intercept_us": round(icpt, 3),
-           "slope_kv_gbs": round(2 * HKV * D * 2 / (slope * 1e-6) / 1e9, 1)}
+    out = {"cache_dtype": cache_dtype, "points": rows, "fit_us_per_token": slope, "fit_intercept_us": round(icpt, 3),
+           "slope_kv_gbs": round(2 * HKV * D * esz / (slope * 1e-6) / 1e9, 1)}
     if fp8_sweep:
         s8, i8 = fp8_sweep["fit_us_per_token"], fp8_sweep["fit_intercept_us"]
-        out["slope_ratio_fp8_over_bf16"] = round(s8 / slope, 4)
+        out["slope_ratio_fp8_over_this"] = round(s8 / slope, 4)
         out["break_even_tokens"] = round((i8 - icpt) / (slope - s8)) if slope > s8 else None
     return out
 
@@ -532,7 +541,8 @@ def ours_arm(args, rank, world, local_rank):
     traffic = decode_traffic()
     sweep = None if args.no_sweep else context_sweep(wl, g_dec)
     pf = None if args.no_prefill else prefill_leg(device)
-    bf = None if (args.no_sweep or args.no_bf16) else bf16_compare(sweep, device)
+    bf = None if (args.no_sweep or args.no_bf16) else format_compare(sweep, device, "bf16")
+    e5 = None if (args.no_sweep or args.no_e5m2) else format_compare(sweep, device, "fp8_e5m2")
     e2e_fn, h2d, d2h = e2e_setup(wl)
     g_e2e = capture(e2e_fn)
     e2e_reps = max(3, args.steps)
@@ -566,6 +576,7 @@ def ours_arm(args, rank, world, local_rank):
         "sweep": sweep,
         "prefill": pf,
         "bf16_compare": bf,
+        "e5m2_compare": e5,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

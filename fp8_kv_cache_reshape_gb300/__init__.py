@@ -30,6 +30,7 @@ KVQ_ERR_DEVICE_FAULT = 4
 
 KVQ_DTYPE_FP8_E4M3 = 0
 KVQ_DTYPE_BF16 = 1
+KVQ_DTYPE_FP8_E5M2 = 2
 
 KVQ_DEV_BAD_SLOT = 0x1
 KVQ_DEV_BAD_BLOCK = 0x2
@@ -110,6 +111,8 @@ def _dtype_code(cache_dtype: str) -> int:
         return KVQ_DTYPE_FP8_E4M3
     if cache_dtype in ("bf16", "bfloat16", KVQ_DTYPE_BF16):
         return KVQ_DTYPE_BF16
+    if cache_dtype in ("fp8_e5m2", KVQ_DTYPE_FP8_E5M2):
+        return KVQ_DTYPE_FP8_E5M2
     raise ValueError(f"unknown cache dtype {cache_dtype!r}")
 
 
@@ -121,7 +124,7 @@ def alloc_kv_cache(num_blocks: int, kv_heads: int, head_dim: int, cache_dtype="f
                    device="cuda", fill=None):
     """Allocate (k_cache, v_cache) as uint8 tensors in the library's paged
     format ([num_blocks][Hkv][P][D] and [num_blocks][Hkv][D][P] elements)."""
-    esz = 1 if _dtype_code(cache_dtype) == KVQ_DTYPE_FP8_E4M3 else 2
+    esz = 2 if _dtype_code(cache_dtype) == KVQ_DTYPE_BF16 else 1
     shape = (num_blocks, kv_heads, PAGE * head_dim * esz)
     if fill is None:
         return (torch.empty(shape, dtype=torch.uint8, device=device),
@@ -135,7 +138,7 @@ def kvq_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_
     """Quantize (or copy) new tokens k, v (bf16 [T][Hkv][D]) into the cache."""
     T, Hkv, D = k.shape
     dt = _dtype_code(cache_dtype)
-    esz = 1 if dt == KVQ_DTYPE_FP8_E4M3 else 2
+    esz = 2 if dt == KVQ_DTYPE_BF16 else 1
     num_blocks = k_cache.numel() // (Hkv * PAGE * D * esz)
     _check(lib.kvq_reshape_and_cache(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
                                      _ptr(k_scale), _ptr(v_scale), T, Hkv, D, PAGE, num_blocks, dt,
@@ -166,7 +169,6 @@ def kvq_paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     B, Hq, D = q.shape
     max_blocks = block_table.shape[1]
     dt = _dtype_code(cache_dtype)
-    esz = 1 if dt == KVQ_DTYPE_FP8_E4M3 else 2
     Hkv = k_cache.shape[1] if k_cache.dim() >= 3 else None
     if Hkv is None:
         raise ValueError("k_cache must be [num_blocks][Hkv][...]")

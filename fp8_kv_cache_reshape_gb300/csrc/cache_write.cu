@@ -31,21 +31,22 @@ KVQ_DEVINL void load16_bf16(const __nv_bfloat16* src, float (&x)[16]) {
   }
 }
 
+template <bool E5>
 KVQ_DEVINL uint4 quant16(const float (&x)[16], float s) {
   uint32_t w[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t b0 = f32_to_e4m3(__fdiv_rn(x[4 * i + 0], s));
-    uint32_t b1 = f32_to_e4m3(__fdiv_rn(x[4 * i + 1], s));
-    uint32_t b2 = f32_to_e4m3(__fdiv_rn(x[4 * i + 2], s));
-    uint32_t b3 = f32_to_e4m3(__fdiv_rn(x[4 * i + 3], s));
+    uint32_t b0 = f32_to_fp8<E5>(__fdiv_rn(x[4 * i + 0], s));
+    uint32_t b1 = f32_to_fp8<E5>(__fdiv_rn(x[4 * i + 1], s));
+    uint32_t b2 = f32_to_fp8<E5>(__fdiv_rn(x[4 * i + 2], s));
+    uint32_t b3 = f32_to_fp8<E5>(__fdiv_rn(x[4 * i + 3], s));
     w[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// FP8 cache write.  grid = (ceil(T / 16), Hkv), block = 128.
-template <int D>
+// FP8 cache write (E4M3, or E5M2 when E5 is set).  grid = (ceil(T / 16), Hkv), block = 128.
+template <int D, bool E5>
 __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
     const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
@@ -86,9 +87,9 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
     const size_t page = (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
     float x[16];
     load16_bf16(k + src, x);
-    *reinterpret_cast<uint4*>(k_cache + page + k_chunk_offset(off, j, D)) = quant16(x, sk);
+    *reinterpret_cast<uint4*>(k_cache + page + k_chunk_offset(off, j, D)) = quant16<E5>(x, sk);
     load16_bf16(v + src, x);
-    uint4 qv = quant16(x, sv);
+    uint4 qv = quant16<E5>(x, sv);
     const uint8_t* qb = reinterpret_cast<const uint8_t*>(&qv);
     const int slot_in_row = fp8_v_slot(off);
     if (fast) {
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(256) quantize_query_kernel(const __nv_bfloat16
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float x[16];
     load16_bf16(q + i * 16, x);
-    *reinterpret_cast<uint4*>(q8 + i * 16) = quant16(x, s);
+    *reinterpret_cast<uint4*>(q8 + i * 16) = quant16<false>(x, s);
   }
   if (blockIdx.x == 0) {
     for (int64_t i = nvec * 16 + threadIdx.x; i < n; i += blockDim.x)
@@ -179,12 +180,13 @@ extern "C" kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, cons
   if (T < 0 || Hkv < 1 || num_blocks < 1) return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: bad sizes");
   if (P != kPage) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache: page size %d (only 16)", P);
   if (D != 64 && D != 128) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache: head_dim %d", D);
-  if (cache_dtype != KVQ_DTYPE_FP8_E4M3 && cache_dtype != KVQ_DTYPE_BF16)
+  if (cache_dtype != KVQ_DTYPE_FP8_E4M3 && cache_dtype != KVQ_DTYPE_FP8_E5M2 && cache_dtype != KVQ_DTYPE_BF16)
     return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: bad cache dtype");
+  const bool fp8 = cache_dtype != KVQ_DTYPE_BF16;
   if (T == 0) return KVQ_OK;
   if (!k || !v || !slot_mapping || !k_cache || !v_cache)
     return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: null pointer");
-  if (cache_dtype == KVQ_DTYPE_FP8_E4M3 && (!k_scale || !v_scale))
+  if (fp8 && (!k_scale || !v_scale))
     return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: FP8 needs k_scale and v_scale");
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
       !aligned(slot_mapping, 8))
@@ -193,17 +195,19 @@ extern "C" kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   dim3 grid((T + kPage - 1) / kPage, Hkv);
   const int64_t num_slots = num_blocks * kPage;
-  if (cache_dtype == KVQ_DTYPE_FP8_E4M3) {
+  if (fp8) {
     auto kb = static_cast<const __nv_bfloat16*>(k);
     auto vb = static_cast<const __nv_bfloat16*>(v);
     auto kc = static_cast<uint8_t*>(k_cache);
     auto vc = static_cast<uint8_t*>(v_cache);
+    auto launch = [&](auto kernel) {
+      kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, k_scale, v_scale, T, Hkv, num_slots, dev_status);
+    };
+    const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
     if (D == 128)
-      reshape_and_cache_fp8_kernel<128><<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, k_scale, v_scale, T, Hkv,
-                                                             num_slots, dev_status);
+      e5 ? launch(reshape_and_cache_fp8_kernel<128, true>) : launch(reshape_and_cache_fp8_kernel<128, false>);
     else
-      reshape_and_cache_fp8_kernel<64><<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, k_scale, v_scale, T, Hkv,
-                                                            num_slots, dev_status);
+      e5 ? launch(reshape_and_cache_fp8_kernel<64, true>) : launch(reshape_and_cache_fp8_kernel<64, false>);
   } else {
     auto kb = static_cast<const uint16_t*>(k);
     auto vb = static_cast<const uint16_t*>(v);

@@ -127,7 +127,8 @@ KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
 // bit 2/3 = page 0/1 had an invalid block id (fully masked).
 constexpr int kPresent0 = 1, kPresent1 = 2, kBad0 = 4, kBad1 = 8;
 
-template <int D, bool FP8, int NW, int NST>
+// E5: the FP8 cache holds E5M2 codes (the MMAs take them as their A operand).
+template <int D, bool FP8, int NW, int NST, bool E5>
 __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const __grid_constant__ DecodeParams p) {
   using G = Geo<D, FP8>;
   static_assert(NST % NW == 0 && NST >= NW, "each ring slot must belong to one consumer warp");
@@ -366,8 +367,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
           for (int kk = 0; kk < D / 32; ++kk) {
             uint32_t x0, x1, x2, x3;
             ldsm_x4(kp + koff[kk], x0, x1, x2, x3);
-            mma_e4m3(a, x0, x1, x2, x3, qh[2 * kk], qh[2 * kk + 1], a);
-            mma_e4m3(b, x0, x1, x2, x3, ql[2 * kk], ql[2 * kk + 1], b);
+            mma_fp8<E5>(a, x0, x1, x2, x3, qh[2 * kk], qh[2 * kk + 1], a);
+            mma_fp8<E5>(b, x0, x1, x2, x3, ql[2 * kk], ql[2 * kk + 1], b);
           }
           s[0] = (a[0] + b[0]) * coef0;
           s[1] = (a[1] + b[1]) * coef1;
@@ -427,8 +428,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
 #pragma unroll
         for (int mt = 0; mt < G::MT; ++mt) {
           float t[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_e4m3(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], ph0, ph1, t);
-          mma_e4m3(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], pl0, pl1, t);
+          mma_fp8<E5>(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], ph0, ph1, t);
+          mma_fp8<E5>(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], pl0, pl1, t);
           O[mt][0] = fmaf(O[mt][0], al0, t[0]);
           O[mt][1] = fmaf(O[mt][1], al1, t[1]);
           O[mt][2] = fmaf(O[mt][2], al0, t[2]);
@@ -623,11 +624,11 @@ void split_plan(int B, int Hkv, int P, int max_blocks, int window, int num_split
   *pps_out = pps;
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool E5 = false>
 kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream_t s) {
   constexpr int NST = stages_for<D, FP8>();
   constexpr size_t smem = decode_smem_bytes<D, FP8, NST>();
-  auto kern = decode_partial_kernel<D, FP8, kNW, NST>;
+  auto kern = decode_partial_kernel<D, FP8, kNW, NST, E5>;
   static int configured_mask = 0;  // devices whose attribute is set
   int dev = 0;
   cudaGetDevice(&dev);
@@ -696,11 +697,12 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
   if (P != kPage) return fail(KVQ_ERR_UNSUPPORTED, "paged_decode: page size %d (only 16)", P);
   if (D != 64 && D != 128) return fail(KVQ_ERR_UNSUPPORTED, "paged_decode: head_dim %d", D);
   if (Hq / Hkv > 8) return fail(KVQ_ERR_UNSUPPORTED, "paged_decode: GQA ratio %d > 8", Hq / Hkv);
-  if (cache_dtype != KVQ_DTYPE_FP8_E4M3 && cache_dtype != KVQ_DTYPE_BF16)
+  if (cache_dtype != KVQ_DTYPE_FP8_E4M3 && cache_dtype != KVQ_DTYPE_FP8_E5M2 && cache_dtype != KVQ_DTYPE_BF16)
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: bad cache dtype");
+  const bool fp8 = cache_dtype != KVQ_DTYPE_BF16;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace)
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: null pointer");
-  if (cache_dtype == KVQ_DTYPE_FP8_E4M3 && (!k_scale || !v_scale))
+  if (fp8 && (!k_scale || !v_scale))
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: FP8 needs k_scale and v_scale");
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(workspace, 16) ||
       !aligned(out, 4))
@@ -738,7 +740,8 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
   prm.dev_status = dev_status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto o = static_cast<__nv_bfloat16*>(out);
-  const bool fp8 = cache_dtype == KVQ_DTYPE_FP8_E4M3;
+  if (cache_dtype == KVQ_DTYPE_FP8_E5M2)
+    return D == 128 ? launch_decode<128, true, true>(prm, o, s) : launch_decode<64, true, true>(prm, o, s);
   if (D == 128) return fp8 ? launch_decode<128, true>(prm, o, s) : launch_decode<128, false>(prm, o, s);
   return fp8 ? launch_decode<64, true>(prm, o, s) : launch_decode<64, false>(prm, o, s);
 }

@@ -161,6 +161,24 @@ KVQ_DEVINL void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, u
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
+// As mma_e4m3, with A holding E5M2 codes (an E5M2 cache) and B E4M3.
+KVQ_DEVINL void mma_e5m2_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                              uint32_t b1, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e5m2.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+// A operand in the cache's 8-bit format (E4M3, or E5M2 when A5 is set), B E4M3.
+template <bool A5>
+KVQ_DEVINL void mma_fp8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1,
+                        const float (&c)[4]) {
+  if constexpr (A5)
+    mma_e5m2_e4m3(d, a0, a1, a2, a3, b0, b1, c);
+  else
+    mma_e4m3(d, a0, a1, a2, a3, b0, b1, c);
+}
 // Two float32 -> two E4M3 codes (lo -> low byte), RNE, saturating.
 KVQ_DEVINL uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
@@ -224,6 +242,17 @@ KVQ_DEVINL float ex2(float x) {
 // float32 -> E4M3, round-to-nearest-even, saturating to +-448.
 KVQ_DEVINL uint8_t f32_to_e4m3(float x) {
   return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+}
+// float32 -> E5M2, round-to-nearest-even, saturating to +-57344.
+KVQ_DEVINL uint8_t f32_to_e5m2(float x) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E5M2));
+}
+template <bool E5>
+KVQ_DEVINL uint8_t f32_to_fp8(float x) {
+  if constexpr (E5)
+    return f32_to_e5m2(x);
+  else
+    return f32_to_e4m3(x);
 }
 
 }  // namespace kvq

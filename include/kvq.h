@@ -74,7 +74,13 @@ typedef enum kvq_status {
 
 typedef enum kvq_dtype {
   KVQ_DTYPE_FP8_E4M3 = 0,    /* 1-byte E4M3 codes with per-KV-head scales */
-  KVQ_DTYPE_BF16 = 1         /* unquantized bfloat16 ("skip layers") */
+  KVQ_DTYPE_BF16 = 1,        /* unquantized bfloat16 ("skip layers") */
+  KVQ_DTYPE_FP8_E5M2 = 2     /* 1-byte E5M2 codes with per-KV-head scales:
+                                [FP8KV] "How to enable it in the engine" lists
+                                fp8_e5m2 among the cache dtypes; [GTNT] section
+                                1: 5 exponent bits, 2 mantissa bits, about
+                                +-57344.  Bias 15, RNE, saturating to +-57344.
+                                Decode only (kvq_prefill_attention reads E4M3). */
 } kvq_dtype_t;
 
 /* Bits OR-ed into *dev_status by the kernels. */
@@ -106,7 +112,10 @@ const char* kvq_last_error_string(void);
  *  k_scale,      float32 [Hkv] per-KV-head scales (FP8 only; may be NULL for
  *  v_scale       BF16).  Must be finite and > 0.
  *  T >= 0 (T == 0 launches nothing), Hkv >= 1, D in {64, 128}, P == 16,
- *  num_blocks >= 1.  For BF16 the values are copied bit for bit.
+ *  num_blocks >= 1.  For BF16 the values are copied bit for bit.  FP8:
+ *  code = encode(fl32(x / s[h])), one float32 division, then one
+ *  round-to-nearest-even conversion saturating at the format's largest
+ *  finite value (448 for E4M3, 57344 for E5M2).
  *  Only the bytes of the given slots are written; everything else in the
  *  caches is left as it was.  Slots must be distinct within one call.
  */
@@ -179,7 +188,9 @@ size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P, int max_b
  *  max_d |q_d|)) and q * sigma = hi + lo with hi = e4m3(q * sigma), lo =
  *  e4m3(q * sigma - hi) (float32, RNE, saturating): exact except for
  *  elements below 2^-9 of the head's maximum; K and V codes are used
- *  exactly; scores s2 = fl32(sum_d (hi + lo)_d k8_d) * c / sigma with c =
+ *  exactly (E4M3 or E5M2: the MMA takes either as its cache operand, with
+ *  the query / probability operand in E4M3); scores s2 = fl32(sum_d
+ *  (hi + lo)_d k8_d) * c / sigma with c =
  *  fl32(fl32(k_scale * sm_scale) * log2(e)); probabilities 2^(s2 - m) * 2^8
  *  are rounded to float16 and fed to the P.V MMA as two E4M3 terms (hi + lo,
  *  about 8 significant bits); the result is multiplied by v_scale.  BF16 -- scores use
@@ -244,7 +255,8 @@ kvq_status_t kvq_paged_decode_attention_static_scratch(const void* q, const void
  *  q8            uint8 [Tq][Hq][D] E4M3 codes (kvq_quantize_query), Tq =
  *                cu_seqlens_q[B].
  *  q_scale       float32 [1].
- *  k_cache, v_cache, k_scale, v_scale, block_table  as for decode (FP8 only).
+ *  k_cache, v_cache, k_scale, v_scale, block_table  as for decode (E4M3 caches
+ *                only; the call cannot tell an E5M2 cache apart).
  *  cu_seqlens_q  int32 [B+1], non-decreasing, cu_seqlens_q[0] = 0.
  *  seq_lens      int32 [B].
  *  out           bf16 [Tq][Hq][D] (written).

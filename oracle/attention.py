@@ -50,6 +50,8 @@ Mirrored quantization points
   o = s_v * sum_j 2^(s2_j - m) v8_j / sum_j 2^(s2_j - m).  The kernel's
   rounding of P into two E4M3 terms is not mirrored (it depends on the
   running maximum); the tolerance covers it.
+  An E5M2 cache is mirrored the same way: its codes are decoded as E5M2,
+  the query and probability terms stay E4M3.
 * prefill: s2 = (sum_d q8[d] * k8[d]) * c with
   c = fl32(fl32(fl32(q_scale * k_scale) * sm_scale) * log2(e)), and P8 as
   above (running maximum over 128-key tiles).
@@ -62,7 +64,7 @@ import math
 import numpy as np
 
 from . import e4m3
-from .kv_cache import FP8, BF16, bf16_bits_to_f32, gather_tokens
+from .kv_cache import FP8, BF16, FP8_TYPES, bf16_bits_to_f32, codec, gather_tokens
 
 LOG2E_F32 = np.float32(1.4426950408889634)
 
@@ -136,9 +138,9 @@ def paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
             continue
         for kv in range(Hkv):
             kk, vv = gather_tokens(k_cache, v_cache, block_table[b], pos, kv)
-            if cache_dtype == FP8:
-                k_codes = e4m3.decode(kk)  # [n][D]
-                v_codes = e4m3.decode(vv)
+            if cache_dtype in FP8_TYPES:
+                k_codes = codec(cache_dtype).decode(kk)  # [n][D]
+                v_codes = codec(cache_dtype).decode(vv)
                 sk = float(np.float32(k_scale[kv]))
                 sv = float(np.float32(v_scale[kv]))
             else:
@@ -148,7 +150,7 @@ def paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
             for h in range(kv * g, (kv + 1) * g):
                 qh = q[b, h].astype(np.float64)
                 if mode == "mirror":
-                    if cache_dtype == FP8:
+                    if cache_dtype in FP8_TYPES:  # q terms are E4M3 for either cache format
                         qe = split_query_e4m3(q[b, h])
                         c = float(decode_score_coef(k_scale[kv], sm_scale))
                     else:

@@ -9,7 +9,8 @@ Cache layout (the library's documented format; the pages fix none)
   tokens, each a row of D values.
 * V cache: ``[num_blocks][Hkv][D][P]`` -- the same page transposed, one row
   of P tokens per dimension.
-* Element type: E4M3 bytes (uint8) or bfloat16 (stored as uint16 bits).
+* Element type: E4M3 or E5M2 bytes (uint8) or bfloat16 (stored as uint16
+  bits).
 * Token slot s lives in block s // P at offset s % P (PagedAttention as
   described in "FP8 quantization and long-context inference", section 6).
 
@@ -27,15 +28,28 @@ Sources
   sequence), and the decode lower bound is bytes read / peak bandwidth.
 * "kv-cache-quantization-fp8-scale-granularity" (inference-research note):
   327,680 bytes (320 KiB) per token for 80 x 8 x 128 in BF16, 40.0 GiB at 128K.
+* "FP8 and KV cache", "How to enable it in the engine": the cache dtypes
+  include fp8_e4m3 and fp8_e5m2 (codec in e5m2.py).
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import e4m3
+from . import e4m3, e5m2
 
 FP8 = "fp8_e4m3"
+FP8_E5M2 = "fp8_e5m2"
 BF16 = "bf16"
+FP8_TYPES = (FP8, FP8_E5M2)
+
+
+def codec(cache_dtype):
+    """The 8-bit codec module of an FP8 cache dtype."""
+    if cache_dtype == FP8:
+        return e4m3
+    if cache_dtype == FP8_E5M2:
+        return e5m2
+    raise ValueError(f"not an FP8 cache dtype: {cache_dtype!r}")
 
 
 # ---------------------------------------------------------------- bfloat16 ---
@@ -72,10 +86,11 @@ def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
     k, v: float32 arrays [T][Hkv][D] holding bfloat16 values.
     slot_mapping: int64 [T]; a negative slot means "skip this token".
     k_cache: [num_blocks][Hkv][P][D]; v_cache: [num_blocks][Hkv][D][P];
-    uint8 for FP8, uint16 (bf16 bits) for BF16.
+    uint8 for FP8 (E4M3 or E5M2), uint16 (bf16 bits) for BF16.
     k_scale, v_scale: float32 [Hkv] (ignored for BF16).
 
-    For FP8 each element becomes encode(fl32(x / s[h])).  A slot at or beyond
+    For FP8 each element becomes encode(fl32(x / s[h])) in the cache's
+    8-bit format.  A slot at or beyond
     num_blocks * P is an error: the token is skipped and the returned flag is
     True.  Returns (k_cache, v_cache, bad_slot_seen).
     """
@@ -84,7 +99,8 @@ def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
     T, Hkv, D = k.shape
     num_blocks, _, P, _ = k_cache.shape
     slots = np.asarray(slot_mapping, dtype=np.int64)
-    if cache_dtype == FP8:
+    if cache_dtype in FP8_TYPES:
+        fmt = codec(cache_dtype)
         ks = np.asarray(k_scale, np.float32)
         vs = np.asarray(v_scale, np.float32)
         kb, vb = _bf16_bits_or_none(k), _bf16_bits_or_none(v)
@@ -92,11 +108,11 @@ def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
             kq = np.empty(k.shape, np.uint8)
             vq = np.empty(v.shape, np.uint8)
             for h in range(Hkv):  # one table per head: encode(fl32(x / s[h])) for every bf16 x
-                kq[:, h] = e4m3.quantize_bf16_bits(kb[:, h], ks[h])
-                vq[:, h] = e4m3.quantize_bf16_bits(vb[:, h], vs[h])
+                kq[:, h] = fmt.quantize_bf16_bits(kb[:, h], ks[h])
+                vq[:, h] = fmt.quantize_bf16_bits(vb[:, h], vs[h])
         else:
-            kq = e4m3.quantize(k, ks[None, :, None])
-            vq = e4m3.quantize(v, vs[None, :, None])
+            kq = fmt.quantize(k, ks[None, :, None])
+            vq = fmt.quantize(v, vs[None, :, None])
     else:
         kq = f32_to_bf16_bits_exact(k)
         vq = f32_to_bf16_bits_exact(v)

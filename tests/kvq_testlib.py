@@ -29,7 +29,7 @@ def oracle_cache(case, sentinel=SENTINEL):
     """Logical oracle caches holding every token of the case."""
     cfg = case.cfg
     D, H = cfg.head_dim, cfg.kv_heads
-    dt = np.uint8 if case.cache_dtype == FP8 else np.uint16
+    dt = np.uint16 if case.cache_dtype == BF16 else np.uint8
     fill = sentinel if dt == np.uint8 else (sentinel << 8) | sentinel
     kc = np.full((case.num_blocks, H, 16, D), fill, dt)
     vc = np.full((case.num_blocks, H, D, 16), fill, dt)

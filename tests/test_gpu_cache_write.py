@@ -9,7 +9,7 @@ import torch
 
 import workloads as W
 from oracle import kv_cache, layout
-from oracle.kv_cache import FP8, BF16
+from oracle.kv_cache import FP8, FP8_E5M2, BF16
 from tests.kvq_testlib import SENTINEL, f32, oracle_cache
 
 pytestmark = pytest.mark.gpu
@@ -35,7 +35,7 @@ def _expected(case):
     return layout.to_device_format(kc, vc)
 
 
-@pytest.mark.parametrize("dtype", [FP8, BF16])
+@pytest.mark.parametrize("dtype", [FP8, FP8_E5M2, BF16])
 @pytest.mark.parametrize("D,Hkv,lengths", [(128, 8, [1000, 333]), (64, 8, [17, 16, 1]), (64, 1, [512])])
 def test_cache_write_bit_exact(dtype, D, Hkv, lengths):
     cfg = W.DecodeConfig("t", batch=len(lengths), q_heads=Hkv, kv_heads=Hkv, head_dim=D, context=max(lengths),
@@ -48,7 +48,7 @@ def test_cache_write_bit_exact(dtype, D, Hkv, lengths):
     assert np.array_equal(gv, ev), "V cache bytes differ"
 
 
-@pytest.mark.parametrize("dtype", [FP8, BF16])
+@pytest.mark.parametrize("dtype", [FP8, FP8_E5M2, BF16])
 def test_cache_write_scattered_slots_and_skips(dtype):
     """Slots in random order (slow path), negative slots skipped, ragged T."""
     cfg = W.DecodeConfig("t", batch=1, q_heads=8, kv_heads=8, head_dim=128, context=300)
@@ -80,6 +80,21 @@ def test_cache_write_saturation_and_extremes():
     k = case.k.float()
     k[0, 0, :8] = torch.tensor([1e4, -1e4, 449.0, -448.5, 1e-30, -1e-30, 0.0, -0.0])
     k[1, 0, :4] = torch.tensor([float(2 ** -10), float(3 * 2 ** -11), 464.0, 432.0])
+    case.k = k.bfloat16()
+    case.k_scale = torch.tensor([1.0])
+    gk, gv, st = _run_gpu_write(case)
+    ek, ev = _expected(case)
+    assert np.array_equal(gk, ek) and np.array_equal(gv, ev)
+
+
+def test_cache_write_e5m2_saturation_and_extremes():
+    """E5M2: values beyond 57344 * scale saturate; values below half its
+    smallest subnormal (2^-17) flush to signed zero; ties round to even."""
+    cfg = W.DecodeConfig("t", batch=1, q_heads=1, kv_heads=1, head_dim=64, context=32, calibrated=False)
+    case = W.decode_case(cfg, lengths=[32], cache_dtype=FP8_E5M2)
+    k = case.k.float()
+    k[0, 0, :8] = torch.tensor([1e6, -1e6, 61440.0, -57344.0, 1e-30, -1e-30, 0.0, -0.0])
+    k[1, 0, :6] = torch.tensor([float(2 ** -17), float(3 * 2 ** -17), float(2 ** -16), 1.125, 1.375, 3.0])
     case.k = k.bfloat16()
     case.k_scale = torch.tensor([1.0])
     gk, gv, st = _run_gpu_write(case)

@@ -13,7 +13,7 @@ import torch
 
 import workloads as W
 from oracle import attention
-from oracle.kv_cache import FP8, BF16
+from oracle.kv_cache import FP8, FP8_E5M2, BF16
 from tests.kvq_testlib import assert_close, errors, f32, oracle_cache, oracle_decode, to_device_cache
 
 pytestmark = pytest.mark.gpu
@@ -66,6 +66,15 @@ CASES = {
     "window_bf16_d128": (dict(batch=2, q_heads=32, kv_heads=8, head_dim=128, context=700), [700, 99], BF16, 128),
     "bf16_full_d128": (dict(batch=2, q_heads=32, kv_heads=8, head_dim=128, context=1300), [1300, 64], BF16, -1),
     "bf16_full_d64": (dict(batch=1, q_heads=16, kv_heads=2, head_dim=64, context=900), [900], BF16, -1),
+    "e5m2_llama_small": (dict(batch=2, q_heads=32, kv_heads=8, head_dim=128, context=1000, outliers=4), [1000, 333],
+                         FP8_E5M2, -1),
+    "e5m2_ragged_g4": (dict(batch=5, q_heads=8, kv_heads=2, head_dim=128, context=2049), [1, 16, 17, 250, 2049],
+                       FP8_E5M2, -1),
+    "e5m2_gptoss_d64": (dict(batch=2, q_heads=64, kv_heads=8, head_dim=64, context=1500), [700, 1500], FP8_E5M2, -1),
+    "e5m2_uncalibrated": (dict(batch=1, q_heads=4, kv_heads=1, head_dim=64, context=512, calibrated=False), [512],
+                          FP8_E5M2, -1),
+    "e5m2_window": (dict(batch=4, q_heads=64, kv_heads=8, head_dim=64, context=1000), [50, 128, 129, 1000],
+                    FP8_E5M2, 128),
 }
 
 

@@ -29,6 +29,7 @@ from typing import Optional
 import torch
 
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
 PAGE = 16
 
 
@@ -110,10 +111,11 @@ def apply_outliers(x: torch.Tensor, channels: torch.Tensor, factor: float = 20.0
     return y.to(torch.bfloat16)
 
 
-def calibrate_amax(x: torch.Tensor) -> torch.Tensor:
-    """Caller-side static calibration: per-head amax / 448, float32 [Hkv]."""
+def calibrate_amax(x: torch.Tensor, fmt_max: float = None) -> torch.Tensor:
+    """Caller-side static calibration: per-head amax / (the format's largest
+    value: 448 for E4M3, 57344 for E5M2), float32 [Hkv]."""
     a = x.float().abs().amax(dim=(0, 2))
-    s = (a / E4M3_MAX).to(torch.float32)
+    s = (a / (E4M3_MAX if fmt_max is None else fmt_max)).to(torch.float32)
     return torch.where(s > 0, s, torch.ones_like(s))
 
 
@@ -162,7 +164,7 @@ class DecodeCase:
     v_scale: torch.Tensor
     sm_scale: float
     window: int
-    cache_dtype: str           # "fp8_e4m3" | "bf16"
+    cache_dtype: str           # "fp8_e4m3" | "fp8_e5m2" | "bf16"
 
 
 def decode_case(cfg: DecodeConfig, layer: int = 0, seed_base: int = 0, lengths=None,
@@ -192,8 +194,9 @@ def decode_case(cfg: DecodeConfig, layer: int = 0, seed_base: int = 0, lengths=N
         k = apply_outliers(k, ch)
         v = apply_outliers(v, ch)
     q = randn_bf16((cfg.batch if lengths is None else len(lens), cfg.q_heads, cfg.head_dim), gen)
-    if cfg.calibrated and cache_dtype == "fp8_e4m3" and T > 0:
-        k_scale, v_scale = calibrate_amax(k), calibrate_amax(v)
+    if cfg.calibrated and cache_dtype in ("fp8_e4m3", "fp8_e5m2") and T > 0:
+        fmt_max = E5M2_MAX if cache_dtype == "fp8_e5m2" else E4M3_MAX
+        k_scale, v_scale = calibrate_amax(k, fmt_max), calibrate_amax(v, fmt_max)
     else:
         k_scale = torch.ones(cfg.kv_heads, dtype=torch.float32)
         v_scale = torch.ones(cfg.kv_heads, dtype=torch.float32)
