@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-e5m2", action="store_true")
+    ap.add_argument("--no-per-token", action="store_true")
     ap.add_argument("--layers", type=int, default=32,
                     help="layers per step (fewer only for small profiling runs; the metric uses 32)")
     return ap.parse_args()
@@ -290,12 +291,14 @@ def context_sweep(wl, g_dec, reps=10):
 BF16_LAYERS = 8
 
 
-def format_compare(fp8_sweep, device, cache_dtype, reps=20):
+def format_compare(fp8_sweep, device, cache_dtype, reps=20, per_token=False):
     """The same decode on another cache format over 8 distinct 128K layer
     caches: us per layer vs context, the linear fit, and the slope ratio and
     break-even context against the FP8 E4M3 sweep.  For the BF16 cache (the
     "skip layers" format) this is the vLLM blog's ITL-slope comparison at
-    kernel level; the E5M2 cache reads the same bytes as E4M3."""
+    kernel level; the E5M2 cache reads the same bytes as E4M3.  per_token:
+    dynamic per-token scales (kvq_reshape_and_cache_per_token and the
+    matching decode); the scale bytes count toward GB/s."""
     import torch
     import fp8_kv_cache_reshape_gb300 as kvq
     import workloads as W
@@ -308,15 +311,21 @@ def format_compare(fp8_sweep, device, cache_dtype, reps=20):
         gl = W.generator(502 * 1000 + l, device=device)
         kd, vd = kvq.alloc_kv_cache(nb, HKV, D, cache_dtype=cache_dtype, device=device, fill=0)
         ks = vs = None
-        if esz == 1:  # unit-variance data: per-head scale amax / 57344 taken from one chunk
+        if per_token:
+            ks = kvq.alloc_scale_cache(nb, HKV, device=device, fill=0.0)
+        elif esz == 1:  # unit-variance data: per-head scale amax / 57344 taken from one chunk
             probe = W.randn_bf16((16384, HKV, D), gl, device=device)
             ks = W.calibrate_amax(probe, W.E5M2_MAX).to(device)
             vs = ks.clone()
         for t0 in range(0, CONTEXT, 16384):
             k = W.randn_bf16((16384, HKV, D), gl, device=device)
             v = W.randn_bf16((16384, HKV, D), gl, device=device)
-            kvq.kvq_reshape_and_cache(k, v, slots[t0:t0 + 16384].contiguous(), kd, vd, ks, vs,
-                                      cache_dtype=cache_dtype)
+            if per_token:
+                kvq.kvq_reshape_and_cache_per_token(k, v, slots[t0:t0 + 16384].contiguous(), kd, vd, ks,
+                                                    cache_dtype=cache_dtype)
+            else:
+                kvq.kvq_reshape_and_cache(k, v, slots[t0:t0 + 16384].contiguous(), kd, vd, ks, vs,
+                                          cache_dtype=cache_dtype)
         layers.append(dict(kd=kd, vd=vd, ks=ks, vs=vs, q=W.randn_bf16((1, HQ, D), gl, device=device),
                            out=torch.empty((1, HQ, D), dtype=torch.bfloat16, device=device)))
     btd = bt.to(device)
@@ -325,9 +334,14 @@ def format_compare(fp8_sweep, device, cache_dtype, reps=20):
 
     def run():
         for ly in layers:
-            kvq.kvq_paged_decode_attention(ly["q"], ly["kd"], ly["vd"], ly["ks"], ly["vs"], btd, seq, ly["out"],
-                                           num_blocks=nb, sm_scale=1.0 / math.sqrt(D), cache_dtype=cache_dtype,
-                                           workspace=ws)
+            if per_token:
+                kvq.kvq_paged_decode_attention_per_token(ly["q"], ly["kd"], ly["vd"], ly["ks"], btd, seq, ly["out"],
+                                                         num_blocks=nb, sm_scale=1.0 / math.sqrt(D),
+                                                         cache_dtype=cache_dtype, workspace=ws)
+            else:
+                kvq.kvq_paged_decode_attention(ly["q"], ly["kd"], ly["vd"], ly["ks"], ly["vs"], btd, seq, ly["out"],
+                                               num_blocks=nb, sm_scale=1.0 / math.sqrt(D), cache_dtype=cache_dtype,
+                                               workspace=ws)
 
     gr = capture(run)
     rows = []
@@ -335,7 +349,7 @@ def format_compare(fp8_sweep, device, cache_dtype, reps=20):
         seq.fill_(L)
         gr.replay()
         us = time_graph(gr, reps) * 1e3 / (reps * BF16_LAYERS)
-        kvb = 2 * L * HKV * D * esz
+        kvb = 2 * L * HKV * (D * esz + (4 if per_token else 0))
         rows.append({"context": L, "us_per_layer_decode": round(us, 3), "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1)})
     xs = [r["context"] for r in rows]
     ys = [r["us_per_layer_decode"] for r in rows]
@@ -343,8 +357,9 @@ def format_compare(fp8_sweep, device, cache_dtype, reps=20):
     mx, my = sum(xs) / n, sum(ys) / n
     slope = sum((x - mx) * (y - my) for x, y in zip(xs, ys)) / sum((x - mx) ** 2 for x in xs)
     icpt = my - slope * mx
-    out = {"cache_dtype": cache_dtype, "points": rows, "fit_us_per_token": slope, "fit_intercept_us": round(icpt, 3),
-           "slope_kv_gbs": round(2 * HKV * D * esz / (slope * 1e-6) / 1e9, 1)}
+    out = {"cache_dtype": cache_dtype, "per_token_scales": per_token, "points": rows, "fit_us_per_token": slope,
+           "fit_intercept_us": round(icpt, 3),
+           "slope_kv_gbs": round(2 * HKV * (D * esz + (4 if per_token else 0)) / (slope * 1e-6) / 1e9, 1)}
     if fp8_sweep:
         s8, i8 = fp8_sweep["fit_us_per_token"], fp8_sweep["fit_intercept_us"]
         out["slope_ratio_fp8_over_this"] = round(s8 / slope, 4)
@@ -543,6 +558,7 @@ def ours_arm(args, rank, world, local_rank):
     pf = None if args.no_prefill else prefill_leg(device)
     bf = None if (args.no_sweep or args.no_bf16) else format_compare(sweep, device, "bf16")
     e5 = None if (args.no_sweep or args.no_e5m2) else format_compare(sweep, device, "fp8_e5m2")
+    pt = None if (args.no_sweep or args.no_per_token) else format_compare(sweep, device, "fp8_e4m3", per_token=True)
     e2e_fn, h2d, d2h = e2e_setup(wl)
     g_e2e = capture(e2e_fn)
     e2e_reps = max(3, args.steps)
@@ -577,6 +593,7 @@ def ours_arm(args, rank, world, local_rank):
         "prefill": pf,
         "bf16_compare": bf,
         "e5m2_compare": e5,
+        "per_token_compare": pt,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

@@ -71,6 +71,11 @@ lib.kvq_decode_static_scratch_bytes.argtypes = []
 lib.kvq_paged_decode_attention_static_scratch.restype = _i
 lib.kvq_paged_decode_attention_static_scratch.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
                                                           _i64, _f, _i, _i, _i, _p, _p]
+lib.kvq_reshape_and_cache_per_token.restype = _i
+lib.kvq_reshape_and_cache_per_token.argtypes = [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i64, _i, _p, _p]
+lib.kvq_paged_decode_attention_per_token.restype = _i
+lib.kvq_paged_decode_attention_per_token.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64,
+                                                     _f, _i, _i, _i, _p, _sz, _p, _p]
 lib.kvq_prefill_attention.restype = _i
 lib.kvq_prefill_attention.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
                                       _f, _i, _p, _p]
@@ -145,6 +150,27 @@ def kvq_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_
                                      _ptr(dev_status), _stream(stream)), "kvq_reshape_and_cache")
 
 
+def alloc_scale_cache(num_blocks: int, kv_heads: int, device="cuda", fill=None):
+    """Allocate the interleaved per-token scale cache, float32
+    [num_blocks][Hkv][2][16] ([..][0][t]: K scale, [..][1][t]: V scale)."""
+    shape = (num_blocks, kv_heads, 2, PAGE)
+    if fill is None:
+        return torch.empty(shape, dtype=torch.float32, device=device)
+    return torch.full(shape, fill, dtype=torch.float32, device=device)
+
+
+def kvq_reshape_and_cache_per_token(k, v, slot_mapping, k_cache, v_cache, kv_scale_cache,
+                                    cache_dtype="fp8_e4m3", dev_status=None, stream=None):
+    """Quantize new tokens k, v (bf16 [T][Hkv][D]) with one dynamic scale per
+    token and head; the scales go to the interleaved scale cache."""
+    T, Hkv, D = k.shape
+    num_blocks = k_cache.numel() // (Hkv * PAGE * D)
+    _check(lib.kvq_reshape_and_cache_per_token(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+                                               _ptr(kv_scale_cache), T, Hkv, D, PAGE, num_blocks,
+                                               _dtype_code(cache_dtype), _ptr(dev_status), _stream(stream)),
+           "kvq_reshape_and_cache_per_token")
+
+
 def kvq_quantize_query(q, q8, q_scale, stream=None):
     """q8 = E4M3(q / q_scale), per tensor."""
     _check(lib.kvq_quantize_query(_ptr(q), _ptr(q8), _ptr(q_scale), q.numel(), _stream(stream)),
@@ -184,6 +210,27 @@ def kvq_paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_tabl
                                           max_blocks, num_blocks, float(sm_scale), window, dt, num_splits,
                                           _ptr(workspace), workspace.numel(), _ptr(dev_status),
                                           _stream(stream)), "kvq_paged_decode_attention")
+    return out
+
+
+def kvq_paged_decode_attention_per_token(q, k_cache, v_cache, kv_scale_cache, block_table, seq_lens, out, num_blocks=None, sm_scale=None, window=-1, cache_dtype="fp8_e4m3",
+                                         num_splits=0, workspace=None, dev_status=None, stream=None):
+    """Decode over a cache written by kvq_reshape_and_cache_per_token."""
+    B, Hq, D = q.shape
+    max_blocks = block_table.shape[1]
+    Hkv = k_cache.shape[1]
+    if num_blocks is None:
+        num_blocks = k_cache.shape[0]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    need = kvq_decode_workspace_size(B, Hq, Hkv, D, max_blocks, window, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib.kvq_paged_decode_attention_per_token(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_scale_cache), _ptr(block_table),
+        _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, PAGE, max_blocks, num_blocks, float(sm_scale), window,
+        _dtype_code(cache_dtype), num_splits, _ptr(workspace), workspace.numel(), _ptr(dev_status),
+        _stream(stream)), "kvq_paged_decode_attention_per_token")
     return out
 
 

@@ -46,12 +46,16 @@ KVQ_DEVINL uint4 quant16(const float (&x)[16], float s) {
 }
 
 // FP8 cache write (E4M3, or E5M2 when E5 is set).  grid = (ceil(T / 16), Hkv), block = 128.
-template <int D, bool E5>
+// PT: per-token dynamic scales -- each (token, head) is quantized with
+// amax_d |x| / (format maximum) of its own values, and the K and V scales are
+// stored in the token's slot of the interleaved scale cache
+// [num_blocks][Hkv][2][P] (k_scale / v_scale are unused).
+template <int D, bool E5, bool PT>
 __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
     const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
-    const float* __restrict__ k_scale, const float* __restrict__ v_scale, int T, int Hkv, int64_t num_slots,
-    int* dev_status) {
+    const float* __restrict__ k_scale, const float* __restrict__ v_scale, float* __restrict__ kv_scale_cache,
+    int T, int Hkv, int64_t num_slots, int* dev_status) {
   constexpr int CH = D / 16;          // 16-byte chunks per row
   constexpr int PAGE_BYTES = kPage * D;
   __shared__ __align__(16) uint8_t vt[D * kPage];  // transposed V page
@@ -75,9 +79,64 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
       if (slots[i] >= num_slots) set_status(dev_status, KVQ_DEV_BAD_SLOT);
   }
   __syncthreads();
-  const float sk = k_scale[h], sv = v_scale[h];
+  if constexpr (PT) {
+    // one (token, 16-byte chunk) per thread; a token's CH chunks sit in CH
+    // consecutive lanes, so its maximum is a CH-lane shuffle reduction
+    static_assert(kPage * CH <= 128 && (CH & (CH - 1)) == 0, "one item per thread, CH a power of two");
+    constexpr float kFmtMax = E5 ? 57344.f : 448.f;
+    if (tid < kPage * CH) {  // whole warps: kPage * CH is a multiple of 32
+      const int t = tid / CH, j = tid % CH;
+      const int64_t slot = slots[t];
+      const bool valid = slot >= 0 && slot < num_slots;
+      float xk[16], xv[16];
+      if (valid) {
+        const size_t src = (static_cast<size_t>(g0 + t) * Hkv + h) * D + j * 16;
+        load16_bf16(k + src, xk);
+        load16_bf16(v + src, xv);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) xk[i] = xv[i] = 0.f;
+      }
+      float ak = 0.f, av = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        ak = fmaxf(ak, fabsf(xk[i]));
+        av = fmaxf(av, fabsf(xv[i]));
+      }
+#pragma unroll
+      for (int o = 1; o < CH; o <<= 1) {
+        ak = fmaxf(ak, __shfl_xor_sync(0xffffffffu, ak, o));
+        av = fmaxf(av, __shfl_xor_sync(0xffffffffu, av, o));
+      }
+      const float skt = ak > 0.f ? __fdiv_rn(ak, kFmtMax) : 1.f;  // an all-zero token keeps scale 1
+      const float svt = av > 0.f ? __fdiv_rn(av, kFmtMax) : 1.f;
+      if (valid) {
+        const int64_t blk = slot / kPage;
+        const int off = static_cast<int>(slot % kPage);
+        const size_t page = (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
+        if (j == 0) {
+          const size_t si = (static_cast<size_t>(blk) * Hkv + h) * 2 * kPage + off;
+          kv_scale_cache[si] = skt;
+          kv_scale_cache[si + kPage] = svt;
+        }
+        *reinterpret_cast<uint4*>(k_cache + page + k_chunk_offset(off, j, D)) = quant16<E5>(xk, skt);
+        const uint4 qv = quant16<E5>(xv, svt);
+        const uint8_t* qb = reinterpret_cast<const uint8_t*>(&qv);
+        const int slot_in_row = fp8_v_slot(off);
+        if (fast) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) vt[(j * 16 + i) * kPage + slot_in_row] = qb[i];
+        } else {
+          uint8_t* vp = v_cache + page + slot_in_row;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) vp[(j * 16 + i) * kPage] = qb[i];
+        }
+      }
+    }
+  }
+  const float sk = PT ? 1.f : k_scale[h], sv = PT ? 1.f : v_scale[h];
 
-  for (int u = tid; u < kPage * CH; u += blockDim.x) {
+  for (int u = tid; u < (PT ? 0 : kPage * CH); u += blockDim.x) {
     const int t = u / CH, j = u % CH;
     const int64_t slot = slots[t];
     if (slot < 0 || slot >= num_slots) continue;
@@ -201,13 +260,15 @@ extern "C" kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, cons
     auto kc = static_cast<uint8_t*>(k_cache);
     auto vc = static_cast<uint8_t*>(v_cache);
     auto launch = [&](auto kernel) {
-      kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, k_scale, v_scale, T, Hkv, num_slots, dev_status);
+      kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, k_scale, v_scale, nullptr, T, Hkv, num_slots,
+                                  dev_status);
     };
     const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
     if (D == 128)
-      e5 ? launch(reshape_and_cache_fp8_kernel<128, true>) : launch(reshape_and_cache_fp8_kernel<128, false>);
+      e5 ? launch(reshape_and_cache_fp8_kernel<128, true, false>)
+         : launch(reshape_and_cache_fp8_kernel<128, false, false>);
     else
-      e5 ? launch(reshape_and_cache_fp8_kernel<64, true>) : launch(reshape_and_cache_fp8_kernel<64, false>);
+      e5 ? launch(reshape_and_cache_fp8_kernel<64, true, false>) : launch(reshape_and_cache_fp8_kernel<64, false, false>);
   } else {
     auto kb = static_cast<const uint16_t*>(k);
     auto vb = static_cast<const uint16_t*>(v);
@@ -221,6 +282,43 @@ extern "C" kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, cons
                                                              dev_status);
   }
   return cuda_status(cudaGetLastError(), "reshape_and_cache launch");
+}
+
+extern "C" kvq_status_t kvq_reshape_and_cache_per_token(const void* k, const void* v, const int64_t* slot_mapping,
+                                                        void* k_cache, void* v_cache, float* kv_scale_cache, int T,
+                                                        int Hkv, int D, int P, int64_t num_blocks,
+                                                        kvq_dtype_t cache_dtype, int* dev_status,
+                                                        kvq_stream_t stream) {
+  clear_error();
+  if (T < 0 || Hkv < 1 || num_blocks < 1) return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache_per_token: bad sizes");
+  if (P != kPage) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache_per_token: page size %d (only 16)", P);
+  if (D != 64 && D != 128) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache_per_token: head_dim %d", D);
+  if (cache_dtype != KVQ_DTYPE_FP8_E4M3 && cache_dtype != KVQ_DTYPE_FP8_E5M2)
+    return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache_per_token: cache dtype must be E4M3 or E5M2");
+  if (T == 0) return KVQ_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !kv_scale_cache)
+    return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache_per_token: null pointer");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8) || !aligned(kv_scale_cache, 16))
+    return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache_per_token: misaligned pointer");
+  if (Hkv > 65535) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache_per_token: too many KV heads");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  dim3 grid((T + kPage - 1) / kPage, Hkv);
+  const int64_t num_slots = num_blocks * kPage;
+  auto kb = static_cast<const __nv_bfloat16*>(k);
+  auto vb = static_cast<const __nv_bfloat16*>(v);
+  auto kc = static_cast<uint8_t*>(k_cache);
+  auto vc = static_cast<uint8_t*>(v_cache);
+  auto launch = [&](auto kernel) {
+    kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, nullptr, nullptr, kv_scale_cache, T, Hkv, num_slots,
+                                dev_status);
+  };
+  const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
+  if (D == 128)
+    e5 ? launch(reshape_and_cache_fp8_kernel<128, true, true>) : launch(reshape_and_cache_fp8_kernel<128, false, true>);
+  else
+    e5 ? launch(reshape_and_cache_fp8_kernel<64, true, true>) : launch(reshape_and_cache_fp8_kernel<64, false, true>);
+  return cuda_status(cudaGetLastError(), "reshape_and_cache_per_token launch");
 }
 
 extern "C" kvq_status_t kvq_quantize_query(const void* q, uint8_t* q8, const float* q_scale, int64_t n,

@@ -79,15 +79,24 @@ constexpr int kCtasPerSm = 3;
 // order.  (If two warps shared a slot, a warp could test a slot whose
 // previous fill has not landed yet, and a parity wait would then see the
 // phase before it as complete.)
-template <int D, bool FP8>
+// Per-token scales (PT): each stage also holds the scale records of its two
+// pages after the pages, [K0 V0][K1 V1] (16 floats each, one 128-byte copy
+// per page from the interleaved scale cache).
+constexpr int kScaleBytes = 4 * kPage * 4;
+template <int D, bool FP8, bool PT>
+constexpr int stage_stride() {
+  return Geo<D, FP8>::STAGE + (PT ? kScaleBytes : 0);
+}
+
+template <int D, bool FP8, bool PT = false>
 constexpr int stages_for() {
-  constexpr int n = (81920 / Geo<D, FP8>::STAGE) > 32 ? 32 : (81920 / Geo<D, FP8>::STAGE);
+  constexpr int n = (81920 / stage_stride<D, FP8, PT>()) > 32 ? 32 : (81920 / stage_stride<D, FP8, PT>());
   return (n / kNW) * kNW < kNW ? kNW : (n / kNW) * kNW;
 }
 
-template <int D, bool FP8, int NST>
+template <int D, bool FP8, int NST, bool PT = false>
 constexpr size_t decode_smem_bytes() {
-  return size_t(NST) * Geo<D, FP8>::STAGE + 2 * NST * sizeof(uint64_t) + NST * sizeof(int) + 16;
+  return size_t(NST) * stage_stride<D, FP8, PT>() + 2 * NST * sizeof(uint64_t) + NST * sizeof(int) + 16;
 }
 
 struct ItemRange {
@@ -128,13 +137,18 @@ KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
 constexpr int kPresent0 = 1, kPresent1 = 2, kBad0 = 4, kBad1 = 8;
 
 // E5: the FP8 cache holds E5M2 codes (the MMAs take them as their A operand).
-template <int D, bool FP8, int NW, int NST, bool E5>
+// PT: per-token scales; p.k_scale points to the interleaved float32 scale
+// cache [num_blocks][Hkv][2][P] (K then V) instead of per-head scales (FP8
+// only; p.v_scale is unused).
+template <int D, bool FP8, int NW, int NST, bool E5, bool PT>
 __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const __grid_constant__ DecodeParams p) {
   using G = Geo<D, FP8>;
   static_assert(NST % NW == 0 && NST >= NW, "each ring slot must belong to one consumer warp");
+  static_assert(FP8 || !PT, "per-token scales apply to FP8 caches");
+  constexpr int STRIDE = stage_stride<D, FP8, PT>();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(NST) * G::STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(NST) * STRIDE);
   uint64_t* empty = full + NST;
   int* stage_info = reinterpret_cast<int*>(empty + NST);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(stage_info + NST);
@@ -177,25 +191,45 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
           const int b1 = __shfl_sync(0xffffffffu, blk, (j + 1) & 31);
           const int d1 = __shfl_sync(0xffffffffu, bad, (j + 1) & 31);
           const bool two = j + 1 < cnt;
+          // one stage = pages j, j + 1: a bulk copy per K page and per V page
+          auto issue_pages = [&](int st, uint32_t extra_per_page) {
+            int info = kPresent0 | (d0 ? kBad0 : 0);
+            if (two) info |= kPresent1 | (d1 ? kBad1 : 0);
+            stage_info[st] = info;
+            mbar_arrive_expect_tx(&full[st], (two ? 2u : 1u) * (2u * G::PAGE + extra_per_page));
+            uint8_t* sk = stages + size_t(st) * STRIDE;  // [K0][K1][V0][V1]
+            const size_t pg0 = (static_cast<size_t>(b0) * p.Hkv + r.kvh) * G::PAGE;
+            bulk_g2s(sk, p.k_cache + pg0, G::PAGE, &full[st], pol);
+            bulk_g2s(sk + 2 * G::PAGE, p.v_cache + pg0, G::PAGE, &full[st], pol);
+            if (two) {
+              const size_t pg1 = (static_cast<size_t>(b1) * p.Hkv + r.kvh) * G::PAGE;
+              bulk_g2s(sk + G::PAGE, p.k_cache + pg1, G::PAGE, &full[st], pol);
+              bulk_g2s(sk + 3 * G::PAGE, p.v_cache + pg1, G::PAGE, &full[st], pol);
+            }
+          };
           int ok = 1;
-          if (lane == 0) {
+          if constexpr (PT) {
+            if (lane == 0) {
+              const int st = it % NST;
+              if (*abort_flag || !mbar_wait(&empty[st], ((it / NST) & 1) ^ 1, abort_flag)) {
+                ok = 0;
+              } else {
+                // the pages, then each page's scale record (16 K, 16 V) after them
+                constexpr uint32_t REC = 2 * kPage * 4;
+                issue_pages(st, REC);
+                uint8_t* scl = stages + size_t(st) * STRIDE + 4 * G::PAGE;  // [K0 V0][K1 V1]
+                bulk_g2s(scl, p.k_scale + (static_cast<size_t>(b0) * p.Hkv + r.kvh) * 2 * kPage, REC, &full[st], pol);
+                if (two)
+                  bulk_g2s(scl + REC, p.k_scale + (static_cast<size_t>(b1) * p.Hkv + r.kvh) * 2 * kPage, REC,
+                           &full[st], pol);
+              }
+            }
+          } else if (lane == 0) {
             const int st = it % NST;
             if (*abort_flag || !mbar_wait(&empty[st], ((it / NST) & 1) ^ 1, abort_flag)) {
               ok = 0;
             } else {
-              int info = kPresent0 | (d0 ? kBad0 : 0);
-              if (two) info |= kPresent1 | (d1 ? kBad1 : 0);
-              stage_info[st] = info;
-              mbar_arrive_expect_tx(&full[st], (two ? 2u : 1u) * 2u * G::PAGE);
-              uint8_t* sk = stages + size_t(st) * G::STAGE;  // [K0][K1][V0][V1]
-              const size_t pg0 = (static_cast<size_t>(b0) * p.Hkv + r.kvh) * G::PAGE;
-              bulk_g2s(sk, p.k_cache + pg0, G::PAGE, &full[st], pol);
-              bulk_g2s(sk + 2 * G::PAGE, p.v_cache + pg0, G::PAGE, &full[st], pol);
-              if (two) {
-                const size_t pg1 = (static_cast<size_t>(b1) * p.Hkv + r.kvh) * G::PAGE;
-                bulk_g2s(sk + G::PAGE, p.k_cache + pg1, G::PAGE, &full[st], pol);
-                bulk_g2s(sk + 3 * G::PAGE, p.v_cache + pg1, G::PAGE, &full[st], pol);
-              }
+              issue_pages(st, 0u);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -286,7 +320,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
           qh[w] = h01 | (h23 << 16);
           ql[w] = f32x2_to_e4m3x2(y0 - d01.x, y1 - d01.y) | (f32x2_to_e4m3x2(y2 - d23.x, y3 - d23.y) << 16);
         }
-        const float cf = __fmul_rn(__fmul_rn(p.k_scale[rg.kvh], p.sm_scale), kLog2e);
+        // per-head K scale folded in here; per-token K scales multiply each score later
+        const float cf = PT ? __fmul_rn(p.sm_scale, kLog2e) : __fmul_rn(__fmul_rn(p.k_scale[rg.kvh], p.sm_scale), kLog2e);
         // 1/sigma of heads 2c and 2c + 1 lives in lanes 8c and 8c + 4
         coef0 = cf * __shfl_sync(0xffffffffu, inv_sigma, 8 * c);
         coef1 = cf * __shfl_sync(0xffffffffu, inv_sigma, 8 * c + 4);
@@ -320,7 +355,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
         }
         break;
       }
-      const uint32_t kb = smem_u32(stages + size_t(st) * G::STAGE);
+      const uint32_t kb = smem_u32(stages + size_t(st) * STRIDE);
       const uint32_t vb = kb + 2 * G::PAGE;
       const int info = stage_info[st];
       const bool two = (info & kPresent1) != 0;
@@ -360,8 +395,21 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
       };
 
       if constexpr (FP8) {
+        // per-token scales (PT) of this lane's tokens r and r + 8 of both pages
+        float sk00 = 1.f, sk01 = 1.f, sk10 = 1.f, sk11 = 1.f, sv00 = 0.f, sv01 = 0.f, sv10 = 0.f, sv11 = 0.f;
+        if constexpr (PT) {
+          const float* scl = reinterpret_cast<const float*>(stages + size_t(st) * STRIDE + 4 * G::PAGE);
+          sk00 = scl[r];  // [K0 V0][K1 V1]
+          sk01 = scl[r + 8];
+          sv00 = scl[kPage + r];
+          sv01 = scl[kPage + r + 8];
+          sk10 = scl[2 * kPage + r];
+          sk11 = scl[2 * kPage + r + 8];
+          sv10 = scl[3 * kPage + r];
+          sv11 = scl[3 * kPage + r + 8];
+        }
         // ---- S^T = K Q^T, E4M3 MMA, q as hi + lo (two independent chains) ----
-        auto qk = [&](uint32_t kp, float (&s)[4]) {
+        auto qk = [&](uint32_t kp, float (&s)[4], float ska, float skb) {  // ska, skb: tokens r, r + 8
           float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk) {
@@ -374,9 +422,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
           s[1] = (a[1] + b[1]) * coef1;
           s[2] = (a[2] + b[2]) * coef0;
           s[3] = (a[3] + b[3]) * coef1;
+          if constexpr (PT) {
+            s[0] *= ska;
+            s[1] *= ska;
+            s[2] *= skb;
+            s[3] *= skb;
+          }
         };
-        qk(kb, s0);
-        if (two) qk(kb + G::PAGE, s1);
+        qk(kb, s0, sk00, sk01);
+        if (two) qk(kb + G::PAGE, s1, sk10, sk11);
         else s1[0] = s1[1] = s1[2] = s1[3] = NEG_INF;
         // ---- V fragments to registers, then release the ring slot ----
         uint32_t va[G::MT][4];
@@ -407,9 +461,57 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
 #pragma unroll
           for (int mt = 0; mt < G::MT; ++mt) va[mt][2] = va[mt][3] = 0u;
         }
+        // PT: V scales enter P as weights sv / c with c the stage's largest live
+        // V scale (so P stays in E4M3's range); the stage's P.V is scaled by c
+        float cst = 1.f, w00 = 1.f, w01 = 1.f, w10 = 1.f, w11 = 1.f;
+        if constexpr (PT) {
+          if (!two) sv10 = sv11 = 0.f;
+          if (edge) {
+            if (!live(0, r)) sv00 = 0.f;
+            if (!live(0, r + 8)) sv01 = 0.f;
+            if (!live(1, r)) sv10 = 0.f;
+            if (!live(1, r + 8)) sv11 = 0.f;
+          }
+          cst = fmaxf(fmaxf(sv00, sv01), fmaxf(sv10, sv11));
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) cst = fmaxf(cst, __shfl_xor_sync(0xffffffffu, cst, o));
+          const float rc = cst > 0.f ? 1.f / cst : 0.f;
+          w00 = sv00 * rc;
+          w01 = sv01 * rc;
+          w10 = sv10 * rc;
+          w11 = sv11 * rc;
+        }
         softmax();
-        // ---- P^T fragments: transpose f16 pairs, then two E4M3 terms ----
-        auto pterms = [&](float x0, float x1, float x2, float x3, uint32_t& hi, uint32_t& lo) {
+        float g0 = 1.f, g1 = 1.f;  // PT: factor of the stage's P.V of heads 2c, 2c + 1
+        if constexpr (PT) {  // l above summed the unweighted p
+          p00 *= w00; p01 *= w00; p02 *= w01; p03 *= w01;
+          p10 *= w10; p11 *= w10; p12 *= w11; p13 *= w11;
+          // Weights below 1 push probabilities toward E4M3's lower end, where the
+          // two-term split loses them.  Per head, a power of two f moves the stage's
+          // largest weighted probability into [128, 256); P.V is then scaled by c / f.
+          float pm0 = fmaxf(fmaxf(p00, p02), fmaxf(p10, p12));
+          float pm1 = fmaxf(fmaxf(p01, p03), fmaxf(p11, p13));
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            pm0 = fmaxf(pm0, __shfl_xor_sync(0xffffffffu, pm0, o));
+            pm1 = fmaxf(pm1, __shfl_xor_sync(0xffffffffu, pm1, o));
+          }
+          auto pow2_exp = [](float x) {  // e with 2^e <= x < 2^(e+1), clamped to [-119, 127]
+            const int e = x > 0.f ? static_cast<int>((__float_as_uint(x) >> 23) & 0xFF) - 127 : 7;
+            return e < -119 ? -119 : e;
+          };
+          const int e0 = pow2_exp(pm0), e1 = pow2_exp(pm1);
+          const float f0 = __uint_as_float(static_cast<uint32_t>(127 + 7 - e0) << 23);  // 2^(7 - e0)
+          const float f1 = __uint_as_float(static_cast<uint32_t>(127 + 7 - e1) << 23);
+          g0 = cst * __uint_as_float(static_cast<uint32_t>(127 - 7 + e0) << 23);  // c / f0, exact
+          g1 = cst * __uint_as_float(static_cast<uint32_t>(127 - 7 + e1) << 23);
+          p00 *= f0; p01 *= f1; p02 *= f0; p03 *= f1;
+          p10 *= f0; p11 *= f1; p12 *= f0; p13 *= f1;
+        }
+        // ---- P^T fragments: transpose f16 pairs, then two E4M3 terms (three with
+        // per-token weights, which make even the largest probability inexact in
+        // E4M3); each residual is an exact f16 difference of nearby values ----
+        auto pterms = [&](float x0, float x1, float x2, float x3, uint32_t& hi, uint32_t& lo, uint32_t& lo2) {
           const uint32_t t0 = movmatrix_t(pack_f16x2(x0, x1));  // tokens 2c, 2c+1 of head r
           const uint32_t t1 = movmatrix_t(pack_f16x2(x2, x3));  // tokens 2c+8, 2c+9
           const uint32_t h0 = f16x2_to_e4m3x2(t0), h1 = f16x2_to_e4m3x2(t1);
@@ -418,22 +520,39 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
           const uint32_t d1 = e4m3x2_to_f16x2(static_cast<uint16_t>(h1));
           const __half2 r0 = __hsub2(*reinterpret_cast<const __half2*>(&t0), *reinterpret_cast<const __half2*>(&d0));
           const __half2 r1 = __hsub2(*reinterpret_cast<const __half2*>(&t1), *reinterpret_cast<const __half2*>(&d1));
-          lo = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&r0)) |
-               (f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&r1)) << 16);
+          const uint32_t l0 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&r0));
+          const uint32_t l1 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&r1));
+          lo = l0 | (l1 << 16);
+          if constexpr (PT) {
+            const uint32_t e0 = e4m3x2_to_f16x2(static_cast<uint16_t>(l0));
+            const uint32_t e1 = e4m3x2_to_f16x2(static_cast<uint16_t>(l1));
+            const __half2 u0 = __hsub2(r0, *reinterpret_cast<const __half2*>(&e0));
+            const __half2 u1 = __hsub2(r1, *reinterpret_cast<const __half2*>(&e1));
+            lo2 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&u0)) |
+                  (f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&u1)) << 16);
+          }
         };
-        uint32_t ph0, pl0, ph1 = 0u, pl1 = 0u;
-        pterms(p00, p01, p02, p03, ph0, pl0);
-        pterms(p10, p11, p12, p13, ph1, pl1);
+        uint32_t ph0, pl0, pt0 = 0u, ph1 = 0u, pl1 = 0u, pt1 = 0u;
+        pterms(p00, p01, p02, p03, ph0, pl0, pt0);
+        pterms(p10, p11, p12, p13, ph1, pl1, pt1);
         // ---- O^T += V^T P^T (32 token slots per MMA), fresh FP32 per stage ----
 #pragma unroll
         for (int mt = 0; mt < G::MT; ++mt) {
           float t[4] = {0.f, 0.f, 0.f, 0.f};
           mma_fp8<E5>(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], ph0, ph1, t);
           mma_fp8<E5>(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], pl0, pl1, t);
-          O[mt][0] = fmaf(O[mt][0], al0, t[0]);
-          O[mt][1] = fmaf(O[mt][1], al1, t[1]);
-          O[mt][2] = fmaf(O[mt][2], al0, t[2]);
-          O[mt][3] = fmaf(O[mt][3], al1, t[3]);
+          if constexpr (PT) mma_fp8<E5>(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], pt0, pt1, t);
+          if constexpr (PT) {
+            O[mt][0] = fmaf(t[0], g0, O[mt][0] * al0);
+            O[mt][1] = fmaf(t[1], g1, O[mt][1] * al1);
+            O[mt][2] = fmaf(t[2], g0, O[mt][2] * al0);
+            O[mt][3] = fmaf(t[3], g1, O[mt][3] * al1);
+          } else {
+            O[mt][0] = fmaf(O[mt][0], al0, t[0]);
+            O[mt][1] = fmaf(O[mt][1], al1, t[1]);
+            O[mt][2] = fmaf(O[mt][2], al0, t[2]);
+            O[mt][3] = fmaf(O[mt][3], al1, t[3]);
+          }
         }
       } else {
         // ---- BF16 cache: S^T via bf16 MMA straight from shared memory ----
@@ -523,7 +642,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
       l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
     }
     {
-      const float vs = FP8 ? p.v_scale[rg.kvh] : 1.f;
+      const float vs = (FP8 && !PT) ? p.v_scale[rg.kvh] : 1.f;  // PT: V scales are inside O
       const size_t row0 = static_cast<size_t>(rg.b) * p.Hq + rg.kvh * p.g;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -624,11 +743,11 @@ void split_plan(int B, int Hkv, int P, int max_blocks, int window, int num_split
   *pps_out = pps;
 }
 
-template <int D, bool FP8, bool E5 = false>
+template <int D, bool FP8, bool E5 = false, bool PT = false>
 kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream_t s) {
-  constexpr int NST = stages_for<D, FP8>();
-  constexpr size_t smem = decode_smem_bytes<D, FP8, NST>();
-  auto kern = decode_partial_kernel<D, FP8, kNW, NST, E5>;
+  constexpr int NST = stages_for<D, FP8, PT>();
+  constexpr size_t smem = decode_smem_bytes<D, FP8, NST, PT>();
+  auto kern = decode_partial_kernel<D, FP8, kNW, NST, E5, PT>;
   static int configured_mask = 0;  // devices whose attribute is set
   int dev = 0;
   cudaGetDevice(&dev);
@@ -681,14 +800,15 @@ extern "C" size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P
   return o_bytes + ((rows * sizeof(float) + 15) / 16) * 16;
 }
 
-extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
-                                                   const float* k_scale, const float* v_scale,
-                                                   const int32_t* block_table, const int32_t* seq_lens, void* out,
-                                                   int B, int Hq, int Hkv, int D, int P, int max_blocks,
-                                                   int64_t num_blocks, float sm_scale, int window,
-                                                   kvq_dtype_t cache_dtype, int num_splits, void* workspace,
-                                                   size_t workspace_bytes, int* dev_status, kvq_stream_t stream) {
-  clear_error();
+namespace {
+
+// Shared by the per-head and the per-token entry points.  per_token: k_scale
+// (= v_scale) is the interleaved scale cache [num_blocks][Hkv][2][P].
+kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                          const float* v_scale, const int32_t* block_table, const int32_t* seq_lens, void* out, int B,
+                          int Hq, int Hkv, int D, int P, int max_blocks, int64_t num_blocks, float sm_scale, int window,
+                          kvq_dtype_t cache_dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                          int* dev_status, kvq_stream_t stream, bool per_token) {
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0)
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: bad sizes");
   if (Hq % Hkv != 0) return fail(KVQ_ERR_INVALID_ARG, "paged_decode: Hq %% Hkv != 0");
@@ -704,6 +824,9 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: null pointer");
   if (fp8 && (!k_scale || !v_scale))
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: FP8 needs k_scale and v_scale");
+  if (per_token && !fp8) return fail(KVQ_ERR_INVALID_ARG, "paged_decode: per-token scales need an FP8 cache");
+  if (per_token && (!aligned(k_scale, 16) || !aligned(v_scale, 16)))
+    return fail(KVQ_ERR_INVALID_ARG, "paged_decode: scale caches must be 16-byte aligned");
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(workspace, 16) ||
       !aligned(out, 4))
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: misaligned pointer");
@@ -740,10 +863,41 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
   prm.dev_status = dev_status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto o = static_cast<__nv_bfloat16*>(out);
-  if (cache_dtype == KVQ_DTYPE_FP8_E5M2)
-    return D == 128 ? launch_decode<128, true, true>(prm, o, s) : launch_decode<64, true, true>(prm, o, s);
+  const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
+  if (per_token) {
+    if (D == 128)
+      return e5 ? launch_decode<128, true, true, true>(prm, o, s) : launch_decode<128, true, false, true>(prm, o, s);
+    return e5 ? launch_decode<64, true, true, true>(prm, o, s) : launch_decode<64, true, false, true>(prm, o, s);
+  }
+  if (e5) return D == 128 ? launch_decode<128, true, true>(prm, o, s) : launch_decode<64, true, true>(prm, o, s);
   if (D == 128) return fp8 ? launch_decode<128, true>(prm, o, s) : launch_decode<128, false>(prm, o, s);
   return fp8 ? launch_decode<64, true>(prm, o, s) : launch_decode<64, false>(prm, o, s);
+}
+
+}  // namespace
+
+extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                                   const float* k_scale, const float* v_scale,
+                                                   const int32_t* block_table, const int32_t* seq_lens, void* out,
+                                                   int B, int Hq, int Hkv, int D, int P, int max_blocks,
+                                                   int64_t num_blocks, float sm_scale, int window,
+                                                   kvq_dtype_t cache_dtype, int num_splits, void* workspace,
+                                                   size_t workspace_bytes, int* dev_status, kvq_stream_t stream) {
+  clear_error();
+  return paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, B, Hq, Hkv, D, P,
+                      max_blocks, num_blocks, sm_scale, window, cache_dtype, num_splits, workspace, workspace_bytes,
+                      dev_status, stream, false);
+}
+
+extern "C" kvq_status_t kvq_paged_decode_attention_per_token(
+    const void* q, const void* k_cache, const void* v_cache, const float* kv_scale_cache, const int32_t* block_table,
+    const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int D, int P, int max_blocks, int64_t num_blocks,
+    float sm_scale, int window, kvq_dtype_t cache_dtype, int num_splits, void* workspace, size_t workspace_bytes,
+    int* dev_status, kvq_stream_t stream) {
+  clear_error();
+  return paged_decode(q, k_cache, v_cache, kv_scale_cache, kv_scale_cache, block_table, seq_lens, out, B, Hq, Hkv, D, P,
+                      max_blocks, num_blocks, sm_scale, window, cache_dtype, num_splits, workspace, workspace_bytes,
+                      dev_status, stream, true);
 }
 
 // ---------------------------------------------------------------------------

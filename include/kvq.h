@@ -208,6 +208,61 @@ kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_cache, cons
                                         int* dev_status, kvq_stream_t stream);
 
 /*
+ * kvq_reshape_and_cache_per_token -- quantize new K/V tokens into the paged
+ * cache with a dynamic scale per token and KV head.
+ * [FP8KV] "Dynamic or static scale": with per-token scales each token's
+ * largest value lands on the format's maximum (scales 3.2/448 and 180/448 in
+ * the worked example), at the cost of one maximum per token; [GTNT] section
+ * 2.2: per-token dynamic quantization computes a scale for every new token.
+ *
+ *  As kvq_reshape_and_cache (FP8 E4M3 or E5M2 only), plus:
+ *  kv_scale_cache  float32 [num_blocks][Hkv][2][P], 16-byte aligned
+ *                  (written): [block][h][0][offset] is the K scale and
+ *                  [block][h][1][offset] the V scale of the token in that
+ *                  slot, s = fl32(amax_d |x_d| / M) with M = 448 (E4M3) or
+ *                  57344 (E5M2); a token whose values are all zero gets s = 1.
+ *                  (K and V scales of a page share one 128-byte record, which
+ *                  decode fetches with one copy.)
+ *  Each element is then code = encode(fl32(x / s)) as in
+ *  kvq_reshape_and_cache.  Only the given slots' bytes and scales are
+ *  written.
+ */
+kvq_status_t kvq_reshape_and_cache_per_token(const void* k, const void* v, const int64_t* slot_mapping,
+                                             void* k_cache, void* v_cache, float* kv_scale_cache,
+                                             int T, int Hkv, int D, int P, int64_t num_blocks,
+                                             kvq_dtype_t cache_dtype, int* dev_status, kvq_stream_t stream);
+
+/*
+ * kvq_paged_decode_attention_per_token -- kvq_paged_decode_attention over a
+ * cache written by kvq_reshape_and_cache_per_token (same citations; the
+ * per-token scales as above).
+ *
+ *  kv_scale_cache  the scale cache of that call (read); every other argument
+ *                  as for kvq_paged_decode_attention, with an FP8 (E4M3 or
+ *                  E5M2) cache.
+ *  Declared rounding: the query terms and the per-head score coefficient as
+ *  for kvq_paged_decode_attention with c = fl32(sm_scale * log2(e)); each
+ *  score is then multiplied by its token's K scale.  V scales enter the
+ *  probabilities: per stage of 32 tokens, with c the stage's largest V scale
+ *  of a live token and f a power of two per query head that moves the
+ *  stage's largest weighted probability into [128, 256), P.V runs on
+ *  p_j * (sv_j / c) * f, rounded to float16 and split into three E4M3 terms
+ *  (about 11 significant bits: the weights make even the largest
+ *  probability inexact in E4M3), and the stage's result is multiplied by
+ *  c / f before it is added to the running FP32 sum.  The row sum uses the
+ *  unweighted p_j.
+ *  Workspace: kvq_decode_workspace_size() of the same arguments.
+ */
+kvq_status_t kvq_paged_decode_attention_per_token(const void* q, const void* k_cache, const void* v_cache,
+                                                  const float* kv_scale_cache,
+                                                  const int32_t* block_table, const int32_t* seq_lens,
+                                                  void* out, int B, int Hq, int Hkv, int D, int P,
+                                                  int max_blocks, int64_t num_blocks, float sm_scale,
+                                                  int window, kvq_dtype_t cache_dtype, int num_splits,
+                                                  void* workspace, size_t workspace_bytes,
+                                                  int* dev_status, kvq_stream_t stream);
+
+/*
  * kvq_paged_decode_attention_static_scratch -- kvq_paged_decode_attention
  * for callers that cannot allocate device memory where they run decode (a
  * memory-pool policy that forbids new allocations, a real-time loop, a plugin

@@ -64,7 +64,7 @@ import math
 import numpy as np
 
 from . import e4m3
-from .kv_cache import FP8, BF16, FP8_TYPES, bf16_bits_to_f32, codec, gather_tokens
+from .kv_cache import FP8, BF16, FP8_TYPES, bf16_bits_to_f32, codec, gather_scales, gather_tokens
 
 LOG2E_F32 = np.float32(1.4426950408889634)
 
@@ -166,6 +166,52 @@ def paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                     s = (k_codes * sk) @ qh * float(np.float32(sm_scale))
                     p, m, l = _softmax_row(s)
                     out[b, h] = (p @ (v_codes * sv)) / l
+                    lse[b, h] = m + math.log(l)
+    return out, lse
+
+
+def paged_decode_per_token(q, k_cache, v_cache, kv_scale_cache, block_table, seq_lens,
+                           sm_scale, window=-1, cache_dtype=FP8, mode="mirror"):
+    """paged_decode over a cache written with per-token dynamic scales
+    (kv_cache.reshape_and_cache_per_token; kv_scale_cache [nb][Hkv][2][P]):
+    token j dequantizes as decode(k8_j) * sk_j and decode(v8_j) * sv_j.
+
+    mirror: the query terms as in paged_decode; s2_j = (sum_d (hi + lo)_d
+    k8_jd) / sigma * c_j with c_j = fl32(fl32(sm_scale * log2(e)) * sk_j);
+    o = sum_j 2^(s2_j - m) sv_j v8_j / sum_j 2^(s2_j - m).
+    pure: exact dequantized values, natural exponentials.
+    Returns (out float64 [B][Hq][D], lse float64 [B][Hq])."""
+    q = np.asarray(q, dtype=np.float32)
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    g = Hq // Hkv
+    fmt = codec(cache_dtype)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    lse = np.full((B, Hq), -np.inf, dtype=np.float64)
+    c0 = np.float32(_f32(sm_scale) * LOG2E_F32)
+    for b in range(B):
+        pos = decode_positions(int(seq_lens[b]), window)
+        if pos.size == 0:
+            continue
+        for kv in range(Hkv):
+            kk, vv = gather_tokens(k_cache, v_cache, block_table[b], pos, kv)
+            k_codes, v_codes = fmt.decode(kk), fmt.decode(vv)
+            sk = gather_scales(kv_scale_cache[:, :, 0], block_table[b], pos, kv).astype(np.float32)
+            sv = gather_scales(kv_scale_cache[:, :, 1], block_table[b], pos, kv).astype(np.float64)
+            for h in range(kv * g, (kv + 1) * g):
+                if mode == "mirror":
+                    c = (c0 * sk).astype(np.float32).astype(np.float64)
+                    s2 = (k_codes @ split_query_e4m3(q[b, h])) * c
+                    m2 = np.max(s2)
+                    p = np.exp2(s2 - m2)
+                    l = p.sum()
+                    out[b, h] = (p * sv) @ v_codes / l
+                    lse[b, h] = (m2 + math.log2(l)) * math.log(2.0)
+                else:
+                    s = (k_codes * sk.astype(np.float64)[:, None]) @ q[b, h].astype(np.float64)
+                    s = s * float(np.float32(sm_scale))
+                    p, m, l = _softmax_row(s)
+                    out[b, h] = (p @ (v_codes * sv[:, None])) / l
                     lse[b, h] = m + math.log(l)
     return out, lse
 

@@ -124,6 +124,61 @@ def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
     return k_cache, v_cache, bad
 
 
+# ------------------------------------------------- per-token dynamic scales ---
+def fmt_max(cache_dtype):
+    """Largest finite value of an FP8 cache format (448 or 57344)."""
+    return codec(cache_dtype).E4M3_MAX if cache_dtype == FP8 else codec(cache_dtype).E5M2_MAX
+
+
+def per_token_scales(x, cache_dtype=FP8):
+    """Dynamic scale of every token and head: s[t][h] = fl32(amax_d |x[t][h][d]|
+    / fmt_max), so each token's largest element maps onto the format's largest
+    value ("FP8 and KV cache", "Dynamic or static scale": per-token scales
+    3.2/448 and 180/448; "FP8 quantization and long-context inference",
+    section 2.2: every new token gets its own scale).  A token whose values
+    are all zero gets scale 1.0 (reading: the pages do not cover it)."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x), axis=-1).astype(np.float32)
+    s = (amax / np.float32(fmt_max(cache_dtype))).astype(np.float32)
+    return np.where(amax > 0, s, np.float32(1.0)).astype(np.float32)
+
+
+def reshape_and_cache_per_token(k, v, slot_mapping, k_cache, v_cache, kv_scale_cache, cache_dtype=FP8):
+    """Cache write with per-token dynamic scales, in place.
+
+    As reshape_and_cache, but each (token, head) is quantized with its own
+    scale from per_token_scales(); the K and V scales are stored at the
+    token's slot of kv_scale_cache (float32 [num_blocks][Hkv][2][P]:
+    [..][0][off] K, [..][1][off] V -- the library's interleaved layout).
+    Returns (k_cache, v_cache, kv_scale_cache, bad_slot_seen)."""
+    k = np.asarray(k, dtype=np.float32)
+    v = np.asarray(v, dtype=np.float32)
+    fmt = codec(cache_dtype)
+    num_blocks, _, P, _ = k_cache.shape
+    slots = np.asarray(slot_mapping, dtype=np.int64)
+    sk = per_token_scales(k, cache_dtype)  # [T][Hkv]
+    sv = per_token_scales(v, cache_dtype)
+    kq = fmt.quantize(k, sk[:, :, None])
+    vq = fmt.quantize(v, sv[:, :, None])
+    bad = bool(np.any(slots >= num_blocks * P))
+    keep = (slots >= 0) & (slots < num_blocks * P)
+    blk, off = slots[keep] // P, slots[keep] % P
+    k_cache[blk, :, off, :] = kq[keep]
+    v_cache[blk, :, :, off] = vq[keep]
+    kv_scale_cache[blk, :, 0, off] = sk[keep]
+    kv_scale_cache[blk, :, 1, off] = sv[keep]
+    return k_cache, v_cache, kv_scale_cache, bad
+
+
+def gather_scales(scale_cache, block_table_row, positions, kv_head):
+    """Per-token scales ([n]) of the given positions of one sequence and head
+    from one plane [num_blocks][Hkv][P] of the scale cache."""
+    P = scale_cache.shape[2]
+    pos = np.asarray(positions, dtype=np.int64)
+    blocks = np.asarray(block_table_row, dtype=np.int64)[pos // P]
+    return scale_cache[blocks, kv_head, pos % P]
+
+
 def quantize_query(q, q_scale):
     """q8 = encode(fl32(q / s_q)) with one per-tensor scale s_q."""
     return e4m3.quantize(q, np.float32(q_scale))
