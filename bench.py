@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--no-bf16", action="store_true")
     ap.add_argument("--no-e5m2", action="store_true")
     ap.add_argument("--no-per-token", action="store_true")
+    ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--layers", type=int, default=32,
                     help="layers per step (fewer only for small profiling runs; the metric uses 32)")
     return ap.parse_args()
@@ -291,14 +292,15 @@ def context_sweep(wl, g_dec, reps=10):
 BF16_LAYERS = 8
 
 
-def format_compare(fp8_sweep, device, cache_dtype, reps=20, per_token=False):
+def format_compare(fp8_sweep, device, cache_dtype, reps=20, per_token=False, accumulation=None):
     """The same decode on another cache format over 8 distinct 128K layer
     caches: us per layer vs context, the linear fit, and the slope ratio and
     break-even context against the FP8 E4M3 sweep.  For the BF16 cache (the
     "skip layers" format) this is the vLLM blog's ITL-slope comparison at
     kernel level; the E5M2 cache reads the same bytes as E4M3.  per_token:
     dynamic per-token scales (kvq_reshape_and_cache_per_token and the
-    matching decode); the scale bytes count toward GB/s."""
+    matching decode); the scale bytes count toward GB/s.  accumulation:
+    "single_level" for the accumulation ablation."""
     import torch
     import fp8_kv_cache_reshape_gb300 as kvq
     import workloads as W
@@ -313,9 +315,9 @@ def format_compare(fp8_sweep, device, cache_dtype, reps=20, per_token=False):
         ks = vs = None
         if per_token:
             ks = kvq.alloc_scale_cache(nb, HKV, device=device, fill=0.0)
-        elif esz == 1:  # unit-variance data: per-head scale amax / 57344 taken from one chunk
+        elif esz == 1:  # unit-variance data: per-head scale amax / M taken from one chunk
             probe = W.randn_bf16((16384, HKV, D), gl, device=device)
-            ks = W.calibrate_amax(probe, W.E5M2_MAX).to(device)
+            ks = W.calibrate_amax(probe, W.E5M2_MAX if cache_dtype == "fp8_e5m2" else W.E4M3_MAX).to(device)
             vs = ks.clone()
         for t0 in range(0, CONTEXT, 16384):
             k = W.randn_bf16((16384, HKV, D), gl, device=device)
@@ -341,7 +343,7 @@ def format_compare(fp8_sweep, device, cache_dtype, reps=20, per_token=False):
             else:
                 kvq.kvq_paged_decode_attention(ly["q"], ly["kd"], ly["vd"], ly["ks"], ly["vs"], btd, seq, ly["out"],
                                                num_blocks=nb, sm_scale=1.0 / math.sqrt(D), cache_dtype=cache_dtype,
-                                               workspace=ws)
+                                               workspace=ws, accumulation=accumulation)
 
     gr = capture(run)
     rows = []
@@ -357,7 +359,8 @@ def format_compare(fp8_sweep, device, cache_dtype, reps=20, per_token=False):
     mx, my = sum(xs) / n, sum(ys) / n
     slope = sum((x - mx) * (y - my) for x, y in zip(xs, ys)) / sum((x - mx) ** 2 for x in xs)
     icpt = my - slope * mx
-    out = {"cache_dtype": cache_dtype, "per_token_scales": per_token, "points": rows, "fit_us_per_token": slope,
+    out = {"cache_dtype": cache_dtype, "per_token_scales": per_token, "accumulation": accumulation or "two_level",
+           "points": rows, "fit_us_per_token": slope,
            "fit_intercept_us": round(icpt, 3),
            "slope_kv_gbs": round(2 * HKV * (D * esz + (4 if per_token else 0)) / (slope * 1e-6) / 1e9, 1)}
     if fp8_sweep:
@@ -378,7 +381,7 @@ def prefill_flops(new=PF_NEW, cached=PF_CACHED, hq=HQ, d=D):
     return pairs * hq * 4 * d
 
 
-def prefill_leg(device, reps=10):
+def prefill_leg(device, reps=10, accumulation=None):
     """Chunked causal prefill of 4,096 new tokens on 28,672 cached FP8
     tokens (32/8 heads, head_dim 128): TFLOP/s of kvq_prefill_attention."""
     import torch
@@ -406,7 +409,7 @@ def prefill_leg(device, reps=10):
 
     def call():
         kvq.kvq_prefill_attention(q8, qs, kd, vd, ks, vs, btd, cu, sl, out, max_q_tokens=PF_NEW,
-                                  sm_scale=1.0 / math.sqrt(D), dev_status=st)
+                                  sm_scale=1.0 / math.sqrt(D), dev_status=st, accumulation=accumulation)
 
     for _ in range(3):
         call()
@@ -559,6 +562,11 @@ def ours_arm(args, rank, world, local_rank):
     bf = None if (args.no_sweep or args.no_bf16) else format_compare(sweep, device, "bf16")
     e5 = None if (args.no_sweep or args.no_e5m2) else format_compare(sweep, device, "fp8_e5m2")
     pt = None if (args.no_sweep or args.no_per_token) else format_compare(sweep, device, "fp8_e4m3", per_token=True)
+    abl = None
+    if not (args.no_sweep or args.no_ablation):  # single- against two-level accumulation
+        sl = format_compare(sweep, device, "fp8_e4m3", accumulation="single_level")
+        abl = {"decode_single_level": sl,
+               "prefill_single_level": None if args.no_prefill else prefill_leg(device, accumulation="single_level")}
     e2e_fn, h2d, d2h = e2e_setup(wl)
     g_e2e = capture(e2e_fn)
     e2e_reps = max(3, args.steps)
@@ -594,6 +602,7 @@ def ours_arm(args, rank, world, local_rank):
         "bf16_compare": bf,
         "e5m2_compare": e5,
         "per_token_compare": pt,
+        "accumulation_ablation": abl,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

@@ -32,6 +32,9 @@ KVQ_DTYPE_FP8_E4M3 = 0
 KVQ_DTYPE_BF16 = 1
 KVQ_DTYPE_FP8_E5M2 = 2
 
+KVQ_ACC_TWO_LEVEL = 0
+KVQ_ACC_SINGLE_LEVEL = 1
+
 KVQ_DEV_BAD_SLOT = 0x1
 KVQ_DEV_BAD_BLOCK = 0x2
 KVQ_DEV_BAD_SEQLEN = 0x4
@@ -76,6 +79,11 @@ lib.kvq_reshape_and_cache_per_token.argtypes = [_p, _p, _p, _p, _p, _p, _i, _i, 
 lib.kvq_paged_decode_attention_per_token.restype = _i
 lib.kvq_paged_decode_attention_per_token.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64,
                                                      _f, _i, _i, _i, _p, _sz, _p, _p]
+lib.kvq_paged_decode_attention_acc.restype = _i
+lib.kvq_paged_decode_attention_acc.argtypes = lib.kvq_paged_decode_attention.argtypes + [_i]
+lib.kvq_prefill_attention_acc.restype = _i
+lib.kvq_prefill_attention_acc.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
+                                          _f, _i, _p, _p, _i]
 lib.kvq_prefill_attention.restype = _i
 lib.kvq_prefill_attention.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
                                       _f, _i, _p, _p]
@@ -119,6 +127,14 @@ def _dtype_code(cache_dtype: str) -> int:
     if cache_dtype in ("fp8_e5m2", KVQ_DTYPE_FP8_E5M2):
         return KVQ_DTYPE_FP8_E5M2
     raise ValueError(f"unknown cache dtype {cache_dtype!r}")
+
+
+def _acc_code(accumulation) -> int:
+    if accumulation in ("two_level", KVQ_ACC_TWO_LEVEL):
+        return KVQ_ACC_TWO_LEVEL
+    if accumulation in ("single_level", KVQ_ACC_SINGLE_LEVEL):
+        return KVQ_ACC_SINGLE_LEVEL
+    raise ValueError(f"unknown accumulation mode {accumulation!r}")
 
 
 def version() -> int:
@@ -187,11 +203,13 @@ def kvq_decode_workspace_size(B, Hq, Hkv, D, max_blocks, window=-1, num_splits=0
 
 def kvq_paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out,
                                num_blocks=None, sm_scale=None, window=-1, cache_dtype="fp8_e4m3",
-                               num_splits=0, workspace=None, dev_status=None, stream=None):
+                               num_splits=0, workspace=None, dev_status=None, stream=None, accumulation=None):
     """One decode step over the paged cache; writes out (bf16 [B][Hq][D]).
 
     workspace: a uint8 CUDA tensor of at least kvq_decode_workspace_size()
-    bytes (allocated here when omitted)."""
+    bytes (allocated here when omitted).  accumulation: None (the default,
+    two-level) or "two_level" / "single_level" through
+    kvq_paged_decode_attention_acc."""
     B, Hq, D = q.shape
     max_blocks = block_table.shape[1]
     dt = _dtype_code(cache_dtype)
@@ -205,11 +223,13 @@ def kvq_paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     need = kvq_decode_workspace_size(B, Hq, Hkv, D, max_blocks, window, num_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    _check(lib.kvq_paged_decode_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                                          _ptr(block_table), _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, PAGE,
-                                          max_blocks, num_blocks, float(sm_scale), window, dt, num_splits,
-                                          _ptr(workspace), workspace.numel(), _ptr(dev_status),
-                                          _stream(stream)), "kvq_paged_decode_attention")
+    args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+            _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, PAGE, max_blocks, num_blocks, float(sm_scale), window, dt,
+            num_splits, _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream))
+    if accumulation is None:
+        _check(lib.kvq_paged_decode_attention(*args), "kvq_paged_decode_attention")
+    else:
+        _check(lib.kvq_paged_decode_attention_acc(*args, _acc_code(accumulation)), "kvq_paged_decode_attention_acc")
     return out
 
 
@@ -236,8 +256,10 @@ def kvq_paged_decode_attention_per_token(q, k_cache, v_cache, kv_scale_cache, bl
 
 def kvq_prefill_attention(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q,
                           seq_lens, out, max_q_tokens, num_blocks=None, sm_scale=None, causal=True,
-                          dev_status=None, stream=None):
-    """Chunked causal prefill over the FP8 cache; writes out (bf16 [Tq][Hq][D])."""
+                          dev_status=None, stream=None, accumulation=None):
+    """Chunked causal prefill over the FP8 cache; writes out (bf16 [Tq][Hq][D]).
+    accumulation: None (two-level) or "two_level" / "single_level" through
+    kvq_prefill_attention_acc."""
     Tq, Hq, D = q8.shape
     B = cu_seqlens_q.numel() - 1
     Hkv = k_cache.shape[1]
@@ -245,9 +267,12 @@ def kvq_prefill_attention(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block
         num_blocks = k_cache.shape[0]
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
-    _check(lib.kvq_prefill_attention(_ptr(q8), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-                                     _ptr(v_scale), _ptr(block_table), _ptr(cu_seqlens_q), _ptr(seq_lens),
-                                     _ptr(out), B, Hq, Hkv, D, PAGE, block_table.shape[1], num_blocks,
-                                     int(max_q_tokens), float(sm_scale), 1 if causal else 0,
-                                     _ptr(dev_status), _stream(stream)), "kvq_prefill_attention")
+    args = (_ptr(q8), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+            _ptr(block_table), _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, PAGE,
+            block_table.shape[1], num_blocks, int(max_q_tokens), float(sm_scale), 1 if causal else 0,
+            _ptr(dev_status), _stream(stream))
+    if accumulation is None:
+        _check(lib.kvq_prefill_attention(*args), "kvq_prefill_attention")
+    else:
+        _check(lib.kvq_prefill_attention_acc(*args, _acc_code(accumulation)), "kvq_prefill_attention_acc")
     return out

@@ -140,11 +140,15 @@ constexpr int kPresent0 = 1, kPresent1 = 2, kBad0 = 4, kBad1 = 8;
 // PT: per-token scales; p.k_scale points to the interleaved float32 scale
 // cache [num_blocks][Hkv][2][P] (K then V) instead of per-head scales (FP8
 // only; p.v_scale is unused).
-template <int D, bool FP8, int NW, int NST, bool E5, bool PT>
+// SL: single-level accumulation (an ablation of the two-level scheme): the
+// P.V MMAs accumulate into the running sum O * alpha directly instead of a
+// fresh FP32 tile per stage (FP8, per-head scales only).
+template <int D, bool FP8, int NW, int NST, bool E5, bool PT, bool SL>
 __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const __grid_constant__ DecodeParams p) {
   using G = Geo<D, FP8>;
   static_assert(NST % NW == 0 && NST >= NW, "each ring slot must belong to one consumer warp");
   static_assert(FP8 || !PT, "per-token scales apply to FP8 caches");
+  static_assert(!SL || (FP8 && !PT), "the single-level ablation covers the per-head FP8 path");
   constexpr int STRIDE = stage_stride<D, FP8, PT>();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
@@ -538,6 +542,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
         // ---- O^T += V^T P^T (32 token slots per MMA), fresh FP32 per stage ----
 #pragma unroll
         for (int mt = 0; mt < G::MT; ++mt) {
+          if constexpr (SL) {  // the MMAs add this stage into O * alpha themselves
+            float c4[4] = {O[mt][0] * al0, O[mt][1] * al1, O[mt][2] * al0, O[mt][3] * al1};
+            mma_fp8<E5>(c4, va[mt][0], va[mt][1], va[mt][2], va[mt][3], ph0, ph1, c4);
+            mma_fp8<E5>(O[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], pl0, pl1, c4);
+            continue;
+          }
           float t[4] = {0.f, 0.f, 0.f, 0.f};
           mma_fp8<E5>(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], ph0, ph1, t);
           mma_fp8<E5>(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], pl0, pl1, t);
@@ -743,11 +753,11 @@ void split_plan(int B, int Hkv, int P, int max_blocks, int window, int num_split
   *pps_out = pps;
 }
 
-template <int D, bool FP8, bool E5 = false, bool PT = false>
+template <int D, bool FP8, bool E5 = false, bool PT = false, bool SL = false>
 kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream_t s) {
   constexpr int NST = stages_for<D, FP8, PT>();
   constexpr size_t smem = decode_smem_bytes<D, FP8, NST, PT>();
-  auto kern = decode_partial_kernel<D, FP8, kNW, NST, E5, PT>;
+  auto kern = decode_partial_kernel<D, FP8, kNW, NST, E5, PT, SL>;
   static int configured_mask = 0;  // devices whose attribute is set
   int dev = 0;
   cudaGetDevice(&dev);
@@ -808,7 +818,7 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
                           const float* v_scale, const int32_t* block_table, const int32_t* seq_lens, void* out, int B,
                           int Hq, int Hkv, int D, int P, int max_blocks, int64_t num_blocks, float sm_scale, int window,
                           kvq_dtype_t cache_dtype, int num_splits, void* workspace, size_t workspace_bytes,
-                          int* dev_status, kvq_stream_t stream, bool per_token) {
+                          int* dev_status, kvq_stream_t stream, bool per_token, bool single_level = false) {
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0)
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: bad sizes");
   if (Hq % Hkv != 0) return fail(KVQ_ERR_INVALID_ARG, "paged_decode: Hq %% Hkv != 0");
@@ -864,6 +874,12 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto o = static_cast<__nv_bfloat16*>(out);
   const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
+  if (single_level) {
+    if (cache_dtype != KVQ_DTYPE_FP8_E4M3 || per_token)
+      return fail(KVQ_ERR_UNSUPPORTED, "paged_decode: single-level accumulation covers E4M3 per-head caches");
+    return D == 128 ? launch_decode<128, true, false, false, true>(prm, o, s)
+                    : launch_decode<64, true, false, false, true>(prm, o, s);
+  }
   if (per_token) {
     if (D == 128)
       return e5 ? launch_decode<128, true, true, true>(prm, o, s) : launch_decode<128, true, false, true>(prm, o, s);
@@ -887,6 +903,19 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
   return paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, B, Hq, Hkv, D, P,
                       max_blocks, num_blocks, sm_scale, window, cache_dtype, num_splits, workspace, workspace_bytes,
                       dev_status, stream, false);
+}
+
+extern "C" kvq_status_t kvq_paged_decode_attention_acc(
+    const void* q, const void* k_cache, const void* v_cache, const float* k_scale, const float* v_scale,
+    const int32_t* block_table, const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int D, int P,
+    int max_blocks, int64_t num_blocks, float sm_scale, int window, kvq_dtype_t cache_dtype, int num_splits,
+    void* workspace, size_t workspace_bytes, int* dev_status, kvq_stream_t stream, kvq_accumulation_t accumulation) {
+  clear_error();
+  if (accumulation != KVQ_ACC_TWO_LEVEL && accumulation != KVQ_ACC_SINGLE_LEVEL)
+    return fail(KVQ_ERR_INVALID_ARG, "paged_decode: bad accumulation mode");
+  return paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, B, Hq, Hkv, D, P,
+                      max_blocks, num_blocks, sm_scale, window, cache_dtype, num_splits, workspace, workspace_bytes,
+                      dev_status, stream, false, accumulation == KVQ_ACC_SINGLE_LEVEL);
 }
 
 extern "C" kvq_status_t kvq_paged_decode_attention_per_token(

@@ -189,6 +189,10 @@ KVQ_DEVINL Job make_job(const PrefillParams& p) {
   return j;
 }
 
+// SL: single-level accumulation (an ablation of the two-level scheme): P.V
+// of every tile accumulates into one TMEM sum O, which the softmax warps
+// rescale by alpha in place (skipped when alpha is 1 for the whole warp).
+template <bool SL>
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -337,17 +341,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       if (j + 1 < nkv) issue_s(j + 1);
       if (!ok) break;
       if (!wait(&bars->p_full[j & 1], (j >> 1) & 1)) break;
-      if (j >= 1 && !wait(&bars->o_free, (j - 1) & 1)) break;  // O_tile of tile j - 1 has been read
+      if (!SL && j >= 1 && !wait(&bars->o_free, (j - 1) & 1)) break;  // O_tile of tile j - 1 has been read
       tc_fence_after();
       if (lane == 0) {
         const int st = j % NKV;
         const uint32_t p_s = sbase + OFF_P + (j & 1) * (TQ * TK);
         const uint32_t v_s = sbase + OFF_KV + st * STAGE_B + TILE_B;
-        const uint32_t d = tmem + 2 * TK;  // O_tile
+        const uint32_t d = tmem + 2 * TK;  // O_tile (SL: the running sum O)
 #pragma unroll
         for (int kk = 0; kk < TK / 32; ++kk)  // 32 keys = 2 V pages per MMA
           umma_f8(d, desc_sw128(p_s + kk * 32), desc_interleave(v_s + kk * 2 * PAGE_B, PAGE_B, 128), IDESC,
-                  kk > 0 ? 1u : 0u);
+                  (kk > 0 || (SL && j > 0)) ? 1u : 0u);
         umma_commit(&bars->o_full);
         umma_commit(&bars->kv_empty[st]);
       }
@@ -390,7 +394,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
 
     const uint32_t o_tile = tmem + t_lane + 2 * TK + half * HC;  // this half's columns of O_tile
     const uint32_t o_run = o_tile + HD;                           // ... and of O_run
-    {  // O_run = 0
+    if (!SL) {  // O_run = 0
       uint32_t z[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) z[i] = 0u;
@@ -434,6 +438,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         }
         tmem_st16(o_run + 16 * c, o);
       }
+    };
+
+    auto rescale = [&](int jt, float alpha) {  // SL: O *= alpha once P.V of tile jt has landed
+      if (!wait_all(&bars->o_full, jt & 1)) return;
+      tc_fence_after();
+      if (__all_sync(0xffffffffu, alpha == 1.f)) return;  // exact: nothing to do
+#pragma unroll
+      for (int c = 0; c < HC / 16; ++c) {
+        uint32_t o[16];
+        tmem_ld16_async(o_tile + 16 * c, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st16(o_tile + 16 * c, o);
+      }
+      tmem_wait_st();
     };
 
     // every softmax thread runs every tile's named barrier, also after a
@@ -503,13 +523,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         l = l * alpha + (rs2.x + rs2.y);
         m = m_new;
         fence_proxy_async_smem();
+        if constexpr (SL) {
+          if (j >= 1) rescale(j - 1, alpha);  // before P.V of tile j adds into O
+        }
         tc_fence_before();
         mbar_arrive(&bars->p_full[j & 1]);
-        if (j >= 1) accumulate(j - 1, alpha_prev);
+        if constexpr (!SL) {
+          if (j >= 1) accumulate(j - 1, alpha_prev);
+        }
         alpha_prev = alpha;
       }
     }
-    if (ok && nkv >= 1) accumulate(nkv - 1, alpha_prev);
+    if constexpr (SL) {
+      if (nkv >= 1 && wait_all(&bars->o_full, (nkv - 1) & 1)) tc_fence_after();
+    } else {
+      if (ok && nkv >= 1) accumulate(nkv - 1, alpha_prev);
+    }
 
     // epilogue: out = O * v_scale / l (O and l both in units of 2^8 p), l summed over both halves
     xsum[half * TQ + row] = l;
@@ -521,7 +550,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
 #pragma unroll
       for (int c = 0; c < HC / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(o_run + 32 * c, o);
+        tmem_ld32((SL ? o_tile : o_run) + 32 * c, o);
 #pragma unroll
         for (int i = 0; i < 32; ++i) O[32 * c + i] = __uint_as_float(o[i]);
       }
@@ -555,13 +584,27 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
 
 using namespace kvq;
 
-extern "C" kvq_status_t kvq_prefill_attention(const uint8_t* q8, const float* q_scale, const void* k_cache,
-                                              const void* v_cache, const float* k_scale, const float* v_scale,
-                                              const int32_t* block_table, const int32_t* cu_seqlens_q,
-                                              const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int D,
-                                              int P, int max_blocks, int64_t num_blocks, int max_q_tokens,
-                                              float sm_scale, int causal, int* dev_status, kvq_stream_t stream) {
-  clear_error();
+namespace {
+
+template <bool SL>
+kvq_status_t launch_prefill(const PrefillParams& prm, dim3 grid, cudaStream_t stream) {
+  static int configured_mask = 0;  // devices whose shared-memory attribute is set
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!(configured_mask & (1 << (dev & 31)))) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<SL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_status(e, "prefill: set shared memory size");
+    configured_mask |= 1 << (dev & 31);
+  }
+  prefill_kernel<SL><<<grid, NTHREADS, SMEM_BYTES, stream>>>(prm);
+  return cuda_status(cudaGetLastError(), "prefill launch");
+}
+
+kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cache, const void* v_cache,
+                     const float* k_scale, const float* v_scale, const int32_t* block_table,
+                     const int32_t* cu_seqlens_q, const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int D,
+                     int P, int max_blocks, int64_t num_blocks, int max_q_tokens, float sm_scale, int causal,
+                     int* dev_status, kvq_stream_t stream, bool single_level) {
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || max_q_tokens < 0)
     return fail(KVQ_ERR_INVALID_ARG, "prefill: bad sizes");
   if (Hq % Hkv != 0) return fail(KVQ_ERR_INVALID_ARG, "prefill: Hq %% Hkv != 0");
@@ -595,15 +638,35 @@ extern "C" kvq_status_t kvq_prefill_attention(const uint8_t* q8, const float* q_
   prm.sm_scale = sm_scale;
   prm.causal = causal ? 1 : 0;
   prm.dev_status = dev_status;
-  static int configured_mask = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!(configured_mask & (1 << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return cuda_status(e, "prefill: set shared memory size");
-    configured_mask |= 1 << (dev & 31);
-  }
   dim3 grid((max_q_tokens + TQ - 1) / TQ, Hq, B);
-  prefill_kernel<<<grid, NTHREADS, SMEM_BYTES, static_cast<cudaStream_t>(stream)>>>(prm);
-  return cuda_status(cudaGetLastError(), "prefill launch");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return single_level ? launch_prefill<true>(prm, grid, st) : launch_prefill<false>(prm, grid, st);
+}
+
+}  // namespace
+
+extern "C" kvq_status_t kvq_prefill_attention(const uint8_t* q8, const float* q_scale, const void* k_cache,
+                                              const void* v_cache, const float* k_scale, const float* v_scale,
+                                              const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                              const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int D,
+                                              int P, int max_blocks, int64_t num_blocks, int max_q_tokens,
+                                              float sm_scale, int causal, int* dev_status, kvq_stream_t stream) {
+  clear_error();
+  return prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q, seq_lens, out, B, Hq,
+                 Hkv, D, P, max_blocks, num_blocks, max_q_tokens, sm_scale, causal, dev_status, stream, false);
+}
+
+extern "C" kvq_status_t kvq_prefill_attention_acc(const uint8_t* q8, const float* q_scale, const void* k_cache,
+                                                  const void* v_cache, const float* k_scale, const float* v_scale,
+                                                  const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                                  const int32_t* seq_lens, void* out, int B, int Hq, int Hkv,
+                                                  int D, int P, int max_blocks, int64_t num_blocks,
+                                                  int max_q_tokens, float sm_scale, int causal, int* dev_status,
+                                                  kvq_stream_t stream, kvq_accumulation_t accumulation) {
+  clear_error();
+  if (accumulation != KVQ_ACC_TWO_LEVEL && accumulation != KVQ_ACC_SINGLE_LEVEL)
+    return fail(KVQ_ERR_INVALID_ARG, "prefill: bad accumulation mode");
+  return prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q, seq_lens, out, B, Hq,
+                 Hkv, D, P, max_blocks, num_blocks, max_q_tokens, sm_scale, causal, dev_status, stream,
+                 accumulation == KVQ_ACC_SINGLE_LEVEL);
 }

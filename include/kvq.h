@@ -83,6 +83,22 @@ typedef enum kvq_dtype {
                                 Decode only (kvq_prefill_attention reads E4M3). */
 } kvq_dtype_t;
 
+/*
+ * How attention sums P.V over the keys.
+ * [vLLM] "Problems we found" / "Kernel and vLLM improvements": FP8 tensor
+ * cores can keep partial sums in less than FP32, which degrades long
+ * contexts; two-level accumulation adds each tile's P.V, computed into a
+ * fresh FP32 accumulator, into a running FP32 sum.  [FP8KV] training
+ * section, "accumulation precision": DeepSeek-V3 promotes partial sums to
+ * FP32 every 128 elements after measuring about 14 bits on H800.
+ */
+typedef enum kvq_accumulation {
+  KVQ_ACC_TWO_LEVEL = 0,     /* the default of every call without an _acc suffix */
+  KVQ_ACC_SINGLE_LEVEL = 1   /* ablation: the tensor cores add each tile into the
+                                running sum themselves (rescaled by the online
+                                softmax in place); E4M3 per-head caches only */
+} kvq_accumulation_t;
+
 /* Bits OR-ed into *dev_status by the kernels. */
 #define KVQ_DEV_BAD_SLOT     0x1  /* slot_mapping[t] >= num_blocks * P: token skipped */
 #define KVQ_DEV_BAD_BLOCK    0x2  /* block id outside [0, num_blocks): page masked out */
@@ -206,6 +222,24 @@ kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_cache, cons
                                         int window, kvq_dtype_t cache_dtype, int num_splits,
                                         void* workspace, size_t workspace_bytes,
                                         int* dev_status, kvq_stream_t stream);
+
+/*
+ * kvq_paged_decode_attention_acc -- kvq_paged_decode_attention with an
+ * explicit accumulation mode (kvq_accumulation_t above).  Two-level is the
+ * call above; single-level feeds O * alpha to the P.V MMAs as their
+ * accumulator input, so the tensor cores add each stage of 32 tokens into the
+ * running sum.  Single-level: E4M3 cache, per-head scales only (else
+ * KVQ_ERR_UNSUPPORTED).  It exists to measure what two-level costs and buys.
+ */
+kvq_status_t kvq_paged_decode_attention_acc(const void* q, const void* k_cache, const void* v_cache,
+                                            const float* k_scale, const float* v_scale,
+                                            const int32_t* block_table, const int32_t* seq_lens,
+                                            void* out, int B, int Hq, int Hkv, int D, int P,
+                                            int max_blocks, int64_t num_blocks, float sm_scale,
+                                            int window, kvq_dtype_t cache_dtype, int num_splits,
+                                            void* workspace, size_t workspace_bytes,
+                                            int* dev_status, kvq_stream_t stream,
+                                            kvq_accumulation_t accumulation);
 
 /*
  * kvq_reshape_and_cache_per_token -- quantize new K/V tokens into the paged
@@ -333,6 +367,24 @@ kvq_status_t kvq_prefill_attention(const uint8_t* q8, const float* q_scale,
                                    int B, int Hq, int Hkv, int D, int P, int max_blocks,
                                    int64_t num_blocks, int max_q_tokens, float sm_scale,
                                    int causal, int* dev_status, kvq_stream_t stream);
+
+/*
+ * kvq_prefill_attention_acc -- kvq_prefill_attention with an explicit
+ * accumulation mode.  Single-level: every tile's P8.V8 MMA accumulates into
+ * one tensor-memory sum, which the softmax warps multiply by alpha in place
+ * before the next tile's MMA (skipped when alpha is 1 for all 32 rows of a
+ * warp, which changes nothing).  It exists to measure what two-level costs
+ * and buys.
+ */
+kvq_status_t kvq_prefill_attention_acc(const uint8_t* q8, const float* q_scale,
+                                       const void* k_cache, const void* v_cache,
+                                       const float* k_scale, const float* v_scale,
+                                       const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                       const int32_t* seq_lens, void* out,
+                                       int B, int Hq, int Hkv, int D, int P, int max_blocks,
+                                       int64_t num_blocks, int max_q_tokens, float sm_scale,
+                                       int causal, int* dev_status, kvq_stream_t stream,
+                                       kvq_accumulation_t accumulation);
 
 #ifdef __cplusplus
 }
