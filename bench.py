@@ -381,9 +381,10 @@ def prefill_flops(new=PF_NEW, cached=PF_CACHED, hq=HQ, d=D):
     return pairs * hq * 4 * d
 
 
-def prefill_leg(device, reps=10, accumulation=None):
+def prefill_leg(device, reps=10, accumulation=None, head_dim=D):
     """Chunked causal prefill of 4,096 new tokens on 28,672 cached FP8
-    tokens (32/8 heads, head_dim 128): TFLOP/s of kvq_prefill_attention."""
+    tokens (32/8 heads, head_dim 128, or 256): TFLOP/s of
+    kvq_prefill_attention."""
     import torch
     import fp8_kv_cache_reshape_gb300 as kvq
     import workloads as W
@@ -392,12 +393,12 @@ def prefill_leg(device, reps=10, accumulation=None):
     bt, nb = W.paged_layout([L], P, g)
     slots = W.slots_for(bt, 0, torch.arange(L), P).to(device)
     gd = W.generator(78, device=device)
-    k = W.randn_bf16((L, HKV, D), gd, device=device)
-    v = W.randn_bf16((L, HKV, D), gd, device=device)
-    q = W.randn_bf16((PF_NEW, HQ, D), gd, device=device)
+    k = W.randn_bf16((L, HKV, head_dim), gd, device=device)
+    v = W.randn_bf16((L, HKV, head_dim), gd, device=device)
+    q = W.randn_bf16((PF_NEW, HQ, head_dim), gd, device=device)
     ks, vs = W.calibrate_amax(k), W.calibrate_amax(v)
     qs = (q.float().abs().amax() / 448.0).reshape(1).to(torch.float32)
-    kd, vd = kvq.alloc_kv_cache(nb, HKV, D, device=device, fill=0)
+    kd, vd = kvq.alloc_kv_cache(nb, HKV, head_dim, device=device, fill=0)
     kvq.kvq_reshape_and_cache(k, v, slots, kd, vd, ks, vs)
     q8 = torch.empty(q.shape, dtype=torch.uint8, device=device)
     kvq.kvq_quantize_query(q, q8, qs)
@@ -409,7 +410,7 @@ def prefill_leg(device, reps=10, accumulation=None):
 
     def call():
         kvq.kvq_prefill_attention(q8, qs, kd, vd, ks, vs, btd, cu, sl, out, max_q_tokens=PF_NEW,
-                                  sm_scale=1.0 / math.sqrt(D), dev_status=st, accumulation=accumulation)
+                                  sm_scale=1.0 / math.sqrt(head_dim), dev_status=st, accumulation=accumulation)
 
     for _ in range(3):
         call()
@@ -418,8 +419,11 @@ def prefill_leg(device, reps=10, accumulation=None):
     peaks, src = measured_peaks()
     bf16 = float(peaks.get("bf16_tflops", 1900.0))
     fp8_peak = 2.0 * bf16  # nominal FP8:BF16 dense ratio 4.5 : 2.25
-    tf = prefill_flops() / (ms * 1e-3) / 1e12
-    return {"workload": "llama31_8b_chunked_prefill_4k_on_28k", "ms": round(ms, 4), "flops": prefill_flops(),
+    flops = prefill_flops(d=head_dim)
+    tf = flops / (ms * 1e-3) / 1e12
+    name = "llama31_8b_chunked_prefill_4k_on_28k" + ("" if head_dim == 128 else f"_head_dim_{head_dim}")
+    return {"workload": name, "ms": round(ms, 4), "flops": flops, "head_dim": head_dim,
+            "accumulation": accumulation or ("two_level" if head_dim == 128 else "single_level"),
             "bound": "tensor", "achieved": round(tf, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
             "frac": round(tf / fp8_peak, 4),
             "peak_source": f"{src} bf16_tflops x 2 (nominal FP8:BF16 dense ratio)",
@@ -566,7 +570,8 @@ def ours_arm(args, rank, world, local_rank):
     if not (args.no_sweep or args.no_ablation):  # single- against two-level accumulation
         sl = format_compare(sweep, device, "fp8_e4m3", accumulation="single_level")
         abl = {"decode_single_level": sl,
-               "prefill_single_level": None if args.no_prefill else prefill_leg(device, accumulation="single_level")}
+               "prefill_single_level": None if args.no_prefill else prefill_leg(device, accumulation="single_level"),
+               "prefill_head_dim_256": None if args.no_prefill else prefill_leg(device, head_dim=256)}
     e2e_fn, h2d, d2h = e2e_setup(wl)
     g_e2e = capture(e2e_fn)
     e2e_reps = max(3, args.steps)

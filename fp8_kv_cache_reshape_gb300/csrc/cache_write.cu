@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
           kv_scale_cache[si] = skt;
           kv_scale_cache[si + kPage] = svt;
         }
-        *reinterpret_cast<uint4*>(k_cache + page + k_chunk_offset(off, j, D)) = quant16<E5>(xk, skt);
+        *reinterpret_cast<uint4*>(k_cache + page + fp8_k_offset(off, j, D)) = quant16<E5>(xk, skt);
         const uint4 qv = quant16<E5>(xv, svt);
         const uint8_t* qb = reinterpret_cast<const uint8_t*>(&qv);
         const int slot_in_row = fp8_v_slot(off);
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
     const size_t page = (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
     float x[16];
     load16_bf16(k + src, x);
-    *reinterpret_cast<uint4*>(k_cache + page + k_chunk_offset(off, j, D)) = quant16<E5>(x, sk);
+    *reinterpret_cast<uint4*>(k_cache + page + fp8_k_offset(off, j, D)) = quant16<E5>(x, sk);
     load16_bf16(v + src, x);
     uint4 qv = quant16<E5>(x, sv);
     const uint8_t* qb = reinterpret_cast<const uint8_t*>(&qv);
@@ -238,10 +238,11 @@ extern "C" kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, cons
   clear_error();
   if (T < 0 || Hkv < 1 || num_blocks < 1) return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: bad sizes");
   if (P != kPage) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache: page size %d (only 16)", P);
-  if (D != 64 && D != 128) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache: head_dim %d", D);
   if (cache_dtype != KVQ_DTYPE_FP8_E4M3 && cache_dtype != KVQ_DTYPE_FP8_E5M2 && cache_dtype != KVQ_DTYPE_BF16)
     return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: bad cache dtype");
   const bool fp8 = cache_dtype != KVQ_DTYPE_BF16;
+  if (D != 64 && D != 128 && !(fp8 && D == 256))
+    return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache: head_dim %d (64 or 128; 256 for FP8)", D);
   if (T == 0) return KVQ_OK;
   if (!k || !v || !slot_mapping || !k_cache || !v_cache)
     return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache: null pointer");
@@ -264,7 +265,10 @@ extern "C" kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, cons
                                   dev_status);
     };
     const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
-    if (D == 128)
+    if (D == 256)
+      e5 ? launch(reshape_and_cache_fp8_kernel<256, true, false>)
+         : launch(reshape_and_cache_fp8_kernel<256, false, false>);
+    else if (D == 128)
       e5 ? launch(reshape_and_cache_fp8_kernel<128, true, false>)
          : launch(reshape_and_cache_fp8_kernel<128, false, false>);
     else

@@ -32,6 +32,14 @@ KVQ_DEVINL int k_chunk_offset(int t, int j, int row_bytes) {
   else pj = (j & 8) | ((j ^ t) & 7);  // 256-byte rows: each half like a 128-byte row
   return t * row_bytes + (pj << 4);
 }
+// Byte offset of 16-byte chunk j of token t in an FP8 K page.  D <= 128: row
+// t, chunk swizzled as above.  D = 256: two 2 KiB half-pages (dims 0-127,
+// 128-255), each 16 rows of 128 bytes with the 128-byte-row swizzle, so that
+// each half is a canonical SWIZZLE_128B K-major operand for tcgen05.mma.
+KVQ_DEVINL int fp8_k_offset(int t, int j, int D) {
+  if (D == 256) return (j >> 3) * (kPage * 128) + t * 128 + (((j & 7) ^ (t & 7)) << 4);
+  return k_chunk_offset(t, j, D);
+}
 __host__ __device__ __forceinline__ int fp8_v_slot(int t) {  // rho in include/kvq.h
   return t < 8 ? (((t >> 1) << 2) | (t & 1)) : ((((t - 8) >> 1) << 2) | 2 | (t & 1));
 }

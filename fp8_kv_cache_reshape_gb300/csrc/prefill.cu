@@ -44,22 +44,36 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int TQ = 128;           // query rows per CTA
 constexpr int TK = 128;           // keys per tile (8 pages)
-constexpr int HD = 128;           // head dim
-constexpr int NKV = 4;            // K/V stages
 constexpr int NPROD = 2;          // producer warps; tile j comes from producer j % NPROD
-static_assert(NKV % NPROD == 0, "each stage belongs to one producer, which refills it in tile order");
-constexpr int PAGE_B = kPage * HD;             // 2048 bytes per page (K or V)
-constexpr int TILE_B = TK * HD;                // 16 KB per K tile (= V tile)
-constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + TQ * HD;        // 16 KB
-constexpr int STAGE_B = 2 * TILE_B;            // K tile + V tile
-constexpr int OFF_P = OFF_KV + NKV * STAGE_B;  // 2 P buffers of 16 KB
-constexpr int OFF_BAR = OFF_P + 2 * TQ * TK;
-constexpr int OFF_XCH = OFF_BAR + 512;             // row max / row sum exchange between column halves
-constexpr int SMEM_BYTES = OFF_XCH + 3 * 2 * TQ * 4 + 1024;  // + alignment slack
+constexpr int PLANE = 128;        // bytes of one K-major operand row: 128 dims of FP8, 128-byte swizzle
 constexpr int NSOFT = 8;                           // softmax warps: two per TMEM lane quarter
 constexpr int NTHREADS = (NPROD + 1 + NSOFT) * 32;  // producer 0, MMA, softmax warps, producer 1
-constexpr uint32_t TMEM_COLS = 512;            // S0 | S1 | O_tile | O_run, 128 columns each
+// TMEM: S0 | S1 | O_tile | O_run at head_dim 128 (128 columns each); at 256,
+// S0 | S1 | O (single-level accumulation: O_tile and O_run do not both fit).
+constexpr uint32_t TMEM_COLS = 512;
+
+// Shared-memory plan for one head dimension.  Q and the K tile are stored as
+// HD / 128 planes of 128-byte rows (dims 128h .. 128h + 127), each a canonical
+// SWIZZLE_128B K-major operand; V pages stay [d][16 slots].
+template <int HD_>
+struct Geo {
+  static constexpr int HD = HD_;
+  static constexpr int NKV = HD == 128 ? 4 : 2;  // K/V stages (2 x 64 KiB at head_dim 256)
+  static_assert(NKV % NPROD == 0, "each stage belongs to one producer, which refills it in tile order");
+  static constexpr int PAGE_B = kPage * HD;      // bytes per page (K or V)
+  static constexpr int TILE_B = TK * HD;         // bytes per K tile (= V tile)
+  static constexpr int PLANE_Q = TQ * PLANE;     // one plane of Q
+  static constexpr int PLANE_K = TK * PLANE;     // one plane of a K tile
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + TQ * HD;
+  static constexpr int STAGE_B = 2 * TILE_B;     // K tile + V tile
+  static constexpr int OFF_P = OFF_KV + NKV * STAGE_B;  // 2 P buffers of 16 KB
+  static constexpr int OFF_BAR = OFF_P + 2 * TQ * TK;
+  static constexpr int OFF_XCH = OFF_BAR + 512;  // row max / row sum exchange between column halves
+  static constexpr int SMEM_BYTES = OFF_XCH + 3 * 2 * TQ * 4 + 1024;  // + alignment slack
+  static constexpr int HO = HD / 2;              // output dims per softmax thread
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+};
 
 struct PrefillParams {
   const uint8_t* q8;
@@ -79,6 +93,7 @@ struct PrefillParams {
   int* dev_status;
 };
 
+template <int NKV>
 struct Bars {
   uint64_t q_full;
   uint64_t kv_full[NKV];
@@ -192,13 +207,21 @@ KVQ_DEVINL Job make_job(const PrefillParams& p) {
 // SL: single-level accumulation (an ablation of the two-level scheme): P.V
 // of every tile accumulates into one TMEM sum O, which the softmax warps
 // rescale by alpha in place (skipped when alpha is 1 for the whole warp).
-template <bool SL>
+// Head dim 256 needs it: two-level would need 2 x 256 TMEM columns for O.
+template <int HD, bool SL>
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
+  using G = Geo<HD>;
+  static_assert(HD == 128 || (HD == 256 && SL), "head_dim 256 runs with single-level accumulation");
+  constexpr int NKV = G::NKV, PAGE_B = G::PAGE_B, TILE_B = G::TILE_B, STAGE_B = G::STAGE_B;
+  constexpr int OFF_Q = G::OFF_Q, OFF_KV = G::OFF_KV, OFF_P = G::OFF_P, OFF_XCH = G::OFF_XCH;
+  constexpr int HO = G::HO;
+  using BarsN = Bars<NKV>;
+  static_assert(sizeof(BarsN) <= 512, "barrier block");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023) & ~1023u) - raw);
   const uint32_t sbase = smem_u32(smem);
-  Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  BarsN* bars = reinterpret_cast<BarsN*>(smem + G::OFF_BAR);
   volatile int* abort_flag = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -281,10 +304,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       if (load_mask != 0xFFu) {
         for (int pg = 0; pg < TK / kPage; ++pg) {
           if (load_mask & (1u << pg)) continue;
-          uint4* kz = reinterpret_cast<uint4*>(ks + pg * PAGE_B);
           uint4* vz = reinterpret_cast<uint4*>(vs + pg * PAGE_B);
           for (int i = lane; i < PAGE_B / 16; i += 32) {
-            kz[i] = make_uint4(0, 0, 0, 0);
+            // K: the page's kPage rows in each plane
+            const int pl = i / (kPage * PLANE / 16), w = i % (kPage * PLANE / 16);
+            reinterpret_cast<uint4*>(ks + pl * G::PLANE_K + pg * kPage * PLANE)[w] = make_uint4(0, 0, 0, 0);
             vz[i] = make_uint4(0, 0, 0, 0);
           }
         }
@@ -298,7 +322,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       __syncwarp();
       if (lane < TK / kPage && blk >= 0) {
         const size_t off = (static_cast<size_t>(blk) * p.Hkv + job.kvh) * PAGE_B;
-        bulk_g2s(ks + lane * PAGE_B, p.k_cache + off, PAGE_B, &bars->kv_full[st], policy_evict_first());
+        // K: one copy per plane (a K page of head dim 256 is stored as two half-pages)
+#pragma unroll
+        for (int pl = 0; pl < HD / PLANE; ++pl)
+          bulk_g2s(ks + pl * G::PLANE_K + lane * kPage * PLANE, p.k_cache + off + pl * kPage * PLANE, kPage * PLANE,
+                   &bars->kv_full[st], policy_evict_first());
         bulk_g2s(vs + lane * PAGE_B, p.v_cache + off, PAGE_B, &bars->kv_full[st], policy_evict_first());
       }
     }
@@ -309,7 +337,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer --
-    constexpr uint32_t IDESC = idesc_e4m3(TQ, TK);
+    constexpr uint32_t IDESC_S = idesc_e4m3(TQ, TK);  // S = Q K^T: N = keys
+    constexpr uint32_t IDESC_O = idesc_e4m3(TQ, HD);  // O += P V: N = head dim
     const uint32_t q_s = sbase + OFF_Q;
     bool ok = true;
     auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -330,8 +359,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         const uint32_t k_s = sbase + OFF_KV + st * STAGE_B;
         const uint32_t d = tmem + (j & 1) * TK;
 #pragma unroll
-        for (int kk = 0; kk < HD / 32; ++kk)
-          umma_f8(d, desc_sw128(q_s + kk * 32), desc_sw128(k_s + kk * 32), IDESC, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < HD / 32; ++kk)  // 32 dims per MMA, four per 128-byte plane
+          umma_f8(d, desc_sw128(q_s + (kk >> 2) * G::PLANE_Q + (kk & 3) * 32),
+                  desc_sw128(k_s + (kk >> 2) * G::PLANE_K + (kk & 3) * 32), IDESC_S, kk > 0 ? 1u : 0u);
         umma_commit(&bars->s_full[j & 1]);
       }
       __syncwarp();
@@ -350,7 +380,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         const uint32_t d = tmem + 2 * TK;  // O_tile (SL: the running sum O)
 #pragma unroll
         for (int kk = 0; kk < TK / 32; ++kk)  // 32 keys = 2 V pages per MMA
-          umma_f8(d, desc_sw128(p_s + kk * 32), desc_interleave(v_s + kk * 2 * PAGE_B, PAGE_B, 128), IDESC,
+          umma_f8(d, desc_sw128(p_s + kk * 32), desc_interleave(v_s + kk * 2 * PAGE_B, PAGE_B, 128), IDESC_O,
                   (kk > 0 || (SL && j > 0)) ? 1u : 0u);
         umma_commit(&bars->o_full);
         umma_commit(&bars->kv_empty[st]);
@@ -375,15 +405,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const int kend = (p.causal && qpos + 1 < job.L) ? qpos + 1 : job.L;  // this row attends to keys [0, kend)
     const size_t out_row = (static_cast<size_t>(p.cu_seqlens_q[job.b]) + job.q0 + row) * p.Hq + job.h;
 
-    // Q row (this thread's half) -> shared memory, 128-byte swizzled
+    // Q row (this thread's half) -> shared memory, 128-byte swizzled planes
     {
-      uint8_t* qs = smem + OFF_Q + row * HD;
       const uint4* src = reinterpret_cast<const uint4*>(p.q8 + out_row * HD);
 #pragma unroll
       for (int cc = 0; cc < HD / 32; ++cc) {
-        const int c = half * (HD / 32) + cc;
+        const int c = half * (HD / 32) + cc;  // 16-byte chunk of the row
         const uint4 v = live_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qs + ((c ^ (row & 7)) << 4)) = v;
+        uint8_t* qs = smem + OFF_Q + (c >> 3) * G::PLANE_Q + row * PLANE;
+        *reinterpret_cast<uint4*>(qs + (((c & 7) ^ (row & 7)) << 4)) = v;
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars->q_full);
@@ -392,14 +422,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const int tail = job.L % kPage;          // valid tokens in the last page (0 = full)
     const int last_page = (job.L - 1) / kPage;
 
-    const uint32_t o_tile = tmem + t_lane + 2 * TK + half * HC;  // this half's columns of O_tile
-    const uint32_t o_run = o_tile + HD;                           // ... and of O_run
+    const uint32_t o_tile = tmem + t_lane + 2 * TK + half * HO;  // this half's columns of O_tile (SL: of O)
+    const uint32_t o_run = o_tile + HD;                           // ... and of O_run (two-level)
     if (!SL) {  // O_run = 0
       uint32_t z[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll
-      for (int c = 0; c < HC / 16; ++c) tmem_st16(o_run + 16 * c, z);
+      for (int c = 0; c < HO / 16; ++c) tmem_st16(o_run + 16 * c, z);
     }
     float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
     bool ok = true;  // warp-uniform, since tcgen05.ld / st need every lane of the warp
@@ -420,12 +450,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       tmem_wait_st();  // the previous update of O_run
       const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-      for (int c = 0; c < HC / 16; ++c) {  // 16 columns at a time
+      for (int c = 0; c < HO / 16; ++c) {  // 16 columns at a time
         uint32_t t[16], o[16];
         tmem_ld16_async(o_tile + 16 * c, t);
         tmem_ld16_async(o_run + 16 * c, o);
         tmem_wait_ld();
-        if (c == HC / 16 - 1) {  // the whole tile has been read: the next P.V may overwrite it
+        if (c == HO / 16 - 1) {  // the whole tile has been read: the next P.V may overwrite it
           tc_fence_before();
           mbar_arrive(&bars->o_free);
         }
@@ -445,7 +475,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       tc_fence_after();
       if (__all_sync(0xffffffffu, alpha == 1.f)) return;  // exact: nothing to do
 #pragma unroll
-      for (int c = 0; c < HC / 16; ++c) {
+      for (int c = 0; c < HO / 16; ++c) {
         uint32_t o[16];
         tmem_ld16_async(o_tile + 16 * c, o);
         tmem_wait_ld();
@@ -468,9 +498,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       if (wait_all(&bars->s_full[j & 1], (j >> 1) & 1) && wait_all(&bars->kv_full[st], (j / NKV) & 1)) {
         tc_fence_after();
         bad = bars->stage_bad[st];
-        if (half == 0 && tail != 0 && last_page / (TK / kPage) == j) {
-          uint8_t* vrow = smem + OFF_KV + st * STAGE_B + TILE_B + (last_page % (TK / kPage)) * PAGE_B + row * kPage;
-          for (int t = tail; t < kPage; ++t) vrow[fp8_v_slot(t)] = 0;
+        if (tail != 0 && last_page / (TK / kPage) == j) {
+          // V rows (dims) row and row + 128 .. of the last page: slots past the sequence end
+          for (int d = row + half * TQ; d < HD; d += 2 * TQ) {
+            uint8_t* vrow = smem + OFF_KV + st * STAGE_B + TILE_B + (last_page % (TK / kPage)) * PAGE_B + d * kPage;
+            for (int t = tail; t < kPage; ++t) vrow[fp8_v_slot(t)] = 0;
+          }
         }
         const bool need_mask = (key0 + HC > kend) || bad != 0;
         const uint32_t sbuf = tmem + t_lane + (j & 1) * TK + half * HC;
@@ -545,26 +578,23 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     named_bar_sync(1, NSOFT * 32);
     const float lt = l + xsum[(half ^ 1) * TQ + row];
     if (ok) {
-      float O[HC];
-      tmem_wait_st();
+      if (!SL) tmem_wait_st();
+      const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD + half * HO);
 #pragma unroll
-      for (int c = 0; c < HC / 32; ++c) {
+      for (int c = 0; c < HO / 32; ++c) {  // 32 columns of O at a time
         uint32_t o[32];
         tmem_ld32((SL ? o_tile : o_run) + 32 * c, o);
+        if (live_row) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) O[32 * c + i] = __uint_as_float(o[i]);
-      }
-      if (live_row) {
-        const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD + half * HC);
-#pragma unroll
-        for (int c = 0; c < HC / 8; ++c) {
-          uint4 w;
-          w.x = pack_bf16x2(O[8 * c + 0] * f, O[8 * c + 1] * f);
-          w.y = pack_bf16x2(O[8 * c + 2] * f, O[8 * c + 3] * f);
-          w.z = pack_bf16x2(O[8 * c + 4] * f, O[8 * c + 5] * f);
-          w.w = pack_bf16x2(O[8 * c + 6] * f, O[8 * c + 7] * f);
-          dst[c] = w;
+          for (int w = 0; w < 4; ++w) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(o[8 * w + 0]) * f, __uint_as_float(o[8 * w + 1]) * f);
+            u.y = pack_bf16x2(__uint_as_float(o[8 * w + 2]) * f, __uint_as_float(o[8 * w + 3]) * f);
+            u.z = pack_bf16x2(__uint_as_float(o[8 * w + 4]) * f, __uint_as_float(o[8 * w + 5]) * f);
+            u.w = pack_bf16x2(__uint_as_float(o[8 * w + 6]) * f, __uint_as_float(o[8 * w + 7]) * f);
+            dst[4 * c + w] = u;
+          }
         }
       }
     }
@@ -586,17 +616,18 @@ using namespace kvq;
 
 namespace {
 
-template <bool SL>
+template <int HD, bool SL>
 kvq_status_t launch_prefill(const PrefillParams& prm, dim3 grid, cudaStream_t stream) {
+  constexpr int smem = Geo<HD>::SMEM_BYTES;
   static int configured_mask = 0;  // devices whose shared-memory attribute is set
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(configured_mask & (1 << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<SL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<HD, SL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_status(e, "prefill: set shared memory size");
     configured_mask |= 1 << (dev & 31);
   }
-  prefill_kernel<SL><<<grid, NTHREADS, SMEM_BYTES, stream>>>(prm);
+  prefill_kernel<HD, SL><<<grid, NTHREADS, smem, stream>>>(prm);
   return cuda_status(cudaGetLastError(), "prefill launch");
 }
 
@@ -604,13 +635,18 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
                      const float* k_scale, const float* v_scale, const int32_t* block_table,
                      const int32_t* cu_seqlens_q, const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int D,
                      int P, int max_blocks, int64_t num_blocks, int max_q_tokens, float sm_scale, int causal,
-                     int* dev_status, kvq_stream_t stream, bool single_level) {
+                     int* dev_status, kvq_stream_t stream, int accumulation) {
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || max_q_tokens < 0)
     return fail(KVQ_ERR_INVALID_ARG, "prefill: bad sizes");
   if (Hq % Hkv != 0) return fail(KVQ_ERR_INVALID_ARG, "prefill: Hq %% Hkv != 0");
   if (!(sm_scale > 0.f) || !(sm_scale < FLT_MAX)) return fail(KVQ_ERR_INVALID_ARG, "prefill: bad sm_scale");
   if (P != kPage) return fail(KVQ_ERR_UNSUPPORTED, "prefill: page size %d (only 16)", P);
-  if (D != HD) return fail(KVQ_ERR_UNSUPPORTED, "prefill: head_dim %d (only 128)", D);
+  if (D != 128 && D != 256) return fail(KVQ_ERR_UNSUPPORTED, "prefill: head_dim %d (128 or 256)", D);
+  // head_dim 256: single-level accumulation (two-level would need 2 x 256 TMEM
+  // columns for O beside the score buffers); -1 = the default for the head dim
+  if (D == 256 && accumulation == KVQ_ACC_TWO_LEVEL)
+    return fail(KVQ_ERR_UNSUPPORTED, "prefill: head_dim 256 runs with single-level accumulation only");
+  const bool single_level = D == 256 || accumulation == KVQ_ACC_SINGLE_LEVEL;
   if (max_q_tokens == 0) return KVQ_OK;
   if (!q8 || !q_scale || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !cu_seqlens_q ||
       !seq_lens || !out)
@@ -640,7 +676,8 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
   prm.dev_status = dev_status;
   dim3 grid((max_q_tokens + TQ - 1) / TQ, Hq, B);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return single_level ? launch_prefill<true>(prm, grid, st) : launch_prefill<false>(prm, grid, st);
+  if (D == 256) return launch_prefill<256, true>(prm, grid, st);
+  return single_level ? launch_prefill<128, true>(prm, grid, st) : launch_prefill<128, false>(prm, grid, st);
 }
 
 }  // namespace
@@ -653,7 +690,7 @@ extern "C" kvq_status_t kvq_prefill_attention(const uint8_t* q8, const float* q_
                                               float sm_scale, int causal, int* dev_status, kvq_stream_t stream) {
   clear_error();
   return prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q, seq_lens, out, B, Hq,
-                 Hkv, D, P, max_blocks, num_blocks, max_q_tokens, sm_scale, causal, dev_status, stream, false);
+                 Hkv, D, P, max_blocks, num_blocks, max_q_tokens, sm_scale, causal, dev_status, stream, -1);
 }
 
 extern "C" kvq_status_t kvq_prefill_attention_acc(const uint8_t* q8, const float* q_scale, const void* k_cache,
@@ -668,5 +705,5 @@ extern "C" kvq_status_t kvq_prefill_attention_acc(const uint8_t* q8, const float
     return fail(KVQ_ERR_INVALID_ARG, "prefill: bad accumulation mode");
   return prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q, seq_lens, out, B, Hq,
                  Hkv, D, P, max_blocks, num_blocks, max_q_tokens, sm_scale, causal, dev_status, stream,
-                 accumulation == KVQ_ACC_SINGLE_LEVEL);
+                 static_cast<int>(accumulation));
 }

@@ -9,7 +9,10 @@ V[block][h][d][t]; these functions permute bytes between that and the
 physical layout:
 * K page: row t of D elements (row_bytes = D * esize); its 16-byte chunk j
   sits at chunk j ^ (t % 8) for 128-byte rows, j ^ ((t // 2) % 4) for 64-byte
-  rows, and (j & 8) | ((j ^ t) & 7) for 256-byte rows.
+  rows, and (j & 8) | ((j ^ t) & 7) for 256-byte rows (BF16 at D = 128).
+* FP8 K page at D = 256: two 2 KiB half-pages, half h holding dims
+  128h .. 128h + 127 of all 16 tokens as 128-byte rows; chunk j of token t
+  at byte (j // 8) * 2048 + t * 128 + ((j % 8) ^ (t % 8)) * 16.
 * V page (FP8): row d of 16 slots; token t in slot rho(t),
   rho = [0,1,4,5,8,9,12,13,2,3,6,7,10,11,14,15].
 * V page (BF16): row d of 16 bf16; token t in slot t, and the two 16-byte
@@ -40,8 +43,11 @@ def _k_perm(D: int, esize: int) -> np.ndarray:
     perm = np.empty(P * rb, dtype=np.int64)
     for t in range(P):
         for j in range(rb // 16):
-            pj = k_chunk_position(t, j, rb)
-            perm[t * rb + pj * 16: t * rb + pj * 16 + 16] = t * rb + j * 16 + np.arange(16)
+            if esize == 1 and D == 256:
+                phys = (j // 8) * 2048 + t * 128 + ((j % 8) ^ (t % 8)) * 16
+            else:
+                phys = t * rb + k_chunk_position(t, j, rb) * 16
+            perm[phys: phys + 16] = t * rb + j * 16 + np.arange(16)
     return perm
 
 

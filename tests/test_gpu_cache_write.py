@@ -36,8 +36,11 @@ def _expected(case):
 
 
 @pytest.mark.parametrize("dtype", [FP8, FP8_E5M2, BF16])
-@pytest.mark.parametrize("D,Hkv,lengths", [(128, 8, [1000, 333]), (64, 8, [17, 16, 1]), (64, 1, [512])])
+@pytest.mark.parametrize("D,Hkv,lengths", [(128, 8, [1000, 333]), (64, 8, [17, 16, 1]), (64, 1, [512]),
+                                           (256, 4, [300, 17])])
 def test_cache_write_bit_exact(dtype, D, Hkv, lengths):
+    if D == 256 and dtype == BF16:
+        pytest.skip("head_dim 256 caches are FP8 only")
     cfg = W.DecodeConfig("t", batch=len(lengths), q_heads=Hkv, kv_heads=Hkv, head_dim=D, context=max(lengths),
                          outliers=4 if D == 128 else 0)
     case = W.decode_case(cfg, lengths=lengths, cache_dtype=dtype)

@@ -22,25 +22,25 @@ def _k():
     return k
 
 
-def build(nq_list, cached_list, Hq=32, Hkv=8, seed=0, sentinel=0xA5):
+def build(nq_list, cached_list, Hq=32, Hkv=8, seed=0, sentinel=0xA5, D=128):
     """Oracle caches for sequences of nq new + cached old tokens; q8 codes."""
     gen = W.generator(9000 + seed)
     lens = [a + b for a, b in zip(nq_list, cached_list)]
     bt, nb = W.paged_layout(lens, 16, gen)
     slots = torch.cat([W.slots_for(bt, b, torch.arange(L), 16) for b, L in enumerate(lens)])
     T = int(slots.numel())
-    k = W.randn_bf16((T, Hkv, 128), gen)
-    v = W.randn_bf16((T, Hkv, 128), gen)
-    q = W.randn_bf16((sum(nq_list), Hq, 128), gen)
+    k = W.randn_bf16((T, Hkv, D), gen)
+    v = W.randn_bf16((T, Hkv, D), gen)
+    q = W.randn_bf16((sum(nq_list), Hq, D), gen)
     ks, vs = W.calibrate_amax(k), W.calibrate_amax(v)
     qs = np.float32(q.float().abs().max().item() / 448)
-    kc = np.full((nb, Hkv, 16, 128), sentinel, np.uint8)
-    vc = np.full((nb, Hkv, 128, 16), sentinel, np.uint8)
+    kc = np.full((nb, Hkv, 16, D), sentinel, np.uint8)
+    vc = np.full((nb, Hkv, D, 16), sentinel, np.uint8)
     kv_cache.reshape_and_cache(f32(k), f32(v), slots.numpy(), kc, vc, ks.numpy(), vs.numpy())
     q8 = kv_cache.quantize_query(f32(q), qs)
     cu = np.concatenate([[0], np.cumsum(nq_list)]).astype(np.int32)
     return dict(kc=kc, vc=vc, q8=q8, qs=qs, ks=ks.numpy(), vs=vs.numpy(), bt=bt.numpy(), nb=nb,
-                cu=cu, lens=np.array(lens, np.int32), Hq=Hq, Hkv=Hkv, sm=1 / np.sqrt(128.0))
+                cu=cu, lens=np.array(lens, np.int32), Hq=Hq, Hkv=Hkv, sm=1 / np.sqrt(float(D)))
 
 
 def gpu_prefill(c, causal=True, block_table=None, status=False):
@@ -109,6 +109,21 @@ def test_prefill_parity(nq, cached):
     # met against the mirrored oracle above
     mx, mn = check_rows_vs_pure(got, pure, rows, c)
     assert mn <= 10 * MEAN_ABS
+
+
+@pytest.mark.parametrize("nq,cached", [([256], [384]), ([1, 130, 300], [0, 17, 1000]), ([77], [2000])])
+def test_prefill_head_dim_256(nq, cached):
+    """Head dim 256 (single-level accumulation): two 128-dim planes per
+    operand, P.V with N = 256; NaN-poisoned bytes outside the tokens."""
+    c = build(nq, cached, Hq=8, Hkv=2, seed=11 + len(nq), sentinel=0x7F, D=256)
+    got = gpu_prefill(c)
+    Tq = c["q8"].shape[0]
+    rng = np.random.default_rng(5)
+    rows = [(t, h) for t in range(Tq) for h in range(c["Hq"])]
+    if len(rows) > 2000:
+        rows = [rows[i] for i in rng.choice(len(rows), 2000, replace=False)]
+    check_rows(got, oracle(c, rows=rows), rows)
+    check_rows_vs_pure(got, oracle(c, rows=rows, mode="pure"), rows, c)
 
 
 def test_prefill_non_causal():
