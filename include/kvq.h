@@ -40,13 +40,18 @@
  *    conflicts: with 128-byte rows chunk j sits at chunk j ^ (t % 8); with
  *    64-byte rows at j ^ ((t / 2) % 4); with 256-byte rows (BF16, D = 128)
  *    each 128-byte half is swizzled as a 128-byte row.  Row bytes = D * esize.
+ *    FP8 at D = 256 (prefill): the page is two 2 KiB half-pages, half h
+ *    holding dims 128h .. 128h + 127 of the 16 tokens as 128-byte rows
+ *    swizzled as above (byte (j / 8) * 2048 + t * 128 + ((j % 8) ^ (t % 8)) *
+ *    16 for chunk j of token t), so each half is a tensor-core operand.
  *  - V cache, element [block][h][d][slot]: the page transposed, one row of P
  *    token slots per dimension d.  FP8: token t occupies slot rho(t) with
  *    rho = {0,1,4,5,8,9,12,13,2,3,6,7,10,11,14,15} (tokens 2c,2c+1,2c+8,2c+9
  *    share the 4-byte word c).  BF16: slot = t, and the two 16-byte halves of
  *    row d are swapped when (d / 4) is odd.
  *  - FP8 elements are E4M3 ("OCP FN": bias 7, max 448, min subnormal 2^-9,
- *    0x7F/0xFF NaN, no infinity).  Page bytes = P * D * esize.
+ *    0x7F/0xFF NaN, no infinity) or E5M2 (KVQ_DTYPE_FP8_E5M2).  Page bytes =
+ *    P * D * esize.
  *
  * Quantization (kvq_reshape_and_cache, kvq_quantize_query):
  *    code = e4m3_rne_satfinite( fl32(x / scale) )
@@ -127,7 +132,8 @@ const char* kvq_last_error_string(void);
  *  v_cache       [num_blocks][Hkv][D][P] in the format above (written).
  *  k_scale,      float32 [Hkv] per-KV-head scales (FP8 only; may be NULL for
  *  v_scale       BF16).  Must be finite and > 0.
- *  T >= 0 (T == 0 launches nothing), Hkv >= 1, D in {64, 128}, P == 16,
+ *  T >= 0 (T == 0 launches nothing), Hkv >= 1, D in {64, 128} (and 256 for
+ *  FP8 caches, which only kvq_prefill_attention reads), P == 16,
  *  num_blocks >= 1.  For BF16 the values are copied bit for bit.  FP8:
  *  code = encode(fl32(x / s[h])), one float32 division, then one
  *  round-to-nearest-even conversion saturating at the format's largest
@@ -350,7 +356,11 @@ kvq_status_t kvq_paged_decode_attention_static_scratch(const void* q, const void
  *  seq_lens      int32 [B].
  *  out           bf16 [Tq][Hq][D] (written).
  *  max_q_tokens  an upper bound of max_b nq_b (sizes the launch).
- *  Supported: D == 128, P == 16, Hq % Hkv == 0.
+ *  Supported: D in {128, 256}, P == 16, Hq % Hkv == 0.  D = 256 runs with
+ *  single-level accumulation (every tile's P8.V8 MMA adds into one
+ *  tensor-memory sum rescaled in place): two-level would need two 256-column
+ *  FP32 accumulators beside the score buffers, more than the 512 columns of
+ *  tensor memory.
  *  Declared rounding: S = sum_d q8[d] k8[d] (exact products, FP32 sums),
  *  s2 = S * c with c = fl32(fl32(fl32(q_scale * k_scale) * sm_scale) *
  *  log2(e)); P8 = e4m3_rne_sat(fl32(2^(s2 - m) * 256)) against the running
