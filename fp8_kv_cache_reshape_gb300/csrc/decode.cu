@@ -23,10 +23,12 @@
 // 2) covers the stage's 32 tokens; P is transposed in registers (movmatrix)
 // and split into two E4M3 terms, and O^T = V^T P^T (M = dims, K = the 32
 // token slots of both pages) goes into fresh FP32 fragments that are then
-// added into the running output.  BF16 cache: the same flow on bf16 MMAs.  At the end of an item the NW warp states
-// are merged through shared memory and one normalized partial output plus
-// its log2-sum-exp is written per query head.  A combine kernel, launched as
-// a programmatic dependent of the partial kernel, merges the page ranges.
+// added into the running output.  BF16 cache: the same flow on bf16 MMAs.
+// At the end of an item each consumer warp writes its own normalized partial
+// output and log2-sum-exp per query head (no cross-warp merge).  Items are
+// ordered so that consecutive CTAs serve different (sequence, KV head)
+// pairs.  A combine kernel, launched as a programmatic dependent of the
+// partial kernel, merges the S x NW partials of each query head in one pass.
 #include <cfloat>
 #include <cmath>
 #include <mutex>
@@ -108,8 +110,11 @@ struct ItemRange {
 KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
   ItemRange r;
   const int S = p.num_splits;
-  const int bh = item / S;
-  r.split = item - bh * S;
+  // consecutive items belong to different (sequence, KV head) pairs, so each
+  // pair's ranges run on CTAs spread over the whole GPU
+  const int NG = p.B * p.Hkv;
+  const int bh = item % NG;
+  r.split = item / NG;
   r.b = bh / p.Hkv;
   r.kvh = bh - r.b * p.Hkv;
   int L = p.seq_lens[r.b];
@@ -675,51 +680,71 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
 }
 
 // out[row][d] = sum_s 2^(lse_s - M) o_s[d] / sum_s 2^(lse_s - M) over the
-// S' partials of row = (b, hq).  Grid (rows, D / 32); 32 warps split the
-// partials (lane = dimension), so each thread issues a handful of
-// independent loads.
+// S' partials of row = (b, hq).  Grid (rows, D / 32); warp w takes partials
+// w, w + 32, ... (lane = dimension) and loads their log-sum-exps and outputs
+// together (one round trip), merges them against its own maximum, and the
+// warps' results are merged through shared memory.
 constexpr int kCombineWarps = 32;
+constexpr int kCombinePer = 8;  // partials per warp and pass
 __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const float* __restrict__ o_part,
                                                                             const float* __restrict__ lse_part,
                                                                             __nv_bfloat16* __restrict__ out, int S,
                                                                             int D) {
-  __shared__ float red[kCombineWarps];
-  __shared__ float acc_s[kCombineWarps][33];
+  __shared__ float m_s[kCombineWarps];
   __shared__ float den_s[kCombineWarps];
+  __shared__ float acc_s[kCombineWarps][33];
   grid_dependency_wait();  // the partial kernel's writes are visible past this point
   const int row = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int d = blockIdx.y * 32 + lane;
   const float* lp = lse_part + static_cast<size_t>(row) * S;
-  float mx = -INFINITY;
-  for (int s = tid; s < S; s += kCombineWarps * 32) mx = fmaxf(mx, lp[s]);
+  const float* op = o_part + static_cast<size_t>(row) * S * D + d;
+  float m = -INFINITY, den = 0.f, acc = 0.f;
+  for (int s0 = wid; s0 < S; s0 += kCombineWarps * kCombinePer) {
+    float l[kCombinePer], o[kCombinePer];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) red[wid] = mx;
-  __syncthreads();
-  float M = red[lane];
+    for (int i = 0; i < kCombinePer; ++i) {
+      const int s = s0 + i * kCombineWarps;
+      l[i] = s < S ? __ldg(lp + s) : -INFINITY;
+      o[i] = s < S ? __ldg(op + s * D) : 0.f;  // S * D < 2^31: at most 65535 x 4 partials of 128 dims
+    }
+    float mn = m;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float acc = 0.f, den = 0.f;
-  if (M != -INFINITY) {
-    const float* op = o_part + static_cast<size_t>(row) * S * D + d;
-#pragma unroll 4
-    for (int s = wid; s < S; s += kCombineWarps) {
-      const float w = ex2(lp[s] - M);
-      den += w;
-      acc = fmaf(w, op[static_cast<size_t>(s) * D], acc);
+    for (int i = 0; i < kCombinePer; ++i) mn = fmaxf(mn, l[i]);
+    if (mn != -INFINITY) {
+      const float a = ex2(m - mn);  // m = -inf gives 0
+      den *= a;
+      acc *= a;
+#pragma unroll
+      for (int i = 0; i < kCombinePer; ++i) {
+        const float w = ex2(l[i] - mn);
+        den += w;
+        acc = fmaf(w, o[i], acc);
+      }
+      m = mn;
     }
   }
+  if (lane == 0) {
+    m_s[wid] = m;
+    den_s[wid] = den;
+  }
   acc_s[wid][lane] = acc;
-  if (lane == 0) den_s[wid] = den;
   __syncthreads();
   if (wid == 0) {
-    float t = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < kCombineWarps; ++k) t += acc_s[k][lane];
-    float dd = den_s[lane];
+    const float mw = m_s[lane];
+    float M = mw;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float t = 0.f, dd = 0.f;
+    if (M != -INFINITY) {
+      // this lane's factor for warp `lane`, then a per-warp broadcast
+      const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
+      dd = den_s[lane] * f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+#pragma unroll 8
+      for (int k = 0; k < kCombineWarps; ++k) t = fmaf(__shfl_sync(0xffffffffu, f, k), acc_s[k][lane], t);
+    }
     out[static_cast<size_t>(row) * D + d] = __float2bfloat16_rn(dd > 0.f ? t / dd : 0.f);
   }
 }
