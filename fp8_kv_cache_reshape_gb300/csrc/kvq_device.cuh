@@ -130,6 +130,18 @@ KVQ_DEVINL void grid_launch_dependents() { asm volatile("griddepcontrol.launch_d
 KVQ_DEVINL void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+KVQ_DEVINL void named_bar_arrive(int id, int threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+// Per-warpgroup register budget (all four warps of the warpgroup execute it).
+template <int N>
+KVQ_DEVINL void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+KVQ_DEVINL void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // ---------------------------------------------------------- tensor-core ops ---
 KVQ_DEVINL void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {

@@ -10,24 +10,27 @@
 // quantized to FP8 too (kvq_quantize_query).
 //
 // One CTA = 128 query rows of one sequence x one query head.  Keys come in
-// tiles of 128 (8 pages).  Warp roles:
-//  warps 0, 10  producers of the even / odd key tiles: block ids (read a
+// tiles of 128 (8 pages).  Warp roles (by warpgroup; setmaxnreg gives the
+// softmax warpgroups 184 registers and the others fewer):
+//  warps 12, 14  producers of the even / odd key tiles: block ids (read a
 //             group of 4 tiles ahead) -> one bulk copy per K page and V page
 //             into a 4-stage ring, each producer owning two of the stages
 //             (pages of unknown / out-of-range blocks are zero filled and
 //             masked).  Two issuing warps, because a page-sized bulk copy
 //             costs the issuing warp tens of cycles;
-//  warp 1     TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
+//  warp 13    TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
 //             score buffers, then O_j = P_j V_j into a fresh TMEM accumulator
-//             (first level);
-//  warps 2-9  two threads per query row (warps w and w + 4 share TMEM lane
-//             quarter w % 4), each owning 64 of the 128 columns of S_j and of
-//             O_j: online softmax in base 2 (the two halves exchange their
-//             tile maxima through shared memory), P_j = e4m3(2^(s - m) * 256)
-//             into swizzled shared memory, and O_run = O_run * alpha + O_j in
-//             FP32 (second level; O_run lives in its own TMEM columns and is
-//             updated through registers, which keeps the softmax warps free
-//             of spills).
+//             O_tile (first level);
+//  warps 0-7  two threads per query row (warps w and w + 4 share TMEM lane
+//             quarter w % 4), each owning 64 of the 128 columns of S_j:
+//             online softmax in base 2 (the two halves exchange their tile
+//             maxima through shared memory), P_j = e4m3(2^(s - m) * 256) into
+//             swizzled shared memory, and the tile's rescale factor alpha_j;
+//  warps 8-11 correction: O_run = O_run * alpha_j + O_tile_j in FP32 (second
+//             level; O_run has its own TMEM columns), one thread per query
+//             row, off the softmax warps' path; then the output rows.
+// With single-level accumulation (SL) the P.V MMAs add into one TMEM sum O
+// that the softmax warps rescale in place, and the correction warps idle.
 // Shared-memory operands use the UMMA canonical K-major layouts: Q, K and P
 // with the 128-byte swizzle (K pages are stored pre-swizzled by the cache
 // format), V pages ([d][16 token slots]) without swizzle.
@@ -46,8 +49,19 @@ constexpr int TQ = 128;           // query rows per CTA
 constexpr int TK = 128;           // keys per tile (8 pages)
 constexpr int NPROD = 2;          // producer warps; tile j comes from producer j % NPROD
 constexpr int PLANE = 128;        // bytes of one K-major operand row: 128 dims of FP8, 128-byte swizzle
-constexpr int NSOFT = 8;                           // softmax warps: two per TMEM lane quarter
-constexpr int NTHREADS = (NPROD + 1 + NSOFT) * 32;  // producer 0, MMA, softmax warps, producer 1
+// Warp roles, in warpgroups (setmaxnreg works per warpgroup):
+//   warps 0-7   softmax (warpgroups 0, 1), two per TMEM lane quarter;
+//   warps 8-11  correction (warpgroup 2): the second accumulation level;
+//   warps 12-14 producer 0, MMA issuer, producer 1 (warpgroup 3; warp 15 idle).
+constexpr int NSOFT = 8;
+constexpr int NCORR = 4;
+constexpr int W_PROD0 = 12, W_MMA = 13, W_PROD1 = 14;
+constexpr int NTHREADS = 16 * 32;
+// registers per thread: 65,536 / 512 = 128 at launch, then 184 for softmax,
+// 80 for correction, 56 for producers and MMA (256 x 184 + 128 x 80 + 128 x 56
+// = 64,512 <= 65,536)
+constexpr int REG_SOFT = 184, REG_CORR = 80, REG_CTRL = 56;
+static_assert(2 * 128 * REG_SOFT + 128 * REG_CORR + 128 * REG_CTRL <= 65536, "register split");
 // TMEM: S0 | S1 | O_tile | O_run at head_dim 128 (128 columns each); at 256,
 // S0 | S1 | O (single-level accumulation: O_tile and O_run do not both fit).
 constexpr uint32_t TMEM_COLS = 512;
@@ -70,7 +84,8 @@ struct Geo {
   static constexpr int OFF_P = OFF_KV + NKV * STAGE_B;  // 2 P buffers of 16 KB
   static constexpr int OFF_BAR = OFF_P + 2 * TQ * TK;
   static constexpr int OFF_XCH = OFF_BAR + 512;  // row max / row sum exchange between column halves
-  static constexpr int SMEM_BYTES = OFF_XCH + 3 * 2 * TQ * 4 + 1024;  // + alignment slack
+  static constexpr int OFF_ALPHA = OFF_XCH + 3 * 2 * TQ * 4;  // [2][TQ] rescale factors, softmax -> correction
+  static constexpr int SMEM_BYTES = OFF_ALPHA + 2 * TQ * 4 + 1024;  // + alignment slack
   static constexpr int HO = HD / 2;              // output dims per softmax thread
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
@@ -101,7 +116,7 @@ struct Bars {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full;  // P.V of the current tile is in O_tile
-  uint64_t o_free;  // O_tile has been read
+  uint64_t o_free;  // O_tile has been folded into O_run (correction warps)
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -241,12 +256,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       mbar_init(&bars->p_full[i], NSOFT * 32);
     }
     mbar_init(&bars->o_full, 1);
-    mbar_init(&bars->o_free, NSOFT * 32);
+    mbar_init(&bars->o_free, NCORR * 32);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if (warp == W_MMA) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&bars->tmem_base)),
                  "r"(TMEM_COLS)
@@ -258,142 +273,236 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const int nkv = job.nkv;
-
-  if (warp == 0 || warp >= 2 + NSOFT) {
-    // ----------------------------------------------------------- producers --
-    const int n_pages = (job.L + kPage - 1) / kPage;
-    const int32_t* bt = p.block_table + static_cast<size_t>(job.b) * p.max_blocks;
-    // Block ids come one warp-wide load per group of 4 tiles (32 pages), issued
-    // a group ahead so that its latency hides behind the copies; lane
-    // (j % 4) * 8 + i of `ids` holds the block of page i of tile j.
-    auto load_ids = [&](int grp) {
-      const int page = grp * 32 + lane;
-      return page < n_pages ? __ldg(bt + page) : -1;
-    };
-    int ids = load_ids(0);
-    int ids_next = load_ids(1);
-    int cur_grp = 0;
-    int j = (warp == 0) ? 0 : warp - (1 + NSOFT);  // this producer's first tile
-    for (; j < nkv; j += NPROD) {
-      if ((j >> 2) != cur_grp) {  // steps of NPROD < 4 tiles: at most one group ahead
-        cur_grp = j >> 2;
-        ids = ids_next;
-        ids_next = load_ids(cur_grp + 1);
+  // each warpgroup sets its register budget at the top of its own branch
+  if (warp >= W_PROD0) {
+    setmaxnreg_dec<REG_CTRL>();
+    if (warp == W_PROD0 || warp == W_PROD1) {
+      // ----------------------------------------------------------- producers --
+      const int n_pages = (job.L + kPage - 1) / kPage;
+      const int32_t* bt = p.block_table + static_cast<size_t>(job.b) * p.max_blocks;
+      // Block ids come one warp-wide load per group of 4 tiles (32 pages), issued
+      // a group ahead so that its latency hides behind the copies; lane
+      // (j % 4) * 8 + i of `ids` holds the block of page i of tile j.
+      auto load_ids = [&](int grp) {
+        const int page = grp * 32 + lane;
+        return page < n_pages ? __ldg(bt + page) : -1;
+      };
+      int ids = load_ids(0);
+      int ids_next = load_ids(1);
+      int cur_grp = 0;
+      int j = (warp == W_PROD0) ? 0 : 1;  // this producer's first tile
+      for (; j < nkv; j += NPROD) {
+        if ((j >> 2) != cur_grp) {  // steps of NPROD < 4 tiles: at most one group ahead
+          cur_grp = j >> 2;
+          ids = ids_next;
+          ids_next = load_ids(cur_grp + 1);
+        }
+        const int st = j % NKV;
+        int ok = 1;
+        if (lane == 0) ok = (!*abort_flag && mbar_wait(&bars->kv_empty[st], ((j / NKV) & 1) ^ 1, abort_flag)) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        uint8_t* ks = smem + OFF_KV + st * STAGE_B;
+        uint8_t* vs = ks + TILE_B;
+        // lanes 0..7: one page each
+        int blk = __shfl_sync(0xffffffffu, ids, ((j & 3) << 3) | (lane & 7));
+        uint32_t bad = 0;
+        const int page = j * (TK / kPage) + lane;
+        if (lane >= TK / kPage || page >= n_pages) {
+          blk = -1;
+        } else if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
+          set_status(p.dev_status, KVQ_DEV_BAD_BLOCK);
+          blk = -1;
+          bad = 1;
+        }
+        const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad != 0);
+        const uint32_t load_mask = __ballot_sync(0xffffffffu, blk >= 0) & 0xFFu;
+        // zero-fill pages that are not loaded (past the end, or bad block ids)
+        if (load_mask != 0xFFu) {
+          for (int pg = 0; pg < TK / kPage; ++pg) {
+            if (load_mask & (1u << pg)) continue;
+            uint4* vz = reinterpret_cast<uint4*>(vs + pg * PAGE_B);
+            for (int i = lane; i < PAGE_B / 16; i += 32) {
+              // K: the page's kPage rows in each plane
+              const int pl = i / (kPage * PLANE / 16), w = i % (kPage * PLANE / 16);
+              reinterpret_cast<uint4*>(ks + pl * G::PLANE_K + pg * kPage * PLANE)[w] = make_uint4(0, 0, 0, 0);
+              vz[i] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_proxy_async_smem();  // the zeros, before the tensor cores read the stage
+        }
+        __syncwarp();
+        if (lane == 0) {
+          bars->stage_bad[st] = bad_mask & 0xFFu;
+          mbar_arrive_expect_tx(&bars->kv_full[st], 2u * PAGE_B * __popc(load_mask));
+        }
+        __syncwarp();
+        if (lane < TK / kPage && blk >= 0) {
+          const size_t off = (static_cast<size_t>(blk) * p.Hkv + job.kvh) * PAGE_B;
+          // K: one copy per plane (a K page of head dim 256 is stored as two half-pages)
+#pragma unroll
+          for (int pl = 0; pl < HD / PLANE; ++pl)
+            bulk_g2s(ks + pl * G::PLANE_K + lane * kPage * PLANE, p.k_cache + off + pl * kPage * PLANE, kPage * PLANE,
+                     &bars->kv_full[st], policy_evict_first());
+          bulk_g2s(vs + lane * PAGE_B, p.v_cache + off, PAGE_B, &bars->kv_full[st], policy_evict_first());
+        }
       }
-      const int st = j % NKV;
-      int ok = 1;
-      if (lane == 0) ok = (!*abort_flag && mbar_wait(&bars->kv_empty[st], ((j / NKV) & 1) ^ 1, abort_flag)) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      uint8_t* ks = smem + OFF_KV + st * STAGE_B;
-      uint8_t* vs = ks + TILE_B;
-      // lanes 0..7: one page each
-      int blk = __shfl_sync(0xffffffffu, ids, ((j & 3) << 3) | (lane & 7));
-      uint32_t bad = 0;
-      const int page = j * (TK / kPage) + lane;
-      if (lane >= TK / kPage || page >= n_pages) {
-        blk = -1;
-      } else if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
-        set_status(p.dev_status, KVQ_DEV_BAD_BLOCK);
-        blk = -1;
-        bad = 1;
+      if (j < nkv && lane == 0) {  // abandoned: let this producer's issued copies land
+        set_status(p.dev_status, KVQ_DEV_TIMEOUT);
+        *abort_flag = 1;
+        for (int k = j - NPROD; k >= 0 && k >= j - NKV; k -= NPROD) mbar_wait(&bars->kv_full[k % NKV], (k / NKV) & 1);
       }
-      const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad != 0);
-      const uint32_t load_mask = __ballot_sync(0xffffffffu, blk >= 0) & 0xFFu;
-      // zero-fill pages that are not loaded (past the end, or bad block ids)
-      if (load_mask != 0xFFu) {
-        for (int pg = 0; pg < TK / kPage; ++pg) {
-          if (load_mask & (1u << pg)) continue;
-          uint4* vz = reinterpret_cast<uint4*>(vs + pg * PAGE_B);
-          for (int i = lane; i < PAGE_B / 16; i += 32) {
-            // K: the page's kPage rows in each plane
-            const int pl = i / (kPage * PLANE / 16), w = i % (kPage * PLANE / 16);
-            reinterpret_cast<uint4*>(ks + pl * G::PLANE_K + pg * kPage * PLANE)[w] = make_uint4(0, 0, 0, 0);
-            vz[i] = make_uint4(0, 0, 0, 0);
+    } else if (warp == W_MMA) {
+      // ------------------------------------------------------------ MMA issuer --
+      constexpr uint32_t IDESC_S = idesc_e4m3(TQ, TK);  // S = Q K^T: N = keys
+      constexpr uint32_t IDESC_O = idesc_e4m3(TQ, HD);  // O += P V: N = head dim
+      const uint32_t q_s = sbase + OFF_Q;
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        if (ok && !mbar_wait(bar, parity, abort_flag)) {
+          ok = false;
+          if (lane == 0) {
+            set_status(p.dev_status, KVQ_DEV_TIMEOUT);
+            *abort_flag = 1;
           }
         }
-        fence_proxy_async_smem();  // the zeros, before the tensor cores read the stage
-      }
-      __syncwarp();
-      if (lane == 0) {
-        bars->stage_bad[st] = bad_mask & 0xFFu;
-        mbar_arrive_expect_tx(&bars->kv_full[st], 2u * PAGE_B * __popc(load_mask));
-      }
-      __syncwarp();
-      if (lane < TK / kPage && blk >= 0) {
-        const size_t off = (static_cast<size_t>(blk) * p.Hkv + job.kvh) * PAGE_B;
-        // K: one copy per plane (a K page of head dim 256 is stored as two half-pages)
-#pragma unroll
-        for (int pl = 0; pl < HD / PLANE; ++pl)
-          bulk_g2s(ks + pl * G::PLANE_K + lane * kPage * PLANE, p.k_cache + off + pl * kPage * PLANE, kPage * PLANE,
-                   &bars->kv_full[st], policy_evict_first());
-        bulk_g2s(vs + lane * PAGE_B, p.v_cache + off, PAGE_B, &bars->kv_full[st], policy_evict_first());
-      }
-    }
-    if (j < nkv && lane == 0) {  // abandoned: let this producer's issued copies land
-      set_status(p.dev_status, KVQ_DEV_TIMEOUT);
-      *abort_flag = 1;
-      for (int k = j - NPROD; k >= 0 && k >= j - NKV; k -= NPROD) mbar_wait(&bars->kv_full[k % NKV], (k / NKV) & 1);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer --
-    constexpr uint32_t IDESC_S = idesc_e4m3(TQ, TK);  // S = Q K^T: N = keys
-    constexpr uint32_t IDESC_O = idesc_e4m3(TQ, HD);  // O += P V: N = head dim
-    const uint32_t q_s = sbase + OFF_Q;
-    bool ok = true;
-    auto wait = [&](uint64_t* bar, uint32_t parity) {
-      if (ok && !mbar_wait(bar, parity, abort_flag)) {
-        ok = false;
+        return ok;
+      };
+      auto issue_s = [&](int j) {  // S[j%2] = Q K_j^T
+        const int st = j % NKV;
+        if (!wait(&bars->kv_full[st], (j / NKV) & 1)) return;
+        tc_fence_after();
         if (lane == 0) {
+          const uint32_t k_s = sbase + OFF_KV + st * STAGE_B;
+          const uint32_t d = tmem + (j & 1) * TK;
+#pragma unroll
+          for (int kk = 0; kk < HD / 32; ++kk)  // 32 dims per MMA, four per 128-byte plane
+            umma_f8(d, desc_sw128(q_s + (kk >> 2) * G::PLANE_Q + (kk & 3) * 32),
+                    desc_sw128(k_s + (kk >> 2) * G::PLANE_K + (kk & 3) * 32), IDESC_S, kk > 0 ? 1u : 0u);
+          umma_commit(&bars->s_full[j & 1]);
+        }
+        __syncwarp();
+      };
+      if (wait(&bars->q_full, 0) && nkv > 0) issue_s(0);
+      for (int j = 0; j < nkv && ok; ++j) {
+        if (j + 1 < nkv) issue_s(j + 1);
+        if (!ok) break;
+        if (!wait(&bars->p_full[j & 1], (j >> 1) & 1)) break;
+        if (!SL && j >= 1 && !wait(&bars->o_free, (j - 1) & 1)) break;  // O_tile of tile j - 1 has been read
+        tc_fence_after();
+        if (lane == 0) {
+          const int st = j % NKV;
+          const uint32_t p_s = sbase + OFF_P + (j & 1) * (TQ * TK);
+          const uint32_t v_s = sbase + OFF_KV + st * STAGE_B + TILE_B;
+          const uint32_t d = tmem + 2 * TK;  // O_tile (SL: the running sum O)
+#pragma unroll
+          for (int kk = 0; kk < TK / 32; ++kk)  // 32 keys = 2 V pages per MMA
+            umma_f8(d, desc_sw128(p_s + kk * 32), desc_interleave(v_s + kk * 2 * PAGE_B, PAGE_B, 128), IDESC_O,
+                    (kk > 0 || (SL && j > 0)) ? 1u : 0u);
+          umma_commit(&bars->o_full);
+          umma_commit(&bars->kv_empty[st]);
+        }
+        __syncwarp();
+      }
+      // every MMA this thread issued has completed before TMEM is released
+      if (lane == 0) umma_commit(&bars->mma_done);
+      __syncwarp();
+      mbar_wait(&bars->mma_done, 0);
+    }
+  } else if (warp >= NSOFT) {
+    setmaxnreg_dec<REG_CORR>();
+    // -------------------------------------------------- correction warps --
+    // Second accumulation level: O_run = O_run * alpha_j + O_tile_j in FP32
+    // for every key tile j, then the output rows.  One thread per query row
+    // (TMEM lane), all HD columns, so the softmax warps never wait for it.
+    if constexpr (!SL) {
+      const int quarter = warp & 3;
+      const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+      const int row = quarter * 32 + lane;
+      const uint32_t o_tile = tmem + t_lane + 2 * TK;
+      const uint32_t o_run = o_tile + HD;
+      const float* alpha_s = reinterpret_cast<const float*>(smem + G::OFF_ALPHA);
+      const float* xsum = reinterpret_cast<const float*>(smem + OFF_XCH) + 2 * 2 * TQ;
+      bool ok = true;
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        if (!ok) return false;
+        const bool got = mbar_wait(bar, parity, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
           set_status(p.dev_status, KVQ_DEV_TIMEOUT);
           *abort_flag = 1;
         }
-      }
-      return ok;
-    };
-    auto issue_s = [&](int j) {  // S[j%2] = Q K_j^T
-      const int st = j % NKV;
-      if (!wait(&bars->kv_full[st], (j / NKV) & 1)) return;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t k_s = sbase + OFF_KV + st * STAGE_B;
-        const uint32_t d = tmem + (j & 1) * TK;
+        return ok;
+      };
+      {  // O_run = 0
+        uint32_t z[16];
 #pragma unroll
-        for (int kk = 0; kk < HD / 32; ++kk)  // 32 dims per MMA, four per 128-byte plane
-          umma_f8(d, desc_sw128(q_s + (kk >> 2) * G::PLANE_Q + (kk & 3) * 32),
-                  desc_sw128(k_s + (kk >> 2) * G::PLANE_K + (kk & 3) * 32), IDESC_S, kk > 0 ? 1u : 0u);
-        umma_commit(&bars->s_full[j & 1]);
-      }
-      __syncwarp();
-    };
-    if (wait(&bars->q_full, 0) && nkv > 0) issue_s(0);
-    for (int j = 0; j < nkv && ok; ++j) {
-      if (j + 1 < nkv) issue_s(j + 1);
-      if (!ok) break;
-      if (!wait(&bars->p_full[j & 1], (j >> 1) & 1)) break;
-      if (!SL && j >= 1 && !wait(&bars->o_free, (j - 1) & 1)) break;  // O_tile of tile j - 1 has been read
-      tc_fence_after();
-      if (lane == 0) {
-        const int st = j % NKV;
-        const uint32_t p_s = sbase + OFF_P + (j & 1) * (TQ * TK);
-        const uint32_t v_s = sbase + OFF_KV + st * STAGE_B + TILE_B;
-        const uint32_t d = tmem + 2 * TK;  // O_tile (SL: the running sum O)
+        for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll
-        for (int kk = 0; kk < TK / 32; ++kk)  // 32 keys = 2 V pages per MMA
-          umma_f8(d, desc_sw128(p_s + kk * 32), desc_interleave(v_s + kk * 2 * PAGE_B, PAGE_B, 128), IDESC_O,
-                  (kk > 0 || (SL && j > 0)) ? 1u : 0u);
-        umma_commit(&bars->o_full);
-        umma_commit(&bars->kv_empty[st]);
+        for (int c = 0; c < HD / 16; ++c) tmem_st16(o_run + 16 * c, z);
       }
-      __syncwarp();
+      float alpha = 0.f;  // tile 0: O_run is zero
+      for (int j = 0; j < nkv && ok; ++j) {
+        if (!wait_all(&bars->o_full, j & 1)) break;  // P.V of tile j is in O_tile
+        tc_fence_after();
+        tmem_wait_st();  // this thread's previous O_run update
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+        for (int c = 0; c < HD / 16; ++c) {
+          uint32_t t[16], o[16];
+          tmem_ld16_async(o_tile + 16 * c, t);
+          tmem_ld16_async(o_run + 16 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            const float2 r = ffma2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2,
+                                   make_float2(__uint_as_float(t[i]), __uint_as_float(t[i + 1])));
+            o[i] = __float_as_uint(r.x);
+            o[i + 1] = __float_as_uint(r.y);
+          }
+          tmem_st16(o_run + 16 * c, o);
+        }
+        // alpha of tile j + 1 (the softmax warps store it before publishing
+        // P_{j+1}); O_tile is released only after that wait, so P.V of tile
+        // j + 2 -- and the slot's next alpha -- cannot come before this read
+        if (j + 1 < nkv) {
+          if (!wait_all(&bars->p_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) break;
+          alpha = alpha_s[((j + 1) & 1) * TQ + row];
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->o_free);
+      }
+      named_bar_sync(2, (NSOFT + NCORR) * 32);  // the row sums of both softmax halves
+      if (ok) {
+        // out = O_run * v_scale / l (both in units of 2^8 p)
+        const float lt = xsum[row] + xsum[TQ + row];
+        const bool live_row = job.q0 + row < job.nq;
+        const size_t out_row = (static_cast<size_t>(p.cu_seqlens_q[job.b]) + job.q0 + row) * p.Hq + job.h;
+        const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
+        tmem_wait_st();
+        uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD);
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_run + 32 * c, o);
+          if (live_row) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(o[8 * w + 0]) * f, __uint_as_float(o[8 * w + 1]) * f);
+              u.y = pack_bf16x2(__uint_as_float(o[8 * w + 2]) * f, __uint_as_float(o[8 * w + 3]) * f);
+              u.z = pack_bf16x2(__uint_as_float(o[8 * w + 4]) * f, __uint_as_float(o[8 * w + 5]) * f);
+              u.w = pack_bf16x2(__uint_as_float(o[8 * w + 6]) * f, __uint_as_float(o[8 * w + 7]) * f);
+              dst[4 * c + w] = u;
+            }
+          }
+        }
+      }
     }
-    // every MMA this thread issued has completed before TMEM is released
-    if (lane == 0) umma_commit(&bars->mma_done);
-    __syncwarp();
-    mbar_wait(&bars->mma_done, 0);
   } else {
+    setmaxnreg_inc<REG_SOFT>();
     // ------------------------------------------------------ softmax warps --
-    const int half = (warp - 2) >> 2;      // columns half*64 .. +63 of S and of O
+    const int half = warp >> 2;            // columns half*64 .. +63 of S (SL: and of O)
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     const int row = quarter * 32 + lane;   // TMEM lane == query row
@@ -422,16 +531,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const int tail = job.L % kPage;          // valid tokens in the last page (0 = full)
     const int last_page = (job.L - 1) / kPage;
 
-    const uint32_t o_tile = tmem + t_lane + 2 * TK + half * HO;  // this half's columns of O_tile (SL: of O)
-    const uint32_t o_run = o_tile + HD;                           // ... and of O_run (two-level)
-    if (!SL) {  // O_run = 0
-      uint32_t z[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) z[i] = 0u;
-#pragma unroll
-      for (int c = 0; c < HO / 16; ++c) tmem_st16(o_run + 16 * c, z);
-    }
-    float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+    const uint32_t o_tile = tmem + t_lane + 2 * TK + half * HO;  // SL: this half's columns of O
+    float* alpha_s = reinterpret_cast<float*>(smem + G::OFF_ALPHA);  // [2][TQ], read by the correction warps
+    float m = -INFINITY, l = 0.f;
     bool ok = true;  // warp-uniform, since tcgen05.ld / st need every lane of the warp
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       if (!ok) return false;
@@ -442,32 +544,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         *abort_flag = 1;
       }
       return ok;
-    };
-
-    auto accumulate = [&](int jt, float alpha) {  // O_run = O_run * alpha + O_tile (this half's dims)
-      if (!wait_all(&bars->o_full, jt & 1)) return;
-      tc_fence_after();
-      tmem_wait_st();  // the previous update of O_run
-      const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll
-      for (int c = 0; c < HO / 16; ++c) {  // 16 columns at a time
-        uint32_t t[16], o[16];
-        tmem_ld16_async(o_tile + 16 * c, t);
-        tmem_ld16_async(o_run + 16 * c, o);
-        tmem_wait_ld();
-        if (c == HO / 16 - 1) {  // the whole tile has been read: the next P.V may overwrite it
-          tc_fence_before();
-          mbar_arrive(&bars->o_free);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          const float2 r = ffma2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2,
-                                 make_float2(__uint_as_float(t[i]), __uint_as_float(t[i + 1])));
-          o[i] = __float_as_uint(r.x);
-          o[i + 1] = __float_as_uint(r.y);
-        }
-        tmem_st16(o_run + 16 * c, o);
-      }
     };
 
     auto rescale = [&](int jt, float alpha) {  // SL: O *= alpha once P.V of tile jt has landed
@@ -532,6 +608,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         const float m_new = fmaxf(m, fmaxf(mx, xmax[((j & 1) * 2 + (half ^ 1)) * TQ + row]));
         const float nb = (m_new == -INFINITY) ? 0.f : 8.f - m_new * coef;
         const float alpha = (m == -INFINITY) ? 0.f : ex2((m - m_new) * coef);
+        if (!SL && half == 0) alpha_s[(j & 1) * TQ + row] = alpha;  // for the correction warps
         float2 rs2 = make_float2(0.f, 0.f);  // in units of 2^8 p
         const float2 coef2 = make_float2(coef, coef), nb2 = make_float2(nb, nb);
         uint8_t* prow = smem + OFF_P + (j & 1) * (TQ * TK) + row * TK;
@@ -561,39 +638,34 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         }
         tc_fence_before();
         mbar_arrive(&bars->p_full[j & 1]);
-        if constexpr (!SL) {
-          if (j >= 1) accumulate(j - 1, alpha_prev);
-        }
-        alpha_prev = alpha;
       }
     }
-    if constexpr (SL) {
-      if (nkv >= 1 && wait_all(&bars->o_full, (nkv - 1) & 1)) tc_fence_after();
+    if constexpr (!SL) {  // the correction warps finish O_run and write the output
+      xsum[half * TQ + row] = l;
+      named_bar_arrive(2, (NSOFT + NCORR) * 32);
     } else {
-      if (ok && nkv >= 1) accumulate(nkv - 1, alpha_prev);
-    }
-
-    // epilogue: out = O * v_scale / l (O and l both in units of 2^8 p), l summed over both halves
-    xsum[half * TQ + row] = l;
-    named_bar_sync(1, NSOFT * 32);
-    const float lt = l + xsum[(half ^ 1) * TQ + row];
-    if (ok) {
-      if (!SL) tmem_wait_st();
-      const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD + half * HO);
+      if (nkv >= 1 && wait_all(&bars->o_full, (nkv - 1) & 1)) tc_fence_after();
+      // epilogue: out = O * v_scale / l (O and l both in units of 2^8 p), l summed over both halves
+      xsum[half * TQ + row] = l;
+      named_bar_sync(1, NSOFT * 32);
+      const float lt = l + xsum[(half ^ 1) * TQ + row];
+      if (ok) {
+        const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD + half * HO);
 #pragma unroll
-      for (int c = 0; c < HO / 32; ++c) {  // 32 columns of O at a time
-        uint32_t o[32];
-        tmem_ld32((SL ? o_tile : o_run) + 32 * c, o);
-        if (live_row) {
+        for (int c = 0; c < HO / 32; ++c) {  // 32 columns of O at a time
+          uint32_t o[32];
+          tmem_ld32(o_tile + 32 * c, o);
+          if (live_row) {
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(o[8 * w + 0]) * f, __uint_as_float(o[8 * w + 1]) * f);
-            u.y = pack_bf16x2(__uint_as_float(o[8 * w + 2]) * f, __uint_as_float(o[8 * w + 3]) * f);
-            u.z = pack_bf16x2(__uint_as_float(o[8 * w + 4]) * f, __uint_as_float(o[8 * w + 5]) * f);
-            u.w = pack_bf16x2(__uint_as_float(o[8 * w + 6]) * f, __uint_as_float(o[8 * w + 7]) * f);
-            dst[4 * c + w] = u;
+            for (int w = 0; w < 4; ++w) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(o[8 * w + 0]) * f, __uint_as_float(o[8 * w + 1]) * f);
+              u.y = pack_bf16x2(__uint_as_float(o[8 * w + 2]) * f, __uint_as_float(o[8 * w + 3]) * f);
+              u.z = pack_bf16x2(__uint_as_float(o[8 * w + 4]) * f, __uint_as_float(o[8 * w + 5]) * f);
+              u.w = pack_bf16x2(__uint_as_float(o[8 * w + 6]) * f, __uint_as_float(o[8 * w + 7]) * f);
+              dst[4 * c + w] = u;
+            }
           }
         }
       }
@@ -602,7 +674,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == W_MMA) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
   }
