@@ -127,6 +127,12 @@ KVQ_DEVINL void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" :::
 // this grid's completion in grid_dependency_wait()).
 KVQ_DEVINL void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// max(a, b, c) in one instruction (sm_100 and later); NaN inputs are ignored as by fmaxf.
+KVQ_DEVINL float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 KVQ_DEVINL void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }

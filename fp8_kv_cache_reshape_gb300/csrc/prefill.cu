@@ -84,8 +84,8 @@ struct Geo {
   static constexpr int OFF_P = OFF_KV + NKV * STAGE_B;  // 2 P buffers of 16 KB
   static constexpr int OFF_BAR = OFF_P + 2 * TQ * TK;
   static constexpr int OFF_XCH = OFF_BAR + 512;  // row max / row sum exchange between column halves
-  static constexpr int OFF_ALPHA = OFF_XCH + 3 * 2 * TQ * 4;  // [2][TQ] rescale factors, softmax -> correction
-  static constexpr int SMEM_BYTES = OFF_ALPHA + 2 * TQ * 4 + 1024;  // + alignment slack
+  static constexpr int OFF_ALPHA = OFF_XCH + 3 * 2 * TQ * 4;  // [4][TQ] rescale factors, softmax -> correction
+  static constexpr int SMEM_BYTES = OFF_ALPHA + 4 * TQ * 4 + 1024;  // + alignment slack
   static constexpr int HO = HD / 2;              // output dims per softmax thread
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
@@ -117,6 +117,7 @@ struct Bars {
   uint64_t p_full[2];
   uint64_t o_full;  // P.V of the current tile is in O_tile
   uint64_t o_free;  // O_tile has been folded into O_run (correction warps)
+  uint64_t a_full[4];  // alpha of tile j is in slot j % 4 (softmax half 0 -> correction warps)
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -183,6 +184,26 @@ KVQ_DEVINL void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
       : "r"(taddr));
   tmem_wait_ld();
+}
+// tcgen05.ld without the wait; the registers are valid after tmem_wait_ld(),
+// and tmem_pin32() after that wait keeps the compiler from using them earlier.
+KVQ_DEVINL void tmem_ld32_nowait(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+KVQ_DEVINL void tmem_pin32(uint32_t (&v)[32]) {
+  asm volatile(""
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                 "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                 "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                 "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
+                 "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
 }
 
 struct Job {
@@ -257,6 +278,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     }
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_free, NCORR * 32);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars->a_full[i], NSOFT / 2 * 32);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -441,8 +463,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
 #pragma unroll
         for (int c = 0; c < HD / 16; ++c) tmem_st16(o_run + 16 * c, z);
       }
-      float alpha = 0.f;  // tile 0: O_run is zero
+      // The softmax warps cannot finish tile j + 3 before O_tile of tile j
+      // is released here (S_{j+3} is issued after P.V of tile j + 1, which
+      // waits for that release), so four alpha slots and their barriers'
+      // parities never alias.
       for (int j = 0; j < nkv && ok; ++j) {
+        float alpha = 0.f;  // tile 0: O_run is zero
+        if (j > 0) {
+          if (!wait_all(&bars->a_full[j & 3], (j >> 2) & 1)) break;
+          alpha = alpha_s[(j & 3) * TQ + row];
+        }
         if (!wait_all(&bars->o_full, j & 1)) break;  // P.V of tile j is in O_tile
         tc_fence_after();
         tmem_wait_st();  // this thread's previous O_run update
@@ -453,6 +483,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
           tmem_ld16_async(o_tile + 16 * c, t);
           tmem_ld16_async(o_run + 16 * c, o);
           tmem_wait_ld();
+          if (c == HD / 16 - 1) {  // all of O_tile has been read: P.V of the next tile may overwrite it
+            tc_fence_before();
+            mbar_arrive(&bars->o_free);
+          }
 #pragma unroll
           for (int i = 0; i < 16; i += 2) {
             const float2 r = ffma2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2,
@@ -462,15 +496,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
           }
           tmem_st16(o_run + 16 * c, o);
         }
-        // alpha of tile j + 1 (the softmax warps store it before publishing
-        // P_{j+1}); O_tile is released only after that wait, so P.V of tile
-        // j + 2 -- and the slot's next alpha -- cannot come before this read
-        if (j + 1 < nkv) {
-          if (!wait_all(&bars->p_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) break;
-          alpha = alpha_s[((j + 1) & 1) * TQ + row];
-        }
-        tc_fence_before();
-        mbar_arrive(&bars->o_free);
       }
       named_bar_sync(2, (NSOFT + NCORR) * 32);  // the row sums of both softmax halves
       if (ok) {
@@ -532,7 +557,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const int last_page = (job.L - 1) / kPage;
 
     const uint32_t o_tile = tmem + t_lane + 2 * TK + half * HO;  // SL: this half's columns of O
-    float* alpha_s = reinterpret_cast<float*>(smem + G::OFF_ALPHA);  // [2][TQ], read by the correction warps
+    float* alpha_s = reinterpret_cast<float*>(smem + G::OFF_ALPHA);  // [4][TQ], read by the correction warps
     float m = -INFINITY, l = 0.f;
     bool ok = true;  // warp-uniform, since tcgen05.ld / st need every lane of the warp
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
@@ -584,12 +609,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         const bool need_mask = (key0 + HC > kend) || bad != 0;
         const uint32_t sbuf = tmem + t_lane + (j & 1) * TK + half * HC;
         // raw scores (the positive scale is applied in the exponent below)
+        {  // both 32-column loads in flight, one wait
+          static_assert(HC == 64, "two 32-column loads");
+          uint32_t v0[32], v1[32];
+          tmem_ld32_nowait(sbuf, v0);
+          tmem_ld32_nowait(sbuf + 32, v1);
+          tmem_wait_ld();
+          tmem_pin32(v0);
+          tmem_pin32(v1);
 #pragma unroll
-        for (int c = 0; c < HC / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(sbuf + c * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 32; ++i) {
+            sv[i] = __uint_as_float(v0[i]);
+            sv[32 + i] = __uint_as_float(v1[i]);
+          }
         }
         if (need_mask) {  // last tiles only; static indices keep sv in registers
           const int lim = kend - key0;  // columns k < lim are causally visible
@@ -598,8 +630,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
           for (int k = 0; k < HC; ++k)
             sv[k] = (k >= lim || ((badh >> (k / kPage)) & 1)) ? -INFINITY : sv[k];
         }
+        // row maximum as a tree of three-input maxima (depth 4, not a 64-long chain)
+        static_assert(HC == 64, "the max tree below covers 64 columns");
+        float m1[22], m2[8];
 #pragma unroll
-        for (int k = 0; k < HC; ++k) mx = fmaxf(mx, sv[k]);
+        for (int i = 0; i < 21; ++i) m1[i] = fmax3(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
+        m1[21] = sv[63];
+#pragma unroll
+        for (int i = 0; i < 7; ++i) m2[i] = fmax3(m1[3 * i], m1[3 * i + 1], m1[3 * i + 2]);
+        m2[7] = m1[21];
+        mx = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
       }
       xmax[((j & 1) * 2 + half) * TQ + row] = mx;
       named_bar_sync(1, NSOFT * 32);
@@ -608,8 +648,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         const float m_new = fmaxf(m, fmaxf(mx, xmax[((j & 1) * 2 + (half ^ 1)) * TQ + row]));
         const float nb = (m_new == -INFINITY) ? 0.f : 8.f - m_new * coef;
         const float alpha = (m == -INFINITY) ? 0.f : ex2((m - m_new) * coef);
-        if (!SL && half == 0) alpha_s[(j & 1) * TQ + row] = alpha;  // for the correction warps
-        float2 rs2 = make_float2(0.f, 0.f);  // in units of 2^8 p
+        if (!SL && half == 0) {  // for the correction warps
+          alpha_s[(j & 3) * TQ + row] = alpha;
+          mbar_arrive(&bars->a_full[j & 3]);
+        }
+        float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // in units of 2^8 p; two chains
         const float2 coef2 = make_float2(coef, coef), nb2 = make_float2(nb, nb);
         uint8_t* prow = smem + OFF_P + (j & 1) * (TQ * TK) + row * TK;
 #pragma unroll
@@ -620,7 +663,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
             const float2 e = ffma2(make_float2(sv[pg * 16 + t], sv[pg * 16 + t + 1]), coef2, nb2);
             q[t] = ex2(e.x);
             q[t + 1] = ex2(e.y);
-            rs2 = fadd2(rs2, make_float2(q[t], q[t + 1]));
+            rs2[(t >> 1) & 1] = fadd2(rs2[(t >> 1) & 1], make_float2(q[t], q[t + 1]));
           }
           // word w of a page holds keys 2w, 2w+1, 2w+8, 2w+9 (the V slot order)
           uint32_t w[4];
@@ -630,7 +673,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
           const int chunk = half * (HC / kPage) + pg;  // page index within the tile
           *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        l = l * alpha + (rs2.x + rs2.y);
+        l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
         m = m_new;
         fence_proxy_async_smem();
         if constexpr (SL) {
