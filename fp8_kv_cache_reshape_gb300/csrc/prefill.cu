@@ -86,7 +86,6 @@ struct Geo {
   static constexpr int OFF_XCH = OFF_BAR + 512;  // row max / row sum exchange between column halves
   static constexpr int OFF_ALPHA = OFF_XCH + 3 * 2 * TQ * 4;  // [4][TQ] rescale factors, softmax -> correction
   static constexpr int SMEM_BYTES = OFF_ALPHA + 4 * TQ * 4 + 1024;  // + alignment slack
-  static constexpr int HO = HD / 2;              // output dims per softmax thread
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -250,7 +249,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
   static_assert(HD == 128 || (HD == 256 && SL), "head_dim 256 runs with single-level accumulation");
   constexpr int NKV = G::NKV, PAGE_B = G::PAGE_B, TILE_B = G::TILE_B, STAGE_B = G::STAGE_B;
   constexpr int OFF_Q = G::OFF_Q, OFF_KV = G::OFF_KV, OFF_P = G::OFF_P, OFF_XCH = G::OFF_XCH;
-  constexpr int HO = G::HO;
   using BarsN = Bars<NKV>;
   static_assert(sizeof(BarsN) <= 512, "barrier block");
   extern __shared__ uint8_t smem_raw[];
@@ -410,7 +408,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         if (j + 1 < nkv) issue_s(j + 1);
         if (!ok) break;
         if (!wait(&bars->p_full[j & 1], (j >> 1) & 1)) break;
-        if (!SL && j >= 1 && !wait(&bars->o_free, (j - 1) & 1)) break;  // O_tile of tile j - 1 has been read
+        // two-level: O_tile of tile j - 1 has been read; SL: O has been rescaled for tile j
+        if (j >= 1 && !wait(&bars->o_free, (j - 1) & 1)) break;
         tc_fence_after();
         if (lane == 0) {
           const int st = j % NKV;
@@ -434,28 +433,35 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
   } else if (warp >= NSOFT) {
     setmaxnreg_dec<REG_CORR>();
     // -------------------------------------------------- correction warps --
-    // Second accumulation level: O_run = O_run * alpha_j + O_tile_j in FP32
-    // for every key tile j, then the output rows.  One thread per query row
-    // (TMEM lane), all HD columns, so the softmax warps never wait for it.
+    // The rescale of the running sum, off the softmax warps' path, then the
+    // output rows.  One thread per query row (TMEM lane), all HD columns.
+    //  two-level: O_run = O_run * alpha_j + O_tile_j in FP32 for every key
+    //             tile j (the second level), O_tile released for P.V j + 1;
+    //  SL:        O = O * alpha_j in place (skipped when alpha_j is 1 for the
+    //             whole warp) once P.V of tile j - 1 has landed, released for
+    //             P.V of tile j, which adds into O.
+    // The softmax warps cannot finish tile j + 3 before the release for tile
+    // j (S_{j+3} is issued after P.V of tile j + 1, which waits for it), so
+    // the four alpha slots and their barriers' parities never alias.
+    const int quarter = warp & 3;
+    const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+    const int row = quarter * 32 + lane;
+    const uint32_t o_tile = tmem + t_lane + 2 * TK;  // SL: O
+    const uint32_t o_run = o_tile + HD;              // two-level only
+    const float* alpha_s = reinterpret_cast<const float*>(smem + G::OFF_ALPHA);
+    const float* xsum = reinterpret_cast<const float*>(smem + OFF_XCH) + 2 * 2 * TQ;
+    bool ok = true;
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      if (!ok) return false;
+      const bool got = mbar_wait(bar, parity, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        set_status(p.dev_status, KVQ_DEV_TIMEOUT);
+        *abort_flag = 1;
+      }
+      return ok;
+    };
     if constexpr (!SL) {
-      const int quarter = warp & 3;
-      const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
-      const int row = quarter * 32 + lane;
-      const uint32_t o_tile = tmem + t_lane + 2 * TK;
-      const uint32_t o_run = o_tile + HD;
-      const float* alpha_s = reinterpret_cast<const float*>(smem + G::OFF_ALPHA);
-      const float* xsum = reinterpret_cast<const float*>(smem + OFF_XCH) + 2 * 2 * TQ;
-      bool ok = true;
-      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-        if (!ok) return false;
-        const bool got = mbar_wait(bar, parity, abort_flag);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          set_status(p.dev_status, KVQ_DEV_TIMEOUT);
-          *abort_flag = 1;
-        }
-        return ok;
-      };
       {  // O_run = 0
         uint32_t z[16];
 #pragma unroll
@@ -463,10 +469,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
 #pragma unroll
         for (int c = 0; c < HD / 16; ++c) tmem_st16(o_run + 16 * c, z);
       }
-      // The softmax warps cannot finish tile j + 3 before O_tile of tile j
-      // is released here (S_{j+3} is issued after P.V of tile j + 1, which
-      // waits for that release), so four alpha slots and their barriers'
-      // parities never alias.
       for (int j = 0; j < nkv && ok; ++j) {
         float alpha = 0.f;  // tile 0: O_run is zero
         if (j > 0) {
@@ -497,29 +499,52 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
           tmem_st16(o_run + 16 * c, o);
         }
       }
-      named_bar_sync(2, (NSOFT + NCORR) * 32);  // the row sums of both softmax halves
-      if (ok) {
-        // out = O_run * v_scale / l (both in units of 2^8 p)
-        const float lt = xsum[row] + xsum[TQ + row];
-        const bool live_row = job.q0 + row < job.nq;
-        const size_t out_row = (static_cast<size_t>(p.cu_seqlens_q[job.b]) + job.q0 + row) * p.Hq + job.h;
-        const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
-        tmem_wait_st();
-        uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD);
+    } else {
+      for (int j = 1; j < nkv && ok; ++j) {
+        if (!wait_all(&bars->a_full[j & 3], (j >> 2) & 1)) break;
+        const float alpha = alpha_s[(j & 3) * TQ + row];
+        if (!wait_all(&bars->o_full, (j - 1) & 1)) break;  // P.V of tile j - 1 has landed in O
+        tc_fence_after();
+        if (!__all_sync(0xffffffffu, alpha == 1.f)) {  // exact when skipped
+#pragma unroll 4
+          for (int c = 0; c < HD / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld16_async(o_tile + 16 * c, o);
+            tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(o_run + 32 * c, o);
-          if (live_row) {
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st16(o_tile + 16 * c, o);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&bars->o_free);  // P.V of tile j may add into O
+      }
+      if (nkv >= 1 && wait_all(&bars->o_full, (nkv - 1) & 1)) tc_fence_after();
+    }
+    named_bar_sync(2, (NSOFT + NCORR) * 32);  // the row sums of both softmax halves
+    if (ok) {
+      // out = O * v_scale / l (both in units of 2^8 p)
+      const float lt = xsum[row] + xsum[TQ + row];
+      const bool live_row = job.q0 + row < job.nq;
+      const size_t out_row = (static_cast<size_t>(p.cu_seqlens_q[job.b]) + job.q0 + row) * p.Hq + job.h;
+      const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
+      tmem_wait_st();
+      const uint32_t o_out = SL ? o_tile : o_run;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD);
+#pragma unroll 2
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(o_out + 32 * c, o);
+        if (live_row) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(o[8 * w + 0]) * f, __uint_as_float(o[8 * w + 1]) * f);
-              u.y = pack_bf16x2(__uint_as_float(o[8 * w + 2]) * f, __uint_as_float(o[8 * w + 3]) * f);
-              u.z = pack_bf16x2(__uint_as_float(o[8 * w + 4]) * f, __uint_as_float(o[8 * w + 5]) * f);
-              u.w = pack_bf16x2(__uint_as_float(o[8 * w + 6]) * f, __uint_as_float(o[8 * w + 7]) * f);
-              dst[4 * c + w] = u;
-            }
+          for (int w = 0; w < 4; ++w) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(o[8 * w + 0]) * f, __uint_as_float(o[8 * w + 1]) * f);
+            u.y = pack_bf16x2(__uint_as_float(o[8 * w + 2]) * f, __uint_as_float(o[8 * w + 3]) * f);
+            u.z = pack_bf16x2(__uint_as_float(o[8 * w + 4]) * f, __uint_as_float(o[8 * w + 5]) * f);
+            u.w = pack_bf16x2(__uint_as_float(o[8 * w + 6]) * f, __uint_as_float(o[8 * w + 7]) * f);
+            dst[4 * c + w] = u;
           }
         }
       }
@@ -527,7 +552,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
   } else {
     setmaxnreg_inc<REG_SOFT>();
     // ------------------------------------------------------ softmax warps --
-    const int half = warp >> 2;            // columns half*64 .. +63 of S (SL: and of O)
+    const int half = warp >> 2;            // columns half*64 .. +63 of S
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     const int row = quarter * 32 + lane;   // TMEM lane == query row
@@ -556,7 +581,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const int tail = job.L % kPage;          // valid tokens in the last page (0 = full)
     const int last_page = (job.L - 1) / kPage;
 
-    const uint32_t o_tile = tmem + t_lane + 2 * TK + half * HO;  // SL: this half's columns of O
     float* alpha_s = reinterpret_cast<float*>(smem + G::OFF_ALPHA);  // [4][TQ], read by the correction warps
     float m = -INFINITY, l = 0.f;
     bool ok = true;  // warp-uniform, since tcgen05.ld / st need every lane of the warp
@@ -569,22 +593,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         *abort_flag = 1;
       }
       return ok;
-    };
-
-    auto rescale = [&](int jt, float alpha) {  // SL: O *= alpha once P.V of tile jt has landed
-      if (!wait_all(&bars->o_full, jt & 1)) return;
-      tc_fence_after();
-      if (__all_sync(0xffffffffu, alpha == 1.f)) return;  // exact: nothing to do
-#pragma unroll
-      for (int c = 0; c < HO / 16; ++c) {
-        uint32_t o[16];
-        tmem_ld16_async(o_tile + 16 * c, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st16(o_tile + 16 * c, o);
-      }
-      tmem_wait_st();
     };
 
     // every softmax thread runs every tile's named barrier, also after a
@@ -648,7 +656,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         const float m_new = fmaxf(m, fmaxf(mx, xmax[((j & 1) * 2 + (half ^ 1)) * TQ + row]));
         const float nb = (m_new == -INFINITY) ? 0.f : 8.f - m_new * coef;
         const float alpha = (m == -INFINITY) ? 0.f : ex2((m - m_new) * coef);
-        if (!SL && half == 0) {  // for the correction warps
+        if (half == 0) {  // for the correction warps
           alpha_s[(j & 3) * TQ + row] = alpha;
           mbar_arrive(&bars->a_full[j & 3]);
         }
@@ -676,43 +684,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
         m = m_new;
         fence_proxy_async_smem();
-        if constexpr (SL) {
-          if (j >= 1) rescale(j - 1, alpha);  // before P.V of tile j adds into O
-        }
         tc_fence_before();
         mbar_arrive(&bars->p_full[j & 1]);
       }
     }
-    if constexpr (!SL) {  // the correction warps finish O_run and write the output
-      xsum[half * TQ + row] = l;
-      named_bar_arrive(2, (NSOFT + NCORR) * 32);
-    } else {
-      if (nkv >= 1 && wait_all(&bars->o_full, (nkv - 1) & 1)) tc_fence_after();
-      // epilogue: out = O * v_scale / l (O and l both in units of 2^8 p), l summed over both halves
-      xsum[half * TQ + row] = l;
-      named_bar_sync(1, NSOFT * 32);
-      const float lt = l + xsum[(half ^ 1) * TQ + row];
-      if (ok) {
-        const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD + half * HO);
-#pragma unroll
-        for (int c = 0; c < HO / 32; ++c) {  // 32 columns of O at a time
-          uint32_t o[32];
-          tmem_ld32(o_tile + 32 * c, o);
-          if (live_row) {
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(o[8 * w + 0]) * f, __uint_as_float(o[8 * w + 1]) * f);
-              u.y = pack_bf16x2(__uint_as_float(o[8 * w + 2]) * f, __uint_as_float(o[8 * w + 3]) * f);
-              u.z = pack_bf16x2(__uint_as_float(o[8 * w + 4]) * f, __uint_as_float(o[8 * w + 5]) * f);
-              u.w = pack_bf16x2(__uint_as_float(o[8 * w + 6]) * f, __uint_as_float(o[8 * w + 7]) * f);
-              dst[4 * c + w] = u;
-            }
-          }
-        }
-      }
-    }
+    // the correction warps finish the sum and write the output rows
+    xsum[half * TQ + row] = l;
+    named_bar_arrive(2, (NSOFT + NCORR) * 32);
   }
 
   tc_fence_before();
