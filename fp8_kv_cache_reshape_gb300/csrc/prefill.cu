@@ -50,18 +50,23 @@ constexpr int TK = 128;           // keys per tile (8 pages)
 constexpr int NPROD = 2;          // producer warps; tile j comes from producer j % NPROD
 constexpr int PLANE = 128;        // bytes of one K-major operand row: 128 dims of FP8, 128-byte swizzle
 // Warp roles, in warpgroups (setmaxnreg works per warpgroup):
-//   warps 0-7   softmax (warpgroups 0, 1), two per TMEM lane quarter;
-//   warps 8-11  correction (warpgroup 2): the second accumulation level;
-//   warps 12-14 producer 0, MMA issuer, producer 1 (warpgroup 3; warp 15 idle).
+//   warps 0 .. NSOFT-1  softmax, NPART per TMEM lane quarter (NPART threads
+//                       per query row, TK / NPART columns of S each);
+//   the next 4 warps    correction: the second accumulation level;
+//   the last 4 warps    producer 0, MMA issuer, producer 1 (and one idle).
 constexpr int NSOFT = 8;
+constexpr int NPART = NSOFT / 4;
 constexpr int NCORR = 4;
-constexpr int W_PROD0 = 12, W_MMA = 13, W_PROD1 = 14;
-constexpr int NTHREADS = 16 * 32;
-// registers per thread: 65,536 / 512 = 128 at launch, then 184 for softmax,
-// 80 for correction, 56 for producers and MMA (256 x 184 + 128 x 80 + 128 x 56
-// = 64,512 <= 65,536)
-constexpr int REG_SOFT = 184, REG_CORR = 80, REG_CTRL = 56;
-static_assert(2 * 128 * REG_SOFT + 128 * REG_CORR + 128 * REG_CTRL <= 65536, "register split");
+constexpr int W_CORR = NSOFT;
+constexpr int W_PROD0 = NSOFT + NCORR, W_MMA = W_PROD0 + 1, W_PROD1 = W_PROD0 + 2;
+constexpr int NTHREADS = (NSOFT + NCORR + 4) * 32;
+// Registers per thread: the launch gives every thread the same count; the
+// control and correction warpgroups then give some back and the softmax
+// warpgroups take them (the sum must stay within the launch's allocation).
+constexpr int REG_LAUNCH = (65536 / NTHREADS) / 8 * 8;
+constexpr int REG_SOFT = NSOFT == 16 ? 88 : 184, REG_CORR = NSOFT == 16 ? 72 : 80, REG_CTRL = NSOFT == 16 ? 48 : 56;
+static_assert(NSOFT * 32 * REG_SOFT + NCORR * 32 * REG_CORR + 128 * REG_CTRL <= NTHREADS * REG_LAUNCH,
+              "register split");
 // TMEM: S0 | S1 | O_tile | O_run at head_dim 128 (128 columns each); at 256,
 // S0 | S1 | O (single-level accumulation: O_tile and O_run do not both fit).
 constexpr uint32_t TMEM_COLS = 512;
@@ -83,8 +88,8 @@ struct Geo {
   static constexpr int STAGE_B = 2 * TILE_B;     // K tile + V tile
   static constexpr int OFF_P = OFF_KV + NKV * STAGE_B;  // 2 P buffers of 16 KB
   static constexpr int OFF_BAR = OFF_P + 2 * TQ * TK;
-  static constexpr int OFF_XCH = OFF_BAR + 512;  // row max / row sum exchange between column halves
-  static constexpr int OFF_ALPHA = OFF_XCH + 3 * 2 * TQ * 4;  // [4][TQ] rescale factors, softmax -> correction
+  static constexpr int OFF_XCH = OFF_BAR + 512;  // row max [2][NPART][TQ] / row sum [NPART][TQ] exchange
+  static constexpr int OFF_ALPHA = OFF_XCH + 3 * NPART * TQ * 4;  // [4][TQ] rescale factors, softmax -> correction
   static constexpr int SMEM_BYTES = OFF_ALPHA + 4 * TQ * 4 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
@@ -116,7 +121,7 @@ struct Bars {
   uint64_t p_full[2];
   uint64_t o_full;  // P.V of the current tile is in O_tile
   uint64_t o_free;  // O_tile has been folded into O_run (correction warps)
-  uint64_t a_full[4];  // alpha of tile j is in slot j % 4 (softmax half 0 -> correction warps)
+  uint64_t a_full[4];  // alpha of tile j is in slot j % 4 (softmax part 0 -> correction warps)
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -213,10 +218,13 @@ struct Job {
 
 KVQ_DEVINL Job make_job(const PrefillParams& p) {
   Job j;
+  // grid (heads, query tiles, sequences), query tiles in reverse: the CTAs
+  // start in order of decreasing work (later query tiles attend to more keys
+  // under the causal mask), so the last, partial wave holds the lightest ones
   j.b = blockIdx.z;
-  j.h = blockIdx.y;
+  j.h = blockIdx.x;
   j.kvh = j.h / p.g;
-  j.q0 = blockIdx.x * TQ;
+  j.q0 = (gridDim.y - 1 - blockIdx.y) * TQ;
   const int c0 = p.cu_seqlens_q[j.b];
   const int c1 = p.cu_seqlens_q[j.b + 1];
   j.nq = c1 - c0;
@@ -276,7 +284,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     }
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_free, NCORR * 32);
-    for (int i = 0; i < 4; ++i) mbar_init(&bars->a_full[i], NSOFT / 2 * 32);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars->a_full[i], NSOFT / NPART * 32);
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -430,7 +438,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       __syncwarp();
       mbar_wait(&bars->mma_done, 0);
     }
-  } else if (warp >= NSOFT) {
+  } else if (warp >= W_CORR) {
     setmaxnreg_dec<REG_CORR>();
     // -------------------------------------------------- correction warps --
     // The rescale of the running sum, off the softmax warps' path, then the
@@ -449,7 +457,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const uint32_t o_tile = tmem + t_lane + 2 * TK;  // SL: O
     const uint32_t o_run = o_tile + HD;              // two-level only
     const float* alpha_s = reinterpret_cast<const float*>(smem + G::OFF_ALPHA);
-    const float* xsum = reinterpret_cast<const float*>(smem + OFF_XCH) + 2 * 2 * TQ;
+    const float* xsum = reinterpret_cast<const float*>(smem + OFF_XCH) + 2 * NPART * TQ;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       if (!ok) return false;
@@ -522,10 +530,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       }
       if (nkv >= 1 && wait_all(&bars->o_full, (nkv - 1) & 1)) tc_fence_after();
     }
-    named_bar_sync(2, (NSOFT + NCORR) * 32);  // the row sums of both softmax halves
+    named_bar_sync(2, (NSOFT + NCORR) * 32);  // the softmax parts' row sums
     if (ok) {
       // out = O * v_scale / l (both in units of 2^8 p)
-      const float lt = xsum[row] + xsum[TQ + row];
+      float lt = 0.f;
+#pragma unroll
+      for (int pt = 0; pt < NPART; ++pt) lt += xsum[pt * TQ + row];
       const bool live_row = job.q0 + row < job.nq;
       const size_t out_row = (static_cast<size_t>(p.cu_seqlens_q[job.b]) + job.q0 + row) * p.Hq + job.h;
       const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
@@ -552,24 +562,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
   } else {
     setmaxnreg_inc<REG_SOFT>();
     // ------------------------------------------------------ softmax warps --
-    const int half = warp >> 2;            // columns half*64 .. +63 of S
+    const int part = warp >> 2;            // columns part*HC .. +HC-1 of S
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     const int row = quarter * 32 + lane;   // TMEM lane == query row
-    constexpr int HC = TK / 2;             // columns per thread
-    float* xmax = reinterpret_cast<float*>(smem + OFF_XCH);   // [2 tiles][2 halves][TQ]
-    float* xsum = xmax + 2 * 2 * TQ;                           // [2 halves][TQ]
+    constexpr int HC = TK / NPART;         // columns per thread
+    float* xmax = reinterpret_cast<float*>(smem + OFF_XCH);   // [2 tiles][NPART][TQ]
+    float* xsum = xmax + 2 * NPART * TQ;                       // [NPART][TQ]
     const bool live_row = job.q0 + row < job.nq;
     const int qpos = job.first_q + job.q0 + row;  // absolute position of this query
     const int kend = (p.causal && qpos + 1 < job.L) ? qpos + 1 : job.L;  // this row attends to keys [0, kend)
     const size_t out_row = (static_cast<size_t>(p.cu_seqlens_q[job.b]) + job.q0 + row) * p.Hq + job.h;
 
-    // Q row (this thread's half) -> shared memory, 128-byte swizzled planes
+    // Q row (this thread's part) -> shared memory, 128-byte swizzled planes
     {
       const uint4* src = reinterpret_cast<const uint4*>(p.q8 + out_row * HD);
 #pragma unroll
-      for (int cc = 0; cc < HD / 32; ++cc) {
-        const int c = half * (HD / 32) + cc;  // 16-byte chunk of the row
+      for (int cc = 0; cc < HD / 16 / NPART; ++cc) {
+        const int c = part * (HD / 16 / NPART) + cc;  // 16-byte chunk of the row
         const uint4 v = live_row ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
         uint8_t* qs = smem + OFF_Q + (c >> 3) * G::PLANE_Q + row * PLANE;
         *reinterpret_cast<uint4*>(qs + (((c & 7) ^ (row & 7)) << 4)) = v;
@@ -599,7 +609,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     // failed wait, so no warp is left behind at bar.sync
     for (int j = 0; j < nkv; ++j) {
       const int st = j % NKV;
-      const int key0 = j * TK + half * HC;
+      const int key0 = j * TK + part * HC;
       float sv[HC];
       float mx = -INFINITY;
       uint32_t bad = 0;
@@ -609,54 +619,66 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         bad = bars->stage_bad[st];
         if (tail != 0 && last_page / (TK / kPage) == j) {
           // V rows (dims) row and row + 128 .. of the last page: slots past the sequence end
-          for (int d = row + half * TQ; d < HD; d += 2 * TQ) {
+          for (int d = row + part * TQ; d < HD; d += NPART * TQ) {
             uint8_t* vrow = smem + OFF_KV + st * STAGE_B + TILE_B + (last_page % (TK / kPage)) * PAGE_B + d * kPage;
             for (int t = tail; t < kPage; ++t) vrow[fp8_v_slot(t)] = 0;
           }
         }
         const bool need_mask = (key0 + HC > kend) || bad != 0;
-        const uint32_t sbuf = tmem + t_lane + (j & 1) * TK + half * HC;
+        const uint32_t sbuf = tmem + t_lane + (j & 1) * TK + part * HC;
         // raw scores (the positive scale is applied in the exponent below)
-        {  // both 32-column loads in flight, one wait
-          static_assert(HC == 64, "two 32-column loads");
-          uint32_t v0[32], v1[32];
-          tmem_ld32_nowait(sbuf, v0);
-          tmem_ld32_nowait(sbuf + 32, v1);
-          tmem_wait_ld();
-          tmem_pin32(v0);
-          tmem_pin32(v1);
+        {  // all 32-column loads in flight, one wait
+          static_assert(HC % 32 == 0, "32-column loads");
+          uint32_t v[HC / 32][32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            sv[i] = __uint_as_float(v0[i]);
-            sv[32 + i] = __uint_as_float(v1[i]);
+          for (int c = 0; c < HC / 32; ++c) tmem_ld32_nowait(sbuf + 32 * c, v[c]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < HC / 32; ++c) {
+            tmem_pin32(v[c]);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sv[32 * c + i] = __uint_as_float(v[c][i]);
           }
         }
         if (need_mask) {  // last tiles only; static indices keep sv in registers
           const int lim = kend - key0;  // columns k < lim are causally visible
-          const uint32_t badh = bad >> (half * (HC / kPage));
+          const uint32_t badh = bad >> (part * (HC / kPage));
 #pragma unroll
           for (int k = 0; k < HC; ++k)
             sv[k] = (k >= lim || ((badh >> (k / kPage)) & 1)) ? -INFINITY : sv[k];
         }
-        // row maximum as a tree of three-input maxima (depth 4, not a 64-long chain)
-        static_assert(HC == 64, "the max tree below covers 64 columns");
-        float m1[22], m2[8];
+        // row maximum as a tree of three-input maxima, not a long chain
+        static_assert(HC == 64 || HC == 32, "the max trees below cover 64 or 32 columns");
+        if constexpr (HC == 64) {
+          float m1[22], m2[8];
 #pragma unroll
-        for (int i = 0; i < 21; ++i) m1[i] = fmax3(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
-        m1[21] = sv[63];
+          for (int i = 0; i < 21; ++i) m1[i] = fmax3(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
+          m1[21] = sv[63];
 #pragma unroll
-        for (int i = 0; i < 7; ++i) m2[i] = fmax3(m1[3 * i], m1[3 * i + 1], m1[3 * i + 2]);
-        m2[7] = m1[21];
-        mx = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
+          for (int i = 0; i < 7; ++i) m2[i] = fmax3(m1[3 * i], m1[3 * i + 1], m1[3 * i + 2]);
+          m2[7] = m1[21];
+          mx = fmax3(fmax3(m2[0], m2[1], m2[2]), fmax3(m2[3], m2[4], m2[5]), fmaxf(m2[6], m2[7]));
+        } else {
+          float m1[11], m2[4];
+#pragma unroll
+          for (int i = 0; i < 10; ++i) m1[i] = fmax3(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
+          m1[10] = fmaxf(sv[30], sv[31]);
+#pragma unroll
+          for (int i = 0; i < 3; ++i) m2[i] = fmax3(m1[3 * i], m1[3 * i + 1], m1[3 * i + 2]);
+          m2[3] = fmaxf(m1[9], m1[10]);
+          mx = fmax3(m2[0], m2[1], fmaxf(m2[2], m2[3]));
+        }
       }
-      xmax[((j & 1) * 2 + half) * TQ + row] = mx;
+      xmax[((j & 1) * NPART + part) * TQ + row] = mx;
       named_bar_sync(1, NSOFT * 32);
       if (ok) {
         // m and the maxima are raw scores; 2^(s - m) * 256 = 2^(raw * coef - (m * coef - 8))
-        const float m_new = fmaxf(m, fmaxf(mx, xmax[((j & 1) * 2 + (half ^ 1)) * TQ + row]));
+        float m_new = m;
+#pragma unroll
+        for (int pt = 0; pt < NPART; ++pt) m_new = fmaxf(m_new, xmax[((j & 1) * NPART + pt) * TQ + row]);
         const float nb = (m_new == -INFINITY) ? 0.f : 8.f - m_new * coef;
         const float alpha = (m == -INFINITY) ? 0.f : ex2((m - m_new) * coef);
-        if (half == 0) {  // for the correction warps
+        if (part == 0) {  // for the correction warps
           alpha_s[(j & 3) * TQ + row] = alpha;
           mbar_arrive(&bars->a_full[j & 3]);
         }
@@ -664,7 +686,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         const float2 coef2 = make_float2(coef, coef), nb2 = make_float2(nb, nb);
         uint8_t* prow = smem + OFF_P + (j & 1) * (TQ * TK) + row * TK;
 #pragma unroll
-        for (int pg = 0; pg < HC / kPage; ++pg) {  // 4 pages of 16 keys
+        for (int pg = 0; pg < HC / kPage; ++pg) {  // pages of 16 keys
           float q[16];
 #pragma unroll
           for (int t = 0; t < 16; t += 2) {
@@ -678,7 +700,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
 #pragma unroll
           for (int ww = 0; ww < 4; ++ww)
             w[ww] = f32x2_to_e4m3x2(q[2 * ww], q[2 * ww + 1]) | (f32x2_to_e4m3x2(q[2 * ww + 8], q[2 * ww + 9]) << 16);
-          const int chunk = half * (HC / kPage) + pg;  // page index within the tile
+          const int chunk = part * (HC / kPage) + pg;  // page index within the tile
           *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
         l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
@@ -689,7 +711,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       }
     }
     // the correction warps finish the sum and write the output rows
-    xsum[half * TQ + row] = l;
+    xsum[part * TQ + row] = l;
     named_bar_arrive(2, (NSOFT + NCORR) * 32);
   }
 
@@ -746,7 +768,7 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
     return fail(KVQ_ERR_INVALID_ARG, "prefill: null pointer");
   if (!aligned(q8, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
     return fail(KVQ_ERR_INVALID_ARG, "prefill: pointers must be 16-byte aligned");
-  if (B > 65535 || Hq > 65535) return fail(KVQ_ERR_UNSUPPORTED, "prefill: grid too large");
+  if (B > 65535 || (max_q_tokens + TQ - 1) / TQ > 65535) return fail(KVQ_ERR_UNSUPPORTED, "prefill: grid too large");
   PrefillParams prm;
   prm.q8 = q8;
   prm.q_scale = q_scale;
@@ -767,7 +789,7 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
   prm.sm_scale = sm_scale;
   prm.causal = causal ? 1 : 0;
   prm.dev_status = dev_status;
-  dim3 grid((max_q_tokens + TQ - 1) / TQ, Hq, B);
+  dim3 grid(Hq, (max_q_tokens + TQ - 1) / TQ, B);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (D == 256) return launch_prefill<256, true>(prm, grid, st);
   return single_level ? launch_prefill<128, true>(prm, grid, st) : launch_prefill<128, false>(prm, grid, st);
