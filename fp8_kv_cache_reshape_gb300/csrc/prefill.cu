@@ -9,9 +9,10 @@
 // "FP8 and KV cache", "How to enable it in the engine": the query is
 // quantized to FP8 too (kvq_quantize_query).
 //
-// One CTA = 128 query rows of one sequence x one query head.  Keys come in
-// tiles of 128 (8 pages).  Warp roles (by warpgroup; setmaxnreg gives the
-// softmax warpgroups 184 registers and the others fewer):
+// One CTA = 128 query rows of one sequence x one query head; CTAs start
+// heaviest query tile first.  Keys come in tiles of 128 (8 pages).  Warp
+// roles (by warpgroup; setmaxnreg gives the softmax warpgroups 184 registers
+// and the others fewer):
 //  warps 12, 14  producers of the even / odd key tiles: block ids (read a
 //             group of 4 tiles ahead) -> one bulk copy per K page and V page
 //             into a 4-stage ring, each producer owning two of the stages
@@ -19,21 +20,23 @@
 //             masked).  Two issuing warps, because a page-sized bulk copy
 //             costs the issuing warp tens of cycles;
 //  warp 13    TMEM owner and MMA issuer: S_j = Q K_j^T into one of two TMEM
-//             score buffers, then O_j = P_j V_j into a fresh TMEM accumulator
-//             O_tile (first level);
+//             score buffers, then O_j = P_j V_j (P_j from TMEM, V_j from
+//             shared memory) into a fresh TMEM accumulator O_tile (first
+//             level);
 //  warps 0-7  two threads per query row (warps w and w + 4 share TMEM lane
 //             quarter w % 4), each owning 64 of the 128 columns of S_j:
 //             online softmax in base 2 (the two halves exchange their tile
-//             maxima through shared memory), P_j = e4m3(2^(s - m) * 256) into
-//             swizzled shared memory, and the tile's rescale factor alpha_j;
+//             maxima through shared memory), P_j = e4m3(2^(s - m) * 256)
+//             written back to TMEM over the first 16 of the thread's own S_j
+//             columns, and the tile's rescale factor alpha_j;
 //  warps 8-11 correction: O_run = O_run * alpha_j + O_tile_j in FP32 (second
 //             level; O_run has its own TMEM columns), one thread per query
 //             row, off the softmax warps' path; then the output rows.
 // With single-level accumulation (SL) the P.V MMAs add into one TMEM sum O
-// that the softmax warps rescale in place, and the correction warps idle.
-// Shared-memory operands use the UMMA canonical K-major layouts: Q, K and P
-// with the 128-byte swizzle (K pages are stored pre-swizzled by the cache
-// format), V pages ([d][16 token slots]) without swizzle.
+// that the correction warps rescale in place.
+// Shared-memory operands use the UMMA canonical K-major layouts: Q and K with
+// the 128-byte swizzle (K pages are stored pre-swizzled by the cache format),
+// V pages ([d][16 token slots]) without swizzle.
 #include <cfloat>
 #include <cmath>
 
@@ -56,6 +59,10 @@ constexpr int PLANE = 128;        // bytes of one K-major operand row: 128 dims 
 //   the last 4 warps    producer 0, MMA issuer, producer 1 (and one idle).
 constexpr int NSOFT = 8;
 constexpr int NPART = NSOFT / 4;
+// P_j goes to tensor memory, over the first columns of each part's slice of
+// S_j (already read by the thread that owns them), and P.V takes its A
+// operand from there.
+static_assert(NPART == 2, "P in TMEM: 16 columns of 4 keys per thread");
 constexpr int NCORR = 4;
 constexpr int W_CORR = NSOFT;
 constexpr int W_PROD0 = NSOFT + NCORR, W_MMA = W_PROD0 + 1, W_PROD1 = W_PROD0 + 2;
@@ -86,8 +93,7 @@ struct Geo {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + TQ * HD;
   static constexpr int STAGE_B = 2 * TILE_B;     // K tile + V tile
-  static constexpr int OFF_P = OFF_KV + NKV * STAGE_B;  // 2 P buffers of 16 KB
-  static constexpr int OFF_BAR = OFF_P + 2 * TQ * TK;
+  static constexpr int OFF_BAR = OFF_KV + NKV * STAGE_B;
   static constexpr int OFF_XCH = OFF_BAR + 512;  // row max [2][NPART][TQ] / row sum [NPART][TQ] exchange
   static constexpr int OFF_ALPHA = OFF_XCH + 3 * NPART * TQ * 4;  // [4][TQ] rescale factors, softmax -> correction
   static constexpr int SMEM_BYTES = OFF_ALPHA + 4 * TQ * 4 + 1024;  // + alignment slack
@@ -154,6 +160,15 @@ KVQ_DEVINL void umma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The same with the A operand in tensor memory (one row per TMEM lane, four
+// FP8 elements of K per 32-bit column).
+KVQ_DEVINL void umma_f8_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 KVQ_DEVINL void umma_commit(uint64_t* bar) {
@@ -256,7 +271,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
   using G = Geo<HD>;
   static_assert(HD == 128 || (HD == 256 && SL), "head_dim 256 runs with single-level accumulation");
   constexpr int NKV = G::NKV, PAGE_B = G::PAGE_B, TILE_B = G::TILE_B, STAGE_B = G::STAGE_B;
-  constexpr int OFF_Q = G::OFF_Q, OFF_KV = G::OFF_KV, OFF_P = G::OFF_P, OFF_XCH = G::OFF_XCH;
+  constexpr int OFF_Q = G::OFF_Q, OFF_KV = G::OFF_KV, OFF_XCH = G::OFF_XCH;
   using BarsN = Bars<NKV>;
   static_assert(sizeof(BarsN) <= 512, "barrier block");
   extern __shared__ uint8_t smem_raw[];
@@ -421,13 +436,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         tc_fence_after();
         if (lane == 0) {
           const int st = j % NKV;
-          const uint32_t p_s = sbase + OFF_P + (j & 1) * (TQ * TK);
           const uint32_t v_s = sbase + OFF_KV + st * STAGE_B + TILE_B;
           const uint32_t d = tmem + 2 * TK;  // O_tile (SL: the running sum O)
 #pragma unroll
-          for (int kk = 0; kk < TK / 32; ++kk)  // 32 keys = 2 V pages per MMA
-            umma_f8(d, desc_sw128(p_s + kk * 32), desc_interleave(v_s + kk * 2 * PAGE_B, PAGE_B, 128), IDESC_O,
-                    (kk > 0 || (SL && j > 0)) ? 1u : 0u);
+          for (int kk = 0; kk < TK / 32; ++kk) {  // 32 keys = 2 V pages per MMA
+            const uint32_t acc = (kk > 0 || (SL && j > 0)) ? 1u : 0u;
+            const uint64_t vdesc = desc_interleave(v_s + kk * 2 * PAGE_B, PAGE_B, 128);
+            // P for keys 32kk .. 32kk + 31: 8 columns at the start of part pt's slice of S_j
+            constexpr int KPP = TK / NPART / 32;  // 32-key steps per part
+            const int pt = kk / KPP;
+            umma_f8_ta(d, tmem + (j & 1) * TK + pt * (TK / NPART) + 8 * (kk - pt * KPP), vdesc, IDESC_O, acc);
+          }
           umma_commit(&bars->o_full);
           umma_commit(&bars->kv_empty[st]);
         }
@@ -610,6 +629,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     for (int j = 0; j < nkv; ++j) {
       const int st = j % NKV;
       const int key0 = j * TK + part * HC;
+      const uint32_t sbuf = tmem + t_lane + (j & 1) * TK + part * HC;  // this thread's columns of S_j
+      const bool tail_tile = tail != 0 && last_page / (TK / kPage) == j;  // holds the partial last page
       float sv[HC];
       float mx = -INFINITY;
       uint32_t bad = 0;
@@ -617,7 +638,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       if (wait_all(&bars->s_full[j & 1], (j >> 1) & 1) && wait_all(&bars->kv_full[st], (j / NKV) & 1)) {
         tc_fence_after();
         bad = bars->stage_bad[st];
-        if (tail != 0 && last_page / (TK / kPage) == j) {
+        if (tail_tile) {
           // V rows (dims) row and row + 128 .. of the last page: slots past the sequence end
           for (int d = row + part * TQ; d < HD; d += NPART * TQ) {
             uint8_t* vrow = smem + OFF_KV + st * STAGE_B + TILE_B + (last_page % (TK / kPage)) * PAGE_B + d * kPage;
@@ -625,7 +646,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
           }
         }
         const bool need_mask = (key0 + HC > kend) || bad != 0;
-        const uint32_t sbuf = tmem + t_lane + (j & 1) * TK + part * HC;
         // raw scores (the positive scale is applied in the exponent below)
         {  // all 32-column loads in flight, one wait
           static_assert(HC % 32 == 0, "32-column loads");
@@ -684,7 +704,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         }
         float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // in units of 2^8 p; two chains
         const float2 coef2 = make_float2(coef, coef), nb2 = make_float2(nb, nb);
-        uint8_t* prow = smem + OFF_P + (j & 1) * (TQ * TK) + row * TK;
+        uint32_t pw[4 * (HC / kPage)];  // this thread's P8 words (four keys each)
 #pragma unroll
         for (int pg = 0; pg < HC / kPage; ++pg) {  // pages of 16 keys
           float q[16];
@@ -696,16 +716,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
             rs2[(t >> 1) & 1] = fadd2(rs2[(t >> 1) & 1], make_float2(q[t], q[t + 1]));
           }
           // word w of a page holds keys 2w, 2w+1, 2w+8, 2w+9 (the V slot order)
-          uint32_t w[4];
 #pragma unroll
           for (int ww = 0; ww < 4; ++ww)
-            w[ww] = f32x2_to_e4m3x2(q[2 * ww], q[2 * ww + 1]) | (f32x2_to_e4m3x2(q[2 * ww + 8], q[2 * ww + 9]) << 16);
-          const int chunk = part * (HC / kPage) + pg;  // page index within the tile
-          *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            pw[4 * pg + ww] =
+                f32x2_to_e4m3x2(q[2 * ww], q[2 * ww + 1]) | (f32x2_to_e4m3x2(q[2 * ww + 8], q[2 * ww + 9]) << 16);
         }
         l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
         m = m_new;
-        fence_proxy_async_smem();
+        tmem_st16(sbuf, pw);  // over the first 16 of this thread's 64 columns of S_j
+        tmem_wait_st();
+        if (tail_tile) fence_proxy_async_smem();  // the zeroed V slots, before the tensor cores read them
         tc_fence_before();
         mbar_arrive(&bars->p_full[j & 1]);
       }
