@@ -381,10 +381,9 @@ kvq_status_t kvq_prefill_attention(const uint8_t* q8, const float* q_scale,
 /*
  * kvq_prefill_attention_acc -- kvq_prefill_attention with an explicit
  * accumulation mode.  Single-level: every tile's P8.V8 MMA accumulates into
- * one tensor-memory sum, which the softmax warps multiply by alpha in place
- * before the next tile's MMA (skipped when alpha is 1 for all 32 rows of a
- * warp, which changes nothing).  It exists to measure what two-level costs
- * and buys.
+ * one tensor-memory sum, which is multiplied by alpha in place before the
+ * next tile's MMA (skipped when alpha is 1 for all 32 rows of a warp, which
+ * changes nothing).  It exists to measure what two-level costs and buys.
  */
 kvq_status_t kvq_prefill_attention_acc(const uint8_t* q8, const float* q_scale,
                                        const void* k_cache, const void* v_cache,
