@@ -185,3 +185,26 @@ def test_prefill_full_size_sampled():
     ref = attention.prefill(q8_ref, qs, kc, vc, pc.k_scale.numpy(), pc.v_scale.numpy(), pc.block_table.numpy(),
                             pc.cu_seqlens_q.numpy(), pc.seq_lens.numpy(), float(np.float32(pc.sm_scale)), rows=rows)
     check_rows(f32(out), ref, rows)
+
+
+def test_prefill_bad_lengths_reported():
+    """A sequence with more new tokens than cached tokens is skipped
+    (KVQ_DEV_BAD_QROWS) while the others are computed; a length beyond the
+    block table is clamped (KVQ_DEV_BAD_SEQLEN); the context stays usable."""
+    c = build([64, 40], [200, 10], Hq=8, Hkv=2, seed=13)
+    good = dict(c)
+    bad_rows = dict(c)
+    bad_rows["lens"] = c["lens"].copy()
+    bad_rows["lens"][1] = 30  # 40 new tokens but only 30 cached
+    out, st = gpu_prefill(bad_rows, status=True)
+    assert st & 0x10
+    rows = [(t, h) for t in range(0, 64, 3) for h in range(8)]  # sequence 0 only
+    check_rows(out, oracle(good, rows=rows), rows)
+    bad_len = dict(c)
+    bad_len["lens"] = c["lens"].copy()
+    bad_len["lens"][0] = c["bt"].shape[1] * 16 + 5
+    out, st = gpu_prefill(bad_len, status=True)
+    assert st & 0x4
+    got = gpu_prefill(good)  # the context stays usable
+    rows = [(t, h) for t in range(0, 104, 5) for h in range(8)]
+    check_rows(got, oracle(good, rows=rows), rows)
