@@ -120,6 +120,12 @@ KVQ_DEVINL uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+// L2 policy for data that other CTAs read again soon (kept over evict-first lines).
+KVQ_DEVINL uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 
 // Programmatic dependent launch: wait until the preceding grid's memory is visible.
 KVQ_DEVINL void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -386,8 +386,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
 #pragma unroll
           for (int pl = 0; pl < HD / PLANE; ++pl)
             bulk_g2s(ks + pl * G::PLANE_K + lane * kPage * PLANE, p.k_cache + off + pl * kPage * PLANE, kPage * PLANE,
-                     &bars->kv_full[st], policy_evict_first());
-          bulk_g2s(vs + lane * PAGE_B, p.v_cache + off, PAGE_B, &bars->kv_full[st], policy_evict_first());
+                     &bars->kv_full[st], policy_evict_last());
+          bulk_g2s(vs + lane * PAGE_B, p.v_cache + off, PAGE_B, &bars->kv_full[st], policy_evict_last());
         }
       }
       if (j < nkv && lane == 0) {  // abandoned: let this producer's issued copies land
