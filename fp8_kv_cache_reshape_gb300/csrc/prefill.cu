@@ -71,7 +71,7 @@ constexpr int NTHREADS = (NSOFT + NCORR + 4) * 32;
 // control and correction warpgroups then give some back and the softmax
 // warpgroups take them (the sum must stay within the launch's allocation).
 constexpr int REG_LAUNCH = (65536 / NTHREADS) / 8 * 8;
-constexpr int REG_SOFT = NSOFT == 16 ? 88 : 184, REG_CORR = NSOFT == 16 ? 72 : 80, REG_CTRL = NSOFT == 16 ? 48 : 56;
+constexpr int REG_SOFT = 184, REG_CORR = 80, REG_CTRL = 56;  // 64,512 of the launch's 65,536
 static_assert(NSOFT * 32 * REG_SOFT + NCORR * 32 * REG_CORR + 128 * REG_CTRL <= NTHREADS * REG_LAUNCH,
               "register split");
 // TMEM: S0 | S1 | O_tile | O_run at head_dim 128 (128 columns each); at 256,
