@@ -79,6 +79,9 @@ lib.kvq_reshape_and_cache_per_token.argtypes = [_p, _p, _p, _p, _p, _p, _i, _i, 
 lib.kvq_paged_decode_attention_per_token.restype = _i
 lib.kvq_paged_decode_attention_per_token.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64,
                                                      _f, _i, _i, _i, _p, _sz, _p, _p]
+lib.kvq_paged_decode_attention_append.restype = _i
+lib.kvq_paged_decode_attention_append.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
+                                                  _i64, _f, _i, _i, _i, _p, _sz, _p, _p]
 lib.kvq_paged_decode_attention_acc.restype = _i
 lib.kvq_paged_decode_attention_acc.argtypes = lib.kvq_paged_decode_attention.argtypes + [_i]
 lib.kvq_prefill_attention_acc.restype = _i
@@ -230,6 +233,36 @@ def kvq_paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_tabl
         _check(lib.kvq_paged_decode_attention(*args), "kvq_paged_decode_attention")
     else:
         _check(lib.kvq_paged_decode_attention_acc(*args, _acc_code(accumulation)), "kvq_paged_decode_attention_acc")
+    return out
+
+
+def kvq_paged_decode_attention_append(q, k_new, v_new, slot_new, k_cache, v_cache, k_scale, v_scale, block_table,
+                                      seq_lens, out, num_blocks=None, sm_scale=None, window=-1,
+                                      cache_dtype="fp8_e4m3", num_splits=0, workspace=None, dev_status=None,
+                                      stream=None):
+    """One decode step that also writes the step's new token (k_new, v_new:
+    bf16 [B][Hkv][D], slot_new: int64 [B]) into the cache, as
+    kvq_reshape_and_cache followed by kvq_paged_decode_attention would."""
+    B, Hq, D = q.shape
+    max_blocks = block_table.shape[1]
+    Hkv = k_cache.shape[1]
+    if num_blocks is None:
+        num_blocks = k_cache.shape[0]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    for t in (k_new, v_new):
+        if t.dtype != torch.bfloat16 or tuple(t.shape) != (B, Hkv, D):
+            raise ValueError("k_new / v_new must be bf16 [B][Hkv][D]")
+    if slot_new.dtype != torch.int64 or slot_new.numel() != B:
+        raise ValueError("slot_new must be int64 [B]")
+    need = kvq_decode_workspace_size(B, Hq, Hkv, D, max_blocks, window, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib.kvq_paged_decode_attention_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_new), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, PAGE, max_blocks, num_blocks,
+        float(sm_scale), window, _dtype_code(cache_dtype), num_splits, _ptr(workspace), workspace.numel(),
+        _ptr(dev_status), _stream(stream)), "kvq_paged_decode_attention_append")
     return out
 
 

@@ -60,6 +60,15 @@ struct DecodeParams {
   int num_splits;
   int num_items;
   int* dev_status;
+  // Append (optional, k_new != nullptr): the new token of each sequence,
+  // bf16 [B][Hkv][D], is written into its cache slot slot_new[b] (-1: none)
+  // exactly as kvq_reshape_and_cache writes it, by the CTA that reads the
+  // sequence's last page, before it reads it.
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int64_t* slot_new;
+  uint8_t* k_cache_w;
+  uint8_t* v_cache_w;
 };
 
 template <int D, bool FP8>
@@ -148,7 +157,9 @@ constexpr int kPresent0 = 1, kPresent1 = 2, kBad0 = 4, kBad1 = 8;
 // SL: single-level accumulation (an ablation of the two-level scheme): the
 // P.V MMAs accumulate into the running sum O * alpha directly instead of a
 // fresh FP32 tile per stage (FP8, per-head scales only).
-template <int D, bool FP8, int NW, int NST, bool E5, bool PT, bool SL>
+// AP: the append entry point's instantiation (the new token's cache write);
+// the plain decode is compiled without it.
+template <int D, bool FP8, int NW, int NST, bool E5, bool PT, bool SL, bool AP = false>
 __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const __grid_constant__ DecodeParams p) {
   using G = Geo<D, FP8>;
   static_assert(NST % NW == 0 && NST >= NW, "each ring slot must belong to one consumer warp");
@@ -183,6 +194,61 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
     for (int item = blockIdx.x; item < p.num_items && !aborted; item += gridDim.x) {
       const ItemRange r = item_range(p, item, lane == 0);
       const int32_t* bt = p.block_table + static_cast<size_t>(r.b) * p.max_blocks + r.pg0;
+      // append: this item holds the page of the sequence's last token
+      const int last_pg = (r.hi - 1) / kPage;
+      const bool append = AP && r.hi > 0 && last_pg >= r.pg0 && last_pg < r.pg0 + r.n;
+      constexpr int EPL = D / 32;  // elements of the new K (and V) row per lane
+      uint16_t kx[EPL], vx[EPL];
+      int64_t slot = -1;
+      if (AP && append) {  // loads in flight while the item's first pages are issued
+        slot = p.slot_new[r.b];
+        const size_t src = (static_cast<size_t>(r.b) * p.Hkv + r.kvh) * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          kx[e] = p.k_new[src + e];
+          vx[e] = p.v_new[src + e];
+        }
+      }
+      auto write_new_token = [&]() {  // the whole warp; then the page may be copied
+        const int64_t num_slots = p.num_blocks * kPage;
+        if (slot >= num_slots) {
+          if (lane == 0) set_status(p.dev_status, KVQ_DEV_BAD_SLOT);
+          return;
+        }
+        if (slot < 0) return;
+        const int off = static_cast<int>(slot % kPage);
+        const size_t page = (static_cast<size_t>(slot / kPage) * p.Hkv + r.kvh) * G::PAGE;
+        uint8_t* kp = p.k_cache_w + page;
+        uint8_t* vp = p.v_cache_w + page;
+        const int d0 = lane * EPL;
+        if constexpr (FP8) {
+          const float sk = p.k_scale[r.kvh], sv = p.v_scale[r.kvh];
+          uint32_t kw = 0;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) {
+            const float xk = __uint_as_float(static_cast<uint32_t>(kx[e]) << 16);
+            const float xv = __uint_as_float(static_cast<uint32_t>(vx[e]) << 16);
+            kw |= f32_to_fp8<E5>(__fdiv_rn(xk, sk)) << (8 * e);
+            vp[(d0 + e) * kPage + fp8_v_slot(off)] = static_cast<uint8_t>(f32_to_fp8<E5>(__fdiv_rn(xv, sv)));
+          }
+          // dims d0 .. d0 + EPL - 1 sit in one 16-byte chunk of the swizzled K row
+          uint8_t* kd = kp + fp8_k_offset(off, d0 / 16, D) + d0 % 16;
+          if constexpr (EPL == 4) {
+            *reinterpret_cast<uint32_t*>(kd) = kw;
+          } else {
+            *reinterpret_cast<uint16_t*>(kd) = static_cast<uint16_t>(kw);
+          }
+        } else {
+          // BF16: a bit copy; dims d0 .. d0 + EPL - 1 sit in one 16-byte chunk of the K row
+          uint16_t* kd = reinterpret_cast<uint16_t*>(kp + k_chunk_offset(off, d0 / 8, G::ROWB) + (d0 % 8) * 2);
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) {
+            kd[e] = kx[e];
+            *reinterpret_cast<uint16_t*>(vp + bf16_v_offset(d0 + e, off)) = vx[e];
+          }
+        }
+        fence_proxy_async_global();  // the stores, before the bulk copy of the page reads them
+      };
       for (int base = 0; base < r.n && !aborted; base += 32) {
         const int cnt = min(32, r.n - base);
         int blk = 0, bad = 0;
@@ -200,6 +266,13 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
           const int b1 = __shfl_sync(0xffffffffu, blk, (j + 1) & 31);
           const int d1 = __shfl_sync(0xffffffffu, bad, (j + 1) & 31);
           const bool two = j + 1 < cnt;
+          if constexpr (AP) {
+            const int pg = r.pg0 + base + j;
+            if (append && (pg == last_pg || (two && pg + 1 == last_pg))) {
+              write_new_token();
+              __syncwarp();
+            }
+          }
           // one stage = pages j, j + 1: a bulk copy per K page and per V page
           auto issue_pages = [&](int st, uint32_t extra_per_page) {
             int info = kPresent0 | (d0 ? kBad0 : 0);
@@ -778,11 +851,11 @@ void split_plan(int B, int Hkv, int P, int max_blocks, int window, int num_split
   *pps_out = pps;
 }
 
-template <int D, bool FP8, bool E5 = false, bool PT = false, bool SL = false>
+template <int D, bool FP8, bool E5 = false, bool PT = false, bool SL = false, bool AP = false>
 kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream_t s) {
   constexpr int NST = stages_for<D, FP8, PT>();
   constexpr size_t smem = decode_smem_bytes<D, FP8, NST, PT>();
-  auto kern = decode_partial_kernel<D, FP8, kNW, NST, E5, PT, SL>;
+  auto kern = decode_partial_kernel<D, FP8, kNW, NST, E5, PT, SL, AP>;
   static int configured_mask = 0;  // devices whose attribute is set
   int dev = 0;
   cudaGetDevice(&dev);
@@ -837,13 +910,21 @@ extern "C" size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P
 
 namespace {
 
+// The new token of each sequence for the append entry point.
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_new;
+};
+
 // Shared by the per-head and the per-token entry points.  per_token: k_scale
 // (= v_scale) is the interleaved scale cache [num_blocks][Hkv][2][P].
 kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                           const float* v_scale, const int32_t* block_table, const int32_t* seq_lens, void* out, int B,
                           int Hq, int Hkv, int D, int P, int max_blocks, int64_t num_blocks, float sm_scale, int window,
                           kvq_dtype_t cache_dtype, int num_splits, void* workspace, size_t workspace_bytes,
-                          int* dev_status, kvq_stream_t stream, bool per_token, bool single_level = false) {
+                          int* dev_status, kvq_stream_t stream, bool per_token, bool single_level = false,
+                          const AppendArgs* app = nullptr) {
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || num_splits < 0)
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: bad sizes");
   if (Hq % Hkv != 0) return fail(KVQ_ERR_INVALID_ARG, "paged_decode: Hq %% Hkv != 0");
@@ -860,6 +941,10 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
   if (fp8 && (!k_scale || !v_scale))
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: FP8 needs k_scale and v_scale");
   if (per_token && !fp8) return fail(KVQ_ERR_INVALID_ARG, "paged_decode: per-token scales need an FP8 cache");
+  if (app && (per_token || single_level))
+    return fail(KVQ_ERR_UNSUPPORTED, "paged_decode_append: per-head scales and two-level accumulation only");
+  if (app && (!app->k_new || !app->v_new || !app->slot_new))
+    return fail(KVQ_ERR_INVALID_ARG, "paged_decode_append: null pointer");
   if (per_token && (!aligned(k_scale, 16) || !aligned(v_scale, 16)))
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: scale caches must be 16-byte aligned");
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(workspace, 16) ||
@@ -896,6 +981,11 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
   prm.num_splits = S;
   prm.num_items = static_cast<int>(items);
   prm.dev_status = dev_status;
+  prm.k_new = app ? static_cast<const uint16_t*>(app->k_new) : nullptr;
+  prm.v_new = app ? static_cast<const uint16_t*>(app->v_new) : nullptr;
+  prm.slot_new = app ? app->slot_new : nullptr;
+  prm.k_cache_w = app ? static_cast<uint8_t*>(const_cast<void*>(k_cache)) : nullptr;
+  prm.v_cache_w = app ? static_cast<uint8_t*>(const_cast<void*>(v_cache)) : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto o = static_cast<__nv_bfloat16*>(out);
   const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
@@ -909,6 +999,16 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
     if (D == 128)
       return e5 ? launch_decode<128, true, true, true>(prm, o, s) : launch_decode<128, true, false, true>(prm, o, s);
     return e5 ? launch_decode<64, true, true, true>(prm, o, s) : launch_decode<64, true, false, true>(prm, o, s);
+  }
+  if (app) {
+    if (e5)
+      return D == 128 ? launch_decode<128, true, true, false, false, true>(prm, o, s)
+                      : launch_decode<64, true, true, false, false, true>(prm, o, s);
+    if (D == 128)
+      return fp8 ? launch_decode<128, true, false, false, false, true>(prm, o, s)
+                 : launch_decode<128, false, false, false, false, true>(prm, o, s);
+    return fp8 ? launch_decode<64, true, false, false, false, true>(prm, o, s)
+               : launch_decode<64, false, false, false, false, true>(prm, o, s);
   }
   if (e5) return D == 128 ? launch_decode<128, true, true>(prm, o, s) : launch_decode<64, true, true>(prm, o, s);
   if (D == 128) return fp8 ? launch_decode<128, true>(prm, o, s) : launch_decode<128, false>(prm, o, s);
@@ -928,6 +1028,19 @@ extern "C" kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_
   return paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, B, Hq, Hkv, D, P,
                       max_blocks, num_blocks, sm_scale, window, cache_dtype, num_splits, workspace, workspace_bytes,
                       dev_status, stream, false);
+}
+
+extern "C" kvq_status_t kvq_paged_decode_attention_append(
+    const void* q, const void* k_new, const void* v_new, const int64_t* slot_new, void* k_cache, void* v_cache,
+    const float* k_scale, const float* v_scale, const int32_t* block_table, const int32_t* seq_lens, void* out, int B,
+    int Hq, int Hkv, int D, int P, int max_blocks, int64_t num_blocks, float sm_scale, int window,
+    kvq_dtype_t cache_dtype, int num_splits, void* workspace, size_t workspace_bytes, int* dev_status,
+    kvq_stream_t stream) {
+  clear_error();
+  const AppendArgs app{k_new, v_new, slot_new};
+  return paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, B, Hq, Hkv, D, P,
+                      max_blocks, num_blocks, sm_scale, window, cache_dtype, num_splits, workspace, workspace_bytes,
+                      dev_status, stream, false, false, &app);
 }
 
 extern "C" kvq_status_t kvq_paged_decode_attention_acc(

@@ -64,6 +64,9 @@ KVQ_DEVINL void mbar_init(uint64_t* bar, unsigned count) {
 KVQ_DEVINL void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+KVQ_DEVINL void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 KVQ_DEVINL void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -230,6 +230,36 @@ kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_cache, cons
                                         int* dev_status, kvq_stream_t stream);
 
 /*
+ * kvq_paged_decode_attention_append -- one decode step with the step's new
+ * token written into the cache by the attention call itself: the result,
+ * the cache bytes and the device status are those of kvq_reshape_and_cache
+ * (one token per sequence, slot_mapping = slot_new) followed by
+ * kvq_paged_decode_attention, in one launch of the partial kernel instead of
+ * a separate cache-write kernel.  [vLLM] "Performance benchmarks" (a decode
+ * step writes the new token and reads the whole context).
+ *
+ *  k_new, v_new  bf16 [B][Hkv][D]: the new token of each sequence, the last
+ *                of its seq_lens[b] tokens.
+ *  slot_new      int64 [B]: its cache slot (block * P + offset); -1 = no
+ *                write; >= num_blocks * P sets KVQ_DEV_BAD_SLOT (no write).
+ *  k_cache,      written (the new tokens' slots) and read.
+ *  v_cache
+ *  Other arguments as for kvq_paged_decode_attention.  The slot must lie in
+ *  the page that block_table gives for the sequence's last token (the page
+ *  the call reads it back from).  Per-KV-head scales (FP8) or BF16 caches;
+ *  two-level accumulation.
+ */
+kvq_status_t kvq_paged_decode_attention_append(const void* q, const void* k_new, const void* v_new,
+                                               const int64_t* slot_new, void* k_cache, void* v_cache,
+                                               const float* k_scale, const float* v_scale,
+                                               const int32_t* block_table, const int32_t* seq_lens,
+                                               void* out, int B, int Hq, int Hkv, int D, int P,
+                                               int max_blocks, int64_t num_blocks, float sm_scale,
+                                               int window, kvq_dtype_t cache_dtype, int num_splits,
+                                               void* workspace, size_t workspace_bytes,
+                                               int* dev_status, kvq_stream_t stream);
+
+/*
  * kvq_paged_decode_attention_acc -- kvq_paged_decode_attention with an
  * explicit accumulation mode (kvq_accumulation_t above).  Two-level is the
  * call above; single-level feeds O * alpha to the P.V MMAs as their

@@ -84,3 +84,20 @@ def test_per_token_entry_points_validate_without_gpu(lib):
     assert d(*([fake] * 3 + [None] + [fake] * 3 + args[7:]), 0, 0, fake, 1 << 30, None, None) == 1  # no scales
     assert d(*([fake] * 3 + [ctypes.c_void_p((1 << 20) + 4)] + [fake] * 3 + args[7:]), 0, 0, fake, 1 << 30,
              None, None) == 1  # scale cache not 16-byte aligned
+
+
+def test_append_entry_point_validates_without_gpu(lib):
+    """The decode-with-append call refuses a missing new token or slot array
+    before any CUDA call (all other arguments valid)."""
+    p = ctypes.c_void_p
+    i, i64, f32, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    d = lib.kvq_paged_decode_attention_append
+    d.restype = i
+    d.argtypes = [p, p, p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, i64, f32, i, i, i, p, sz, p, p]
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the calls return first
+    sizes = [1, 8, 2, 128, 16, 4, 64, 0.088, -1, 0, 0]  # B Hq Hkv D P max_blocks num_blocks sm window E4M3 splits
+    assert d(fake, None, fake, fake, *([fake] * 7), *sizes, fake, 1 << 30, None, None) == 1  # no k_new
+    assert d(fake, fake, fake, None, *([fake] * 7), *sizes, fake, 1 << 30, None, None) == 1  # no slot_new
+    bad_d = list(sizes)
+    bad_d[3] = 96
+    assert d(fake, fake, fake, fake, *([fake] * 7), *bad_d, fake, 1 << 30, None, None) == 2  # head_dim 96
