@@ -242,6 +242,8 @@ kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_cache, cons
  *                of its seq_lens[b] tokens.
  *  slot_new      int64 [B]: its cache slot (block * P + offset); -1 = no
  *                write; >= num_blocks * P sets KVQ_DEV_BAD_SLOT (no write).
+ *                A sequence with seq_lens[b] = 0 has no last token: nothing
+ *                is written for it.
  *  k_cache,      written (the new tokens' slots) and read.
  *  v_cache
  *  Other arguments as for kvq_paged_decode_attention.  The slot must lie in
