@@ -169,7 +169,8 @@ kvq_status_t kvq_quantize_query(const void* q, uint8_t* q8, const float* q_scale
 int kvq_decode_num_splits(int B, int Hkv, int P, int max_blocks, int window, int num_splits);
 
 /* Workspace bytes a decode call with these arguments needs (float32
- * partial outputs [B][Hq][S][D] and log-sum-exps [B][Hq][S]). */
+ * partial outputs [B][Hq][S][4][D] and log-sum-exps [B][Hq][S][4]: one per
+ * consumer warp of each of the S page ranges). */
 size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P, int max_blocks,
                                  int window, int num_splits);
 
