@@ -184,8 +184,9 @@ size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P, int max_b
  * (sliding-window layers keep a BF16 cache).
  *
  * Split-KV: each (sequence, KV head) is cut into num_splits ranges of pages;
- * a partial kernel writes per range a normalized output and a log-sum-exp to
- * the workspace, and a combine kernel merges them:
+ * a partial kernel writes per range (and per consumer warp within it, each
+ * warp taking every fourth pair of pages) a normalized output and a
+ * log-sum-exp to the workspace, and a combine kernel merges them:
  *   lse = log sum_i exp(lse_i),  out = sum_i exp(lse_i - lse) out_i.
  * Accumulation: scores and P.V products are accumulated by tensor-core MMAs
  * into fresh FP32 registers per page of 16 tokens, then added into a running
