@@ -60,6 +60,20 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(ms, dist=None, device="cpu"):
+    """The slowest rank's duration: the job is done when every rank is."""
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, step_bytes, steps, total_ms):
+    """Whole-job GB/s: every rank's steps (weak scaling) over the slowest rank's time."""
+    return world * step_bytes * steps / (total_ms * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -556,16 +570,13 @@ def ours_arm(args, rank, world, local_rank):
         dec_ms = time_graph(g_dec, dec_reps)
     barrier()
     torch.cuda.synchronize()
-    elapsed = torch.tensor([total_ms], dtype=torch.float64, device=device)
-    if dist is not None:
-        dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
-    total_ms = float(elapsed.item())
+    total_ms = max_over_ranks(total_ms, dist, device)
     st = int(wl["status"].item())
     assert st == 0, f"device status {st:#x}"
 
     step_bytes = LAYERS * (decode_bytes(CONTEXT) + cache_write_bytes(1))
     ms_per_step = total_ms / args.steps
-    value = world * step_bytes * args.steps / (total_ms * 1e-3) / 1e9
+    value = job_value(world, step_bytes, args.steps, total_ms)
     peaks, src = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     call_ms = dec_ms / (dec_reps * LAYERS)
