@@ -522,9 +522,9 @@ def cpu_baseline(steps=1, warmup=0, min_seconds=10.0):
 
 # ----------------------------------------------------------------- arms ---
 def reference_arm(args, rank, world):
-    """The oracle (the reference implementation of this build) timed on the
-    host cores, on the same metric, unit and workload shape; each step is
-    one oracle decode call over the bounded sample."""
+    """The reference arm: the CPU oracle timed on the host cores, on the same
+    metric, unit and workload shape; each step is one oracle decode call
+    over the bounded sample."""
     if rank != 0:
         return
     cb = cpu_baseline(steps=args.steps, warmup=args.warmup, min_seconds=0.0)
