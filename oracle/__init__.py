@@ -35,7 +35,10 @@ attention   pure-Python brute force, closed forms (constant V, zero K, one
             token, needle), split / merge, page permutation, window, the last
             prefill row vs decode, sensitivity to a 14-bit accumulator.
 
-Parity unpinned: the prefill's mirrored P8 codes (taken against the row's
-final maximum; a kernel with a running maximum may pick neighbouring codes).
-The prefill result itself is pinned through the unquantized-P mode.
+Prefill P8: the "final" mode (P8 against the row's final maximum) is pinned
+by brute force; the "mirror" mode's tile loop is pinned against the
+single-pass formula (equal without P rounding for any tile size, equal with
+it when the row maximum sits in the first tile).  Which E4M3 code a float32
+exponential near a rounding midpoint gets is not pinned bit for bit (the
+tolerance covers one step).
 """

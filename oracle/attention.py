@@ -30,14 +30,16 @@ Readings where the pages are silent
   cached tokens; query i sits at position L - nq + i and (causal) attends to
   keys 0..L - nq + i.
 * The softmax scale is an input (1/sqrt(D) by default in the callers).
-* Prefill's probabilities feed an FP8 MMA: P8 = encode(fl32(p * 256)).  The
-  online softmax the vLLM page names for its FP8 attention kernel rescales
-  as it walks the keys, so p is taken relative to the running row maximum:
-  keys are visited in tiles of 128 in key order, the maximum is updated per
-  tile, and earlier tiles' sums are rescaled by 2^(m_old - m_new).  The row
-  sum l adds the unquantized p.  The P8 codes themselves are parity
-  unpinned (the kernel's float32 exponentials can land on the other side of
-  a rounding midpoint); the result is pinned through the unquantized mode.
+* Prefill's probabilities feed an FP8 MMA: P8 = encode(fl32(p * 256)), 256
+  a power of two the pages do not fix.  Two readings of "p" are computed:
+  relative to the row's final maximum ("final": one rounding per
+  probability, independent of how the keys are tiled), and relative to the
+  running maximum of an online softmax over key tiles ("mirror": the vLLM
+  page names online-softmax rescaling for its FP8 attention kernel; keys are
+  visited in tiles in key order, the maximum is updated per tile and earlier
+  sums are rescaled by 2^(m_old - m_new)).  Both sum the unquantized p into
+  the row sum l.  The two differ only where the running maximum moved, by
+  at most one E4M3 rounding step of those p.
 
 Mirrored quantization points
 ----------------------------
@@ -54,7 +56,7 @@ Mirrored quantization points
   the query and probability terms stay E4M3.
 * prefill: s2 = (sum_d q8[d] * k8[d]) * c with
   c = fl32(fl32(fl32(q_scale * k_scale) * sm_scale) * log2(e)), and P8 as
-  above (running maximum over 128-key tiles).
+  above ("final" or "mirror" over tiles of 128 keys).
 ``mode="pure"`` uses the exact dequantized values and natural exponentials.
 """
 from __future__ import annotations
@@ -230,18 +232,43 @@ def lse_merge(outs, lses):
     return np.tensordot(w / tot, outs, axes=1), m + math.log(tot)
 
 
+def _p8(p):
+    """P quantized for the FP8 P.V product: decode(encode(fl32(p * 256))) / 256
+    in float64 (256 is a power of two, so the scaling itself is exact)."""
+    return e4m3.decode(e4m3.encode((p * 256.0).astype(np.float32))) / 256.0
+
+
 def prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
             cu_seqlens_q, seq_lens, sm_scale, causal=True, mode="mirror",
-            rows=None, tile=128):
+            rows=None, tile=128, quantize_p=True, chunk=64):
     """Chunked prefill over the FP8 cache (the new tokens are already cached).
 
     q8: uint8 [Tq][Hq][D] E4M3 codes.  cu_seqlens_q: int [B+1].  seq_lens:
     int [B], each counting the cached tokens including the new ones.
     rows: optional iterable of (token_index, head) pairs to evaluate; other
     rows of the result stay NaN (sampled checks at large sizes).
-    tile: keys per online-softmax step of the mirrored P8 quantization.
+
+    Modes (the scores of the mirrored modes are s2 = (sum_d q8_d k8_d) * c in
+    base-2 units, c the float32 coefficient of prefill_score_coef):
+    * "pure": softmax(q_hat . K_hat^T * sm_scale) . V_hat with the exact
+      dequantized values and natural exponentials, no P quantization.
+    * "final": P8_j = encode(fl32(2^(s2_j - m) * 256)) with m the row's final
+      maximum -- one rounding per probability, independent of any tiling;
+      o = s_v * sum_j decode(P8_j) v8_j / (256 * sum_j p_j), the row sum over
+      the unquantized p_j.
+    * "mirror": the online softmax the CUDA path runs: keys in tiles of
+      `tile` in key order; per tile the running maximum m is updated, the
+      earlier numerator and row sum are multiplied by a = 2^(m_old - m_new),
+      and the tile's P8 is taken against the running m.  With every key in
+      one tile (tile >= the row length) this is "final".
+    quantize_p=False keeps P unquantized in "final" / "mirror" (used to pin
+    the tile loop against the single-pass formula).
+    Rows of one (sequence, KV head) are evaluated together, `chunk` at a
+    time; a key past a row's causal limit has score -inf (p = 0).
     Returns out float64 [Tq][Hq][D].
     """
+    if mode not in ("pure", "final", "mirror"):
+        raise ValueError(f"unknown mode {mode!r}")
     q8 = np.asarray(q8, dtype=np.uint8)
     Tq, Hq, D = q8.shape
     Hkv = k_cache.shape[1]
@@ -257,37 +284,52 @@ def prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
     by_seq_head = {}
     for t, h in rows:
         by_seq_head.setdefault((int(seq_of[t]), h // g), []).append((int(t), int(h)))
+    qs = float(np.float32(q_scale))
     for (b, kv), items in by_seq_head.items():
         L = int(seq_lens[b])
         nq = int(cu[b + 1] - cu[b])
         kk, vv = gather_tokens(k_cache, v_cache, block_table[b], np.arange(L), kv)
-        k_codes = e4m3.decode(kk)
+        k_codes = e4m3.decode(kk)   # [L][D]
         v_codes = e4m3.decode(vv)
+        sk = float(np.float32(k_scale[kv]))
         sv = float(np.float32(v_scale[kv]))
-        for t, h in items:
-            i = t - int(cu[b])
-            last = L - nq + i if causal else L - 1
-            qc = e4m3.decode(q8[t, h])
-            if mode == "mirror":
-                c = float(prefill_score_coef(np.float32(q_scale), k_scale[kv], sm_scale))
-                s2 = (k_codes[: last + 1] @ qc) * c
-                m_run, l, num = -np.inf, 0.0, np.zeros(D)
-                for t0 in range(0, last + 1, tile):  # online softmax over key tiles
-                    seg = s2[t0:t0 + tile]
-                    m_new = max(m_run, float(np.max(seg)))
-                    a = math.exp2(m_run - m_new) if np.isfinite(m_run) else 0.0
-                    p = np.exp2(seg - m_new)
-                    p8 = e4m3.encode((p * 256.0).astype(np.float32))
-                    num = num * a + (e4m3.decode(p8) @ v_codes[t0:t0 + seg.size]) / 256.0
-                    l = l * a + p.sum()
-                    m_run = m_new
-                out[t, h] = num / l * sv
+        c = float(prefill_score_coef(np.float32(q_scale), k_scale[kv], sm_scale))
+        for r0 in range(0, len(items), chunk):
+            part = items[r0:r0 + chunk]
+            # keys 0 .. last[r] are visible to row r
+            last = np.array([(L - nq + (t - int(cu[b]))) if causal else L - 1 for t, _ in part])
+            n = int(last.max()) + 1
+            qc = np.stack([e4m3.decode(q8[t, h]) for t, h in part])  # [R][D]
+            visible = np.arange(n)[None, :] <= last[:, None]          # [R][n]
+            if mode == "pure":
+                s = (qc * qs) @ (k_codes[:n] * sk).T * float(np.float32(sm_scale))
+                s = np.where(visible, s, -np.inf)
+                m = np.max(s, axis=1, keepdims=True)
+                p = np.exp(s - m)
+                o = (p @ (v_codes[:n] * sv)) / p.sum(axis=1, keepdims=True)
             else:
-                qs = float(np.float32(q_scale))
-                sk = float(np.float32(k_scale[kv]))
-                s = (k_codes[: last + 1] * sk) @ (qc * qs) * float(np.float32(sm_scale))
-                p, m, l = _softmax_row(s)
-                out[t, h] = (p @ (v_codes[: last + 1] * sv)) / l
+                s2 = np.where(visible, (qc @ k_codes[:n].T) * c, -np.inf)
+                q_of = _p8 if quantize_p else (lambda x: x)
+                if mode == "final":
+                    m = np.max(s2, axis=1, keepdims=True)
+                    p = np.exp2(s2 - m)
+                    o = (q_of(p) @ v_codes[:n]) / p.sum(axis=1, keepdims=True) * sv
+                else:
+                    R = len(part)
+                    m_run = np.full(R, -np.inf)
+                    l = np.zeros(R)
+                    num = np.zeros((R, D))
+                    for t0 in range(0, n, tile):  # online softmax over key tiles
+                        seg = s2[:, t0:t0 + tile]
+                        m_new = np.maximum(m_run, np.max(seg, axis=1))
+                        a = np.where(np.isfinite(m_run), np.exp2(m_run - m_new), 0.0)
+                        p = np.exp2(seg - m_new[:, None])
+                        num = num * a[:, None] + q_of(p) @ v_codes[t0:t0 + seg.shape[1]]
+                        l = l * a + p.sum(axis=1)
+                        m_run = m_new
+                    o = num / l[:, None] * sv
+            for i, (t, h) in enumerate(part):
+                out[t, h] = o[i]
     return out
 
 
