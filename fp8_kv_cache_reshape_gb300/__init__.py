@@ -58,6 +58,8 @@ lib.kvq_version.restype = _i
 lib.kvq_version.argtypes = []
 lib.kvq_last_error_string.restype = ctypes.c_char_p
 lib.kvq_last_error_string.argtypes = []
+lib.kvq_debug_set_stall_ns.restype = None
+lib.kvq_debug_set_stall_ns.argtypes = [ctypes.c_uint64]
 lib.kvq_reshape_and_cache.restype = _i
 lib.kvq_reshape_and_cache.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i64, _i, _p, _p]
 lib.kvq_quantize_query.restype = _i
@@ -142,6 +144,12 @@ def _acc_code(accumulation) -> int:
 
 def version() -> int:
     return lib.kvq_version()
+
+
+def kvq_debug_set_stall_ns(ns: int):
+    """Failure-path test hook (include/kvq.h): > 0 makes later decode and
+    prefill launches fail one bounded wait after `ns` nanoseconds; 0 = off."""
+    lib.kvq_debug_set_stall_ns(int(ns))
 
 
 def alloc_kv_cache(num_blocks: int, kv_heads: int, head_dim: int, cache_dtype="fp8_e4m3",

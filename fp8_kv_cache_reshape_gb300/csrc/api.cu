@@ -1,4 +1,5 @@
 // libkvq: version, per-thread error text, device queries.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -38,7 +39,12 @@ int sm_count() {
   return cache[dev];
 }
 
+static std::atomic<uint64_t> g_stall_ns{0};
+uint64_t stall_ns() { return g_stall_ns.load(std::memory_order_relaxed); }
+
 }  // namespace kvq
+
+extern "C" void kvq_debug_set_stall_ns(uint64_t ns) { kvq::g_stall_ns.store(ns, std::memory_order_relaxed); }
 
 extern "C" int kvq_version(void) { return 10000; }
 

@@ -69,6 +69,10 @@ struct DecodeParams {
   const int64_t* slot_new;
   uint8_t* k_cache_w;
   uint8_t* v_cache_w;
+  // failure-path test hook (kvq_debug_set_stall_ns): > 0 makes consumer warp
+  // 0 wait up to this long on a barrier nothing arrives on before its first
+  // stage, which fails like a stuck pipeline wait
+  uint64_t stall_ns;
 };
 
 template <int D, bool FP8>
@@ -107,7 +111,7 @@ constexpr int stages_for() {
 
 template <int D, bool FP8, int NST, bool PT = false>
 constexpr size_t decode_smem_bytes() {
-  return size_t(NST) * stage_stride<D, FP8, PT>() + 2 * NST * sizeof(uint64_t) + NST * sizeof(int) + 16;
+  return size_t(NST) * stage_stride<D, FP8, PT>() + (2 * NST + 1) * sizeof(uint64_t) + NST * sizeof(int) + 16;
 }
 
 struct ItemRange {
@@ -170,7 +174,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(NST) * STRIDE);
   uint64_t* empty = full + NST;
-  int* stage_info = reinterpret_cast<int*>(empty + NST);
+  uint64_t* stall_bar = empty + NST;  // nothing arrives on it (test hook)
+  int* stage_info = reinterpret_cast<int*>(stall_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(stage_info + NST);
 
   const int warp = threadIdx.x >> 5;
@@ -180,6 +185,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -209,13 +215,17 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
           vx[e] = p.v_new[src + e];
         }
       }
-      auto write_new_token = [&]() {  // the whole warp; then the page may be copied
+      // the whole warp; then the page may be copied.  blk_last: the block id
+      // the table gives for the page of the sequence's last token
+      auto write_new_token = [&](int blk_last) {
+        if (slot < 0) return;
         const int64_t num_slots = p.num_blocks * kPage;
-        if (slot >= num_slots) {
+        // the slot must be the last token's slot under the block table (the
+        // page this CTA reads back); any other slot is not written
+        if (slot >= num_slots || slot / kPage != blk_last || static_cast<int>(slot % kPage) != (r.hi - 1) % kPage) {
           if (lane == 0) set_status(p.dev_status, KVQ_DEV_BAD_SLOT);
           return;
         }
-        if (slot < 0) return;
         const int off = static_cast<int>(slot % kPage);
         const size_t page = (static_cast<size_t>(slot / kPage) * p.Hkv + r.kvh) * G::PAGE;
         uint8_t* kp = p.k_cache_w + page;
@@ -269,7 +279,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
           if constexpr (AP) {
             const int pg = r.pg0 + base + j;
             if (append && (pg == last_pg || (two && pg + 1 == last_pg))) {
-              write_new_token();
+              write_new_token(pg == last_pg ? (d0 ? -1 : b0) : (d1 ? -1 : b1));
               __syncwarp();
             }
           }
@@ -357,6 +367,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
     }
   }
 
+  if (warp == 0 && !stall_wait(stall_bar, p.stall_ns, abort_flag)) {
+    if (lane == 0) {
+      set_status(p.dev_status, KVQ_DEV_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
   uint32_t it0 = 0;
   for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
     const ItemRange rg = item_range(p, item, false);
@@ -454,7 +470,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
 
       float s0[4], s1[4];
       float p00, p01, p02, p03, p10, p11, p12, p13, al0, al1;
-      auto softmax = [&]() {  // online softmax over the stage's 32 tokens (base 2)
+      // online softmax over the stage's 32 tokens (base 2)
+      auto softmax = [&]() {
         float mx0 = fmaxf(fmaxf(s0[0], s0[2]), fmaxf(s1[0], s1[2]));
         float mx1 = fmaxf(fmaxf(s0[1], s0[3]), fmaxf(s1[1], s1[3]));
 #pragma unroll
@@ -464,6 +481,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
         }
         const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
         // probabilities come out scaled by 2^8 (exact): P fills the E4M3 range
+        // and the running maximum itself is exactly 256
         const float base0 = ((mn0 == NEG_INF) ? 0.f : mn0) - 8.f;
         const float base1 = ((mn1 == NEG_INF) ? 0.f : mn1) - 8.f;
         al0 = ex2(m[0] - base0 - 8.f);  // rescale of the running sums
@@ -986,6 +1004,7 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
   prm.slot_new = app ? app->slot_new : nullptr;
   prm.k_cache_w = app ? static_cast<uint8_t*>(const_cast<void*>(k_cache)) : nullptr;
   prm.v_cache_w = app ? static_cast<uint8_t*>(const_cast<void*>(v_cache)) : nullptr;
+  prm.stall_ns = stall_ns();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto o = static_cast<__nv_bfloat16*>(out);
   const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
@@ -1082,8 +1101,32 @@ namespace {
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
+// The array's device address as seen from host code, per device, valid for
+// the context it was looked up in: a new context on the device (after
+// cudaDeviceReset, or another context made current) loads the module again,
+// possibly elsewhere, so the address is looked up again when the current
+// context differs from the one it was taken in.
+struct ScratchAddr {
+  void* ctx = nullptr;
+  void* ptr = nullptr;
+};
 std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {nullptr};  // device address of the array, per device
+ScratchAddr g_scratch_addr[64];
+
+// cuCtxGetCurrent through the runtime's driver entry point (no link-time
+// dependency on the driver library).
+typedef int (*CtxGetCurrentFn)(void**);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(f);
+  }();
+  return fn;
+}
 
 }  // namespace
 
@@ -1107,18 +1150,30 @@ extern "C" kvq_status_t kvq_paged_decode_attention_static_scratch(
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_status(e, "paged_decode_static_scratch: cudaGetDevice");
   if (dev < 0 || dev >= 64) return fail(KVQ_ERR_UNSUPPORTED, "paged_decode_static_scratch: device %d", dev);
+  CtxGetCurrentFn get_ctx = ctx_get_current();
+  if (!get_ctx) return fail(KVQ_ERR_CUDA, "paged_decode_static_scratch: cuCtxGetCurrent unavailable");
+  void* ctx = nullptr;
+  if (get_ctx(&ctx) != 0 || ctx == nullptr) {
+    // no context yet on this thread: cudaSetDevice creates the device's primary context
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return cuda_status(e, "paged_decode_static_scratch: cudaSetDevice");
+    if (get_ctx(&ctx) != 0 || ctx == nullptr)
+      return fail(KVQ_ERR_CUDA, "paged_decode_static_scratch: no current CUDA context");
+  }
   void* ptr = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-      // first call on this device: host code must use the array's device address
-      e = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_decode_scratch);
-      if (e != cudaSuccess) {
-        g_scratch_ptr[dev] = nullptr;
-        return cuda_status(e, "paged_decode_static_scratch: cudaGetSymbolAddress");
-      }
+    ScratchAddr& a = g_scratch_addr[dev];
+    if (a.ptr == nullptr || a.ctx != ctx) {
+      // first call on this device (or in a new context): host code must use
+      // the array's device address, not its host-side name
+      void* addr = nullptr;
+      e = cudaGetSymbolAddress(&addr, g_decode_scratch);
+      if (e != cudaSuccess) return cuda_status(e, "paged_decode_static_scratch: cudaGetSymbolAddress");
+      a.ptr = addr;
+      a.ctx = ctx;
     }
-    ptr = g_scratch_ptr[dev];
+    ptr = a.ptr;
   }
   return kvq_paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, B, Hq, Hkv,
                                     D, P, max_blocks, num_blocks, sm_scale, window, cache_dtype, num_splits, ptr,

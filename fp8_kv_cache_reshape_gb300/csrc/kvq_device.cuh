@@ -95,18 +95,26 @@ KVQ_DEVINL uint64_t globaltimer_ns() {
   return t;
 }
 // Bounded wait: true when the phase completed; false after kWaitPolls polls,
-// kWaitNs nanoseconds, or as soon as *abort_flag (if given) becomes nonzero.
-KVQ_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag = nullptr) {
+// limit_ns nanoseconds (kWaitNs by default), or as soon as *abort_flag (if
+// given) becomes nonzero.
+KVQ_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag = nullptr,
+                          uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (unsigned i = 1; i < kWaitPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63) == 0) {
       if (abort_flag && *abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitNs) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }
   return false;
+}
+// Test hook of the failure path: when stall_ns > 0, a wait of at most stall_ns
+// on `bar`, a barrier that nothing arrives on; it fails exactly like a stuck
+// pipeline wait.  Returns true (no stall) when stall_ns == 0.
+KVQ_DEVINL bool stall_wait(uint64_t* bar, uint64_t stall_ns, volatile int* abort_flag) {
+  return stall_ns == 0 || mbar_wait(bar, 0, abort_flag, stall_ns);
 }
 
 // One contiguous global -> shared bulk copy that completes `bytes` of
@@ -268,6 +276,14 @@ KVQ_DEVINL float2 fadd2(float2 a, float2 b) {
   memcpy(&d, &rd, 8);
   return d;
 }
+// 2^k for an integer-valued k <= 127, exactly (0 for k < -126, -inf or NaN):
+// the rescale between two integer softmax stabilizers.
+KVQ_DEVINL float exp2_int(float k) {
+  if (!(k >= -126.f)) return 0.f;
+  return __uint_as_float(static_cast<uint32_t>(127 + static_cast<int>(k)) << 23);
+}
+// E4M3 1.0 in all four bytes: the A operand of an MMA that sums the columns of B.
+constexpr uint32_t kE4m3OnesX4 = 0x38383838u;
 KVQ_DEVINL float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -17,5 +17,7 @@ kvq_status_t cuda_status(cudaError_t e, const char* where);
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 inline bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+// The failure-path test hook of kvq_debug_set_stall_ns (0 = off).
+uint64_t stall_ns();
 
 }  // namespace kvq

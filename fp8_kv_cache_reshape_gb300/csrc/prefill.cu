@@ -94,9 +94,10 @@ struct Geo {
   static constexpr int OFF_KV = OFF_Q + TQ * HD;
   static constexpr int STAGE_B = 2 * TILE_B;     // K tile + V tile
   static constexpr int OFF_BAR = OFF_KV + NKV * STAGE_B;
-  static constexpr int OFF_XCH = OFF_BAR + 512;  // row max [2][NPART][TQ] / row sum [NPART][TQ] exchange
-  static constexpr int OFF_ALPHA = OFF_XCH + 3 * NPART * TQ * 4;  // [4][TQ] rescale factors, softmax -> correction
-  static constexpr int SMEM_BYTES = OFF_ALPHA + 4 * TQ * 4 + 1024;  // + alignment slack
+  static constexpr int OFF_XCH = OFF_BAR + 512;  // row max exchange [2 tiles][NPART][TQ]
+  static constexpr int OFF_ALPHA = OFF_XCH + 2 * NPART * TQ * 4;  // [4][TQ] rescale factors, softmax -> correction
+  static constexpr int OFF_ONES = OFF_ALPHA + 4 * TQ * 4;          // E4M3 ones: the B operand of the row-sum MMA
+  static constexpr int SMEM_BYTES = OFF_ONES + 1024 + 1024;        // + alignment slack
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -116,6 +117,10 @@ struct PrefillParams {
   float sm_scale;
   int causal;
   int* dev_status;
+  // failure-path test hook (kvq_debug_set_stall_ns): > 0 makes the softmax
+  // warps wait up to this long on a barrier nothing arrives on before the
+  // first key tile, which fails like a stuck pipeline wait
+  uint64_t stall_ns;
 };
 
 template <int NKV>
@@ -127,8 +132,10 @@ struct Bars {
   uint64_t p_full[2];
   uint64_t o_full;  // P.V of the current tile is in O_tile
   uint64_t o_free;  // O_tile has been folded into O_run (correction warps)
+  uint64_t rs_free;  // the row sums of tile j have been read: S_j's buffer may be rewritten
   uint64_t a_full[4];  // alpha of tile j is in slot j % 4 (softmax part 0 -> correction warps)
   uint64_t mma_done;
+  uint64_t stall;  // nothing arrives on it (test hook)
   uint32_t tmem_base;
   int abort;
   uint32_t stage_bad[NKV];  // bit i: page i of the stage was zero-filled (bad block id)
@@ -192,6 +199,12 @@ KVQ_DEVINL void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
                "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
                "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
                : "memory");
+}
+KVQ_DEVINL float tmem_ld1(uint32_t taddr) {  // one column of this warp's 32 lanes
+  uint32_t v;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr));
+  tmem_wait_ld();
+  return __uint_as_float(v);
 }
 KVQ_DEVINL void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
@@ -299,8 +312,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     }
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_free, NCORR * 32);
+    mbar_init(&bars->rs_free, NCORR * 32);
     for (int i = 0; i < 4; ++i) mbar_init(&bars->a_full[i], NSOFT / NPART * 32);
     mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->stall, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -310,6 +325,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
                  "r"(TMEM_COLS)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x < 64) {  // 1 KiB of E4M3 1.0 for the row-sum MMA, before the tensor cores read it
+    reinterpret_cast<uint4*>(smem + G::OFF_ONES)[threadIdx.x] =
+        make_uint4(kE4m3OnesX4, kE4m3OnesX4, kE4m3OnesX4, kE4m3OnesX4);
+    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
@@ -426,9 +446,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         }
         __syncwarp();
       };
+      constexpr uint32_t IDESC_RS = idesc_e4m3(TQ, 16);  // row sums: N = 16 columns of ones
+      const uint64_t ones_desc = desc_interleave(sbase + G::OFF_ONES, 128, 256);  // every byte 1.0
       if (wait(&bars->q_full, 0) && nkv > 0) issue_s(0);
       for (int j = 0; j < nkv && ok; ++j) {
-        if (j + 1 < nkv) issue_s(j + 1);
+        if (j + 1 < nkv) {
+          // S_{j+1} goes into tile j - 1's buffer, which holds that tile's row sums until read
+          if (j >= 1 && !wait(&bars->rs_free, (j - 1) & 1)) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
         if (!ok) break;
         if (!wait(&bars->p_full[j & 1], (j >> 1) & 1)) break;
         // two-level: O_tile of tile j - 1 has been read; SL: O has been rescaled for tile j
@@ -438,14 +465,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
           const int st = j % NKV;
           const uint32_t v_s = sbase + OFF_KV + st * STAGE_B + TILE_B;
           const uint32_t d = tmem + 2 * TK;  // O_tile (SL: the running sum O)
+          constexpr int KPP = TK / NPART / 32;  // 32-key steps per part
 #pragma unroll
           for (int kk = 0; kk < TK / 32; ++kk) {  // 32 keys = 2 V pages per MMA
             const uint32_t acc = (kk > 0 || (SL && j > 0)) ? 1u : 0u;
             const uint64_t vdesc = desc_interleave(v_s + kk * 2 * PAGE_B, PAGE_B, 128);
             // P for keys 32kk .. 32kk + 31: 8 columns at the start of part pt's slice of S_j
-            constexpr int KPP = TK / NPART / 32;  // 32-key steps per part
             const int pt = kk / KPP;
             umma_f8_ta(d, tmem + (j & 1) * TK + pt * (TK / NPART) + 8 * (kk - pt * KPP), vdesc, IDESC_O, acc);
+          }
+          // the tile's row sums of the same P8 codes, sum_k P8[row][k] in each of 16
+          // columns, into S_j's columns 32 .. 47 (already read by the softmax warps)
+#pragma unroll
+          for (int kk = 0; kk < TK / 32; ++kk) {
+            const int pt = kk / KPP;
+            umma_f8_ta(tmem + (j & 1) * TK + 32, tmem + (j & 1) * TK + pt * (TK / NPART) + 8 * (kk - pt * KPP),
+                       ones_desc, IDESC_RS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&bars->o_full);
           umma_commit(&bars->kv_empty[st]);
@@ -476,7 +511,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const uint32_t o_tile = tmem + t_lane + 2 * TK;  // SL: O
     const uint32_t o_run = o_tile + HD;              // two-level only
     const float* alpha_s = reinterpret_cast<const float*>(smem + G::OFF_ALPHA);
-    const float* xsum = reinterpret_cast<const float*>(smem + OFF_XCH) + 2 * NPART * TQ;
+    // the row sum of the rounded probabilities, in units of 2^8 p: the tensor
+    // core's sums of each tile's P8 codes (S_j's columns 32 .. 47), rescaled
+    // like the output
+    float l = 0.f;
+    auto row_sum = [&](int j) {  // after o_full of tile j; then S_j's buffer may be rewritten
+      const float rs = tmem_ld1(tmem + t_lane + (j & 1) * TK + 32);
+      tc_fence_before();
+      mbar_arrive(&bars->rs_free);
+      return rs;
+    };
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       if (!ok) return false;
@@ -504,6 +548,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         }
         if (!wait_all(&bars->o_full, j & 1)) break;  // P.V of tile j is in O_tile
         tc_fence_after();
+        l = fmaf(l, alpha, row_sum(j));
         tmem_wait_st();  // this thread's previous O_run update
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
@@ -528,10 +573,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       }
     } else {
       for (int j = 1; j < nkv && ok; ++j) {
-        if (!wait_all(&bars->a_full[j & 3], (j >> 2) & 1)) break;
-        const float alpha = alpha_s[(j & 3) * TQ + row];
         if (!wait_all(&bars->o_full, (j - 1) & 1)) break;  // P.V of tile j - 1 has landed in O
         tc_fence_after();
+        const float rs = row_sum(j - 1);
+        if (!wait_all(&bars->a_full[j & 3], (j >> 2) & 1)) break;
+        const float alpha = alpha_s[(j & 3) * TQ + row];
+        l = (l + rs) * alpha;
         if (!__all_sync(0xffffffffu, alpha == 1.f)) {  // exact when skipped
 #pragma unroll 4
           for (int c = 0; c < HD / 16; ++c) {
@@ -547,14 +594,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         tc_fence_before();
         mbar_arrive(&bars->o_free);  // P.V of tile j may add into O
       }
-      if (nkv >= 1 && wait_all(&bars->o_full, (nkv - 1) & 1)) tc_fence_after();
+      if (nkv >= 1 && wait_all(&bars->o_full, (nkv - 1) & 1)) {
+        tc_fence_after();
+        l += row_sum(nkv - 1);
+      }
     }
-    named_bar_sync(2, (NSOFT + NCORR) * 32);  // the softmax parts' row sums
     if (ok) {
       // out = O * v_scale / l (both in units of 2^8 p)
-      float lt = 0.f;
-#pragma unroll
-      for (int pt = 0; pt < NPART; ++pt) lt += xsum[pt * TQ + row];
+      const float lt = l;
       const bool live_row = job.q0 + row < job.nq;
       const size_t out_row = (static_cast<size_t>(p.cu_seqlens_q[job.b]) + job.q0 + row) * p.Hq + job.h;
       const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
@@ -587,7 +634,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const int row = quarter * 32 + lane;   // TMEM lane == query row
     constexpr int HC = TK / NPART;         // columns per thread
     float* xmax = reinterpret_cast<float*>(smem + OFF_XCH);   // [2 tiles][NPART][TQ]
-    float* xsum = xmax + 2 * NPART * TQ;                       // [NPART][TQ]
     const bool live_row = job.q0 + row < job.nq;
     const int qpos = job.first_q + job.q0 + row;  // absolute position of this query
     const int kend = (p.causal && qpos + 1 < job.L) ? qpos + 1 : job.L;  // this row attends to keys [0, kend)
@@ -611,7 +657,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const int last_page = (job.L - 1) / kPage;
 
     float* alpha_s = reinterpret_cast<float*>(smem + G::OFF_ALPHA);  // [4][TQ], read by the correction warps
-    float m = -INFINITY, l = 0.f;
+    // m: the running row maximum of the raw scores; M: the stabilizer, the
+    // maximum of the base-2 scores rounded up to an integer, so that every
+    // rescale 2^(M_old - M_new) is an exact power of two and the P8 codes do
+    // not depend on how the keys are tiled (E4M3 rounding commutes with it)
+    float m = -INFINITY, M = -INFINITY;
     bool ok = true;  // warp-uniform, since tcgen05.ld / st need every lane of the warp
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       if (!ok) return false;
@@ -624,6 +674,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       return ok;
     };
 
+    if (!__all_sync(0xffffffffu, stall_wait(&bars->stall, p.stall_ns, abort_flag))) {
+      ok = false;
+      set_status(p.dev_status, KVQ_DEV_TIMEOUT);
+      *abort_flag = 1;
+    }
     // every softmax thread runs every tile's named barrier, also after a
     // failed wait, so no warp is left behind at bar.sync
     for (int j = 0; j < nkv; ++j) {
@@ -692,17 +747,18 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       xmax[((j & 1) * NPART + part) * TQ + row] = mx;
       named_bar_sync(1, NSOFT * 32);
       if (ok) {
-        // m and the maxima are raw scores; 2^(s - m) * 256 = 2^(raw * coef - (m * coef - 8))
+        // m and the maxima are raw scores; 2^(s - M) * 256 = 2^(raw * coef - (M - 8)),
+        // the largest in (128, 256]
         float m_new = m;
 #pragma unroll
         for (int pt = 0; pt < NPART; ++pt) m_new = fmaxf(m_new, xmax[((j & 1) * NPART + pt) * TQ + row]);
-        const float nb = (m_new == -INFINITY) ? 0.f : 8.f - m_new * coef;
-        const float alpha = (m == -INFINITY) ? 0.f : ex2((m - m_new) * coef);
+        const float M_new = (m_new == -INFINITY) ? -INFINITY : ceilf(m_new * coef);
+        const float nb = (m_new == -INFINITY) ? 0.f : 8.f - M_new;
+        const float alpha = exp2_int(M - M_new);  // 0 on the first tile
         if (part == 0) {  // for the correction warps
           alpha_s[(j & 3) * TQ + row] = alpha;
           mbar_arrive(&bars->a_full[j & 3]);
         }
-        float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // in units of 2^8 p; two chains
         const float2 coef2 = make_float2(coef, coef), nb2 = make_float2(nb, nb);
         uint32_t pw[4 * (HC / kPage)];  // this thread's P8 words (four keys each)
 #pragma unroll
@@ -713,7 +769,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
             const float2 e = ffma2(make_float2(sv[pg * 16 + t], sv[pg * 16 + t + 1]), coef2, nb2);
             q[t] = ex2(e.x);
             q[t + 1] = ex2(e.y);
-            rs2[(t >> 1) & 1] = fadd2(rs2[(t >> 1) & 1], make_float2(q[t], q[t + 1]));
           }
           // word w of a page holds keys 2w, 2w+1, 2w+8, 2w+9 (the V slot order)
 #pragma unroll
@@ -721,8 +776,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
             pw[4 * pg + ww] =
                 f32x2_to_e4m3x2(q[2 * ww], q[2 * ww + 1]) | (f32x2_to_e4m3x2(q[2 * ww + 8], q[2 * ww + 9]) << 16);
         }
-        l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
         m = m_new;
+        M = M_new;
         tmem_st16(sbuf, pw);  // over the first 16 of this thread's 64 columns of S_j
         tmem_wait_st();
         if (tail_tile) fence_proxy_async_smem();  // the zeroed V slots, before the tensor cores read them
@@ -730,9 +785,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         mbar_arrive(&bars->p_full[j & 1]);
       }
     }
-    // the correction warps finish the sum and write the output rows
-    xsum[part * TQ + row] = l;
-    named_bar_arrive(2, (NSOFT + NCORR) * 32);
+    // the correction warps hold the row sums and write the output rows
   }
 
   tc_fence_before();
@@ -809,6 +862,7 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
   prm.sm_scale = sm_scale;
   prm.causal = causal ? 1 : 0;
   prm.dev_status = dev_status;
+  prm.stall_ns = stall_ns();
   dim3 grid(Hq, (max_q_tokens + TQ - 1) / TQ, B);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (D == 256) return launch_prefill<256, true>(prm, grid, st);

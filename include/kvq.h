@@ -105,7 +105,7 @@ typedef enum kvq_accumulation {
 } kvq_accumulation_t;
 
 /* Bits OR-ed into *dev_status by the kernels. */
-#define KVQ_DEV_BAD_SLOT     0x1  /* slot_mapping[t] >= num_blocks * P: token skipped */
+#define KVQ_DEV_BAD_SLOT     0x1  /* slot >= num_blocks * P, or (append) not the last token's slot: not written */
 #define KVQ_DEV_BAD_BLOCK    0x2  /* block id outside [0, num_blocks): page masked out */
 #define KVQ_DEV_BAD_SEQLEN   0x4  /* seq_len < 0 or > max_blocks * P: clamped */
 #define KVQ_DEV_TIMEOUT      0x8  /* a pipeline wait exceeded its bound: work abandoned */
@@ -115,6 +115,24 @@ typedef void* kvq_stream_t;   /* cudaStream_t */
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 int kvq_version(void);
+
+/*
+ * kvq_debug_set_stall_ns -- a test hook for the failure path of the bounded
+ * pipeline waits (the pages have no counterpart; it exists so that the path
+ * a stuck wait takes can be run without faulting or hanging a GPU).
+ *
+ * With ns > 0, every decode-partial and prefill kernel launched afterwards
+ * (on any thread) makes one of its waits -- consumer warp 0 of each decode
+ * CTA before its first stage; the softmax warps of each prefill CTA before
+ * the first key tile -- a wait of at most ns nanoseconds on a barrier that
+ * nothing arrives on.  It fails like any pipeline wait that exceeded its
+ * bound: the kernel ORs KVQ_DEV_TIMEOUT into *dev_status, abandons its work
+ * (the outputs are then meaningless), lets every bulk copy it issued land,
+ * frees its tensor memory and returns; the context stays usable.  ns = 0
+ * (the default) turns the hook off.  The setting is read at launch time, so
+ * graphs captured while it was set keep it.
+ */
+void kvq_debug_set_stall_ns(uint64_t ns);
 
 /* Text of the last host-side error on the calling thread ("" if none). */
 const char* kvq_last_error_string(void);
@@ -248,10 +266,12 @@ kvq_status_t kvq_paged_decode_attention(const void* q, const void* k_cache, cons
  *                is written for it.
  *  k_cache,      written (the new tokens' slots) and read.
  *  v_cache
- *  Other arguments as for kvq_paged_decode_attention.  The slot must lie in
- *  the page that block_table gives for the sequence's last token (the page
- *  the call reads it back from).  Per-KV-head scales (FP8) or BF16 caches;
- *  two-level accumulation.
+ *  Other arguments as for kvq_paged_decode_attention.  The slot must be the
+ *  last token's slot under block_table: block block_table[b][(L - 1) / P],
+ *  offset (L - 1) % P (the page the call reads it back from); any other
+ *  slot (or one in a page with an invalid block id) sets KVQ_DEV_BAD_SLOT
+ *  and is not written.  Per-KV-head scales (FP8) or BF16 caches; two-level
+ *  accumulation.
  */
 kvq_status_t kvq_paged_decode_attention_append(const void* q, const void* k_new, const void* v_new,
                                                const int64_t* slot_new, void* k_cache, void* v_cache,
@@ -352,7 +372,10 @@ kvq_status_t kvq_paged_decode_attention_per_token(const void* q, const void* k_c
  *    KVQ_ERR_UNSUPPORTED and launches nothing.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress with that device current); make that first call
- *    before any stream capture on that device.
+ *    before any stream capture on that device.  The address belongs to the
+ *    CUDA context it was looked up in: a call made in another context on
+ *    the device (after cudaDeviceReset, or with another context current)
+ *    looks it up again, so that call too must come before any capture.
  *  - All calls on a device share the one array and it keeps the last call's
  *    contents.  Nothing in it needs to start at zero (each call writes every
  *    partial result before reading it), but calls that overlap on the GPU
@@ -397,11 +420,16 @@ kvq_status_t kvq_paged_decode_attention_static_scratch(const void* q, const void
  *  tensor memory.
  *  Declared rounding: S = sum_d q8[d] k8[d] (exact products, FP32 sums),
  *  s2 = S * c with c = fl32(fl32(fl32(q_scale * k_scale) * sm_scale) *
- *  log2(e)); P8 = e4m3_rne_sat(fl32(2^(s2 - m) * 256)) against the running
- *  row maximum m; each KV tile's P8.V8 product goes into a fresh FP32
+ *  log2(e)); P8_j = e4m3_rne_sat(fl32(2^(s2_j - M) * 256)) with M the
+ *  row's stabilizer, its maximum base-2 score rounded up to an integer
+ *  (kept as a running value over the key tiles; every rescale 2^(M_old -
+ *  M_new) is an exact power of two, with which E4M3 rounding commutes, so
+ *  the result is that of the row's final M for any tiling, up to roundings
+ *  of probabilities below 2^-14); out = v_scale * (sum_j P8_j V8_j) /
+ *  (sum_j P8_j): the row sum adds the same rounded probabilities, summed by
+ *  the tensor core.  Each KV tile's P8.V8 product goes into a fresh FP32
  *  tensor-memory accumulator that is then added in FP32 into the running
- *  output (two-level accumulation); out = O * v_scale / (256 * l), l the
- *  FP32 sum of the unquantized probabilities.
+ *  output (two-level accumulation).
  */
 kvq_status_t kvq_prefill_attention(const uint8_t* q8, const float* q_scale,
                                    const void* k_cache, const void* v_cache,

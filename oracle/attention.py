@@ -30,16 +30,20 @@ Readings where the pages are silent
   cached tokens; query i sits at position L - nq + i and (causal) attends to
   keys 0..L - nq + i.
 * The softmax scale is an input (1/sqrt(D) by default in the callers).
+* Prefill's softmax stabilizer is the row maximum of the base-2 scores
+  rounded up to an integer, M = ceil(m): p_j = 2^(s2_j - M).  Any stabilizer gives the
+  same softmax; an integer one makes every online-softmax rescale
+  2^(M_old - M_new) an exact power of two, and rounding to E4M3 or float16
+  commutes with powers of two, so the rounded probabilities -- and the
+  result -- do not depend on how an implementation tiles or splits the keys.
 * Prefill's probabilities feed an FP8 MMA: P8 = encode(fl32(p * 256)), 256
-  a power of two the pages do not fix.  Two readings of "p" are computed:
-  relative to the row's final maximum ("final": one rounding per
-  probability, independent of how the keys are tiled), and relative to the
-  running maximum of an online softmax over key tiles ("mirror": the vLLM
-  page names online-softmax rescaling for its FP8 attention kernel; keys are
-  visited in tiles in key order, the maximum is updated per tile and earlier
-  sums are rescaled by 2^(m_old - m_new)).  Both sum the unquantized p into
-  the row sum l.  The two differ only where the running maximum moved, by
-  at most one E4M3 rounding step of those p.
+  a power of two the pages do not fix ("final"; "mirror" walks the keys in
+  tiles with a running stabilizer, as the online softmax the vLLM page names
+  for its FP8 attention kernel does, and equals "final").
+* Where P is rounded for an FP8 MMA, the row sum l adds the same rounded
+  values: the output is then a convex combination of the value rows with
+  the weights the MMA actually applied (a lone dominant key reproduces its
+  value row exactly, whatever its rounding).
 
 Mirrored quantization points
 ----------------------------
@@ -50,13 +54,15 @@ Mirrored quantization points
   units, s2 = (sum_d (hi + lo)[d] * k8[d]) / sigma * c with
   c = fl32(fl32(k_scale * sm_scale) * log2(e));
   o = s_v * sum_j 2^(s2_j - m) v8_j / sum_j 2^(s2_j - m).  The kernel's
-  rounding of P into two E4M3 terms is not mirrored (it depends on the
-  running maximum); the tolerance covers it.
+  rounding of P for the P.V MMA (two E4M3 terms of 2^(s2 - m) * 256 taken
+  against the running maximum, about 8 significant bits, the maximum itself
+  exact) is not mirrored: it depends on how the context is cut into stages
+  and splits; the tolerance carries it (2^-8 of |o| where |o| > 1).
   An E5M2 cache is mirrored the same way: its codes are decoded as E5M2,
   the query and probability terms stay E4M3.
 * prefill: s2 = (sum_d q8[d] * k8[d]) * c with
   c = fl32(fl32(fl32(q_scale * k_scale) * sm_scale) * log2(e)), and P8 as
-  above ("final" or "mirror" over tiles of 128 keys).
+  above.
 ``mode="pure"`` uses the exact dequantized values and natural exponentials.
 """
 from __future__ import annotations
@@ -111,6 +117,14 @@ def split_query_e4m3(q_row):
     res = (y.astype(np.float64) - hi).astype(np.float32)
     lo = e4m3.decode(e4m3.encode(res))
     return (hi + lo) / float(sigma)
+
+
+def stabilizer(s2):
+    """The softmax stabilizer of base-2 scores: the row maximum rounded up to
+    an integer, M = ceil(max_j s2_j).  p_j = 2^(s2_j - M) lies in (0, 1] with
+    the largest in (1/2, 1]; any M gives the same softmax, and with an integer
+    M every rescale between two stabilizers is an exact power of two."""
+    return np.ceil(np.max(s2, axis=-1, keepdims=True))
 
 
 def decode_positions(L, window):
@@ -252,17 +266,20 @@ def prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
     base-2 units, c the float32 coefficient of prefill_score_coef):
     * "pure": softmax(q_hat . K_hat^T * sm_scale) . V_hat with the exact
       dequantized values and natural exponentials, no P quantization.
-    * "final": P8_j = encode(fl32(2^(s2_j - m) * 256)) with m the row's final
-      maximum -- one rounding per probability, independent of any tiling;
-      o = s_v * sum_j decode(P8_j) v8_j / (256 * sum_j p_j), the row sum over
-      the unquantized p_j.
-    * "mirror": the online softmax the CUDA path runs: keys in tiles of
-      `tile` in key order; per tile the running maximum m is updated, the
-      earlier numerator and row sum are multiplied by a = 2^(m_old - m_new),
-      and the tile's P8 is taken against the running m.  With every key in
-      one tile (tile >= the row length) this is "final".
-    quantize_p=False keeps P unquantized in "final" / "mirror" (used to pin
-    the tile loop against the single-pass formula).
+    * "final": P8_j = encode(fl32(2^(s2_j - M) * 256)) with M = ceil(max_j
+      s2_j), the row's integer stabilizer -- one rounding per probability,
+      independent of any tiling; o = s_v * sum_j decode(P8_j) v8_j /
+      sum_j decode(P8_j): the output is normalized by the sum of the rounded
+      probabilities it is a combination of.
+    * "mirror": the online softmax: keys in tiles of `tile` in key order; per
+      tile the running integer stabilizer M is updated, the earlier
+      numerator and row sum (of the rounded P) are multiplied by
+      a = 2^(M_old - M_new) (an exact power of two), and the tile's P8 is
+      taken against the running M.
+      E4M3 rounding commutes with powers of two (outside the subnormal
+      range), so this equals "final" for every tile size.
+    quantize_p=False keeps P unquantized in "final" / "mirror", numerator and
+    row sum alike (used to pin the tile loop against the single-pass formula).
     Rows of one (sequence, KV head) are evaluated together, `chunk` at a
     time; a key past a row's causal limit has score -inf (p = 0).
     Returns out float64 [Tq][Hq][D].
@@ -311,9 +328,8 @@ def prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
                 s2 = np.where(visible, (qc @ k_codes[:n].T) * c, -np.inf)
                 q_of = _p8 if quantize_p else (lambda x: x)
                 if mode == "final":
-                    m = np.max(s2, axis=1, keepdims=True)
-                    p = np.exp2(s2 - m)
-                    o = (q_of(p) @ v_codes[:n]) / p.sum(axis=1, keepdims=True) * sv
+                    pq = q_of(np.exp2(s2 - stabilizer(s2)))
+                    o = (pq @ v_codes[:n]) / pq.sum(axis=1, keepdims=True) * sv
                 else:
                     R = len(part)
                     m_run = np.full(R, -np.inf)
@@ -321,11 +337,11 @@ def prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
                     num = np.zeros((R, D))
                     for t0 in range(0, n, tile):  # online softmax over key tiles
                         seg = s2[:, t0:t0 + tile]
-                        m_new = np.maximum(m_run, np.max(seg, axis=1))
+                        m_new = np.maximum(m_run, stabilizer(seg)[:, 0])
                         a = np.where(np.isfinite(m_run), np.exp2(m_run - m_new), 0.0)
-                        p = np.exp2(seg - m_new[:, None])
-                        num = num * a[:, None] + q_of(p) @ v_codes[t0:t0 + seg.shape[1]]
-                        l = l * a + p.sum(axis=1)
+                        pq = q_of(np.exp2(seg - m_new[:, None]))
+                        num = num * a[:, None] + pq @ v_codes[t0:t0 + seg.shape[1]]
+                        l = l * a + pq.sum(axis=1)
                         m_run = m_new
                     o = num / l[:, None] * sv
             for i, (t, h) in enumerate(part):

@@ -11,14 +11,28 @@ from oracle.kv_cache import FP8, BF16
 
 SENTINEL = 0xA5
 
-# Attention tolerance for unit-variance inputs: max-abs 1e-2, mean-abs 1e-3.
-# The output is bfloat16 (8 significant bits): round-to-nearest moves an
-# element o in [2^e, 2^(e+1)) by at most half an ulp, 2^(e-8) <= 2^-8 |o|.
-# Outputs far from unit scale (the x20 outlier channels) get that rounding
-# on top of the absolute budget.
+# Attention tolerance for unit-variance inputs: max-abs 1e-2 and mean-abs
+# 1e-3, flat, for every element with |o| <= 1.  An element with |o| > 1 (in
+# these workloads the x20 outlier channels, |o| up to ~60) gets 2^-8 |o| on
+# top: the output is bfloat16 (8 significant bits), whose nearest value can
+# be half an ulp, up to 2^-8 |o|, from the exact one, and the decode kernels'
+# declared rounding of P for the P.V MMA (two E4M3 terms, about 8
+# significant bits per probability, taken against a running maximum that
+# depends on how the context is cut into stages and splits) is a 2^-8
+# relative effect the oracle does not mirror.  Below |o| = 1 both stay
+# inside the flat 1e-2.
 MAX_ABS = 1e-2
 MEAN_ABS = 1e-3
-BF16_HALF_ULP_REL = 2.0 ** -8
+REL_ABOVE_ONE = 2.0 ** -8
+
+# measured errors of the checks that ran in this process: (what, max, mean)
+ERRORS = []
+
+
+def bound(ref, max_abs=MAX_ABS):
+    """The elementwise tolerance described above."""
+    a = np.abs(np.asarray(ref, np.float64))
+    return max_abs + np.where(a > 1.0, REL_ABOVE_ONE * a, 0.0)
 
 
 def f32(t: torch.Tensor) -> np.ndarray:
@@ -56,16 +70,21 @@ def errors(got: np.ndarray, ref: np.ndarray):
 
 
 def assert_close(got, ref, max_abs=MAX_ABS, mean_abs=MEAN_ABS, what=""):
-    """Elementwise |got - ref| <= max_abs + 2^-8 |ref| and mean |got - ref| <=
-    mean_abs.  Returns (max-abs, mean-abs)."""
+    """Elementwise |got - ref| <= bound(ref) (flat max_abs where |ref| <= 1)
+    and mean |got - ref| <= mean_abs.  Records, prints and returns (max-abs,
+    mean-abs)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
-    mx, mn = errors(got, ref)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
-    bound = max_abs + BF16_HALF_ULP_REL * np.abs(ref)
-    excess = np.abs(got - ref) - bound
+    mx, mn = errors(got, ref)
+    ERRORS.append((what, mx, mn))
+    small = np.abs(ref) <= 1.0
+    mx_small = float(np.max(np.abs(got - ref)[small])) if np.any(small) else 0.0
+    print(f"\n[errors] {what}: max-abs {mx:.3e} (|ref|<=1: {mx_small:.3e}) mean-abs {mn:.3e} (n={got.size})")
+    bnd = bound(ref, max_abs)
+    excess = np.abs(got - ref) - bnd
     worst = np.unravel_index(np.argmax(excess), excess.shape)
-    assert np.all(excess <= 0), (f"{what}: |err| {abs(got[worst] - ref[worst]):.3e} > bound {bound[worst]:.3e} "
+    assert np.all(excess <= 0), (f"{what}: |err| {abs(got[worst] - ref[worst]):.3e} > bound {bnd[worst]:.3e} "
                                  f"at {worst} (ref {ref[worst]:.4f}); max-abs {mx:.3e}")
     assert mn <= mean_abs, f"{what}: mean-abs {mn:.3e}"
     return mx, mn

@@ -91,7 +91,7 @@ def test_single_level_prefill_parity():
         rows = [(t, h) for t in range(c["q8"].shape[0]) for h in range(c["Hq"])]
         if len(rows) > 2000:
             rows = [rows[i] for i in rng.choice(len(rows), 2000, replace=False)]
-        tp.check_rows(f32(out), tp.oracle(c, rows=rows), rows)
+        tp.check_all(f32(out), c, rows, what=f"single-level prefill nq={nq}")
 
 
 @pytest.mark.parametrize("dtype", [BF16, FP8_E5M2])

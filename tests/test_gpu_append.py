@@ -120,3 +120,31 @@ def test_append_without_slot_writes_nothing():
     assert st == 0 and st2 == 0
     assert torch.equal(kd, kd2) and torch.equal(vd, vd2)
     assert torch.equal(got.view(torch.int16), ref_out.view(torch.int16))
+
+
+@pytest.mark.parametrize("where", ["other_page", "wrong_offset"])
+def test_append_slot_not_the_last_tokens_is_reported_and_not_written(where):
+    """The new token's slot must be the last token's slot under the block
+    table (the page the call reads back).  A slot elsewhere -- another page
+    of the sequence, or the right page at another offset -- sets
+    KVQ_DEV_BAD_SLOT and writes nothing; the result is that of the two-call
+    path with that token skipped."""
+    kw, lengths, dtype, window = CASES["ragged_g4"]
+    case = W.decode_case(W.DecodeConfig("app_badslot", **kw), lengths=lengths, cache_dtype=dtype, window=window)
+    kd, vd, last, ks, vs = _prepare(case)
+    kd2, vd2 = kd.clone(), vd.clone()
+    slot_new = case.slot_mapping[last].clone()
+    b = 4  # 2,049 tokens: the last token is alone in page 128
+    good = int(slot_new[b])
+    if where == "other_page":
+        slot_new[b] = int(case.slot_mapping[last[b] - 20])  # token 2,028 sits in page 126
+    else:
+        slot_new[b] = good - good % 16 + 5  # the right page, offset 5 instead of 0
+    got, st = _append(case, kd, vd, last, ks, vs, slot_new.cuda())
+    assert st & 0x1, f"status {st:#x}"
+    skipped = slot_new.clone()
+    skipped[b] = -1
+    ref_out, st2 = _two_calls(case, kd2, vd2, last, ks, vs, skipped.cuda())
+    assert st2 == 0
+    assert torch.equal(kd, kd2) and torch.equal(vd, vd2), "a slot that is not the last token's was written"
+    assert torch.equal(got.view(torch.int16), ref_out.view(torch.int16))

@@ -48,8 +48,9 @@ def run_case(case, num_splits=0):
     got = gpu_decode(case, kd, vd, num_splits=num_splits)
     ref, _ = oracle_decode(case, kc, vc, mode="mirror")
     pure, _ = oracle_decode(case, kc, vc, mode="pure")
-    m1 = assert_close(got, ref, what="vs mirrored oracle")
-    m2 = assert_close(got, pure, what="vs pure oracle")
+    name = f"{case.cfg.name} {case.cache_dtype} L<={int(case.seq_lens.max())}"
+    m1 = assert_close(got, ref, what=f"{name} vs mirrored oracle")
+    m2 = assert_close(got, pure, what=f"{name} vs pure oracle")
     return got, ref, m1, m2
 
 

@@ -264,3 +264,4 @@ def test_split_query_e4m3_is_exact_for_elements_near_the_head_maximum():
         sigma = 2.0 ** (7 - (np.frexp(np.float32(mx))[1] - 1))
         assert np.all(np.abs(got - q) <= 2.0 ** -10 / sigma)
     assert np.all(attention.split_query_e4m3(np.zeros(8, np.float32)) == 0)
+
