@@ -4,17 +4,27 @@ workload -- KV GB/s (% of HBM peak) and us/step vs context length.
 
 One step = one decode step of a 32-layer Llama-3.1-8B-shaped model at batch
 1 and 131,072 tokens of context: for each layer, the new token's K/V is
-quantized into that layer's paged FP8 cache (kvq_reshape_and_cache), then
-paged decode attention (split-KV partial + LSE combine) reads the whole
-cache.  Each layer has its own cache (32 x 256 MiB = 8 GiB), so every step
-streams from HBM (inputs larger than L2).  Inputs are seeded synthetic
-bf16 N(0,1) with 4 outlier channels per KV head (x20) and amax/448 scales.
+quantized into that layer's paged FP8 cache and paged decode attention
+(split-KV partial + LSE combine) reads the whole cache, in one
+kvq_paged_decode_attention_append call.  Each layer has its own cache
+(32 x 256 MiB = 8 GiB), so every step streams from HBM (inputs larger than
+L2).  Inputs are seeded synthetic bf16 N(0,1) with 4 outlier channels per
+KV head (x20) and amax/448 scales.
+
+Beside the headline, a single-GPU run measures the other decode
+configurations (tiny 512-token latency floor; batch 8 at ~20K tokens;
+the 24-layer hybrid full / sliding-window stack), chunked prefill, a
+context sweep, the BF16 / E5M2 / per-token cache formats, the
+accumulation ablation, and the CPU oracle on every configuration; each leg
+carries the SM clocks sampled while it ran.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Under torchrun (N > 1) every rank runs its own replica on its GPU
-(independent sequences; no collective on the data path) and rank 0 prints
-the whole-job throughput over the slowest rank.
+Under torchrun (N > 1) the KV heads are sharded over the ranks (rank r
+holds KV heads [8r/N, 8(r+1)/N) and their query heads, of N sequences, so
+each rank streams the single-GPU step's bytes); there is no collective on
+the data path, and rank 0 prints the whole-job throughput over the slowest
+rank.
 """
 from __future__ import annotations
 
@@ -51,6 +61,7 @@ def parse():
     ap.add_argument("--no-e5m2", action="store_true")
     ap.add_argument("--no-per-token", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the tiny, concurrency-8 and hybrid legs")
     ap.add_argument("--layers", type=int, default=32,
                     help="layers per step (fewer only for small profiling runs; the metric uses 32)")
     return ap.parse_args()
@@ -102,6 +113,24 @@ def decode_bytes(context, batch=1, hq=HQ, hkv=HKV, d=D):
     """Algorithmic bytes of one decode call: FP8 K + V of the attended
     tokens, per-head K and V scales, q and out (bf16)."""
     return 2 * batch * context * hkv * d + 2 * hkv * 4 + 2 * batch * hq * d * 2
+
+
+def decode_bytes_lengths(lengths, hq, hkv, d, window=-1, esize=1):
+    """Algorithmic bytes of one decode call over sequences of the given
+    lengths: K and V of the attended tokens (the last `window` of each for a
+    sliding-window layer) at `esize` bytes per element, the per-head K and V
+    scales of an FP8 cache (none for BF16), q read and out written (bf16)."""
+    attended = sum(min(L, window) if window > 0 else L for L in lengths)
+    scales = 2 * hkv * 4 if esize == 1 else 0
+    return 2 * attended * hkv * d * esize + scales + 2 * len(lengths) * hq * d * 2
+
+
+def hybrid_step_bytes(batch=8, context=32768, hq=64, hkv=8, d=64, layers=24, window=128):
+    """One decode step of the hybrid stack: layers alternate sliding-window
+    BF16 (even) and full-attention FP8 (odd)."""
+    full = decode_bytes_lengths([context] * batch, hq, hkv, d)
+    sw = decode_bytes_lengths([context] * batch, hq, hkv, d, window=window, esize=2)
+    return (layers // 2) * (full + sw), full, sw
 
 
 def cache_write_bytes(tokens, hkv=HKV, d=D):
@@ -166,46 +195,59 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ setup ---
-def build_workload(device, seed):
-    """32 layer caches of 131,072 cached tokens (the last one is re-written
-    by every step), per-layer q and new-token K/V, one shared block table."""
+def build_workload(device, seed, batch=1, q_heads=HQ, kv_heads=HKV):
+    """32 layer caches of `batch` sequences of 131,072 cached tokens (the
+    last one is re-written by every step) over `kv_heads` KV heads, per-layer
+    q and new-token K/V, one shared block table.  One rank of a head-sharded
+    job holds its KV heads of every sequence: batch N with 8 / N heads keeps
+    the bytes per rank (8 GiB) of the single-GPU workload (batch 1, 8 heads)."""
     import torch
 
     import fp8_kv_cache_reshape_gb300 as kvq
     import workloads as W
 
     g = W.generator(seed)
-    bt, num_blocks = W.paged_layout([CONTEXT], P, g)
+    bt, num_blocks = W.paged_layout([CONTEXT] * batch, P, g)
     bt_d = bt.to(device)
     pos = torch.arange(CONTEXT, dtype=torch.int64)
-    slots = W.slots_for(bt, 0, pos, P).to(device)
+    slots = [W.slots_for(bt, b, pos, P).to(device) for b in range(batch)]
     layers = []
     chunk = 16384
     st = torch.zeros(1, dtype=torch.int32, device=device)
     for l in range(LAYERS):
         gl = W.generator(seed * 1000 + l, device=device)
-        k = W.randn_bf16((CONTEXT, HKV, D), gl, device=device)
-        v = W.randn_bf16((CONTEXT, HKV, D), gl, device=device)
-        ch = W.outlier_channels(HKV, D, 4, W.generator(seed * 1000 + l))
-        k = W.apply_outliers(k, ch)
-        v = W.apply_outliers(v, ch)
-        ks, vs = W.calibrate_amax(k), W.calibrate_amax(v)
-        kd, vd = kvq.alloc_kv_cache(num_blocks, HKV, D, device=device, fill=0)
-        for t0 in range(0, CONTEXT - 1, chunk):
-            t1 = min(CONTEXT - 1, t0 + chunk)
-            kvq.kvq_reshape_and_cache(k[t0:t1].contiguous(), v[t0:t1].contiguous(), slots[t0:t1].contiguous(),
-                                      kd, vd, ks, vs, dev_status=st)
+        ch = W.outlier_channels(kv_heads, D, 4, W.generator(seed * 1000 + l))
+        kd, vd = kvq.alloc_kv_cache(num_blocks, kv_heads, D, device=device, fill=0)
+        seqs = []
+        amax_k = torch.zeros(kv_heads, device=device)
+        amax_v = torch.zeros(kv_heads, device=device)
+        for b in range(batch):
+            k = W.apply_outliers(W.randn_bf16((CONTEXT, kv_heads, D), gl, device=device), ch)
+            v = W.apply_outliers(W.randn_bf16((CONTEXT, kv_heads, D), gl, device=device), ch)
+            amax_k = torch.maximum(amax_k, k.float().abs().amax(dim=(0, 2)))
+            amax_v = torch.maximum(amax_v, v.float().abs().amax(dim=(0, 2)))
+            seqs.append((k, v))
+        ks = (amax_k / W.E4M3_MAX).contiguous()  # caller-side calibration: amax / 448 per head
+        vs = (amax_v / W.E4M3_MAX).contiguous()
+        for b, (k, v) in enumerate(seqs):
+            for t0 in range(0, CONTEXT - 1, chunk):
+                t1 = min(CONTEXT - 1, t0 + chunk)
+                kvq.kvq_reshape_and_cache(k[t0:t1].contiguous(), v[t0:t1].contiguous(),
+                                          slots[b][t0:t1].contiguous(), kd, vd, ks, vs, dev_status=st)
         layers.append(dict(kd=kd, vd=vd, ks=ks, vs=vs,
-                           k_new=k[CONTEXT - 1:].contiguous(), v_new=v[CONTEXT - 1:].contiguous(),
-                           q=W.randn_bf16((1, HQ, D), gl, device=device),
-                           out=torch.empty((1, HQ, D), dtype=torch.bfloat16, device=device)))
-        del k, v
+                           k_new=torch.stack([k[CONTEXT - 1] for k, _ in seqs]).contiguous(),
+                           v_new=torch.stack([v[CONTEXT - 1] for _, v in seqs]).contiguous(),
+                           q=W.randn_bf16((batch, q_heads, D), gl, device=device),
+                           out=torch.empty((batch, q_heads, D), dtype=torch.bfloat16, device=device)))
+        del seqs
     torch.cuda.synchronize()
     assert int(st.item()) == 0, "cache fill reported a device fault"
-    ws_bytes = kvq.kvq_decode_workspace_size(1, HQ, HKV, D, bt.shape[1])
+    ws_bytes = kvq.kvq_decode_workspace_size(batch, q_heads, kv_heads, D, bt.shape[1])
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
-    return dict(layers=layers, bt=bt_d, num_blocks=num_blocks, slot_new=slots[CONTEXT - 1:].contiguous(),
-                seq=torch.tensor([CONTEXT], dtype=torch.int32, device=device), ws=ws, status=st)
+    return dict(layers=layers, bt=bt_d, num_blocks=num_blocks,
+                slot_new=torch.stack([sl[CONTEXT - 1] for sl in slots]).contiguous(),
+                seq=torch.full((batch,), CONTEXT, dtype=torch.int32, device=device), ws=ws, status=st,
+                batch=batch, q_heads=q_heads, kv_heads=kv_heads)
 
 
 def run_step(wl, seq=None, decode_only=False, two_calls=False):
@@ -453,96 +495,461 @@ def prefill_leg(device, reps=10, accumulation=None, head_dim=D):
             "exps": PF_NEW * PF_CACHED * HQ + PF_NEW * (PF_NEW + 1) // 2 * HQ}
 
 
-# ---------------------------------------------------------- CPU baseline ---
-CPU_SAMPLE_CONTEXT = 131072
-CPU_SAMPLE_HEADS = 2
+# --------------------------------------------- the other decode configurations ---
+def clocked(gpu, fn, *a, **kw):
+    """Run one bench leg under its own clock sampler; the leg's dict gets the
+    sampled clocks and, per timed figure, time x median SM MHz (so that legs
+    measured at different clocks can be compared)."""
+    with ClockSampler(gpu) as clk:
+        out = fn(*a, **kw)
+    if isinstance(out, dict):
+        c = clk.summary()
+        out["clocks"] = c
+        if c.get("sm_mhz"):
+            for key in ("us_per_call", "us_per_step", "ms"):
+                if out.get(key) is not None:
+                    out[key + "_x_mhz"] = round(out[key] * c["sm_mhz"], 1)
+    return out
 
 
-def _oracle_sample():
-    """One layer of the workload cut to 2 of its 8 KV heads (8 query heads),
-    full 131,072-token context, cached by the oracle (not timed)."""
-    import numpy as np
+def _hbm_peak():
+    peaks, src = measured_peaks()
+    return float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS)), src
+
+
+def _fill_decode_cache(kvq, lengths, bt, num_blocks, hkv, d, gen, device, cache_dtype="fp8_e4m3",
+                       unit_scales=False):
+    """A paged cache holding every position of every sequence (K, V ~ N(0,1)
+    rounded to bf16 on the device; FP8: per-head amax/448 scales, or 1.0
+    with unit_scales)."""
     import torch
     import workloads as W
-    from oracle import kv_cache
-    g = W.generator(4242)
-    H, L = CPU_SAMPLE_HEADS, CPU_SAMPLE_CONTEXT
+    kd, vd = kvq.alloc_kv_cache(num_blocks, hkv, d, cache_dtype=cache_dtype, device=device, fill=0)
+    ks = vs = None
+    chunks = []
+    for b, L in enumerate(lengths):
+        pos = torch.arange(L, dtype=torch.int64)
+        chunks.append((W.slots_for(bt, b, pos, P).to(device), L))
+    if cache_dtype != "bf16":  # caller-side calibration over the whole layer
+        amax_k = torch.zeros(hkv, device=device)
+        amax_v = torch.zeros(hkv, device=device)
+    data = []
+    for slots, L in chunks:
+        k = W.randn_bf16((L, hkv, d), gen, device=device)
+        v = W.randn_bf16((L, hkv, d), gen, device=device)
+        data.append((slots, k, v))
+        if cache_dtype != "bf16":
+            amax_k = torch.maximum(amax_k, k.float().abs().amax(dim=(0, 2)))
+            amax_v = torch.maximum(amax_v, v.float().abs().amax(dim=(0, 2)))
+    if cache_dtype != "bf16":
+        ks = (amax_k / W.E4M3_MAX).float().contiguous()
+        vs = (amax_v / W.E4M3_MAX).float().contiguous()
+        if unit_scales:
+            ks = torch.ones_like(ks)
+            vs = torch.ones_like(vs)
+    for slots, k, v in data:
+        kvq.kvq_reshape_and_cache(k, v, slots, kd, vd, ks, vs, cache_dtype=cache_dtype)
+    return kd, vd, ks, vs
+
+
+def tiny_leg(device, calls=64, reps=50):
+    """The tiny configuration (1 sequence of 512 tokens, 4 query / 1 KV head,
+    head_dim 64, scales 1.0): the latency floor of one decode call.  Its
+    66.6 KB stay in L2, so GB/s is reported but not against HBM."""
+    import torch
+    import fp8_kv_cache_reshape_gb300 as kvq
+    import workloads as W
+    cfg = W.TINY
+    L, hq, hkv, d = cfg.context, cfg.q_heads, cfg.kv_heads, cfg.head_dim
+    g = W.generator(W.config_seed(cfg.name) * 1000)
     bt, nb = W.paged_layout([L], P, g)
-    slots = W.slots_for(bt, 0, torch.arange(L), P).numpy()
-    k = W.randn_bf16((L, H, D), g).float().numpy()
-    v = W.randn_bf16((L, H, D), g).float().numpy()
-    q = W.randn_bf16((1, H * (HQ // HKV), D), g).float().numpy()
-    ks = (np.abs(k).max(axis=(0, 2)) / 448).astype(np.float32)
-    vs = (np.abs(v).max(axis=(0, 2)) / 448).astype(np.float32)
-    kc = np.zeros((nb, H, P, D), np.uint8)
-    vc = np.zeros((nb, H, D, P), np.uint8)
-    kv_cache.reshape_and_cache(k, v, slots, kc, vc, ks, vs)
-    return dict(q=q, kc=kc, vc=vc, ks=ks, vs=vs, bt=bt.numpy(), L=L, H=H)
+    kd, vd, one, _ = _fill_decode_cache(kvq, [L], bt, nb, hkv, d, W.generator(11, device=device), device,
+                                        unit_scales=True)
+    q = W.randn_bf16((1, hq, d), W.generator(12, device=device), device=device)
+    out = torch.empty_like(q)
+    btd, seq = bt.to(device), torch.tensor([L], dtype=torch.int32, device=device)
+    ws = torch.empty(kvq.kvq_decode_workspace_size(1, hq, hkv, d, bt.shape[1]), dtype=torch.uint8, device=device)
+
+    def run():
+        for _ in range(calls):
+            kvq.kvq_paged_decode_attention(q, kd, vd, one, one, btd, seq, out, num_blocks=nb, sm_scale=d ** -0.5,
+                                           workspace=ws)
+
+    gr = capture(run)
+    for _ in range(3):
+        gr.replay()
+    us = time_graph(gr, reps) * 1e3 / (reps * calls)
+    byts = decode_bytes_lengths([L], hq, hkv, d)
+    return {"workload": cfg.name, "us_per_call": round(us, 3), "bytes_per_call": byts,
+            "kv_gbs": round(byts / (us * 1e-6) / 1e9, 1), "l2_resident": True,
+            "timing": f"{reps} replays of a CUDA graph of {calls} decode calls (partial + combine) on one cache"}
 
 
-def cpu_baseline_run(steps, warmup, min_seconds=0.0):
-    """Time the oracle's decode (float64 numpy, one host thread) on the
-    bounded sample: `warmup` untimed calls, then `steps` timed calls (more
-    until `min_seconds` have passed)."""
+def conc8_leg(device, layers=4, reps=20):
+    """The concurrency-8 configuration: batch 8, lengths uniform in [16384,
+    24576] (seeded), 32 query / 8 KV heads, head_dim 128, pages shuffled
+    across sequences.  `layers` distinct caches (about 1.4 GB, larger than
+    L2) are read in turn, one decode call each."""
+    import torch
+    import fp8_kv_cache_reshape_gb300 as kvq
+    import workloads as W
+    cfg = W.CONC8
+    hq, hkv, d = cfg.q_heads, cfg.kv_heads, cfg.head_dim
+    lengths = W.decode_lengths(cfg)
+    bt, nb = W.paged_layout(lengths, P, W.case_generator(cfg))
+    btd = bt.to(device)
+    seq = torch.tensor(lengths, dtype=torch.int32, device=device)
+    caches = []
+    for l in range(layers):
+        gl = W.generator(W.config_seed(cfg.name) * 1000 + 100 + l, device=device)
+        kd, vd, ks, vs = _fill_decode_cache(kvq, lengths, bt, nb, hkv, d, gl, device)
+        caches.append((kd, vd, ks, vs, W.randn_bf16((len(lengths), hq, d), gl, device=device)))
+    out = torch.empty((len(lengths), hq, d), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(kvq.kvq_decode_workspace_size(len(lengths), hq, hkv, d, bt.shape[1]), dtype=torch.uint8,
+                     device=device)
+
+    def run():
+        for kd, vd, ks, vs, q in caches:
+            kvq.kvq_paged_decode_attention(q, kd, vd, ks, vs, btd, seq, out, num_blocks=nb, sm_scale=d ** -0.5,
+                                           workspace=ws)
+
+    gr = capture(run)
+    for _ in range(3):
+        gr.replay()
+    us = time_graph(gr, reps) * 1e3 / (reps * layers)
+    byts = decode_bytes_lengths(lengths, hq, hkv, d)
+    peak, src = _hbm_peak()
+    gbs = byts / (us * 1e-6) / 1e9
+    return {"workload": cfg.name, "lengths": lengths, "us_per_call": round(us, 3), "bytes_per_call": byts,
+            "kv_gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4), "peak_gbs": peak, "peak_source": src,
+            "splits": kvq.kvq_decode_num_splits(len(lengths), hkv, bt.shape[1]),
+            "timing": f"{reps} replays of a CUDA graph of {layers} decode calls on distinct caches"}
+
+
+def hybrid_leg(device, reps=10):
+    """The hybrid gpt-oss-20b-shaped step: 24 layers, even layers sliding
+    window 128 over a BF16 cache, odd layers full attention over an FP8
+    cache; 64 query / 8 KV heads, head_dim 64, batch 8, context 32,768.  One
+    step = 24 decode calls (12 full caches of 268 MB: 3.2 GB, larger than
+    L2).  The sliding-window layers' caches hold their windows' pages; their
+    time is also measured at shorter contexts, where it must stay flat."""
+    import torch
+    import fp8_kv_cache_reshape_gb300 as kvq
+    import workloads as W
+    cfg = W.HYBRID
+    B, L, hq, hkv, d, win = cfg.batch, cfg.context, cfg.q_heads, cfg.kv_heads, cfg.head_dim, cfg.window
+    lengths = [L] * B
+    g = W.case_generator(cfg)
+    bt, nb = W.paged_layout(lengths, P, g)
+    btd = bt.to(device)
+    seq = torch.tensor(lengths, dtype=torch.int32, device=device)
+    # sliding-window caches: 8 pages per sequence, mapped cyclically so that any
+    # window position reads written pages
+    sw_pages = (win + P - 1) // P
+    sw_bt = (torch.arange(B, dtype=torch.int32)[:, None] * sw_pages +
+             torch.arange(bt.shape[1], dtype=torch.int32)[None, :] % sw_pages).to(device)
+    layers = []
+    for l in range(cfg.layers):
+        gl = W.generator(W.config_seed(cfg.name) * 1000 + 200 + l, device=device)
+        q = W.randn_bf16((B, hq, d), gl, device=device)
+        if l % 2 == 0:  # sliding window, BF16
+            kd, vd = kvq.alloc_kv_cache(B * sw_pages, hkv, d, cache_dtype="bf16", device=device, fill=0)
+            for b in range(B):
+                pos = torch.arange(sw_pages * P, dtype=torch.int64)
+                slots = (b * sw_pages + pos // P) * P + pos % P
+                kvq.kvq_reshape_and_cache(W.randn_bf16((pos.numel(), hkv, d), gl, device=device),
+                                          W.randn_bf16((pos.numel(), hkv, d), gl, device=device), slots.to(device),
+                                          kd, vd, cache_dtype="bf16")
+            layers.append(dict(sw=True, kd=kd, vd=vd, ks=None, vs=None, q=q, nb=B * sw_pages))
+        else:
+            kd, vd, ks, vs = _fill_decode_cache(kvq, lengths, bt, nb, hkv, d, gl, device)
+            layers.append(dict(sw=False, kd=kd, vd=vd, ks=ks, vs=vs, q=q, nb=nb))
+    out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(kvq.kvq_decode_workspace_size(B, hq, hkv, d, bt.shape[1]), dtype=torch.uint8, device=device)
+
+    def call(ly):
+        if ly["sw"]:
+            kvq.kvq_paged_decode_attention(ly["q"], ly["kd"], ly["vd"], None, None, sw_bt, seq, out, num_blocks=ly["nb"],
+                                           sm_scale=d ** -0.5, window=win, cache_dtype="bf16", workspace=ws)
+        else:
+            kvq.kvq_paged_decode_attention(ly["q"], ly["kd"], ly["vd"], ly["ks"], ly["vs"], btd, seq, out,
+                                           num_blocks=ly["nb"], sm_scale=d ** -0.5, workspace=ws)
+
+    g_step = capture(lambda: [call(ly) for ly in layers])
+    g_full = capture(lambda: [call(ly) for ly in layers if not ly["sw"]])
+    g_sw = capture(lambda: [call(ly) for ly in layers if ly["sw"]])
+    for _ in range(3):
+        g_step.replay()
+    step_us = time_graph(g_step, reps) * 1e3 / reps
+    full_us = time_graph(g_full, reps) * 1e3 / (reps * (cfg.layers // 2))
+    sw_rows = []
+    for ctx in (4096, 8192, 16384, 32768):
+        seq.fill_(ctx)
+        g_sw.replay()
+        sw_rows.append({"context": ctx, "us_per_sw_layer": round(time_graph(g_sw, 5 * reps) * 1e3 /
+                                                                 (5 * reps * (cfg.layers // 2)), 3)})
+    seq.fill_(L)
+    step_b, full_b, sw_b = hybrid_step_bytes(B, L, hq, hkv, d, cfg.layers, win)
+    peak, src = _hbm_peak()
+    gbs = step_b / (step_us * 1e-6) / 1e9
+    sw_us = [r["us_per_sw_layer"] for r in sw_rows]
+    return {"workload": cfg.name, "us_per_step": round(step_us, 2), "bytes_per_step": step_b,
+            "kv_gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4), "peak_gbs": peak, "peak_source": src,
+            "us_per_full_layer": round(full_us, 3), "bytes_per_full_layer": full_b,
+            "full_layer_frac_hbm": round(full_b / (full_us * 1e-6) / 1e9 / peak, 4),
+            "bytes_per_sw_layer": sw_b, "sw_layer_vs_context": sw_rows,
+            "sw_flatness": round(max(sw_us) / min(sw_us), 3),
+            "timing": f"{reps} replays of a CUDA graph of the 24-layer step; full and sliding-window layers also "
+                      f"timed alone"}
+
+
+# ---------------------------------------------------------- CPU baseline ---
+# The oracle (oracle/, float64 numpy), as it stands, timed on the host cores
+# on each configuration: its decode runs per (sequence, KV head) unit -- the
+# unit the method's arithmetic is independent over -- one after the other on
+# one core, and over a process pool on all cores.  These functions run in a
+# child process that hides the GPU (CUDA_VISIBLE_DEVICES="") and never
+# initialises CUDA, so its pool may fork: the workers inherit the inputs.
+_CPU_PROBLEM = None
+
+
+def _oracle_decode_problem(cfg, layer=0, window=None, cache_dtype="fp8_e4m3", only_window_tokens=False):
+    """Inputs of one decode layer of `cfg` and the oracle's own cache of them."""
     import numpy as np
+    import workloads as W
+    from oracle import kv_cache
+    case = W.decode_case(cfg, layer=layer, window=window, cache_dtype=cache_dtype,
+                         only_window_tokens=only_window_tokens)
+    d, hkv = cfg.head_dim, cfg.kv_heads
+    bf = cache_dtype == "bf16"
+    kc = np.zeros((case.num_blocks, hkv, P, d), np.uint16 if bf else np.uint8)
+    vc = np.zeros((case.num_blocks, hkv, d, P), np.uint16 if bf else np.uint8)
+    kv_cache.reshape_and_cache(case.k.float().numpy(), case.v.float().numpy(), case.slot_mapping.numpy(), kc, vc,
+                               case.k_scale.numpy(), case.v_scale.numpy(), cache_dtype)
+    return dict(q=case.q.float().numpy(), kc=kc, vc=vc, ks=case.k_scale.numpy(), vs=case.v_scale.numpy(),
+                bt=case.block_table.numpy(), sl=case.seq_lens.numpy(), sm=case.sm_scale, window=case.window,
+                dtype=cache_dtype, g=cfg.q_heads // hkv,
+                units=[(b, h) for b in range(case.q.shape[0]) for h in range(hkv)],
+                bytes=decode_bytes_lengths(case.seq_lens.tolist(), cfg.q_heads, hkv, d, window=case.window,
+                                           esize=2 if bf else 1))
+
+
+def _oracle_decode_unit(i):
+    """The oracle's decode (mirrored mode) of unit i of the current problem:
+    one sequence and one KV head with its query-head group."""
     from oracle import attention
-    smp = _oracle_sample()
+    pr = _CPU_PROBLEM
+    b, h = pr["units"][i]
+    g = pr["g"]
+    attention.paged_decode(pr["q"][b:b + 1, h * g:(h + 1) * g], pr["kc"][:, h:h + 1], pr["vc"][:, h:h + 1],
+                           pr["ks"][h:h + 1], pr["vs"][h:h + 1], pr["bt"][b:b + 1], pr["sl"][b:b + 1], pr["sm"],
+                           window=pr["window"], cache_dtype=pr["dtype"])
+    return i
 
-    def call():
-        attention.paged_decode(smp["q"], smp["kc"], smp["vc"], smp["ks"], smp["vs"], smp["bt"],
-                               np.array([smp["L"]]), 1 / math.sqrt(D))
 
-    for _ in range(warmup):
-        call()
-    t0 = time.perf_counter()
-    reps = 0
-    while reps < steps or time.perf_counter() - t0 < min_seconds:
-        call()
+def _oracle_prefill_problem(rows_per_unit=8, n_rows=256):
+    """The chunked-prefill configuration for the oracle, with a stated sample
+    of n_rows (query token, head) rows spread over the chunk."""
+    import numpy as np
+    import workloads as W
+    from oracle import kv_cache
+    pc = W.prefill_case(W.PREFILL)
+    cfg = pc.cfg
+    kc = np.zeros((pc.num_blocks, cfg.kv_heads, P, cfg.head_dim), np.uint8)
+    vc = np.zeros((pc.num_blocks, cfg.kv_heads, cfg.head_dim, P), np.uint8)
+    kv_cache.reshape_and_cache(pc.k.float().numpy(), pc.v.float().numpy(), pc.slot_mapping.numpy(), kc, vc,
+                               pc.k_scale.numpy(), pc.v_scale.numpy())
+    qs = np.float32(pc.q_scale.item())
+    q8 = kv_cache.quantize_query(pc.q.float().numpy(), qs)
+    rng = np.random.default_rng(4)
+    flat = rng.choice(cfg.new_tokens * cfg.q_heads, n_rows, replace=False)
+    rows = sorted((int(f // cfg.q_heads), int(f % cfg.q_heads)) for f in flat)
+    # units: rows of one KV head together (the oracle gathers a head's keys once per call)
+    g = cfg.q_heads // cfg.kv_heads
+    rows.sort(key=lambda r: (r[1] // g, r[0]))
+    units = [rows[i:i + rows_per_unit] for i in range(0, len(rows), rows_per_unit)]
+    return dict(q8=q8, qs=qs, kc=kc, vc=vc, ks=pc.k_scale.numpy(), vs=pc.v_scale.numpy(),
+                bt=pc.block_table.numpy(), cu=pc.cu_seqlens_q.numpy(), sl=pc.seq_lens.numpy(),
+                sm=float(np.float32(pc.sm_scale)), units=units, n_rows=n_rows,
+                total_rows=cfg.new_tokens * cfg.q_heads)
+
+
+def _oracle_prefill_unit(i):
+    from oracle import attention
+    pr = _CPU_PROBLEM
+    attention.prefill(pr["q8"], pr["qs"], pr["kc"], pr["vc"], pr["ks"], pr["vs"], pr["bt"], pr["cu"], pr["sl"],
+                      pr["sm"], rows=pr["units"][i])
+    return i
+
+
+def _time_units(fn, n_units, pool, min_seconds):
+    """Seconds for one pass over all units: on one core (pool None) or over
+    the pool; repeated until min_seconds have passed, the mean taken."""
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        if pool is None:
+            for i in range(n_units):
+                fn(i)
+        else:
+            pool.map(fn, range(n_units), chunksize=1)
         reps += 1
-    dt = (time.perf_counter() - t0) / reps
-    H = smp["H"]
-    byts = decode_bytes(smp["L"], hq=H * HQ // HKV, hkv=H)
-    return {"value": round(byts / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"decode call over one layer cut to {H} of {HKV} KV heads ({H * HQ // HKV} query heads), "
-                      f"context {smp['L']}; {reps} timed calls; float64 numpy, 1 host thread",
-            "seconds_per_call": round(dt, 4), "bytes_per_call": byts, "reps": reps}
+        if time.perf_counter() - t0 >= min_seconds:
+            return (time.perf_counter() - t0) / reps, reps
 
 
-def cpu_baseline(steps=1, warmup=0, min_seconds=10.0):
-    """Run the CPU baseline in a child process pinned to one BLAS thread."""
+def cpu_baselines_run(configs=("tiny", "llama", "conc8", "hybrid", "prefill"), min_seconds=1.0):
+    """The oracle timed per configuration, on one core and on every core of
+    this host (the caller pins BLAS to one thread per process).  Returns
+    {config: {...}} with seconds per call / layer / step and the metric."""
+    import multiprocessing as mp
+    import workloads as W
+    global _CPU_PROBLEM
+    ncpu = os.cpu_count() or 1
+    ctx = mp.get_context("fork")  # this process has no CUDA context (see above)
+    out = {"nproc": ncpu}
+
+    def run(name, fn, n_units):
+        one, r1 = _time_units(fn, n_units, None, min_seconds)
+        with ctx.Pool(min(ncpu, n_units)) as pool:
+            pool.map(fn, range(min(ncpu, n_units)))  # workers started and warm
+            allc, ra = _time_units(fn, n_units, pool, min_seconds)
+        return {"one_core_s": one, "all_core_s": allc, "threads": min(ncpu, n_units), "units": n_units,
+                "reps_one_core": r1, "reps_all_core": ra}
+
+    if "tiny" in configs:
+        _CPU_PROBLEM = _oracle_decode_problem(W.TINY)
+        r = run("tiny", _oracle_decode_unit, len(_CPU_PROBLEM["units"]))
+        r.update(workload=W.TINY.name, per="decode call", bytes=_CPU_PROBLEM["bytes"],
+                 sample="the whole call (1 sequence, 1 KV head)")
+        out["tiny"] = r
+    if "llama" in configs:
+        _CPU_PROBLEM = _oracle_decode_problem(W.LLAMA_128K)
+        r = run("llama", _oracle_decode_unit, len(_CPU_PROBLEM["units"]))
+        r.update(workload=W.LLAMA_128K.name, per="decode layer (a step is 32 of them)", bytes=_CPU_PROBLEM["bytes"],
+                 sample="one whole layer: 8 KV-head units of 131,072 tokens")
+        out["llama"] = r
+    if "conc8" in configs:
+        _CPU_PROBLEM = _oracle_decode_problem(W.CONC8)
+        r = run("conc8", _oracle_decode_unit, len(_CPU_PROBLEM["units"]))
+        r.update(workload=W.CONC8.name, per="decode call", bytes=_CPU_PROBLEM["bytes"],
+                 sample="the whole call: 8 sequences x 8 KV-head units")
+        out["conc8"] = r
+    if "hybrid" in configs:
+        _CPU_PROBLEM = _oracle_decode_problem(W.HYBRID, layer=1, window=-1)
+        full = run("hybrid_full", _oracle_decode_unit, len(_CPU_PROBLEM["units"]))
+        full_b = _CPU_PROBLEM["bytes"]
+        _CPU_PROBLEM = _oracle_decode_problem(W.HYBRID, layer=0, window=W.HYBRID.window, cache_dtype="bf16",
+                                              only_window_tokens=True)
+        sw = run("hybrid_sw", _oracle_decode_unit, len(_CPU_PROBLEM["units"]))
+        n = W.HYBRID.layers // 2
+        out["hybrid"] = {"workload": W.HYBRID.name, "per": "decode step of 24 layers",
+                         "one_core_s": n * (full["one_core_s"] + sw["one_core_s"]),
+                         "all_core_s": n * (full["all_core_s"] + sw["all_core_s"]),
+                         "threads": full["threads"], "bytes": n * (full_b + _CPU_PROBLEM["bytes"]),
+                         "sample": "one full-attention and one sliding-window layer (64 units each), "
+                                   "times 12 each", "full_layer": full, "sw_layer": sw}
+    if "prefill" in configs:
+        _CPU_PROBLEM = _oracle_prefill_problem()
+        r = run("prefill", _oracle_prefill_unit, len(_CPU_PROBLEM["units"]))
+        f = _CPU_PROBLEM["total_rows"] / _CPU_PROBLEM["n_rows"]
+        r.update(workload=W.PREFILL.name, per="chunked prefill call (extrapolated from the row sample)",
+                 flops=prefill_flops(), one_core_s=r["one_core_s"] * f, all_core_s=r["all_core_s"] * f,
+                 sample=f"{_CPU_PROBLEM['n_rows']} of {_CPU_PROBLEM['total_rows']} (query token, head) rows, "
+                        f"spread at random over the chunk; times scaled by {f:.0f}")
+        out["prefill"] = r
+    _CPU_PROBLEM = None
+    for k, r in out.items():
+        if isinstance(r, dict) and "bytes" in r:
+            r["gbs_one_core"] = r["bytes"] / r["one_core_s"] / 1e9
+            r["gbs_all_core"] = r["bytes"] / r["all_core_s"] / 1e9
+        if isinstance(r, dict) and "flops" in r:
+            r["tflops_all_core"] = r["flops"] / r["all_core_s"] / 1e12
+            r["tflops_one_core"] = r["flops"] / r["one_core_s"] / 1e12
+    return out
+
+
+def _cpu_child(args, timeout=1800):
+    """Run `bench.py --_cpu-child <json args>` with the GPU hidden and one
+    BLAS thread per process; returns its last JSON line."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_cpu-baseline-child", str(steps), str(warmup),
-                        str(min_seconds)], env=env, capture_output=True, text=True, timeout=1800)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_cpu-child", json.dumps(args)], env=env,
+                       capture_output=True, text=True, timeout=timeout)
     for line in r.stdout.splitlines()[::-1]:
         if line.startswith("{"):
             return json.loads(line)
-    return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+    return {"error": r.stderr[-400:]}
+
+
+def cpu_baselines(min_seconds=1.0):
+    """The per-configuration oracle times and, for the JSON line's
+    cpu_baseline, the Llama 128K layer on every core."""
+    res = _cpu_child({"what": "configs", "min_seconds": min_seconds})
+    if "llama" not in res:
+        return {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle",
+                "sample": "failed: " + str(res.get("error"))}, res
+    r = res["llama"]
+    head = {"value": round(r["gbs_all_core"], 4), "unit": "GB/s", "cores": r["threads"], "kind": "oracle",
+            "sample": f"one decode layer of the 128K workload (8 KV-head units of 131,072 tokens) over "
+                      f"{r['threads']} processes of {res['nproc']} host cores; float64 numpy",
+            "seconds_per_layer": round(r["all_core_s"], 4), "one_core_seconds_per_layer": round(r["one_core_s"], 4),
+            "nproc": res["nproc"]}
+    return head, res
 
 
 # ----------------------------------------------------------------- arms ---
 def reference_arm(args, rank, world):
-    """The reference arm: the CPU oracle timed on the host cores, on the same
-    metric, unit and workload shape; each step is one oracle decode call
-    over the bounded sample."""
+    """The reference arm: the CPU oracle, as it stands, timed on the host
+    cores on the same metric, unit and workload; each step is the oracle's
+    decode of one whole layer of the 128K workload (8 KV-head units of
+    131,072 tokens) over every core (a bounded sample of the 32-layer step).
+    Under torchrun only rank 0 runs it."""
     if rank != 0:
         return
-    cb = cpu_baseline(steps=args.steps, warmup=args.warmup, min_seconds=0.0)
-    sec = cb.get("seconds_per_call")
-    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": None if sec is None else round(sec * 1e3, 2),
+    res = _cpu_child({"what": "reference", "steps": args.steps, "warmup": args.warmup})
+    if "seconds_per_step" not in res:
+        print(json.dumps({"impl": "reference", "unavailable": "oracle run failed: " + str(res.get("error"))[-200:]}),
+              flush=True)
+        return
+    sec, byts = res["seconds_per_step"], res["bytes_per_step"]
+    value = round(byts / sec / 1e9, 4)
+    cb = {"value": value, "unit": "GB/s", "cores": res["threads"], "kind": "oracle",
+          "sample": f"one decode layer of the 128K workload per step (8 KV-head units of 131,072 tokens) over "
+                    f"{res['threads']} processes on {res['nproc']} host cores; float64 numpy; {args.steps} timed "
+                    f"steps after {args.warmup} warm-up"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "llama31_8b_decode_128k", "layers": LAYERS, "batch": 1, "context": CONTEXT,
                        "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "page": P,
-                       "step": f"one oracle decode call over {CPU_SAMPLE_HEADS} of {HKV} KV heads of one layer"},
+                       "step": "the oracle's decode of one layer (of the 32 in a step)"},
             "cpu_baseline": cb,
-            "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def _reference_steps(steps, warmup):
+    """The reference arm's timed loop (in the CPU child)."""
+    import multiprocessing as mp
+    import workloads as W
+    global _CPU_PROBLEM
+    _CPU_PROBLEM = _oracle_decode_problem(W.LLAMA_128K)
+    n = len(_CPU_PROBLEM["units"])
+    ncpu = os.cpu_count() or 1
+    with mp.get_context("fork").Pool(min(ncpu, n)) as pool:
+        for _ in range(max(1, warmup)):
+            pool.map(_oracle_decode_unit, range(n), chunksize=1)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            pool.map(_oracle_decode_unit, range(n), chunksize=1)
+        sec = (time.perf_counter() - t0) / max(1, steps)
+    return {"seconds_per_step": sec, "bytes_per_step": _CPU_PROBLEM["bytes"], "threads": min(ncpu, n),
+            "nproc": ncpu}
 
 
 def ours_arm(args, rank, world, local_rank):
     import torch
+    from fp8_kv_cache_reshape_gb300.sharding import kv_head_shard
     device = f"cuda:{local_rank}"
     torch.cuda.set_device(local_rank)
     dist = None
@@ -554,7 +961,10 @@ def ours_arm(args, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
 
-    wl = build_workload(device, seed=7 + rank)
+    # head-sharded across ranks: rank r holds KV heads [r * 8 / N, (r + 1) * 8 / N)
+    # (and their query-head groups) of N sequences; no collective on the data path
+    shard = kv_head_shard(HQ, HKV, world, rank)
+    wl = build_workload(device, seed=7 + rank, batch=world, q_heads=shard.q_heads, kv_heads=shard.kv_heads)
     g_step = capture(lambda: run_step(wl))
     g_dec = capture(lambda: run_step(wl, decode_only=True))
     g_two = capture(lambda: run_step(wl, two_calls=True))
@@ -574,71 +984,88 @@ def ours_arm(args, rank, world, local_rank):
     st = int(wl["status"].item())
     assert st == 0, f"device status {st:#x}"
 
-    step_bytes = LAYERS * (decode_bytes(CONTEXT) + cache_write_bytes(1))
+    call_bytes = decode_bytes(CONTEXT, batch=world, hq=shard.q_heads, hkv=shard.kv_heads)
+    step_bytes = LAYERS * (call_bytes + cache_write_bytes(world, hkv=shard.kv_heads))
     ms_per_step = total_ms / args.steps
     value = job_value(world, step_bytes, args.steps, total_ms)
-    peaks, src = measured_peaks()
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    hbm, src = _hbm_peak()
     call_ms = dec_ms / (dec_reps * LAYERS)
-    achieved = decode_bytes(CONTEXT) / (call_ms * 1e-3) / 1e9
-    traffic = decode_traffic()
-    sweep = None if args.no_sweep else context_sweep(wl, g_dec)
-    pf = None if args.no_prefill else prefill_leg(device)
-    bf = None if (args.no_sweep or args.no_bf16) else format_compare(sweep, device, "bf16")
-    e5 = None if (args.no_sweep or args.no_e5m2) else format_compare(sweep, device, "fp8_e5m2")
-    pt = None if (args.no_sweep or args.no_per_token) else format_compare(sweep, device, "fp8_e4m3", per_token=True)
+    achieved = call_bytes / (call_ms * 1e-3) / 1e9
+    traffic = decode_traffic() if world == 1 else None
+    legs = world == 1  # the characterisation legs run on single-GPU runs only
+    sweep = clocked(local_rank, context_sweep, wl, g_dec) if legs and not args.no_sweep else None
+    configs = None
+    if legs and not args.no_configs:
+        configs = {"tiny_decode_512": clocked(local_rank, tiny_leg, device),
+                   "llama31_8b_decode_conc8_20k": clocked(local_rank, conc8_leg, device),
+                   "gpt_oss_20b_hybrid_decode_32k": clocked(local_rank, hybrid_leg, device)}
+    pf = clocked(local_rank, prefill_leg, device) if legs and not args.no_prefill else None
+    no_cmp = not legs or args.no_sweep
+    bf = None if (no_cmp or args.no_bf16) else clocked(local_rank, format_compare, sweep, device, "bf16")
+    e5 = None if (no_cmp or args.no_e5m2) else clocked(local_rank, format_compare, sweep, device, "fp8_e5m2")
+    pt = None if (no_cmp or args.no_per_token) else clocked(local_rank, format_compare, sweep, device, "fp8_e4m3",
+                                                             per_token=True)
     abl = None
-    if not (args.no_sweep or args.no_ablation):  # single- against two-level accumulation
-        sl = format_compare(sweep, device, "fp8_e4m3", accumulation="single_level")
+    if not (no_cmp or args.no_ablation):  # single- against two-level accumulation
+        sl = clocked(local_rank, format_compare, sweep, device, "fp8_e4m3", accumulation="single_level")
         abl = {"decode_single_level": sl,
-               "prefill_single_level": None if args.no_prefill else prefill_leg(device, accumulation="single_level"),
-               "prefill_head_dim_256": None if args.no_prefill else prefill_leg(device, head_dim=256)}
-    two_reps = max(20, args.steps)
-    two_ms = time_graph(g_two, two_reps) / two_reps  # the same step as two calls per layer
-    e2e_fn, h2d, d2h = e2e_setup(wl)
-    g_e2e = capture(e2e_fn)
-    e2e_reps = max(3, args.steps)
-    e2e_ms = time_graph(g_e2e, e2e_reps) / e2e_reps
-    eager_ms = time_eager(e2e_fn, 3) / 3
+               "prefill_single_level": None if args.no_prefill else clocked(local_rank, prefill_leg, device,
+                                                                            accumulation="single_level"),
+               "prefill_head_dim_256": None if args.no_prefill else clocked(local_rank, prefill_leg, device,
+                                                                            head_dim=256)}
+    with ClockSampler(local_rank) as clk2:
+        two_reps = max(20, args.steps)
+        two_ms = time_graph(g_two, two_reps) / two_reps  # the same step as two calls per layer
+        e2e_fn, h2d, d2h = e2e_setup(wl)
+        g_e2e = capture(e2e_fn)
+        e2e_reps = max(3, args.steps)
+        e2e_ms = time_graph(g_e2e, e2e_reps) / e2e_reps
+        eager_ms = time_eager(e2e_fn, 3) / 3
+    e2e_ms = max_over_ranks(e2e_ms, dist, device)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8_e4m3 storage, f16/f32 MMA, f32 accumulate", "data": "synthetic",
-        "config": {"workload": "llama31_8b_decode_128k", "layers": LAYERS, "batch": 1, "context": CONTEXT,
+        "config": {"workload": "llama31_8b_decode_128k", "layers": LAYERS, "batch": world, "context": CONTEXT,
                    "q_heads": HQ, "kv_heads": HKV, "head_dim": D, "page": P, "block_table": "permuted",
                    "scales": "per-KV-head amax/448, 4 outlier channels x20",
-                   "l2": "inputs larger than L2: 32 distinct 256 MiB layer caches per step",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": "inputs larger than L2: 32 distinct 256 MiB layer caches per step and rank",
+                   "parallelism": (f"KV heads sharded over {world} GPUs ({shard.kv_heads} KV / {shard.q_heads} "
+                                   f"query heads each), batch {world}; no collective on the data path")
+                   if world > 1 else "1 GPU",
                    "us_per_layer": round(ms_per_step * 1e3 / LAYERS, 3)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": traffic,
                      "kernel": "paged decode attention call (split-KV partial + LSE combine), per layer",
                      "peak_source": f"{src} hbm_gbs",
-                     "avg_call_us": round(call_ms * 1e3, 3), "bytes_per_call": decode_bytes(CONTEXT),
+                     "avg_call_us": round(call_ms * 1e3, 3), "bytes_per_call": call_bytes,
                      "timing": f"{dec_reps} replays of a CUDA graph of {LAYERS} decode calls"},
-        "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+        "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "how": "public API calls (host->device copies from pinned memory, step, device->host copies) "
                        "captured once in a CUDA graph and replayed",
                 "eager_python_ms_per_step": round(eager_ms, 4),
-                "eager_python_value": round(step_bytes / (eager_ms * 1e-3) / 1e9, 1)},
+                "eager_python_value": round(world * step_bytes / (eager_ms * 1e-3) / 1e9, 1)},
         "gpu_launches": args.steps * LAYERS * 2,
         "timing": "CUDA graph of one step (32 x [decode partial with the new token's cache write + combine]) "
                   "replayed",
         "step_two_calls": {"ms_per_step": round(two_ms, 4),
-                           "value": round(step_bytes / (two_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                           "value": round(world * step_bytes / (two_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                            "how": "the same step as kvq_reshape_and_cache + kvq_paged_decode_attention per layer "
-                                  "(3 kernels per layer)"},
+                                  "(3 kernels per layer)", "clocks": clk2.summary()},
         "clocks": clk.summary(),
         "sweep": sweep,
+        "configs": configs,
         "prefill": pf,
         "bf16_compare": bf,
         "e5m2_compare": e5,
         "per_token_compare": pt,
         "accumulation_ablation": abl,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        head, per_config = cpu_baselines()
+        line["cpu_baseline"] = head
+        line["cpu_baseline_per_config"] = per_config
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -647,8 +1074,12 @@ def ours_arm(args, rank, world, local_rank):
 
 
 def main():
-    if len(sys.argv) == 5 and sys.argv[1] == "--_cpu-baseline-child":
-        print(json.dumps(cpu_baseline_run(int(sys.argv[2]), int(sys.argv[3]), float(sys.argv[4]))), flush=True)
+    if len(sys.argv) == 3 and sys.argv[1] == "--_cpu-child":
+        a = json.loads(sys.argv[2])
+        if a["what"] == "configs":
+            print(json.dumps(cpu_baselines_run(min_seconds=a.get("min_seconds", 1.0))), flush=True)
+        else:
+            print(json.dumps(_reference_steps(a["steps"], a["warmup"])), flush=True)
         return
     args = parse()
     global LAYERS

@@ -149,6 +149,18 @@ def slots_for(block_table: torch.Tensor, seq: int, positions: torch.Tensor, page
     return blocks * page + positions % page
 
 
+def case_generator(cfg: DecodeConfig, layer: int = 0, seed_base: int = 0) -> torch.Generator:
+    """The generator of decode_case(cfg, layer, seed_base); its first draw is
+    the context lengths."""
+    return generator(seed_base + 1000 * config_seed(cfg.name) + layer)
+
+
+def decode_lengths(cfg: DecodeConfig, layer: int = 0, seed_base: int = 0) -> list:
+    """The context lengths decode_case(cfg, layer, seed_base) uses, without
+    building the case (for byte counts and GPU-side workloads)."""
+    return context_lengths(cfg, case_generator(cfg, layer, seed_base))
+
+
 @dataclasses.dataclass
 class DecodeCase:
     """One decode layer: the tokens to cache and the step's query."""
@@ -175,7 +187,7 @@ def decode_case(cfg: DecodeConfig, layer: int = 0, seed_base: int = 0, lengths=N
     Every position 0..L-1 of every sequence is a cached token (the last one
     being the step's own token).  With only_window_tokens, only the last
     `window` positions are produced (what a sliding-window layer reads)."""
-    gen = generator(seed_base + 1000 * config_seed(cfg.name) + layer)
+    gen = case_generator(cfg, layer, seed_base)
     lens = list(lengths) if lengths is not None else context_lengths(cfg, gen)
     win = cfg.window if window is None else window
     bt, num_blocks = paged_layout(lens, cfg.page, gen)
