@@ -53,6 +53,11 @@ struct DecodeParams {
   const int32_t* seq_lens;
   float* o_part;    // [B][Hq][S][D]
   float* lse_part;  // [B][Hq][S], log2 units
+  // direct: one page range per (sequence, KV head) and one item per CTA; the
+  // CTA merges its consumer warps' partials in shared memory and writes the
+  // bf16 output itself (no combine kernel)
+  __nv_bfloat16* out;
+  int direct;
   int B, Hq, Hkv, g, max_blocks;
   int64_t num_blocks;
   float sm_scale;
@@ -88,12 +93,14 @@ struct Geo {
 constexpr int kNW = 4;     // consumer warps per CTA
 constexpr int kCtasPerSm = 3;
 
-// About 80 KiB of pages in flight per CTA, in a multiple of kNW stages: the
-// consumers take stages round-robin, so with NST % NW == 0 every ring slot
-// is always consumed by the same warp, which waits on the slot's phases in
-// order.  (If two warps shared a slot, a warp could test a slot whose
-// previous fill has not landed yet, and a parity wait would then see the
-// phase before it as complete.)
+// As many pages in flight per CTA as fit beside kCtasPerSm CTAs on one SM
+// (228 KiB of shared memory per SM, 1 KiB of it reserved per CTA, a few
+// hundred bytes of barriers), in a multiple of kNW stages: the consumers
+// take stages round-robin, so with NST % NW == 0 every ring slot is always
+// consumed by the same warp, which waits on the slot's phases in order.  (If
+// two warps shared a slot, a warp could test a slot whose previous fill has
+// not landed yet, and a parity wait would then see the phase before it as
+// complete.)
 // Per-token scales (PT): each stage also holds the scale records of its two
 // pages after the pages, [K0 V0][K1 V1] (16 floats each, one 128-byte copy
 // per page from the interleaved scale cache).
@@ -103,9 +110,11 @@ constexpr int stage_stride() {
   return Geo<D, FP8>::STAGE + (PT ? kScaleBytes : 0);
 }
 
+constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kRingBudget = kSmemPerSm / kCtasPerSm - 1024 - 512;
 template <int D, bool FP8, bool PT = false>
 constexpr int stages_for() {
-  constexpr int n = (81920 / stage_stride<D, FP8, PT>()) > 32 ? 32 : (81920 / stage_stride<D, FP8, PT>());
+  constexpr int n = (kRingBudget / stage_stride<D, FP8, PT>()) > 32 ? 32 : (kRingBudget / stage_stride<D, FP8, PT>());
   return (n / kNW) * kNW < kNW ? kNW : (n / kNW) * kNW;
 }
 
@@ -113,6 +122,15 @@ template <int D, bool FP8, int NST, bool PT = false>
 constexpr size_t decode_smem_bytes() {
   return size_t(NST) * stage_stride<D, FP8, PT>() + (2 * NST + 1) * sizeof(uint64_t) + NST * sizeof(int) + 16;
 }
+// kCtasPerSm CTAs of every instantiation fit on one SM
+static_assert(kCtasPerSm * (decode_smem_bytes<128, true, stages_for<128, true>()>() + 1024) <= kSmemPerSm, "smem");
+static_assert(kCtasPerSm * (decode_smem_bytes<64, true, stages_for<64, true>()>() + 1024) <= kSmemPerSm, "smem");
+static_assert(kCtasPerSm * (decode_smem_bytes<128, false, stages_for<128, false>()>() + 1024) <= kSmemPerSm, "smem");
+static_assert(kCtasPerSm * (decode_smem_bytes<64, false, stages_for<64, false>()>() + 1024) <= kSmemPerSm, "smem");
+static_assert(kCtasPerSm * (decode_smem_bytes<128, true, stages_for<128, true, true>(), true>() + 1024) <= kSmemPerSm,
+              "smem");
+static_assert(kCtasPerSm * (decode_smem_bytes<64, true, stages_for<64, true, true>(), true>() + 1024) <= kSmemPerSm,
+              "smem");
 
 struct ItemRange {
   int b, kvh, split;
@@ -259,16 +277,18 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
         }
         fence_proxy_async_global();  // the stores, before the bulk copy of the page reads them
       };
+      // block ids: one coalesced load per 32 pages, issued a batch ahead so
+      // that its latency hides behind the copies of the current batch
+      auto load_ids = [&](int base) { return (base + lane < r.n) ? __ldg(bt + base + lane) : 0; };
+      int blk_next = load_ids(0);
       for (int base = 0; base < r.n && !aborted; base += 32) {
         const int cnt = min(32, r.n - base);
-        int blk = 0, bad = 0;
-        if (lane < cnt) {
-          blk = __ldg(bt + base + lane);
-          if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
-            bad = 1;
-            blk = 0;
-            set_status(p.dev_status, KVQ_DEV_BAD_BLOCK);
-          }
+        int blk = blk_next, bad = 0;
+        if (base + 32 < r.n) blk_next = load_ids(base + 32);
+        if (lane < cnt && (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks)) {
+          bad = 1;
+          blk = 0;
+          set_status(p.dev_status, KVQ_DEV_BAD_BLOCK);
         }
         for (int j = 0; j < cnt; j += PPS, ++it) {
           const int b0 = __shfl_sync(0xffffffffu, blk, j);
@@ -747,6 +767,53 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
       l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
       l[1] += __shfl_xor_sync(0xffffffffu, l[1], o);
     }
+    if (p.direct) {
+      // The ring is idle once every consumer warp is past its last stage (this
+      // CTA's only item).  Each warp leaves (m, l, O) per query head there;
+      // then the 128 consumer threads merge the four in FP32 and write out.
+      // An abandoned call (timeout) writes nothing: bulk copies may still land.
+      constexpr int WS = 16 + 8 * D;  // floats per warp: m[8], l[8], O[8][D]
+      float* xw = reinterpret_cast<float*>(stages);
+      named_bar_sync(1, NW * 32);
+      if (!*abort_flag) {
+        float* mine = xw + warp * WS;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int h = 2 * c + hh;
+          if (r == 0) {
+            mine[h] = m[hh];
+            mine[8 + h] = l[hh];
+          }
+#pragma unroll
+          for (int mt = 0; mt < G::MT; ++mt) {
+            mine[16 + h * D + mt * 16 + r] = O[mt][hh];
+            mine[16 + h * D + mt * 16 + r + 8] = O[mt][hh + 2];
+          }
+        }
+      }
+      named_bar_sync(1, NW * 32);
+      if (!*abort_flag) {
+        const float vs = (FP8 && !PT) ? p.v_scale[rg.kvh] : 1.f;  // PT: V scales are inside O
+        __nv_bfloat16* dst = p.out + (static_cast<size_t>(rg.b) * p.Hq + rg.kvh * p.g) * D;
+        for (int idx = threadIdx.x; idx < p.g * D; idx += NW * 32) {
+          const int h = idx / D, d = idx - h * D;
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < NW; ++w) M = fmaxf(M, xw[w * WS + h]);
+          float num = 0.f, den = 0.f;
+          if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+              const float f = ex2(xw[w * WS + h] - M);  // 0 for a warp that saw no token
+              den = fmaf(f, xw[w * WS + 8 + h], den);
+              num = fmaf(f, xw[w * WS + 16 + h * D + d], num);
+            }
+          }
+          dst[idx] = __float2bfloat16_rn(den > 0.f ? num / den * vs : 0.f);
+        }
+      }
+      continue;  // one item per CTA in this mode
+    }
     {
       const float vs = (FP8 && !PT) ? p.v_scale[rg.kvh] : 1.f;  // PT: V scales are inside O
       const size_t row0 = static_cast<size_t>(rg.b) * p.Hq + rg.kvh * p.g;
@@ -855,9 +922,11 @@ void split_plan(int B, int Hkv, int P, int max_blocks, int window, int num_split
   if (num_splits > 0) {
     S = num_splits;
   } else {
-    const long target = static_cast<long>(kCtasPerSm) * sm_count();  // about one item per CTA
+    // at most one item per resident CTA: a second, partial wave of items would
+    // take as long as the first
+    const long target = static_cast<long>(kCtasPerSm) * sm_count();
     const long pairs = static_cast<long>(B) * Hkv;
-    S = static_cast<int>((target + pairs - 1) / pairs);
+    S = static_cast<int>(target / pairs);
     const int max_s = (pages + 15) / 16;  // at least 16 pages per split
     if (S > max_s) S = max_s;
   }
@@ -883,10 +952,16 @@ kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream
     configured_mask |= 1 << (dev & 31);
   }
   int grid = kCtasPerSm * sm_count();
+  DecodeParams q = p;
+  q.out = out;
+  // one page range per (sequence, KV head) and every item in its own CTA: the
+  // CTAs write the output themselves
+  q.direct = (p.num_splits == 1 && p.num_items <= grid) ? 1 : 0;
   if (grid > p.num_items) grid = p.num_items;
-  kern<<<grid, (kNW + 1) * 32, smem, s>>>(p);
+  kern<<<grid, (kNW + 1) * 32, smem, s>>>(q);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_status(e, "decode partial launch");
+  if (q.direct) return KVQ_OK;
   // combine: programmatic dependent launch (its launch overlaps the partial's tail)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.B * p.Hq, D / 32);
