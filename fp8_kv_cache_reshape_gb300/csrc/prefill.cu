@@ -71,7 +71,7 @@ constexpr int NTHREADS = (NSOFT + NCORR + 4) * 32;
 // control and correction warpgroups then give some back and the softmax
 // warpgroups take them (the sum must stay within the launch's allocation).
 constexpr int REG_LAUNCH = (65536 / NTHREADS) / 8 * 8;
-constexpr int REG_SOFT = 184, REG_CORR = 80, REG_CTRL = 56;  // 64,512 of the launch's 65,536
+constexpr int REG_SOFT = 184, REG_CORR = 88, REG_CTRL = 56;  // all 65,536 of the launch
 static_assert(NSOFT * 32 * REG_SOFT + NCORR * 32 * REG_CORR + 128 * REG_CTRL <= NTHREADS * REG_LAUNCH,
               "register split");
 // TMEM: S0 | S1 | O_tile | O_run at head_dim 128 (128 columns each); at 256,
@@ -551,24 +551,33 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         l = fmaf(l, alpha, row_sum(j));
         tmem_wait_st();  // this thread's previous O_run update
         const float2 a2 = make_float2(alpha, alpha);
+        // 32 columns of O_tile and of O_run per tensor-memory round trip (its
+        // latency, not the arithmetic, sets the pace of this fold, and P.V of
+        // the next tile waits for the last O_tile load)
 #pragma unroll
-        for (int c = 0; c < HD / 16; ++c) {
-          uint32_t t[16], o[16];
-          tmem_ld16_async(o_tile + 16 * c, t);
-          tmem_ld16_async(o_run + 16 * c, o);
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t t[2][16], o[2][16];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            tmem_ld16_async(o_tile + 32 * c + 16 * u, t[u]);
+            tmem_ld16_async(o_run + 32 * c + 16 * u, o[u]);
+          }
           tmem_wait_ld();
-          if (c == HD / 16 - 1) {  // all of O_tile has been read: P.V of the next tile may overwrite it
+          if (c == HD / 32 - 1) {  // all of O_tile has been read: P.V of the next tile may overwrite it
             tc_fence_before();
             mbar_arrive(&bars->o_free);
           }
 #pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            const float2 r = ffma2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2,
-                                   make_float2(__uint_as_float(t[i]), __uint_as_float(t[i + 1])));
-            o[i] = __float_as_uint(r.x);
-            o[i + 1] = __float_as_uint(r.y);
+          for (int u = 0; u < 2; ++u) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+              const float2 r = ffma2(make_float2(__uint_as_float(o[u][i]), __uint_as_float(o[u][i + 1])), a2,
+                                     make_float2(__uint_as_float(t[u][i]), __uint_as_float(t[u][i + 1])));
+              o[u][i] = __float_as_uint(r.x);
+              o[u][i + 1] = __float_as_uint(r.y);
+            }
+            tmem_st16(o_run + 32 * c + 16 * u, o[u]);
           }
-          tmem_st16(o_run + 16 * c, o);
         }
       }
     } else {
