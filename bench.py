@@ -446,10 +446,10 @@ def prefill_flops(new=PF_NEW, cached=PF_CACHED, hq=HQ, d=D):
     return pairs * hq * 4 * d
 
 
-def prefill_leg(device, reps=10, accumulation=None, head_dim=D):
+def prefill_leg(device, reps=10, accumulation=None, head_dim=D, cache_dtype="fp8_e4m3"):
     """Chunked causal prefill of 4,096 new tokens on 28,672 cached FP8
-    tokens (32/8 heads, head_dim 128, or 256): TFLOP/s of
-    kvq_prefill_attention."""
+    tokens (32/8 heads, head_dim 128, or 256; E4M3 or E5M2 cache): TFLOP/s
+    of kvq_prefill_attention."""
     import torch
     import fp8_kv_cache_reshape_gb300 as kvq
     import workloads as W
@@ -461,10 +461,11 @@ def prefill_leg(device, reps=10, accumulation=None, head_dim=D):
     k = W.randn_bf16((L, HKV, head_dim), gd, device=device)
     v = W.randn_bf16((L, HKV, head_dim), gd, device=device)
     q = W.randn_bf16((PF_NEW, HQ, head_dim), gd, device=device)
-    ks, vs = W.calibrate_amax(k), W.calibrate_amax(v)
+    fmt_max = W.E5M2_MAX if cache_dtype == "fp8_e5m2" else W.E4M3_MAX
+    ks, vs = W.calibrate_amax(k, fmt_max), W.calibrate_amax(v, fmt_max)
     qs = (q.float().abs().amax() / 448.0).reshape(1).to(torch.float32)
-    kd, vd = kvq.alloc_kv_cache(nb, HKV, head_dim, device=device, fill=0)
-    kvq.kvq_reshape_and_cache(k, v, slots, kd, vd, ks, vs)
+    kd, vd = kvq.alloc_kv_cache(nb, HKV, head_dim, cache_dtype=cache_dtype, device=device, fill=0)
+    kvq.kvq_reshape_and_cache(k, v, slots, kd, vd, ks, vs, cache_dtype=cache_dtype)
     q8 = torch.empty(q.shape, dtype=torch.uint8, device=device)
     kvq.kvq_quantize_query(q, q8, qs)
     out = torch.empty(q.shape, dtype=torch.bfloat16, device=device)
@@ -475,7 +476,8 @@ def prefill_leg(device, reps=10, accumulation=None, head_dim=D):
 
     def call():
         kvq.kvq_prefill_attention(q8, qs, kd, vd, ks, vs, btd, cu, sl, out, max_q_tokens=PF_NEW,
-                                  sm_scale=1.0 / math.sqrt(head_dim), dev_status=st, accumulation=accumulation)
+                                  sm_scale=1.0 / math.sqrt(head_dim), dev_status=st, accumulation=accumulation,
+                                  cache_dtype=cache_dtype)
 
     for _ in range(3):
         call()
@@ -486,8 +488,9 @@ def prefill_leg(device, reps=10, accumulation=None, head_dim=D):
     fp8_peak = 2.0 * bf16  # nominal FP8:BF16 dense ratio 4.5 : 2.25
     flops = prefill_flops(d=head_dim)
     tf = flops / (ms * 1e-3) / 1e12
-    name = "llama31_8b_chunked_prefill_4k_on_28k" + ("" if head_dim == 128 else f"_head_dim_{head_dim}")
-    return {"workload": name, "ms": round(ms, 4), "flops": flops, "head_dim": head_dim,
+    name = ("llama31_8b_chunked_prefill_4k_on_28k" + ("" if head_dim == 128 else f"_head_dim_{head_dim}") +
+            ("" if cache_dtype == "fp8_e4m3" else "_" + cache_dtype))
+    return {"workload": name, "ms": round(ms, 4), "flops": flops, "head_dim": head_dim, "cache_dtype": cache_dtype,
             "accumulation": accumulation or ("two_level" if head_dim == 128 else "single_level"),
             "bound": "tensor", "achieved": round(tf, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
             "frac": round(tf / fp8_peak, 4),
@@ -1000,6 +1003,8 @@ def ours_arm(args, rank, world, local_rank):
                    "llama31_8b_decode_conc8_20k": clocked(local_rank, conc8_leg, device),
                    "gpt_oss_20b_hybrid_decode_32k": clocked(local_rank, hybrid_leg, device)}
     pf = clocked(local_rank, prefill_leg, device) if legs and not args.no_prefill else None
+    if pf is not None and not args.no_e5m2:
+        pf["e5m2_cache"] = clocked(local_rank, prefill_leg, device, cache_dtype="fp8_e5m2")
     no_cmp = not legs or args.no_sweep
     bf = None if (no_cmp or args.no_bf16) else clocked(local_rank, format_compare, sweep, device, "bf16")
     e5 = None if (no_cmp or args.no_e5m2) else clocked(local_rank, format_compare, sweep, device, "fp8_e5m2")

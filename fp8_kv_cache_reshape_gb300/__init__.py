@@ -89,6 +89,9 @@ lib.kvq_paged_decode_attention_acc.argtypes = lib.kvq_paged_decode_attention.arg
 lib.kvq_prefill_attention_acc.restype = _i
 lib.kvq_prefill_attention_acc.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
                                           _f, _i, _p, _p, _i]
+lib.kvq_prefill_attention_dtype.restype = _i
+lib.kvq_prefill_attention_dtype.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
+                                            _f, _i, _p, _p, _i]
 lib.kvq_prefill_attention.restype = _i
 lib.kvq_prefill_attention.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
                                       _f, _i, _p, _p]
@@ -297,10 +300,11 @@ def kvq_paged_decode_attention_per_token(q, k_cache, v_cache, kv_scale_cache, bl
 
 def kvq_prefill_attention(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q,
                           seq_lens, out, max_q_tokens, num_blocks=None, sm_scale=None, causal=True,
-                          dev_status=None, stream=None, accumulation=None):
+                          dev_status=None, stream=None, accumulation=None, cache_dtype="fp8_e4m3"):
     """Chunked causal prefill over the FP8 cache; writes out (bf16 [Tq][Hq][D]).
     accumulation: None (two-level) or "two_level" / "single_level" through
-    kvq_prefill_attention_acc."""
+    kvq_prefill_attention_acc.  cache_dtype "fp8_e5m2" goes through
+    kvq_prefill_attention_dtype (with the default accumulation)."""
     Tq, Hq, D = q8.shape
     B = cu_seqlens_q.numel() - 1
     Hkv = k_cache.shape[1]
@@ -312,7 +316,12 @@ def kvq_prefill_attention(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block
             _ptr(block_table), _ptr(cu_seqlens_q), _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, PAGE,
             block_table.shape[1], num_blocks, int(max_q_tokens), float(sm_scale), 1 if causal else 0,
             _ptr(dev_status), _stream(stream))
-    if accumulation is None:
+    dt = _dtype_code(cache_dtype)
+    if dt != KVQ_DTYPE_FP8_E4M3:
+        if accumulation is not None:
+            raise ValueError("an explicit accumulation mode takes an E4M3 cache")
+        _check(lib.kvq_prefill_attention_dtype(*args, dt), "kvq_prefill_attention_dtype")
+    elif accumulation is None:
         _check(lib.kvq_prefill_attention(*args), "kvq_prefill_attention")
     else:
         _check(lib.kvq_prefill_attention_acc(*args, _acc_code(accumulation)), "kvq_prefill_attention_acc")

@@ -157,9 +157,10 @@ KVQ_DEVINL uint64_t desc_interleave(uint32_t saddr, uint32_t lbo, uint32_t sbo) 
   d |= static_cast<uint64_t>(1) << 46;
   return d;
 }
-// kind::f8f6f4 instruction descriptor: D f32, A/B e4m3, both K-major, M x N.
-constexpr uint32_t idesc_e4m3(int M, int N) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+// kind::f8f6f4 instruction descriptor: D f32, A e4m3, B e4m3 (b_e5m2: e5m2),
+// both K-major, M x N.  The element types of A and B are separate fields.
+constexpr uint32_t idesc_e4m3(int M, int N, bool b_e5m2 = false) {
+  return (1u << 4) | (0u << 7) | ((b_e5m2 ? 1u : 0u) << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 KVQ_DEVINL void umma_f8(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
@@ -279,7 +280,9 @@ KVQ_DEVINL Job make_job(const PrefillParams& p) {
 // of every tile accumulates into one TMEM sum O, which the softmax warps
 // rescale by alpha in place (skipped when alpha is 1 for the whole warp).
 // Head dim 256 needs it: two-level would need 2 x 256 TMEM columns for O.
-template <int HD, bool SL>
+// E5: the caches hold E5M2 codes: K (the B operand of Q K^T) and V (the B
+// operand of P.V) are E5M2, Q and P stay E4M3.
+template <int HD, bool SL, bool E5 = false>
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using G = Geo<HD>;
   static_assert(HD == 128 || (HD == 256 && SL), "head_dim 256 runs with single-level accumulation");
@@ -417,8 +420,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       }
     } else if (warp == W_MMA) {
       // ------------------------------------------------------------ MMA issuer --
-      constexpr uint32_t IDESC_S = idesc_e4m3(TQ, TK);  // S = Q K^T: N = keys
-      constexpr uint32_t IDESC_O = idesc_e4m3(TQ, HD);  // O += P V: N = head dim
+      constexpr uint32_t IDESC_S = idesc_e4m3(TQ, TK, E5);  // S = Q K^T: N = keys
+      constexpr uint32_t IDESC_O = idesc_e4m3(TQ, HD, E5);  // O += P V: N = head dim
       const uint32_t q_s = sbase + OFF_Q;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -813,18 +816,18 @@ using namespace kvq;
 
 namespace {
 
-template <int HD, bool SL>
+template <int HD, bool SL, bool E5 = false>
 kvq_status_t launch_prefill(const PrefillParams& prm, dim3 grid, cudaStream_t stream) {
   constexpr int smem = Geo<HD>::SMEM_BYTES;
   static int configured_mask = 0;  // devices whose shared-memory attribute is set
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(configured_mask & (1 << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<HD, SL>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<HD, SL, E5>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_status(e, "prefill: set shared memory size");
     configured_mask |= 1 << (dev & 31);
   }
-  prefill_kernel<HD, SL><<<grid, NTHREADS, smem, stream>>>(prm);
+  prefill_kernel<HD, SL, E5><<<grid, NTHREADS, smem, stream>>>(prm);
   return cuda_status(cudaGetLastError(), "prefill launch");
 }
 
@@ -832,7 +835,8 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
                      const float* k_scale, const float* v_scale, const int32_t* block_table,
                      const int32_t* cu_seqlens_q, const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int D,
                      int P, int max_blocks, int64_t num_blocks, int max_q_tokens, float sm_scale, int causal,
-                     int* dev_status, kvq_stream_t stream, int accumulation) {
+                     int* dev_status, kvq_stream_t stream, int accumulation,
+                     kvq_dtype_t cache_dtype = KVQ_DTYPE_FP8_E4M3) {
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || max_q_tokens < 0)
     return fail(KVQ_ERR_INVALID_ARG, "prefill: bad sizes");
   if (Hq % Hkv != 0) return fail(KVQ_ERR_INVALID_ARG, "prefill: Hq %% Hkv != 0");
@@ -844,6 +848,8 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
   if (D == 256 && accumulation == KVQ_ACC_TWO_LEVEL)
     return fail(KVQ_ERR_UNSUPPORTED, "prefill: head_dim 256 runs with single-level accumulation only");
   const bool single_level = D == 256 || accumulation == KVQ_ACC_SINGLE_LEVEL;
+  if (cache_dtype != KVQ_DTYPE_FP8_E4M3 && cache_dtype != KVQ_DTYPE_FP8_E5M2)
+    return fail(KVQ_ERR_UNSUPPORTED, "prefill: FP8 (E4M3 or E5M2) caches only");
   if (max_q_tokens == 0) return KVQ_OK;
   if (!q8 || !q_scale || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !cu_seqlens_q ||
       !seq_lens || !out)
@@ -874,6 +880,11 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
   prm.stall_ns = stall_ns();
   dim3 grid(Hq, (max_q_tokens + TQ - 1) / TQ, B);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cache_dtype == KVQ_DTYPE_FP8_E5M2) {
+    if (D == 256) return launch_prefill<256, true, true>(prm, grid, st);
+    return single_level ? launch_prefill<128, true, true>(prm, grid, st)
+                        : launch_prefill<128, false, true>(prm, grid, st);
+  }
   if (D == 256) return launch_prefill<256, true>(prm, grid, st);
   return single_level ? launch_prefill<128, true>(prm, grid, st) : launch_prefill<128, false>(prm, grid, st);
 }
@@ -889,6 +900,19 @@ extern "C" kvq_status_t kvq_prefill_attention(const uint8_t* q8, const float* q_
   clear_error();
   return prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q, seq_lens, out, B, Hq,
                  Hkv, D, P, max_blocks, num_blocks, max_q_tokens, sm_scale, causal, dev_status, stream, -1);
+}
+
+extern "C" kvq_status_t kvq_prefill_attention_dtype(const uint8_t* q8, const float* q_scale, const void* k_cache,
+                                                    const void* v_cache, const float* k_scale, const float* v_scale,
+                                                    const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                                    const int32_t* seq_lens, void* out, int B, int Hq, int Hkv,
+                                                    int D, int P, int max_blocks, int64_t num_blocks,
+                                                    int max_q_tokens, float sm_scale, int causal, int* dev_status,
+                                                    kvq_stream_t stream, kvq_dtype_t cache_dtype) {
+  clear_error();
+  return prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q, seq_lens, out, B, Hq,
+                 Hkv, D, P, max_blocks, num_blocks, max_q_tokens, sm_scale, causal, dev_status, stream, -1,
+                 cache_dtype);
 }
 
 extern "C" kvq_status_t kvq_prefill_attention_acc(const uint8_t* q8, const float* q_scale, const void* k_cache,

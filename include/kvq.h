@@ -85,7 +85,8 @@ typedef enum kvq_dtype {
                                 fp8_e5m2 among the cache dtypes; [GTNT] section
                                 1: 5 exponent bits, 2 mantissa bits, about
                                 +-57344.  Bias 15, RNE, saturating to +-57344.
-                                Decode only (kvq_prefill_attention reads E4M3). */
+                                Prefill reads it through
+                                kvq_prefill_attention_dtype. */
 } kvq_dtype_t;
 
 /*
@@ -407,8 +408,8 @@ kvq_status_t kvq_paged_decode_attention_static_scratch(const void* q, const void
  *  q8            uint8 [Tq][Hq][D] E4M3 codes (kvq_quantize_query), Tq =
  *                cu_seqlens_q[B].
  *  q_scale       float32 [1].
- *  k_cache, v_cache, k_scale, v_scale, block_table  as for decode (E4M3 caches
- *                only; the call cannot tell an E5M2 cache apart).
+ *  k_cache, v_cache, k_scale, v_scale, block_table  as for decode (E4M3 caches;
+ *                kvq_prefill_attention_dtype below reads E5M2 caches).
  *  cu_seqlens_q  int32 [B+1], non-decreasing, cu_seqlens_q[0] = 0.
  *  seq_lens      int32 [B].
  *  out           bf16 [Tq][Hq][D] (written).
@@ -439,6 +440,25 @@ kvq_status_t kvq_prefill_attention(const uint8_t* q8, const float* q_scale,
                                    int B, int Hq, int Hkv, int D, int P, int max_blocks,
                                    int64_t num_blocks, int max_q_tokens, float sm_scale,
                                    int causal, int* dev_status, kvq_stream_t stream);
+
+/*
+ * kvq_prefill_attention_dtype -- kvq_prefill_attention over a cache of the
+ * given FP8 format: KVQ_DTYPE_FP8_E4M3 (the same as kvq_prefill_attention) or
+ * KVQ_DTYPE_FP8_E5M2 ([FP8KV] "How to enable it in the engine": fp8_e5m2 is
+ * one of the cache dtypes).  With E5M2 the K and V codes enter the tensor-core
+ * products as E5M2 (the B operands of Q K^T and P.V); the query and P codes
+ * stay E4M3; every other step and the declared rounding are those of
+ * kvq_prefill_attention.  Any other dtype: KVQ_ERR_UNSUPPORTED.
+ */
+kvq_status_t kvq_prefill_attention_dtype(const uint8_t* q8, const float* q_scale,
+                                         const void* k_cache, const void* v_cache,
+                                         const float* k_scale, const float* v_scale,
+                                         const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                         const int32_t* seq_lens, void* out,
+                                         int B, int Hq, int Hkv, int D, int P, int max_blocks,
+                                         int64_t num_blocks, int max_q_tokens, float sm_scale,
+                                         int causal, int* dev_status, kvq_stream_t stream,
+                                         kvq_dtype_t cache_dtype);
 
 /*
  * kvq_prefill_attention_acc -- kvq_prefill_attention with an explicit

@@ -254,13 +254,15 @@ def _p8(p):
 
 def prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
             cu_seqlens_q, seq_lens, sm_scale, causal=True, mode="mirror",
-            rows=None, tile=128, quantize_p=True, chunk=64):
+            rows=None, tile=128, quantize_p=True, chunk=64, cache_dtype=FP8):
     """Chunked prefill over the FP8 cache (the new tokens are already cached).
 
     q8: uint8 [Tq][Hq][D] E4M3 codes.  cu_seqlens_q: int [B+1].  seq_lens:
     int [B], each counting the cached tokens including the new ones.
     rows: optional iterable of (token_index, head) pairs to evaluate; other
     rows of the result stay NaN (sampled checks at large sizes).
+    cache_dtype: the cache's FP8 format (E4M3 or E5M2 codes; the query codes
+    and the probabilities P8 are E4M3 either way).
 
     Modes (the scores of the mirrored modes are s2 = (sum_d q8_d k8_d) * c in
     base-2 units, c the float32 coefficient of prefill_score_coef):
@@ -306,8 +308,8 @@ def prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
         L = int(seq_lens[b])
         nq = int(cu[b + 1] - cu[b])
         kk, vv = gather_tokens(k_cache, v_cache, block_table[b], np.arange(L), kv)
-        k_codes = e4m3.decode(kk)   # [L][D]
-        v_codes = e4m3.decode(vv)
+        k_codes = codec(cache_dtype).decode(kk)   # [L][D]; the query and P codes are E4M3
+        v_codes = codec(cache_dtype).decode(vv)
         sk = float(np.float32(k_scale[kv]))
         sv = float(np.float32(v_scale[kv]))
         c = float(prefill_score_coef(np.float32(q_scale), k_scale[kv], sm_scale))

@@ -27,7 +27,7 @@ def _k():
     return k
 
 
-def build(nq_list, cached_list, Hq=32, Hkv=8, seed=0, sentinel=0xA5, D=128):
+def build(nq_list, cached_list, Hq=32, Hkv=8, seed=0, sentinel=0xA5, D=128, cache_dtype=kv_cache.FP8):
     """Oracle caches for sequences of nq new + cached old tokens; q8 codes."""
     gen = W.generator(9000 + seed)
     lens = [a + b for a, b in zip(nq_list, cached_list)]
@@ -37,15 +37,16 @@ def build(nq_list, cached_list, Hq=32, Hkv=8, seed=0, sentinel=0xA5, D=128):
     k = W.randn_bf16((T, Hkv, D), gen)
     v = W.randn_bf16((T, Hkv, D), gen)
     q = W.randn_bf16((sum(nq_list), Hq, D), gen)
-    ks, vs = W.calibrate_amax(k), W.calibrate_amax(v)
+    fmt_max = W.E5M2_MAX if cache_dtype == kv_cache.FP8_E5M2 else W.E4M3_MAX
+    ks, vs = W.calibrate_amax(k, fmt_max), W.calibrate_amax(v, fmt_max)
     qs = np.float32(q.float().abs().max().item() / 448)
     kc = np.full((nb, Hkv, 16, D), sentinel, np.uint8)
     vc = np.full((nb, Hkv, D, 16), sentinel, np.uint8)
-    kv_cache.reshape_and_cache(f32(k), f32(v), slots.numpy(), kc, vc, ks.numpy(), vs.numpy())
+    kv_cache.reshape_and_cache(f32(k), f32(v), slots.numpy(), kc, vc, ks.numpy(), vs.numpy(), cache_dtype)
     q8 = kv_cache.quantize_query(f32(q), qs)
     cu = np.concatenate([[0], np.cumsum(nq_list)]).astype(np.int32)
     return dict(kc=kc, vc=vc, q8=q8, qs=qs, ks=ks.numpy(), vs=vs.numpy(), bt=bt.numpy(), nb=nb,
-                cu=cu, lens=np.array(lens, np.int32), Hq=Hq, Hkv=Hkv, sm=1 / np.sqrt(float(D)))
+                cu=cu, lens=np.array(lens, np.int32), Hq=Hq, Hkv=Hkv, sm=1 / np.sqrt(float(D)), dtype=cache_dtype)
 
 
 def gpu_prefill(c, causal=True, block_table=None, status=False):
@@ -59,7 +60,7 @@ def gpu_prefill(c, causal=True, block_table=None, status=False):
     k.kvq_prefill_attention(q8, torch.tensor([c["qs"]], device="cuda"), kd, vd, torch.from_numpy(c["ks"]).cuda(),
                             torch.from_numpy(c["vs"]).cuda(), bt, torch.from_numpy(c["cu"]).cuda(),
                             torch.from_numpy(c["lens"]).cuda(), out, max_q_tokens=nq_max, num_blocks=c["nb"],
-                            sm_scale=float(c["sm"]), causal=causal, dev_status=st)
+                            sm_scale=float(c["sm"]), causal=causal, dev_status=st, cache_dtype=c["dtype"])
     torch.cuda.synchronize()
     if status:
         return f32(out), int(st.item())
@@ -69,7 +70,8 @@ def gpu_prefill(c, causal=True, block_table=None, status=False):
 
 def oracle(c, rows=None, causal=True, mode="mirror"):
     return attention.prefill(c["q8"], c["qs"], c["kc"], c["vc"], c["ks"], c["vs"], c["bt"], c["cu"], c["lens"],
-                             float(np.float32(c["sm"])), causal=causal, mode=mode, rows=rows)
+                             float(np.float32(c["sm"])), causal=causal, mode=mode, rows=rows,
+                             cache_dtype=c.get("dtype", kv_cache.FP8))
 
 
 def check_rows(got, ref, rows, what=""):
@@ -224,3 +226,19 @@ def test_prefill_bad_lengths_reported():
     got = gpu_prefill(good)  # the context stays usable
     rows = [(t, h) for t in range(0, 104, 5) for h in range(8)]
     check_all(got, good, rows, what="after bad lengths")
+
+
+@pytest.mark.parametrize("D,nq,cached", [(128, [256], [384]), (128, [1, 130, 300], [0, 17, 1000]),
+                                         (256, [77], [2000])])
+def test_prefill_over_an_e5m2_cache(D, nq, cached):
+    """E5M2 K and V codes as the B operands of both products (query and P
+    codes E4M3); NaN-poisoned bytes outside the tokens (0x7F is an E5M2 NaN
+    too)."""
+    c = build(nq, cached, Hq=8, Hkv=2, seed=40 + D + len(nq), sentinel=0x7F, D=D, cache_dtype=kv_cache.FP8_E5M2)
+    got = gpu_prefill(c)
+    Tq = c["q8"].shape[0]
+    rng = np.random.default_rng(6)
+    rows = [(t, h) for t in range(Tq) for h in range(c["Hq"])]
+    if len(rows) > 2000:
+        rows = [rows[i] for i in rng.choice(len(rows), 2000, replace=False)]
+    check_all(got, c, rows, what=f"E5M2 cache head_dim {D} nq={nq}")

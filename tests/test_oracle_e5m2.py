@@ -144,3 +144,34 @@ def test_decode_e5m2_against_definition():
         assert abs(lse[0, h] - (m + math.log(sum(p)))) < 1e-12
     # the mirrored query rounding moves the result by far less than the test tolerance
     assert np.max(np.abs(mir - out)) < 2e-3
+
+
+def test_prefill_over_an_e5m2_cache_non_causal_rows_equal_decode():
+    """Prefill over an E5M2 cache: a non-causal row is decode attention of
+    the dequantized E4M3 query over the same E5M2 codes (pure mode)."""
+    from oracle import attention
+    rng = np.random.default_rng(31)
+    L, Hkv, Hq, D, nq = 90, 2, 4, 16, 6
+    k = torch.from_numpy(rng.standard_normal((L, Hkv, D)).astype(np.float32)).bfloat16().float().numpy()
+    v = torch.from_numpy(rng.standard_normal((L, Hkv, D)).astype(np.float32)).bfloat16().float().numpy()
+    nb = -(-L // 16) + 2
+    bt = rng.permutation(nb)[: -(-L // 16)].astype(np.int32)[None, :]
+    slots = bt[0][np.arange(L) // 16].astype(np.int64) * 16 + np.arange(L) % 16
+    ks = np.full(Hkv, np.abs(k).max() / 57344, np.float32)
+    vs = np.full(Hkv, np.abs(v).max() / 57344, np.float32)
+    kc = np.zeros((nb, Hkv, 16, D), np.uint8)
+    vc = np.zeros((nb, Hkv, D, 16), np.uint8)
+    kv_cache.reshape_and_cache(k, v, slots, kc, vc, ks, vs, kv_cache.FP8_E5M2)
+    qs = np.float32(0.01)
+    q8 = kv_cache.quantize_query(rng.standard_normal((nq, Hq, D)).astype(np.float32), qs)
+    out = attention.prefill(q8, qs, kc, vc, ks, vs, bt, np.array([0, nq]), np.array([L]), 0.3, causal=False,
+                            mode="pure", cache_dtype=kv_cache.FP8_E5M2)
+    qdq = (e4m3.decode(q8) * float(qs)).astype(np.float32)
+    for i in range(nq):
+        dec, _ = attention.paged_decode(qdq[i:i + 1], kc, vc, ks, vs, bt, np.array([L]), 0.3, mode="pure",
+                                        cache_dtype=kv_cache.FP8_E5M2)
+        assert np.allclose(out[i], dec[0], rtol=1e-6, atol=1e-7)
+    # and it is not the E4M3 reading of the same bytes
+    wrong = attention.prefill(q8, qs, kc, vc, ks, vs, bt, np.array([0, nq]), np.array([L]), 0.3, causal=False,
+                              mode="pure")
+    assert not np.allclose(out, wrong, rtol=1e-2)
