@@ -364,7 +364,8 @@ def format_compare(fp8_sweep, device, cache_dtype, reps=20, per_token=False, acc
     "skip layers" format) this is the vLLM blog's ITL-slope comparison at
     kernel level; the E5M2 cache reads the same bytes as E4M3.  per_token:
     dynamic per-token scales (kvq_reshape_and_cache_per_token and the
-    matching decode); the scale bytes count toward GB/s.  accumulation:
+    matching decode; the scales ride in the V pages' tails); the scale
+    bytes count toward GB/s.  accumulation:
     "single_level" for the accumulation ablation."""
     import torch
     import fp8_kv_cache_reshape_gb300 as kvq
@@ -376,11 +377,10 @@ def format_compare(fp8_sweep, device, cache_dtype, reps=20, per_token=False, acc
     layers = []
     for l in range(BF16_LAYERS):
         gl = W.generator(502 * 1000 + l, device=device)
-        kd, vd = kvq.alloc_kv_cache(nb, HKV, D, cache_dtype=cache_dtype, device=device, fill=0)
+        kd, vd = kvq.alloc_kv_cache(nb, HKV, D, cache_dtype=cache_dtype, device=device, fill=0,
+                                    per_token=per_token)
         ks = vs = None
-        if per_token:
-            ks = kvq.alloc_scale_cache(nb, HKV, device=device, fill=0.0)
-        elif esz == 1:  # unit-variance data: per-head scale amax / M taken from one chunk
+        if esz == 1 and not per_token:  # unit-variance data: per-head scale amax / M taken from one chunk
             probe = W.randn_bf16((16384, HKV, D), gl, device=device)
             ks = W.calibrate_amax(probe, W.E5M2_MAX if cache_dtype == "fp8_e5m2" else W.E4M3_MAX).to(device)
             vs = ks.clone()
@@ -388,7 +388,7 @@ def format_compare(fp8_sweep, device, cache_dtype, reps=20, per_token=False, acc
             k = W.randn_bf16((16384, HKV, D), gl, device=device)
             v = W.randn_bf16((16384, HKV, D), gl, device=device)
             if per_token:
-                kvq.kvq_reshape_and_cache_per_token(k, v, slots[t0:t0 + 16384].contiguous(), kd, vd, ks,
+                kvq.kvq_reshape_and_cache_per_token(k, v, slots[t0:t0 + 16384].contiguous(), kd, vd,
                                                     cache_dtype=cache_dtype)
             else:
                 kvq.kvq_reshape_and_cache(k, v, slots[t0:t0 + 16384].contiguous(), kd, vd, ks, vs,
@@ -402,7 +402,7 @@ def format_compare(fp8_sweep, device, cache_dtype, reps=20, per_token=False, acc
     def run():
         for ly in layers:
             if per_token:
-                kvq.kvq_paged_decode_attention_per_token(ly["q"], ly["kd"], ly["vd"], ly["ks"], btd, seq, ly["out"],
+                kvq.kvq_paged_decode_attention_per_token(ly["q"], ly["kd"], ly["vd"], btd, seq, ly["out"],
                                                          num_blocks=nb, sm_scale=1.0 / math.sqrt(D),
                                                          cache_dtype=cache_dtype, workspace=ws)
             else:

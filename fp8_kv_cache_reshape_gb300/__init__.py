@@ -77,9 +77,9 @@ lib.kvq_paged_decode_attention_static_scratch.restype = _i
 lib.kvq_paged_decode_attention_static_scratch.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
                                                           _i64, _f, _i, _i, _i, _p, _p]
 lib.kvq_reshape_and_cache_per_token.restype = _i
-lib.kvq_reshape_and_cache_per_token.argtypes = [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i64, _i, _p, _p]
+lib.kvq_reshape_and_cache_per_token.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i64, _i, _p, _p]
 lib.kvq_paged_decode_attention_per_token.restype = _i
-lib.kvq_paged_decode_attention_per_token.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64,
+lib.kvq_paged_decode_attention_per_token.argtypes = [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64,
                                                      _f, _i, _i, _i, _p, _sz, _p, _p]
 lib.kvq_paged_decode_attention_append.restype = _i
 lib.kvq_paged_decode_attention_append.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i,
@@ -155,17 +155,25 @@ def kvq_debug_set_stall_ns(ns: int):
     lib.kvq_debug_set_stall_ns(int(ns))
 
 
+# per-token scale tail of a V page: 16 K scales and 16 V scales, float32
+SCALE_TAIL_BYTES = 2 * PAGE * 4
+
+
 def alloc_kv_cache(num_blocks: int, kv_heads: int, head_dim: int, cache_dtype="fp8_e4m3",
-                   device="cuda", fill=None):
+                   device="cuda", fill=None, per_token=False):
     """Allocate (k_cache, v_cache) as uint8 tensors in the library's paged
-    format ([num_blocks][Hkv][P][D] and [num_blocks][Hkv][D][P] elements)."""
+    format ([num_blocks][Hkv][P][D] and [num_blocks][Hkv][D][P] elements).
+    per_token: each V page also carries its scale tail (FP8 only)."""
     esz = 2 if _dtype_code(cache_dtype) == KVQ_DTYPE_BF16 else 1
-    shape = (num_blocks, kv_heads, PAGE * head_dim * esz)
+    if per_token and esz != 1:
+        raise ValueError("per-token scales need an FP8 cache")
+    kshape = (num_blocks, kv_heads, PAGE * head_dim * esz)
+    vshape = (num_blocks, kv_heads, PAGE * head_dim * esz + (SCALE_TAIL_BYTES if per_token else 0))
     if fill is None:
-        return (torch.empty(shape, dtype=torch.uint8, device=device),
-                torch.empty(shape, dtype=torch.uint8, device=device))
-    return (torch.full(shape, fill, dtype=torch.uint8, device=device),
-            torch.full(shape, fill, dtype=torch.uint8, device=device))
+        return (torch.empty(kshape, dtype=torch.uint8, device=device),
+                torch.empty(vshape, dtype=torch.uint8, device=device))
+    return (torch.full(kshape, fill, dtype=torch.uint8, device=device),
+            torch.full(vshape, fill, dtype=torch.uint8, device=device))
 
 
 def kvq_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None,
@@ -180,24 +188,22 @@ def kvq_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_
                                      _ptr(dev_status), _stream(stream)), "kvq_reshape_and_cache")
 
 
-def alloc_scale_cache(num_blocks: int, kv_heads: int, device="cuda", fill=None):
-    """Allocate the interleaved per-token scale cache, float32
-    [num_blocks][Hkv][2][16] ([..][0][t]: K scale, [..][1][t]: V scale)."""
-    shape = (num_blocks, kv_heads, 2, PAGE)
-    if fill is None:
-        return torch.empty(shape, dtype=torch.float32, device=device)
-    return torch.full(shape, fill, dtype=torch.float32, device=device)
+def _check_per_token_cache(k_cache, v_cache, Hkv, D):
+    nb = k_cache.numel() // (Hkv * PAGE * D)
+    if k_cache.numel() != nb * Hkv * PAGE * D or v_cache.numel() != nb * Hkv * (PAGE * D + SCALE_TAIL_BYTES):
+        raise ValueError("per-token caches must be alloc_kv_cache(..., per_token=True) tensors")
+    return nb
 
 
-def kvq_reshape_and_cache_per_token(k, v, slot_mapping, k_cache, v_cache, kv_scale_cache,
-                                    cache_dtype="fp8_e4m3", dev_status=None, stream=None):
+def kvq_reshape_and_cache_per_token(k, v, slot_mapping, k_cache, v_cache, cache_dtype="fp8_e4m3",
+                                    dev_status=None, stream=None):
     """Quantize new tokens k, v (bf16 [T][Hkv][D]) with one dynamic scale per
-    token and head; the scales go to the interleaved scale cache."""
+    token and head; the scales go to the scale tails of the V pages."""
     T, Hkv, D = k.shape
-    num_blocks = k_cache.numel() // (Hkv * PAGE * D)
+    num_blocks = _check_per_token_cache(k_cache, v_cache, Hkv, D)
     _check(lib.kvq_reshape_and_cache_per_token(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
-                                               _ptr(kv_scale_cache), T, Hkv, D, PAGE, num_blocks,
-                                               _dtype_code(cache_dtype), _ptr(dev_status), _stream(stream)),
+                                               T, Hkv, D, PAGE, num_blocks, _dtype_code(cache_dtype),
+                                               _ptr(dev_status), _stream(stream)),
            "kvq_reshape_and_cache_per_token")
 
 
@@ -277,8 +283,9 @@ def kvq_paged_decode_attention_append(q, k_new, v_new, slot_new, k_cache, v_cach
     return out
 
 
-def kvq_paged_decode_attention_per_token(q, k_cache, v_cache, kv_scale_cache, block_table, seq_lens, out, num_blocks=None, sm_scale=None, window=-1, cache_dtype="fp8_e4m3",
-                                         num_splits=0, workspace=None, dev_status=None, stream=None):
+def kvq_paged_decode_attention_per_token(q, k_cache, v_cache, block_table, seq_lens, out, num_blocks=None,
+                                         sm_scale=None, window=-1, cache_dtype="fp8_e4m3", num_splits=0,
+                                         workspace=None, dev_status=None, stream=None):
     """Decode over a cache written by kvq_reshape_and_cache_per_token."""
     B, Hq, D = q.shape
     max_blocks = block_table.shape[1]
@@ -291,7 +298,7 @@ def kvq_paged_decode_attention_per_token(q, k_cache, v_cache, kv_scale_cache, bl
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     _check(lib.kvq_paged_decode_attention_per_token(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(kv_scale_cache), _ptr(block_table),
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
         _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, PAGE, max_blocks, num_blocks, float(sm_scale), window,
         _dtype_code(cache_dtype), num_splits, _ptr(workspace), workspace.numel(), _ptr(dev_status),
         _stream(stream)), "kvq_paged_decode_attention_per_token")

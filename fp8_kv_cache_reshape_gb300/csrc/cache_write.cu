@@ -48,16 +48,18 @@ KVQ_DEVINL uint4 quant16(const float (&x)[16], float s) {
 // FP8 cache write (E4M3, or E5M2 when E5 is set).  grid = (ceil(T / 16), Hkv), block = 128.
 // PT: per-token dynamic scales -- each (token, head) is quantized with
 // amax_d |x| / (format maximum) of its own values, and the K and V scales are
-// stored in the token's slot of the interleaved scale cache
-// [num_blocks][Hkv][2][P] (k_scale / v_scale are unused).
+// stored in the token's slot of the scale tail of its V page (a per-token V
+// page is the P x D codes followed by P K scales and P V scales, float32;
+// k_scale / v_scale are unused).
 template <int D, bool E5, bool PT>
 __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
     const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
-    const float* __restrict__ k_scale, const float* __restrict__ v_scale, float* __restrict__ kv_scale_cache,
-    int T, int Hkv, int64_t num_slots, int* dev_status) {
+    const float* __restrict__ k_scale, const float* __restrict__ v_scale, int T, int Hkv, int64_t num_slots,
+    int* dev_status) {
   constexpr int CH = D / 16;          // 16-byte chunks per row
   constexpr int PAGE_BYTES = kPage * D;
+  constexpr int V_STRIDE = PAGE_BYTES + (PT ? kScaleTailBytes : 0);  // bytes per V page
   __shared__ __align__(16) uint8_t vt[D * kPage];  // transposed V page
   __shared__ int64_t slots[kPage];
   __shared__ int fast;
@@ -114,10 +116,11 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
         const int64_t blk = slot / kPage;
         const int off = static_cast<int>(slot % kPage);
         const size_t page = (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
-        if (j == 0) {
-          const size_t si = (static_cast<size_t>(blk) * Hkv + h) * 2 * kPage + off;
-          kv_scale_cache[si] = skt;
-          kv_scale_cache[si + kPage] = svt;
+        const size_t vpage = (static_cast<size_t>(blk) * Hkv + h) * V_STRIDE;
+        if (j == 0) {  // the scale tail: K scales, then V scales, one per token slot
+          float* tail = reinterpret_cast<float*>(v_cache + vpage + PAGE_BYTES);
+          tail[off] = skt;
+          tail[kPage + off] = svt;
         }
         *reinterpret_cast<uint4*>(k_cache + page + fp8_k_offset(off, j, D)) = quant16<E5>(xk, skt);
         const uint4 qv = quant16<E5>(xv, svt);
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
 #pragma unroll
           for (int i = 0; i < 16; ++i) vt[(j * 16 + i) * kPage + slot_in_row] = qb[i];
         } else {
-          uint8_t* vp = v_cache + page + slot_in_row;
+          uint8_t* vp = v_cache + vpage + slot_in_row;
 #pragma unroll
           for (int i = 0; i < 16; ++i) vp[(j * 16 + i) * kPage] = qb[i];
         }
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
   if (fast) {
     __syncthreads();
     const int64_t blk = slots[0] / kPage;
-    uint8_t* vp = v_cache + (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
+    uint8_t* vp = v_cache + (static_cast<size_t>(blk) * Hkv + h) * V_STRIDE;
     for (int d = tid; d < D; d += blockDim.x)
       *reinterpret_cast<uint4*>(vp + d * kPage) = *reinterpret_cast<const uint4*>(vt + d * kPage);
   }
@@ -261,7 +264,7 @@ extern "C" kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, cons
     auto kc = static_cast<uint8_t*>(k_cache);
     auto vc = static_cast<uint8_t*>(v_cache);
     auto launch = [&](auto kernel) {
-      kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, k_scale, v_scale, nullptr, T, Hkv, num_slots,
+      kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, k_scale, v_scale, T, Hkv, num_slots,
                                   dev_status);
     };
     const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
@@ -289,10 +292,9 @@ extern "C" kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, cons
 }
 
 extern "C" kvq_status_t kvq_reshape_and_cache_per_token(const void* k, const void* v, const int64_t* slot_mapping,
-                                                        void* k_cache, void* v_cache, float* kv_scale_cache, int T,
-                                                        int Hkv, int D, int P, int64_t num_blocks,
-                                                        kvq_dtype_t cache_dtype, int* dev_status,
-                                                        kvq_stream_t stream) {
+                                                        void* k_cache, void* v_cache, int T, int Hkv, int D, int P,
+                                                        int64_t num_blocks, kvq_dtype_t cache_dtype,
+                                                        int* dev_status, kvq_stream_t stream) {
   clear_error();
   if (T < 0 || Hkv < 1 || num_blocks < 1) return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache_per_token: bad sizes");
   if (P != kPage) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache_per_token: page size %d (only 16)", P);
@@ -300,10 +302,10 @@ extern "C" kvq_status_t kvq_reshape_and_cache_per_token(const void* k, const voi
   if (cache_dtype != KVQ_DTYPE_FP8_E4M3 && cache_dtype != KVQ_DTYPE_FP8_E5M2)
     return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache_per_token: cache dtype must be E4M3 or E5M2");
   if (T == 0) return KVQ_OK;
-  if (!k || !v || !slot_mapping || !k_cache || !v_cache || !kv_scale_cache)
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
     return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache_per_token: null pointer");
   if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(slot_mapping, 8) || !aligned(kv_scale_cache, 16))
+      !aligned(slot_mapping, 8))
     return fail(KVQ_ERR_INVALID_ARG, "reshape_and_cache_per_token: misaligned pointer");
   if (Hkv > 65535) return fail(KVQ_ERR_UNSUPPORTED, "reshape_and_cache_per_token: too many KV heads");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -314,8 +316,7 @@ extern "C" kvq_status_t kvq_reshape_and_cache_per_token(const void* k, const voi
   auto kc = static_cast<uint8_t*>(k_cache);
   auto vc = static_cast<uint8_t*>(v_cache);
   auto launch = [&](auto kernel) {
-    kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, nullptr, nullptr, kv_scale_cache, T, Hkv, num_slots,
-                                dev_status);
+    kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, nullptr, nullptr, T, Hkv, num_slots, dev_status);
   };
   const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
   if (D == 128)

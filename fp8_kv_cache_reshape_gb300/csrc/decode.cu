@@ -101,13 +101,16 @@ constexpr int kCtasPerSm = 3;
 // two warps shared a slot, a warp could test a slot whose previous fill has
 // not landed yet, and a parity wait would then see the phase before it as
 // complete.)
-// Per-token scales (PT): each stage also holds the scale records of its two
-// pages after the pages, [K0 V0][K1 V1] (16 floats each, one 128-byte copy
-// per page from the interleaved scale cache).
-constexpr int kScaleBytes = 4 * kPage * 4;
+// Per-token scales (PT): a V page carries its scale tail (16 K scales, 16 V
+// scales) and moves with it in one copy; a stage is [K0][K1][V0 tail0][V1 tail1].
 template <int D, bool FP8, bool PT>
 constexpr int stage_stride() {
-  return Geo<D, FP8>::STAGE + (PT ? kScaleBytes : 0);
+  return Geo<D, FP8>::STAGE + (PT ? PPS * kScaleTailBytes : 0);
+}
+// bytes of one V page in the cache and in a stage
+template <int D, bool FP8, bool PT>
+constexpr int v_stride() {
+  return Geo<D, FP8>::PAGE + (PT ? kScaleTailBytes : 0);
 }
 
 constexpr int kSmemPerSm = 228 * 1024;
@@ -173,9 +176,8 @@ KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
 constexpr int kPresent0 = 1, kPresent1 = 2, kBad0 = 4, kBad1 = 8;
 
 // E5: the FP8 cache holds E5M2 codes (the MMAs take them as their A operand).
-// PT: per-token scales; p.k_scale points to the interleaved float32 scale
-// cache [num_blocks][Hkv][2][P] (K then V) instead of per-head scales (FP8
-// only; p.v_scale is unused).
+// PT: per-token scales, in the scale tail of each V page (FP8 only;
+// p.k_scale and p.v_scale are unused).
 // SL: single-level accumulation (an ablation of the two-level scheme): the
 // P.V MMAs accumulate into the running sum O * alpha directly instead of a
 // fresh FP32 tile per stage (FP8, per-head scales only).
@@ -304,44 +306,30 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
             }
           }
           // one stage = pages j, j + 1: a bulk copy per K page and per V page
-          auto issue_pages = [&](int st, uint32_t extra_per_page) {
+          // (per-token scales: the V page with its scale tail)
+          auto issue_pages = [&](int st) {
+            constexpr int VS = v_stride<D, FP8, PT>();
             int info = kPresent0 | (d0 ? kBad0 : 0);
             if (two) info |= kPresent1 | (d1 ? kBad1 : 0);
             stage_info[st] = info;
-            mbar_arrive_expect_tx(&full[st], (two ? 2u : 1u) * (2u * G::PAGE + extra_per_page));
+            mbar_arrive_expect_tx(&full[st], (two ? 2u : 1u) * static_cast<uint32_t>(G::PAGE + VS));
             uint8_t* sk = stages + size_t(st) * STRIDE;  // [K0][K1][V0][V1]
-            const size_t pg0 = (static_cast<size_t>(b0) * p.Hkv + r.kvh) * G::PAGE;
-            bulk_g2s(sk, p.k_cache + pg0, G::PAGE, &full[st], pol);
-            bulk_g2s(sk + 2 * G::PAGE, p.v_cache + pg0, G::PAGE, &full[st], pol);
+            const size_t pg0 = static_cast<size_t>(b0) * p.Hkv + r.kvh;
+            bulk_g2s(sk, p.k_cache + pg0 * G::PAGE, G::PAGE, &full[st], pol);
+            bulk_g2s(sk + 2 * G::PAGE, p.v_cache + pg0 * VS, VS, &full[st], pol);
             if (two) {
-              const size_t pg1 = (static_cast<size_t>(b1) * p.Hkv + r.kvh) * G::PAGE;
-              bulk_g2s(sk + G::PAGE, p.k_cache + pg1, G::PAGE, &full[st], pol);
-              bulk_g2s(sk + 3 * G::PAGE, p.v_cache + pg1, G::PAGE, &full[st], pol);
+              const size_t pg1 = static_cast<size_t>(b1) * p.Hkv + r.kvh;
+              bulk_g2s(sk + G::PAGE, p.k_cache + pg1 * G::PAGE, G::PAGE, &full[st], pol);
+              bulk_g2s(sk + 2 * G::PAGE + VS, p.v_cache + pg1 * VS, VS, &full[st], pol);
             }
           };
           int ok = 1;
-          if constexpr (PT) {
-            if (lane == 0) {
-              const int st = it % NST;
-              if (*abort_flag || !mbar_wait(&empty[st], ((it / NST) & 1) ^ 1, abort_flag)) {
-                ok = 0;
-              } else {
-                // the pages, then each page's scale record (16 K, 16 V) after them
-                constexpr uint32_t REC = 2 * kPage * 4;
-                issue_pages(st, REC);
-                uint8_t* scl = stages + size_t(st) * STRIDE + 4 * G::PAGE;  // [K0 V0][K1 V1]
-                bulk_g2s(scl, p.k_scale + (static_cast<size_t>(b0) * p.Hkv + r.kvh) * 2 * kPage, REC, &full[st], pol);
-                if (two)
-                  bulk_g2s(scl + REC, p.k_scale + (static_cast<size_t>(b1) * p.Hkv + r.kvh) * 2 * kPage, REC,
-                           &full[st], pol);
-              }
-            }
-          } else if (lane == 0) {
+          if (lane == 0) {
             const int st = it % NST;
             if (*abort_flag || !mbar_wait(&empty[st], ((it / NST) & 1) ^ 1, abort_flag)) {
               ok = 0;
             } else {
-              issue_pages(st, 0u);
+              issue_pages(st);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -375,7 +363,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
   }
   // V offsets.  FP8: matrix 0/1 = page 0 rows (16 mt + 0..7 / 8..15), matrix
   // 2/3 = the same rows of page 1.  BF16: one m-tile of one page per x4.
-  const int vofs = (lane >> 4) * G::PAGE + (lane & 15) * kPage;  // FP8: + 256 per m-tile
+  const int vofs = (lane >> 4) * v_stride<D, FP8, PT>() + (lane & 15) * kPage;  // FP8: + 256 per m-tile
   int voff[FP8 ? 1 : G::MT];
   if constexpr (FP8) {
     voff[0] = vofs;
@@ -517,16 +505,18 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
       if constexpr (FP8) {
         // per-token scales (PT) of this lane's tokens r and r + 8 of both pages
         float sk00 = 1.f, sk01 = 1.f, sk10 = 1.f, sk11 = 1.f, sv00 = 0.f, sv01 = 0.f, sv10 = 0.f, sv11 = 0.f;
-        if constexpr (PT) {
-          const float* scl = reinterpret_cast<const float*>(stages + size_t(st) * STRIDE + 4 * G::PAGE);
-          sk00 = scl[r];  // [K0 V0][K1 V1]
-          sk01 = scl[r + 8];
-          sv00 = scl[kPage + r];
-          sv01 = scl[kPage + r + 8];
-          sk10 = scl[2 * kPage + r];
-          sk11 = scl[2 * kPage + r + 8];
-          sv10 = scl[3 * kPage + r];
-          sv11 = scl[3 * kPage + r + 8];
+        if constexpr (PT) {  // the scale tails after each V page: 16 K scales, then 16 V scales
+          const uint8_t* v0 = stages + size_t(st) * STRIDE + 2 * G::PAGE;
+          const float* t0 = reinterpret_cast<const float*>(v0 + G::PAGE);
+          const float* t1 = reinterpret_cast<const float*>(v0 + v_stride<D, FP8, PT>() + G::PAGE);
+          sk00 = t0[r];
+          sk01 = t0[r + 8];
+          sv00 = t0[kPage + r];
+          sv01 = t0[kPage + r + 8];
+          sk10 = t1[r];
+          sk11 = t1[r + 8];
+          sv10 = t1[kPage + r];
+          sv11 = t1[kPage + r + 8];
         }
         // ---- S^T = K Q^T, E4M3 MMA, q as hi + lo (two independent chains) ----
         auto qk = [&](uint32_t kp, float (&s)[4], float ska, float skb) {  // ska, skb: tokens r, r + 8
@@ -1010,8 +1000,8 @@ struct AppendArgs {
   const int64_t* slot_new;
 };
 
-// Shared by the per-head and the per-token entry points.  per_token: k_scale
-// (= v_scale) is the interleaved scale cache [num_blocks][Hkv][2][P].
+// Shared by the per-head and the per-token entry points.  per_token: the
+// scales sit in the tail of each V page; k_scale and v_scale are unused.
 kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                           const float* v_scale, const int32_t* block_table, const int32_t* seq_lens, void* out, int B,
                           int Hq, int Hkv, int D, int P, int max_blocks, int64_t num_blocks, float sm_scale, int window,
@@ -1031,15 +1021,13 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
   const bool fp8 = cache_dtype != KVQ_DTYPE_BF16;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace)
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: null pointer");
-  if (fp8 && (!k_scale || !v_scale))
+  if (fp8 && !per_token && (!k_scale || !v_scale))
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: FP8 needs k_scale and v_scale");
   if (per_token && !fp8) return fail(KVQ_ERR_INVALID_ARG, "paged_decode: per-token scales need an FP8 cache");
   if (app && (per_token || single_level))
     return fail(KVQ_ERR_UNSUPPORTED, "paged_decode_append: per-head scales and two-level accumulation only");
   if (app && (!app->k_new || !app->v_new || !app->slot_new))
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode_append: null pointer");
-  if (per_token && (!aligned(k_scale, 16) || !aligned(v_scale, 16)))
-    return fail(KVQ_ERR_INVALID_ARG, "paged_decode: scale caches must be 16-byte aligned");
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(workspace, 16) ||
       !aligned(out, 4))
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: misaligned pointer");
@@ -1151,12 +1139,12 @@ extern "C" kvq_status_t kvq_paged_decode_attention_acc(
 }
 
 extern "C" kvq_status_t kvq_paged_decode_attention_per_token(
-    const void* q, const void* k_cache, const void* v_cache, const float* kv_scale_cache, const int32_t* block_table,
-    const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int D, int P, int max_blocks, int64_t num_blocks,
-    float sm_scale, int window, kvq_dtype_t cache_dtype, int num_splits, void* workspace, size_t workspace_bytes,
-    int* dev_status, kvq_stream_t stream) {
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+    void* out, int B, int Hq, int Hkv, int D, int P, int max_blocks, int64_t num_blocks, float sm_scale, int window,
+    kvq_dtype_t cache_dtype, int num_splits, void* workspace, size_t workspace_bytes, int* dev_status,
+    kvq_stream_t stream) {
   clear_error();
-  return paged_decode(q, k_cache, v_cache, kv_scale_cache, kv_scale_cache, block_table, seq_lens, out, B, Hq, Hkv, D, P,
+  return paged_decode(q, k_cache, v_cache, nullptr, nullptr, block_table, seq_lens, out, B, Hq, Hkv, D, P,
                       max_blocks, num_blocks, sm_scale, window, cache_dtype, num_splits, workspace, workspace_bytes,
                       dev_status, stream, true);
 }

@@ -17,6 +17,7 @@
 namespace kvq {
 
 constexpr int kPage = 16;                 // tokens per page
+constexpr int kScaleTailBytes = 2 * kPage * 4;  // per-token V page: P K scales, then P V scales (float32)
 constexpr unsigned kWaitPolls = 1u << 26;        // try_wait polls before a wait is declared stuck
 constexpr uint64_t kWaitNs = 2000000000ull;      // ... or 2 s of wall time, whichever comes first
 

@@ -310,31 +310,32 @@ kvq_status_t kvq_paged_decode_attention_acc(const void* q, const void* k_cache, 
  * the worked example), at the cost of one maximum per token; [GTNT] section
  * 2.2: per-token dynamic quantization computes a scale for every new token.
  *
- *  As kvq_reshape_and_cache (FP8 E4M3 or E5M2 only), plus:
- *  kv_scale_cache  float32 [num_blocks][Hkv][2][P], 16-byte aligned
- *                  (written): [block][h][0][offset] is the K scale and
- *                  [block][h][1][offset] the V scale of the token in that
- *                  slot, s = fl32(amax_d |x_d| / M) with M = 448 (E4M3) or
- *                  57344 (E5M2); a token whose values are all zero gets s = 1.
- *                  (K and V scales of a page share one 128-byte record, which
- *                  decode fetches with one copy.)
+ *  As kvq_reshape_and_cache (FP8 E4M3 or E5M2 only), except the V cache:
+ *  v_cache   [num_blocks][Hkv] pages of P*D + 8*P bytes (written): the P x D
+ *            codes in the V format above, then a scale tail of P K scales
+ *            and P V scales, float32 -- tail[offset] is the K scale and
+ *            tail[P + offset] the V scale of the token in slot offset,
+ *            s = fl32(amax_d |x_d| / M) with M = 448 (E4M3) or 57344 (E5M2);
+ *            a token whose values are all zero gets s = 1.  The scales ride
+ *            on the V page so that decode fetches page and scales in one
+ *            copy.  k_cache is as for kvq_reshape_and_cache.
  *  Each element is then code = encode(fl32(x / s)) as in
  *  kvq_reshape_and_cache.  Only the given slots' bytes and scales are
  *  written.
  */
 kvq_status_t kvq_reshape_and_cache_per_token(const void* k, const void* v, const int64_t* slot_mapping,
-                                             void* k_cache, void* v_cache, float* kv_scale_cache,
-                                             int T, int Hkv, int D, int P, int64_t num_blocks,
-                                             kvq_dtype_t cache_dtype, int* dev_status, kvq_stream_t stream);
+                                             void* k_cache, void* v_cache, int T, int Hkv, int D, int P,
+                                             int64_t num_blocks, kvq_dtype_t cache_dtype, int* dev_status,
+                                             kvq_stream_t stream);
 
 /*
  * kvq_paged_decode_attention_per_token -- kvq_paged_decode_attention over a
  * cache written by kvq_reshape_and_cache_per_token (same citations; the
  * per-token scales as above).
  *
- *  kv_scale_cache  the scale cache of that call (read); every other argument
- *                  as for kvq_paged_decode_attention, with an FP8 (E4M3 or
- *                  E5M2) cache.
+ *  Arguments as for kvq_paged_decode_attention without k_scale and
+ *  v_scale, with an FP8 (E4M3 or E5M2) cache in the per-token format (V
+ *  pages of P*D + 8*P bytes, each with its scale tail).
  *  Declared rounding: the query terms and the per-head score coefficient as
  *  for kvq_paged_decode_attention with c = fl32(sm_scale * log2(e)); each
  *  score is then multiplied by its token's K scale.  V scales enter the
@@ -349,7 +350,6 @@ kvq_status_t kvq_reshape_and_cache_per_token(const void* k, const void* v, const
  *  Workspace: kvq_decode_workspace_size() of the same arguments.
  */
 kvq_status_t kvq_paged_decode_attention_per_token(const void* q, const void* k_cache, const void* v_cache,
-                                                  const float* kv_scale_cache,
                                                   const int32_t* block_table, const int32_t* seq_lens,
                                                   void* out, int B, int Hq, int Hkv, int D, int P,
                                                   int max_blocks, int64_t num_blocks, float sm_scale,

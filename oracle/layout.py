@@ -17,6 +17,8 @@ physical layout:
   rho = [0,1,4,5,8,9,12,13,2,3,6,7,10,11,14,15].
 * V page (BF16): row d of 16 bf16; token t in slot t, and the two 16-byte
   halves of the row are swapped when (d // 4) is odd.
+* Per-token V page (FP8): the V page above, then a scale tail of 16 K scales
+  and 16 V scales (float32, slot t at tail[t] and tail[16 + t]).
 No arithmetic of the method lives here.
 """
 from __future__ import annotations
@@ -93,3 +95,21 @@ def from_device_format(kd, vd, D: int, esize: int):
     vl[:, :, vp] = vd
     dt = np.uint8 if esize == 1 else np.uint16
     return (kl.view(dt).reshape(nb, H, P, D), vl.view(dt).reshape(nb, H, D, P))
+
+
+def to_device_format_per_token(k_cache, v_cache, kv_scale_cache):
+    """Logical FP8 caches and the scale cache [nb][Hkv][2][P] (float32) ->
+    (K pages, V pages with their scale tails)."""
+    kd, vd = to_device_format(k_cache, v_cache)
+    tail = np.ascontiguousarray(kv_scale_cache, dtype=np.float32).view(np.uint8).reshape(kd.shape[0], kd.shape[1], -1)
+    return kd, np.concatenate([vd, tail], axis=2)
+
+
+def from_device_format_per_token(kd, vd, D: int):
+    """(K pages, V pages with tails) -> logical FP8 caches and the scale
+    cache [nb][Hkv][2][P] (float32)."""
+    nb, H, _ = vd.shape
+    codes = np.ascontiguousarray(vd[:, :, :P * D])
+    tail = np.ascontiguousarray(vd[:, :, P * D:]).view(np.float32).reshape(nb, H, 2, P)
+    kl, vl = from_device_format(kd, codes, D, 1)
+    return kl, vl, tail

@@ -65,25 +65,28 @@ def test_host_validation_without_gpu(lib):
 
 
 def test_per_token_entry_points_validate_without_gpu(lib):
-    """The per-token calls refuse a BF16 cache and missing scale caches
-    before any CUDA call."""
+    """The per-token calls refuse a BF16 cache, missing caches and misaligned
+    pointers before any CUDA call."""
     p = ctypes.c_void_p
     i, i64, f32, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     w = lib.kvq_reshape_and_cache_per_token
     w.restype = i
-    w.argtypes = [p, p, p, p, p, p, i, i, i, i, i64, i, p, p]
+    w.argtypes = [p, p, p, p, p, i, i, i, i, i64, i, p, p]
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the calls return first
-    assert w(fake, fake, fake, fake, fake, fake, 4, 1, 128, 16, 8, 1, None, None) == 1  # BF16 cache
-    assert w(fake, fake, fake, fake, fake, None, 4, 1, 128, 16, 8, 0, None, None) == 1  # no scale cache
-    assert w(fake, fake, fake, fake, fake, None, 0, 1, 128, 16, 8, 2, None, None) == 0  # T = 0, E5M2
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    assert w(fake, fake, fake, fake, fake, 4, 1, 128, 16, 8, 1, None, None) == 1  # BF16 cache
+    assert w(fake, fake, fake, fake, None, 4, 1, 128, 16, 8, 0, None, None) == 1  # no V cache
+    assert w(fake, fake, fake, fake, odd, 4, 1, 128, 16, 8, 0, None, None) == 1  # V cache not 16-byte aligned
+    assert w(fake, fake, fake, fake, fake, 4, 1, 96, 16, 8, 0, None, None) == 2  # head_dim 96
+    assert w(None, None, None, None, None, 0, 1, 128, 16, 8, 2, None, None) == 0  # T = 0, E5M2
     d = lib.kvq_paged_decode_attention_per_token
     d.restype = i
-    d.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i64, f32, i, i, i, p, sz, p, p]
-    args = [fake] * 7 + [1, 8, 2, 128, 16, 4, 64, 0.088, -1]
-    assert d(*args, 1, 0, fake, 1 << 30, None, None) == 1  # BF16 cache
-    assert d(*([fake] * 3 + [None] + [fake] * 3 + args[7:]), 0, 0, fake, 1 << 30, None, None) == 1  # no scales
-    assert d(*([fake] * 3 + [ctypes.c_void_p((1 << 20) + 4)] + [fake] * 3 + args[7:]), 0, 0, fake, 1 << 30,
-             None, None) == 1  # scale cache not 16-byte aligned
+    d.argtypes = [p, p, p, p, p, p, i, i, i, i, i, i, i64, f32, i, i, i, p, sz, p, p]
+    args = [1, 8, 2, 128, 16, 4, 64, 0.088, -1]
+    assert d(*[fake] * 6, *args, 1, 0, fake, 1 << 30, None, None) == 1  # BF16 cache
+    assert d(fake, fake, None, *[fake] * 3, *args, 0, 0, fake, 1 << 30, None, None) == 1  # no V cache
+    assert d(fake, fake, odd, *[fake] * 3, *args, 0, 0, fake, 1 << 30, None, None) == 1  # V cache misaligned
+    assert d(*[fake] * 6, *args, 0, 0, fake, 16, None, None) == 1  # workspace too small
 
 
 def test_append_entry_point_validates_without_gpu(lib):

@@ -1,6 +1,7 @@
 """GPU parity of the per-token dynamic-scale calls against the float64
 oracle: kvq_reshape_and_cache_per_token bit-exact on every cache byte and
-every scale (unwritten slots keep their sentinel / NaN), and
+every scale in the V pages' scale tails (unwritten slots keep their sentinel
+/ NaN), and
 kvq_paged_decode_attention_per_token within the decode tolerance against
 the mirrored and the pure oracle.  Scale slots that no token wrote are NaN,
 so a scale read for a masked token would show up in the output."""
@@ -34,22 +35,26 @@ def oracle_per_token_cache(case):
 def gpu_per_token_cache(case):
     k = _k()
     cfg = case.cfg
-    kd, vd = k.alloc_kv_cache(case.num_blocks, cfg.kv_heads, cfg.head_dim, case.cache_dtype, fill=SENTINEL)
-    scd = k.alloc_scale_cache(case.num_blocks, cfg.kv_heads, fill=float("nan"))
+    kd, vd = k.alloc_kv_cache(case.num_blocks, cfg.kv_heads, cfg.head_dim, case.cache_dtype, fill=SENTINEL,
+                              per_token=True)
+    # unwritten scale slots hold NaN
+    nan = np.full((case.num_blocks, cfg.kv_heads, 2, 16), np.nan, np.float32).view(np.uint8)
+    vd.view(case.num_blocks, cfg.kv_heads, -1)[:, :, 16 * cfg.head_dim:] = \
+        torch.from_numpy(nan.reshape(case.num_blocks, cfg.kv_heads, -1)).cuda()
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    k.kvq_reshape_and_cache_per_token(case.k.cuda(), case.v.cuda(), case.slot_mapping.cuda(), kd, vd, scd,
+    k.kvq_reshape_and_cache_per_token(case.k.cuda(), case.v.cuda(), case.slot_mapping.cuda(), kd, vd,
                                       case.cache_dtype, dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    return kd, vd, scd
+    return kd, vd
 
 
-def gpu_decode(case, kd, vd, scd, num_splits=0):
+def gpu_decode(case, kd, vd, num_splits=0):
     k = _k()
     B, Hq, D = case.q.shape
     out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    k.kvq_paged_decode_attention_per_token(case.q.cuda(), kd, vd, scd, case.block_table.cuda(),
+    k.kvq_paged_decode_attention_per_token(case.q.cuda(), kd, vd, case.block_table.cuda(),
                                            case.seq_lens.cuda(), out, num_blocks=case.num_blocks,
                                            sm_scale=case.sm_scale, window=case.window,
                                            cache_dtype=case.cache_dtype, num_splits=num_splits, dev_status=st)
@@ -73,12 +78,14 @@ def test_cache_write_per_token_bit_exact(dtype, D, Hkv, lengths, scatter):
         g = torch.Generator().manual_seed(9)
         case.slot_mapping = case.slot_mapping[torch.randperm(case.slot_mapping.numel(), generator=g)].contiguous()
         case.slot_mapping[::5] = -1
-    kd, vd, scd = gpu_per_token_cache(case)
+    kd, vd = gpu_per_token_cache(case)
     kc, vc, sc = oracle_per_token_cache(case)
-    ek, ev = layout.to_device_format(kc, vc)
+    ek, ev = layout.to_device_format_per_token(kc, vc, sc)
     assert np.array_equal(kd.cpu().numpy(), ek), "K cache bytes differ"
-    assert np.array_equal(vd.cpu().numpy(), ev), "V cache bytes differ"
-    assert np.array_equal(_bits(scd.cpu().numpy()), _bits(sc)), "scales differ"
+    code_bytes = 16 * D
+    assert np.array_equal(vd.cpu().numpy()[:, :, :code_bytes], ev[:, :, :code_bytes]), "V cache bytes differ"
+    _, _, got_sc = layout.from_device_format_per_token(kd.cpu().numpy(), vd.cpu().numpy(), D)
+    assert np.array_equal(_bits(got_sc), _bits(sc)), "scales differ"
 
 
 CASES = {
@@ -94,9 +101,9 @@ CASES = {
 
 
 def _check_decode(case, num_splits=0):
-    kd, vd, scd = gpu_per_token_cache(case)
+    kd, vd = gpu_per_token_cache(case)
     kc, vc, sc = oracle_per_token_cache(case)
-    got = gpu_decode(case, kd, vd, scd, num_splits=num_splits)
+    got = gpu_decode(case, kd, vd, num_splits=num_splits)
     args = (f32(case.q), kc, vc, sc, case.block_table.numpy(), case.seq_lens.numpy(), case.sm_scale)
     ref, _ = attention.paged_decode_per_token(*args, window=case.window, cache_dtype=case.cache_dtype, mode="mirror")
     pure, _ = attention.paged_decode_per_token(*args, window=case.window, cache_dtype=case.cache_dtype, mode="pure")
@@ -123,8 +130,8 @@ def test_decode_per_token_full_size_llama_128k():
     """One full Llama-3.1-8B layer at 131,072 tokens (8 KV heads, D 128,
     4 outlier channels) with per-token scales."""
     case = W.decode_case(W.LLAMA_128K, layer=3)
-    kd, vd, scd = gpu_per_token_cache(case)
-    got = gpu_decode(case, kd, vd, scd)
+    kd, vd = gpu_per_token_cache(case)
+    got = gpu_decode(case, kd, vd)
     kc, vc, sc = oracle_per_token_cache(case)
     ref, _ = attention.paged_decode_per_token(f32(case.q), kc, vc, sc, case.block_table.numpy(),
                                               case.seq_lens.numpy(), case.sm_scale, cache_dtype=FP8, mode="mirror")

@@ -141,3 +141,21 @@ def test_zero_token_gets_unit_scale():
     assert ksc[0, 0, 1] == np.float32(np.float32(4.0) / np.float32(448.0))
     kc5, _, ksc5, _ = _write_tokens([[1.0, 2.0, 4.0]], kv_cache.FP8_E5M2)
     assert ksc5[0, 0, 0] == np.float32(np.float32(4.0) / np.float32(57344.0)) and kc5[0, 0, 0, 2] == 0x7B
+
+
+def test_per_token_device_layout_round_trip_and_tail_position():
+    """The per-token V page is the V codes followed by the scale tail:
+    K scale of slot t at byte P*D + 4t, V scale at P*D + 64 + 4t."""
+    from oracle import layout
+    rng = np.random.default_rng(3)
+    nb, H, D = 3, 2, 64
+    kc = rng.integers(0, 256, (nb, H, 16, D), dtype=np.uint8)
+    vc = rng.integers(0, 256, (nb, H, D, 16), dtype=np.uint8)
+    sc = rng.random((nb, H, 2, 16)).astype(np.float32)
+    kd, vd = layout.to_device_format_per_token(kc, vc, sc)
+    assert kd.shape == (nb, H, 16 * D) and vd.shape == (nb, H, 16 * D + 128)
+    for t in (0, 7, 15):
+        assert vd[1, 1, 16 * D + 4 * t: 16 * D + 4 * t + 4].view(np.float32)[0] == sc[1, 1, 0, t]
+        assert vd[2, 0, 16 * D + 64 + 4 * t: 16 * D + 68 + 4 * t].view(np.float32)[0] == sc[2, 0, 1, t]
+    k2, v2, s2 = layout.from_device_format_per_token(kd, vd, D)
+    assert np.array_equal(k2, kc) and np.array_equal(v2, vc) and np.array_equal(s2, sc)
