@@ -51,8 +51,8 @@ struct DecodeParams {
   const float* v_scale;
   const int32_t* block_table;
   const int32_t* seq_lens;
-  float* o_part;    // [B][Hq][S][D]
-  float* lse_part;  // [B][Hq][S], log2 units
+  float* o_part;    // [B][Hq][S][NW][D]
+  float* lse_part;  // [B][Hq][S][NW], log2 units
   // direct: one page range per (sequence, KV head) and one item per CTA; the
   // CTA merges its consumer warps' partials in shared memory and writes the
   // bf16 output itself (no combine kernel)
@@ -115,6 +115,9 @@ constexpr int v_stride() {
 
 constexpr int kSmemPerSm = 228 * 1024;
 constexpr int kRingBudget = kSmemPerSm / kCtasPerSm - 1024 - 512;
+// Dynamic shared memory that lets at most 1 or 2 CTAs reside on an SM (the
+// next count would overrun the SM's budget with the 1 KB each CTA reserves).
+constexpr int kSpreadSmem[2] = {kSmemPerSm / 2 - 1024 + 16, kSmemPerSm / 3 - 1024 + 16};
 template <int D, bool FP8, bool PT = false>
 constexpr int stages_for() {
   constexpr int n = (kRingBudget / stage_stride<D, FP8, PT>()) > 32 ? 32 : (kRingBudget / stage_stride<D, FP8, PT>());
@@ -141,6 +144,34 @@ struct ItemRange {
   int pg0, n;     // first page and page count of this split
 };
 
+// The pages [first, last) that a sequence of L cached tokens attends to, cut
+// into S near-equal ranges of pps pages (so that shorter sequences still
+// spread over all splits); the first `active` ranges hold any page.
+struct SplitPages {
+  int first, last, pps, active;
+};
+
+KVQ_DEVINL SplitPages split_pages(int L, int window, int S) {
+  SplitPages sp;
+  const int lo = (window > 0 && L > window) ? L - window : 0;
+  sp.first = lo / kPage;
+  sp.last = (L + kPage - 1) / kPage;
+  sp.pps = (sp.last - sp.first + S - 1) / S;
+  sp.active = sp.pps > 0 ? (sp.last - sp.first + sp.pps - 1) / sp.pps : 0;
+  return sp;
+}
+
+// seq_lens[b], clamped to what the block table holds (reported once)
+KVQ_DEVINL int seq_len_of(const int32_t* seq_lens, int b, int max_blocks, int* dev_status, bool report) {
+  int L = seq_lens[b];
+  const int cap = max_blocks * kPage;
+  if (L < 0 || L > cap) {
+    if (report) set_status(dev_status, KVQ_DEV_BAD_SEQLEN);
+    L = L < 0 ? 0 : cap;
+  }
+  return L;
+}
+
 KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
   ItemRange r;
   const int S = p.num_splits;
@@ -151,23 +182,14 @@ KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
   r.split = item / NG;
   r.b = bh / p.Hkv;
   r.kvh = bh - r.b * p.Hkv;
-  int L = p.seq_lens[r.b];
-  const int cap = p.max_blocks * kPage;
-  if (L < 0 || L > cap) {
-    if (report) set_status(p.dev_status, KVQ_DEV_BAD_SEQLEN);
-    L = L < 0 ? 0 : cap;
-  }
+  const int L = seq_len_of(p.seq_lens, r.b, p.max_blocks, p.dev_status, report);
   r.hi = L;
   r.lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
-  const int first = r.lo / kPage;
-  const int last = (L + kPage - 1) / kPage;
-  // this sequence's pages are cut into S near-equal ranges, so shorter
-  // sequences still spread over all splits
-  const int pps = (last - first + S - 1) / S;
-  r.pg0 = first + r.split * pps;
-  int pg1 = r.pg0 + pps;
-  if (pg1 > last) pg1 = last;
-  r.n = pg1 > r.pg0 ? pg1 - r.pg0 : 0;
+  const SplitPages sp = split_pages(L, p.window, S);
+  r.pg0 = sp.first + r.split * sp.pps;
+  int pg1 = r.pg0 + sp.pps;
+  if (pg1 > sp.last) pg1 = sp.last;
+  r.n = pg1 > r.pg0 ? pg1 - r.pg0 : 0;  // 0 exactly when split >= sp.active
   return r;
 }
 
@@ -210,6 +232,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
     fence_barrier_init();
   }
   __syncthreads();
+  // launched as a programmatic dependent: the setup above overlaps the
+  // preceding kernel, and nothing in global memory is touched before it has
+  // completed.  The combine kernel may launch once every CTA is past that
+  // point, so it too sees the preceding kernel's writes.
+  grid_dependency_wait();
   grid_launch_dependents();
 
   if (warp == NW) {
@@ -384,6 +411,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
   uint32_t it0 = 0;
   for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
     const ItemRange rg = item_range(p, item, false);
+    // a range past the end of a shorter sequence: no pages, and the combine
+    // reads no partial of it
+    if (rg.n == 0 && !p.direct) continue;
     // ---- query fragments of head (kvh * g + r); heads >= g are zero padding ----
     // FP8: q * sigma = hi + lo, two E4M3 terms (sigma = 2^(7 - floor(log2 max|q|))
     // per head) feed the E4M3 MMA; lanes c hold dims 32kk + 4c..4c+3 (b0) and
@@ -828,7 +858,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
 }
 
 // out[row][d] = sum_s 2^(lse_s - M) o_s[d] / sum_s 2^(lse_s - M) over the
-// S' partials of row = (b, hq).  Grid (rows, D / 32); warp w takes partials
+// partials of row = (b, hq) whose ranges hold pages (the first
+// split_pages().active of `splits`, NW partials each; the rest were never
+// written).  Grid (rows, D / 32); warp w takes partials
 // w, w + 32, ... (lane = dimension) and loads their log-sum-exps and outputs
 // together (one round trip), merges them against its own maximum, and the
 // warps' results are merged through shared memory.
@@ -836,17 +868,25 @@ constexpr int kCombineWarps = 32;
 constexpr int kCombinePer = 8;  // partials per warp and pass
 __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const float* __restrict__ o_part,
                                                                             const float* __restrict__ lse_part,
-                                                                            __nv_bfloat16* __restrict__ out, int S,
-                                                                            int D) {
+                                                                            __nv_bfloat16* __restrict__ out,
+                                                                            const int32_t* __restrict__ seq_lens,
+                                                                            int Hq, int max_blocks, int window,
+                                                                            int splits, int D) {
   __shared__ float m_s[kCombineWarps];
   __shared__ float den_s[kCombineWarps];
   __shared__ float acc_s[kCombineWarps][33];
-  grid_dependency_wait();  // the partial kernel's writes are visible past this point
+  grid_launch_dependents();  // the next call's partial kernel may start its setup
   const int row = blockIdx.x;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int d = blockIdx.y * 32 + lane;
-  const float* lp = lse_part + static_cast<size_t>(row) * S;
-  const float* op = o_part + static_cast<size_t>(row) * S * D + d;
+  const float* lp = lse_part + static_cast<size_t>(row) * splits * kNW;
+  const float* op = o_part + static_cast<size_t>(row) * splits * kNW * D + d;
+  // only the ranges that hold pages wrote partials.  seq_lens is read before
+  // the wait: the partial kernel does not write it, and this grid launches
+  // only after the kernels before the partial kernel have completed.
+  const int L = seq_len_of(seq_lens, row / Hq, max_blocks, nullptr, false);
+  const int S = split_pages(L, window, splits).active * kNW;
+  grid_dependency_wait();  // the partial kernel's writes are visible past this point
   float m = -INFINITY, den = 0.f, acc = 0.f;
   for (int s0 = wid; s0 < S; s0 += kCombineWarps * kCombinePer) {
     float l[kCombinePer], o[kCombinePer];
@@ -937,34 +977,46 @@ kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(configured_mask & (1 << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpreadSmem[0]);
     if (e != cudaSuccess) return cuda_status(e, "decode: set shared memory size");
     configured_mask |= 1 << (dev & 31);
   }
-  int grid = kCtasPerSm * sm_count();
+  const int sms = sm_count();
+  int grid = kCtasPerSm * sms;
   DecodeParams q = p;
   q.out = out;
   // one page range per (sequence, KV head) and every item in its own CTA: the
   // CTAs write the output themselves
   q.direct = (p.num_splits == 1 && p.num_items <= grid) ? 1 : 0;
   if (grid > p.num_items) grid = p.num_items;
-  kern<<<grid, (kNW + 1) * 32, smem, s>>>(q);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_status(e, "decode partial launch");
-  if (q.direct) return KVQ_OK;
-  // combine: programmatic dependent launch (its launch overlaps the partial's tail)
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.B * p.Hq, D / 32);
-  cfg.blockDim = dim3(kCombineWarps * 32);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
+  // A grid smaller than the resident capacity asks for enough shared memory
+  // that at most ceil(grid / SMs) CTAs fit on one SM: its CTAs then spread
+  // over the SMs even when they are placed while the preceding kernel still
+  // holds some of them (programmatic launch, below).
+  const int per_sm = (grid + sms - 1) / sms;
+  size_t dyn = smem;
+  if (per_sm < kCtasPerSm && kSpreadSmem[per_sm - 1] > dyn) dyn = kSpreadSmem[per_sm - 1];
+  // both kernels are programmatic dependents of what precedes them on the
+  // stream: their launch and setup overlap its tail
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3((kNW + 1) * 32);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, q);
+  if (e != cudaSuccess) return cuda_status(e, "decode partial launch");
+  if (q.direct) return KVQ_OK;
+  cfg.gridDim = dim3(p.B * p.Hq, D / 32);
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
   e = cudaLaunchKernelEx(&cfg, decode_combine_kernel, static_cast<const float*>(p.o_part),
-                         static_cast<const float*>(p.lse_part), out, p.num_splits * kNW, D);
+                         static_cast<const float*>(p.lse_part), out, p.seq_lens, p.Hq, p.max_blocks, p.window,
+                         p.num_splits, D);
   return cuda_status(e, "decode combine launch");
 }
 

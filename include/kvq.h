@@ -205,8 +205,16 @@ size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P, int max_b
  * Split-KV: each (sequence, KV head) is cut into num_splits ranges of pages;
  * a partial kernel writes per range (and per consumer warp within it, each
  * warp taking every fourth pair of pages) a normalized output and a
- * log-sum-exp to the workspace, and a combine kernel merges them:
+ * log-sum-exp to the workspace, and a combine kernel merges them (with one
+ * range per sequence and KV head, all within one wave of the GPU, the
+ * partial kernel merges its warps in shared memory and writes the output
+ * itself):
  *   lse = log sum_i exp(lse_i),  out = sum_i exp(lse_i - lse) out_i.
+ * Both kernels are programmatic dependent launches: their launch and setup
+ * overlap the preceding kernel on the stream, and neither touches global
+ * memory before that kernel has completed.  A grid smaller than the GPU's
+ * resident capacity asks for more shared memory per CTA than it uses, so
+ * that its CTAs spread over the SMs.
  * Accumulation: scores and P.V products are accumulated by tensor-core MMAs
  * into fresh FP32 registers per page of 16 tokens, then added into a running
  * FP32 sum (first level), and ranges are merged in FP32 (second level).
