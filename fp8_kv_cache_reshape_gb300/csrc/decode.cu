@@ -146,9 +146,9 @@ struct ItemRange {
 
 // The pages [first, last) that a sequence of L cached tokens attends to, cut
 // into S near-equal ranges of pps pages (so that shorter sequences still
-// spread over all splits); the first `active` ranges hold any page.
+// spread over all splits).
 struct SplitPages {
-  int first, last, pps, active;
+  int first, last, pps;
 };
 
 KVQ_DEVINL SplitPages split_pages(int L, int window, int S) {
@@ -157,7 +157,6 @@ KVQ_DEVINL SplitPages split_pages(int L, int window, int S) {
   sp.first = lo / kPage;
   sp.last = (L + kPage - 1) / kPage;
   sp.pps = (sp.last - sp.first + S - 1) / S;
-  sp.active = sp.pps > 0 ? (sp.last - sp.first + sp.pps - 1) / sp.pps : 0;
   return sp;
 }
 
@@ -189,7 +188,7 @@ KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
   r.pg0 = sp.first + r.split * sp.pps;
   int pg1 = r.pg0 + sp.pps;
   if (pg1 > sp.last) pg1 = sp.last;
-  r.n = pg1 > r.pg0 ? pg1 - r.pg0 : 0;  // 0 exactly when split >= sp.active
+  r.n = pg1 > r.pg0 ? pg1 - r.pg0 : 0;
   return r;
 }
 
@@ -235,9 +234,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
   // launched as a programmatic dependent: the setup above overlaps the
   // preceding kernel, and nothing in global memory is touched before it has
   // completed.  The combine kernel may launch once every CTA is past that
-  // point, so it too sees the preceding kernel's writes.
+  // point, so it too sees the preceding kernel's writes.  Without a combine
+  // (direct output) the next kernel launches as the CTAs exit: its CTAs
+  // waiting beside this grid's slowest ones would slow them.
   grid_dependency_wait();
-  grid_launch_dependents();
+  if (!p.direct) grid_launch_dependents();
 
   if (warp == NW) {
     // ------------------------------------------------------------ producer --
@@ -411,9 +412,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
   uint32_t it0 = 0;
   for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
     const ItemRange rg = item_range(p, item, false);
-    // a range past the end of a shorter sequence: no pages, and the combine
-    // reads no partial of it
-    if (rg.n == 0 && !p.direct) continue;
     // ---- query fragments of head (kvh * g + r); heads >= g are zero padding ----
     // FP8: q * sigma = hi + lo, two E4M3 terms (sigma = 2^(7 - floor(log2 max|q|))
     // per head) feed the E4M3 MMA; lanes c hold dims 32kk + 4c..4c+3 (b0) and
@@ -858,41 +856,36 @@ __global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const 
 }
 
 // out[row][d] = sum_s 2^(lse_s - M) o_s[d] / sum_s 2^(lse_s - M) over the
-// partials of row = (b, hq) whose ranges hold pages (the first
-// split_pages().active of `splits`, NW partials each; the rest were never
-// written).  Grid (rows, D / 32); warp w takes partials
-// w, w + 32, ... (lane = dimension) and loads their log-sum-exps and outputs
+// S' partials of row = (b, hq).  Grid (rows, D / 32), NW warps per CTA
+// (chosen so that NW * kCombinePer covers S'): warp w takes partials w,
+// w + NW, ... (lane = dimension) and loads their log-sum-exps and outputs
 // together (one round trip), merges them against its own maximum, and the
 // warps' results are merged through shared memory.
-constexpr int kCombineWarps = 32;
 constexpr int kCombinePer = 8;  // partials per warp and pass
-__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const float* __restrict__ o_part,
-                                                                            const float* __restrict__ lse_part,
-                                                                            __nv_bfloat16* __restrict__ out,
-                                                                            const int32_t* __restrict__ seq_lens,
-                                                                            int Hq, int max_blocks, int window,
-                                                                            int splits, int D) {
-  __shared__ float m_s[kCombineWarps];
-  __shared__ float den_s[kCombineWarps];
-  __shared__ float acc_s[kCombineWarps][33];
-  grid_launch_dependents();  // the next call's partial kernel may start its setup
+template <int NW>
+__global__ void __launch_bounds__(NW * 32) decode_combine_kernel(const float* __restrict__ o_part,
+                                                                 const float* __restrict__ lse_part,
+                                                                 __nv_bfloat16* __restrict__ out, int S, int D) {
+  static_assert(NW >= 1 && NW <= 32, "one lane per warp in the final merge");
+  __shared__ float m_s[NW];
+  __shared__ float den_s[NW];
+  __shared__ float acc_s[NW][33];
+  grid_dependency_wait();  // the partial kernel's writes are visible past this point
+  // the next call's partial kernel may now start its setup (not earlier: its
+  // CTAs would wait beside this call's partial CTAs, the slowest of which
+  // set the call's time)
+  grid_launch_dependents();
   const int row = blockIdx.x;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int d = blockIdx.y * 32 + lane;
-  const float* lp = lse_part + static_cast<size_t>(row) * splits * kNW;
-  const float* op = o_part + static_cast<size_t>(row) * splits * kNW * D + d;
-  // only the ranges that hold pages wrote partials.  seq_lens is read before
-  // the wait: the partial kernel does not write it, and this grid launches
-  // only after the kernels before the partial kernel have completed.
-  const int L = seq_len_of(seq_lens, row / Hq, max_blocks, nullptr, false);
-  const int S = split_pages(L, window, splits).active * kNW;
-  grid_dependency_wait();  // the partial kernel's writes are visible past this point
+  const float* lp = lse_part + static_cast<size_t>(row) * S;
+  const float* op = o_part + static_cast<size_t>(row) * S * D + d;
   float m = -INFINITY, den = 0.f, acc = 0.f;
-  for (int s0 = wid; s0 < S; s0 += kCombineWarps * kCombinePer) {
+  for (int s0 = wid; s0 < S; s0 += NW * kCombinePer) {
     float l[kCombinePer], o[kCombinePer];
 #pragma unroll
     for (int i = 0; i < kCombinePer; ++i) {
-      const int s = s0 + i * kCombineWarps;
+      const int s = s0 + i * NW;
       l[i] = s < S ? __ldg(lp + s) : -INFINITY;
       o[i] = s < S ? __ldg(op + s * D) : 0.f;  // S * D < 2^31: at most 65535 x 4 partials of 128 dims
     }
@@ -919,7 +912,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
   acc_s[wid][lane] = acc;
   __syncthreads();
   if (wid == 0) {
-    const float mw = m_s[lane];
+    const float mw = lane < NW ? m_s[lane] : -INFINITY;
     float M = mw;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -927,11 +920,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     if (M != -INFINITY) {
       // this lane's factor for warp `lane`, then a per-warp broadcast
       const float f = mw == -INFINITY ? 0.f : ex2(mw - M);
-      dd = den_s[lane] * f;
+      dd = lane < NW ? den_s[lane] * f : 0.f;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
 #pragma unroll 8
-      for (int k = 0; k < kCombineWarps; ++k) t = fmaf(__shfl_sync(0xffffffffu, f, k), acc_s[k][lane], t);
+      for (int k = 0; k < NW; ++k) t = fmaf(__shfl_sync(0xffffffffu, f, k), acc_s[k][lane], t);
     }
     out[static_cast<size_t>(row) * D + d] = __float2bfloat16_rn(dd > 0.f ? t / dd : 0.f);
   }
@@ -1012,11 +1005,24 @@ kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream
   if (e != cudaSuccess) return cuda_status(e, "decode partial launch");
   if (q.direct) return KVQ_OK;
   cfg.gridDim = dim3(p.B * p.Hq, D / 32);
-  cfg.blockDim = dim3(kCombineWarps * 32);
   cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, decode_combine_kernel, static_cast<const float*>(p.o_part),
-                         static_cast<const float*>(p.lse_part), out, p.seq_lens, p.Hq, p.max_blocks, p.window,
-                         p.num_splits, D);
+  // warps per combine CTA: enough for the row's partials in one pass
+  const int parts = p.num_splits * kNW;
+  const float* op = p.o_part;
+  const float* lp = p.lse_part;
+  if (parts <= 4 * kCombinePer) {
+    cfg.blockDim = dim3(4 * 32);
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<4>, op, lp, out, parts, D);
+  } else if (parts <= 8 * kCombinePer) {
+    cfg.blockDim = dim3(8 * 32);
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<8>, op, lp, out, parts, D);
+  } else if (parts <= 16 * kCombinePer) {
+    cfg.blockDim = dim3(16 * 32);
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<16>, op, lp, out, parts, D);
+  } else {
+    cfg.blockDim = dim3(32 * 32);
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<32>, op, lp, out, parts, D);
+  }
   return cuda_status(e, "decode combine launch");
 }
 

@@ -214,7 +214,8 @@ size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P, int max_b
  * overlap the preceding kernel on the stream, and neither touches global
  * memory before that kernel has completed.  A grid smaller than the GPU's
  * resident capacity asks for more shared memory per CTA than it uses, so
- * that its CTAs spread over the SMs.
+ * that its CTAs spread over the SMs; the combine's CTAs have as many warps
+ * as the partials of a row need.
  * Accumulation: scores and P.V products are accumulated by tensor-core MMAs
  * into fresh FP32 registers per page of 16 tokens, then added into a running
  * FP32 sum (first level), and ranges are merged in FP32 (second level).
