@@ -625,7 +625,7 @@ def conc8_leg(device, layers=4, reps=20):
     gbs = byts / (us * 1e-6) / 1e9
     return {"workload": cfg.name, "lengths": lengths, "us_per_call": round(us, 3), "bytes_per_call": byts,
             "kv_gbs": round(gbs, 1), "frac_hbm": round(gbs / peak, 4), "peak_gbs": peak, "peak_source": src,
-            "splits": kvq.kvq_decode_num_splits(len(lengths), hkv, bt.shape[1]),
+            "splits": kvq.kvq_decode_num_splits(len(lengths), hkv, bt.shape[1], head_dim=d),
             "timing": f"{reps} replays of a CUDA graph of {layers} decode calls on distinct caches"}
 
 

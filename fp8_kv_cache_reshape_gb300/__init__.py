@@ -65,7 +65,7 @@ lib.kvq_reshape_and_cache.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i
 lib.kvq_quantize_query.restype = _i
 lib.kvq_quantize_query.argtypes = [_p, _p, _p, _i64, _p]
 lib.kvq_decode_num_splits.restype = _i
-lib.kvq_decode_num_splits.argtypes = [_i, _i, _i, _i, _i, _i]
+lib.kvq_decode_num_splits.argtypes = [_i, _i, _i, _i, _i, _i, _i]
 lib.kvq_decode_workspace_size.restype = _sz
 lib.kvq_decode_workspace_size.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i]
 lib.kvq_paged_decode_attention.restype = _i
@@ -213,8 +213,8 @@ def kvq_quantize_query(q, q8, q_scale, stream=None):
            "kvq_quantize_query")
 
 
-def kvq_decode_num_splits(B, Hkv, max_blocks, window=-1, num_splits=0):
-    return lib.kvq_decode_num_splits(B, Hkv, PAGE, max_blocks, window, num_splits)
+def kvq_decode_num_splits(B, Hkv, max_blocks, window=-1, num_splits=0, head_dim=128):
+    return lib.kvq_decode_num_splits(B, Hkv, head_dim, PAGE, max_blocks, window, num_splits)
 
 
 def kvq_decode_workspace_size(B, Hq, Hkv, D, max_blocks, window=-1, num_splits=0):

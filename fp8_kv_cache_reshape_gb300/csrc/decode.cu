@@ -91,9 +91,16 @@ struct Geo {
 };
 
 constexpr int kNW = 4;     // consumer warps per CTA
-constexpr int kCtasPerSm = 3;
+// Resident CTAs per SM: 3, and 4 at head dim 64, whose stages carry half the
+// bytes for the same per-stage work (the softmax of 32 tokens), so more
+// consumer warps per SM keep the pages streaming.
+template <int D>
+constexpr int ctas_per_sm() {
+  return D == 64 ? 4 : 3;
+}
+inline int ctas_per_sm_of(int D) { return D == 64 ? ctas_per_sm<64>() : ctas_per_sm<128>(); }
 
-// As many pages in flight per CTA as fit beside kCtasPerSm CTAs on one SM
+// As many pages in flight per CTA as fit beside ctas_per_sm() CTAs on one SM
 // (228 KiB of shared memory per SM, 1 KiB of it reserved per CTA, a few
 // hundred bytes of barriers), in a multiple of kNW stages: the consumers
 // take stages round-robin, so with NST % NW == 0 every ring slot is always
@@ -114,13 +121,17 @@ constexpr int v_stride() {
 }
 
 constexpr int kSmemPerSm = 228 * 1024;
-constexpr int kRingBudget = kSmemPerSm / kCtasPerSm - 1024 - 512;
-// Dynamic shared memory that lets at most 1 or 2 CTAs reside on an SM (the
-// next count would overrun the SM's budget with the 1 KB each CTA reserves).
-constexpr int kSpreadSmem[2] = {kSmemPerSm / 2 - 1024 + 16, kSmemPerSm / 3 - 1024 + 16};
+template <int D>
+constexpr int ring_budget() {
+  return kSmemPerSm / ctas_per_sm<D>() - 1024 - 512;
+}
+// Dynamic shared memory that lets at most n CTAs reside on an SM (n + 1
+// would overrun the SM's budget with the 1 KB each CTA reserves).
+constexpr int spread_smem(int n) { return kSmemPerSm / (n + 1) - 1024 + 16; }
 template <int D, bool FP8, bool PT = false>
 constexpr int stages_for() {
-  constexpr int n = (kRingBudget / stage_stride<D, FP8, PT>()) > 32 ? 32 : (kRingBudget / stage_stride<D, FP8, PT>());
+  constexpr int fit = ring_budget<D>() / stage_stride<D, FP8, PT>();
+  constexpr int n = fit > 32 ? 32 : fit;
   return (n / kNW) * kNW < kNW ? kNW : (n / kNW) * kNW;
 }
 
@@ -128,14 +139,14 @@ template <int D, bool FP8, int NST, bool PT = false>
 constexpr size_t decode_smem_bytes() {
   return size_t(NST) * stage_stride<D, FP8, PT>() + (2 * NST + 1) * sizeof(uint64_t) + NST * sizeof(int) + 16;
 }
-// kCtasPerSm CTAs of every instantiation fit on one SM
-static_assert(kCtasPerSm * (decode_smem_bytes<128, true, stages_for<128, true>()>() + 1024) <= kSmemPerSm, "smem");
-static_assert(kCtasPerSm * (decode_smem_bytes<64, true, stages_for<64, true>()>() + 1024) <= kSmemPerSm, "smem");
-static_assert(kCtasPerSm * (decode_smem_bytes<128, false, stages_for<128, false>()>() + 1024) <= kSmemPerSm, "smem");
-static_assert(kCtasPerSm * (decode_smem_bytes<64, false, stages_for<64, false>()>() + 1024) <= kSmemPerSm, "smem");
-static_assert(kCtasPerSm * (decode_smem_bytes<128, true, stages_for<128, true, true>(), true>() + 1024) <= kSmemPerSm,
+// ctas_per_sm() CTAs of every instantiation fit on one SM
+static_assert(ctas_per_sm<128>() * (decode_smem_bytes<128, true, stages_for<128, true>()>() + 1024) <= kSmemPerSm, "smem");
+static_assert(ctas_per_sm<64>() * (decode_smem_bytes<64, true, stages_for<64, true>()>() + 1024) <= kSmemPerSm, "smem");
+static_assert(ctas_per_sm<128>() * (decode_smem_bytes<128, false, stages_for<128, false>()>() + 1024) <= kSmemPerSm, "smem");
+static_assert(ctas_per_sm<64>() * (decode_smem_bytes<64, false, stages_for<64, false>()>() + 1024) <= kSmemPerSm, "smem");
+static_assert(ctas_per_sm<128>() * (decode_smem_bytes<128, true, stages_for<128, true, true>(), true>() + 1024) <= kSmemPerSm,
               "smem");
-static_assert(kCtasPerSm * (decode_smem_bytes<64, true, stages_for<64, true, true>(), true>() + 1024) <= kSmemPerSm,
+static_assert(ctas_per_sm<64>() * (decode_smem_bytes<64, true, stages_for<64, true, true>(), true>() + 1024) <= kSmemPerSm,
               "smem");
 
 struct ItemRange {
@@ -205,7 +216,7 @@ constexpr int kPresent0 = 1, kPresent1 = 2, kBad0 = 4, kBad1 = 8;
 // AP: the append entry point's instantiation (the new token's cache write);
 // the plain decode is compiled without it.
 template <int D, bool FP8, int NW, int NST, bool E5, bool PT, bool SL, bool AP = false>
-__global__ void __launch_bounds__((NW + 1) * 32, 3) decode_partial_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partial_kernel(const __grid_constant__ DecodeParams p) {
   using G = Geo<D, FP8>;
   static_assert(NST % NW == 0 && NST >= NW, "each ring slot must belong to one consumer warp");
   static_assert(FP8 || !PT, "per-token scales apply to FP8 caches");
@@ -939,7 +950,7 @@ int decode_pages(int P, int max_blocks, int window) {
   return pages < 1 ? 1 : pages;
 }
 
-void split_plan(int B, int Hkv, int P, int max_blocks, int window, int num_splits, int* S_out, int* pps_out) {
+void split_plan(int B, int Hkv, int D, int P, int max_blocks, int window, int num_splits, int* S_out, int* pps_out) {
   const int pages = decode_pages(P, max_blocks, window);
   int S;
   if (num_splits > 0) {
@@ -947,7 +958,7 @@ void split_plan(int B, int Hkv, int P, int max_blocks, int window, int num_split
   } else {
     // at most one item per resident CTA: a second, partial wave of items would
     // take as long as the first
-    const long target = static_cast<long>(kCtasPerSm) * sm_count();
+    const long target = static_cast<long>(ctas_per_sm_of(D)) * sm_count();
     const long pairs = static_cast<long>(B) * Hkv;
     S = static_cast<int>(target / pairs);
     const int max_s = (pages + 15) / 16;  // at least 16 pages per split
@@ -970,12 +981,13 @@ kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(configured_mask & (1 << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpreadSmem[0]);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, spread_smem(1));
     if (e != cudaSuccess) return cuda_status(e, "decode: set shared memory size");
     configured_mask |= 1 << (dev & 31);
   }
   const int sms = sm_count();
-  int grid = kCtasPerSm * sms;
+  constexpr int CPS = ctas_per_sm<D>();
+  int grid = CPS * sms;
   DecodeParams q = p;
   q.out = out;
   // one page range per (sequence, KV head) and every item in its own CTA: the
@@ -988,7 +1000,7 @@ kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream
   // holds some of them (programmatic launch, below).
   const int per_sm = (grid + sms - 1) / sms;
   size_t dyn = smem;
-  if (per_sm < kCtasPerSm && kSpreadSmem[per_sm - 1] > dyn) dyn = kSpreadSmem[per_sm - 1];
+  if (per_sm < CPS && static_cast<size_t>(spread_smem(per_sm)) > dyn) dyn = spread_smem(per_sm);
   // both kernels are programmatic dependents of what precedes them on the
   // stream: their launch and setup overlap its tail
   cudaLaunchAttribute attr[1];
@@ -1032,10 +1044,10 @@ kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream
 
 using namespace kvq;
 
-extern "C" int kvq_decode_num_splits(int B, int Hkv, int P, int max_blocks, int window, int num_splits) {
-  if (B < 1 || Hkv < 1 || P < 1 || max_blocks < 1 || num_splits < 0) return 0;
+extern "C" int kvq_decode_num_splits(int B, int Hkv, int D, int P, int max_blocks, int window, int num_splits) {
+  if (B < 1 || Hkv < 1 || D < 1 || P < 1 || max_blocks < 1 || num_splits < 0) return 0;
   int S, pps;
-  split_plan(B, Hkv, P, max_blocks, window, num_splits, &S, &pps);
+  split_plan(B, Hkv, D, P, max_blocks, window, num_splits, &S, &pps);
   return S;
 }
 
@@ -1043,7 +1055,7 @@ extern "C" size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P
                                             int num_splits) {
   if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || P < 1 || max_blocks < 1 || num_splits < 0) return 0;
   int S, pps;
-  split_plan(B, Hkv, P, max_blocks, window, num_splits, &S, &pps);
+  split_plan(B, Hkv, D, P, max_blocks, window, num_splits, &S, &pps);
   const size_t rows = static_cast<size_t>(B) * Hq * S * kNW;  // one partial per consumer warp
   const size_t o_bytes = rows * D * sizeof(float);
   return o_bytes + ((rows * sizeof(float) + 15) / 16) * 16;
@@ -1090,7 +1102,7 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
       !aligned(out, 4))
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: misaligned pointer");
   int S, pps;
-  split_plan(B, Hkv, P, max_blocks, window, num_splits, &S, &pps);
+  split_plan(B, Hkv, D, P, max_blocks, window, num_splits, &S, &pps);
   const size_t need = kvq_decode_workspace_size(B, Hq, Hkv, D, P, max_blocks, window, num_splits);
   if (workspace_bytes < need)
     return fail(KVQ_ERR_INVALID_ARG, "paged_decode: workspace %zu bytes < %zu needed", workspace_bytes, need);

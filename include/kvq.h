@@ -182,10 +182,11 @@ kvq_status_t kvq_quantize_query(const void* q, uint8_t* q8, const float* q_scale
 
 /*
  * Split-KV plan for kvq_paged_decode_attention.  num_splits = 0 asks for the
- * library's choice for this GPU; the function returns the number of splits
- * that a call with the same arguments will use (>= 1), or 0 on bad input.
+ * library's choice for this GPU (one wave of resident CTAs: 3 per SM, 4 at
+ * head dim D = 64); the function returns the number of splits that a call
+ * with the same arguments will use (>= 1), or 0 on bad input.
  */
-int kvq_decode_num_splits(int B, int Hkv, int P, int max_blocks, int window, int num_splits);
+int kvq_decode_num_splits(int B, int Hkv, int D, int P, int max_blocks, int window, int num_splits);
 
 /* Workspace bytes a decode call with these arguments needs (float32
  * partial outputs [B][Hq][S][4][D] and log-sum-exps [B][Hq][S][4]: one per
