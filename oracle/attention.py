@@ -351,6 +351,106 @@ def prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
     return out
 
 
+def prefill_per_token_coef(q_scale, sm_scale):
+    """b = fl32(fl32(q_scale * sm_scale) * log2(e)): the part of the score
+    coefficient shared by all keys when K scales are per token."""
+    return np.float32(np.float32(_f32(q_scale) * _f32(sm_scale)) * LOG2E_F32)
+
+
+def pow2_ceil(x):
+    """2^ceil(log2 x) for x > 0 (exact, from the float's exponent and
+    mantissa); 1.0 for x <= 0."""
+    x = float(x)
+    if not x > 0.0:
+        return 1.0
+    m, e = math.frexp(x)  # x = m * 2^e, m in [1/2, 1)
+    return math.ldexp(1.0, e - 1) if m == 0.5 else math.ldexp(1.0, e)
+
+
+def prefill_per_token(q8, q_scale, k_cache, v_cache, kv_scale_cache, block_table,
+                      cu_seqlens_q, seq_lens, sm_scale, causal=True, mode="final",
+                      rows=None, tile=128, chunk=64, cache_dtype=FP8):
+    """Chunked prefill over a cache written with per-token dynamic scales
+    (kv_cache.reshape_and_cache_per_token; kv_scale_cache [nb][Hkv][2][P]):
+    key j dequantizes as decode(k8_j) * sk_j and decode(v8_j) * sv_j.
+
+    Sources: "FP8 and KV cache", section "Dynamic or static scale" (one
+    scale per token); "FP8 quantization and long-context inference" (gtnt),
+    section 2.2 (a scale for every new token); the prefill of "The state of
+    FP8 KV-cache and attention quantization in vLLM" (FP8 QK^T and P.V).
+
+    Modes:
+    * "pure": softmax(q_hat . K_hat^T * sm_scale) . V_hat with the exact
+      dequantized values and natural exponentials.
+    * "final" (the reading the CUDA path declares): per key the score
+      coefficient is c_j = fl32(sk_j * b), b = prefill_per_token_coef, and
+      s2_j = (sum_d q8_d k8_jd) * c_j in base-2 units; M = ceil(max_j s2_j)
+      (the integer stabilizer of prefill); p_j = 2^(s2_j - M).  The K scales
+      are thus inside the scores; the V scales run along the P.V
+      contraction, so they enter the FP8 probabilities: in each group of
+      `tile` keys (aligned at key 0) with C_t = 2^ceil(log2 max sv_j) over
+      the group's cached keys, the P.V operand is Pw_j = e4m3(fl32(fl32(p_j
+      * 256) * (sv_j / C_t))) (sv_j / C_t exact: a power-of-two division),
+      and the row sum takes the unweighted Pu_j = e4m3(fl32(p_j * 256)):
+      o = sum_t C_t sum_{j in t} decode(Pw_j) v8_j / sum_j decode(Pu_j).
+      With sv_j = C_t (all V scales of a group one power of two) Pw = Pu
+      and this is prefill(mode="final") with the per-head scales.
+    Returns out float64 [Tq][Hq][D] (rows not in `rows` stay NaN).
+    """
+    if mode not in ("pure", "final"):
+        raise ValueError(f"unknown mode {mode!r}")
+    q8 = np.asarray(q8, dtype=np.uint8)
+    Tq, Hq, D = q8.shape
+    Hkv = k_cache.shape[1]
+    g = Hq // Hkv
+    out = np.full((Tq, Hq, D), np.nan, dtype=np.float64)
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    B = len(cu) - 1
+    seq_of = np.zeros(Tq, dtype=np.int64)
+    for b in range(B):
+        seq_of[cu[b]:cu[b + 1]] = b
+    if rows is None:
+        rows = [(t, h) for t in range(Tq) for h in range(Hq)]
+    by_seq_head = {}
+    for t, h in rows:
+        by_seq_head.setdefault((int(seq_of[t]), h // g), []).append((int(t), int(h)))
+    qs = float(np.float32(q_scale))
+    bcoef = np.float32(prefill_per_token_coef(q_scale, sm_scale))
+    for (b, kv), items in by_seq_head.items():
+        L = int(seq_lens[b])
+        nq = int(cu[b + 1] - cu[b])
+        pos = np.arange(L)
+        kk, vv = gather_tokens(k_cache, v_cache, block_table[b], pos, kv)
+        k_codes = codec(cache_dtype).decode(kk)
+        v_codes = codec(cache_dtype).decode(vv)
+        sk = gather_scales(kv_scale_cache[:, :, 0], block_table[b], pos, kv).astype(np.float32)
+        sv = gather_scales(kv_scale_cache[:, :, 1], block_table[b], pos, kv).astype(np.float32)
+        c = (sk * bcoef).astype(np.float32).astype(np.float64)          # [L]
+        C = np.array([pow2_ceil(np.max(sv[t0:t0 + tile])) for t0 in range(0, L, tile)])
+        w = (sv.astype(np.float64) / np.repeat(C, tile)[:L]).astype(np.float32)  # exact
+        for r0 in range(0, len(items), chunk):
+            part = items[r0:r0 + chunk]
+            last = np.array([(L - nq + (t - int(cu[b]))) if causal else L - 1 for t, _ in part])
+            n = int(last.max()) + 1
+            qc = np.stack([e4m3.decode(q8[t, h]) for t, h in part])
+            visible = np.arange(n)[None, :] <= last[:, None]
+            if mode == "pure":
+                s = (qc * qs) @ (k_codes[:n] * sk[:n, None].astype(np.float64)).T * float(np.float32(sm_scale))
+                s = np.where(visible, s, -np.inf)
+                m = np.max(s, axis=1, keepdims=True)
+                p = np.exp(s - m)
+                o = (p @ (v_codes[:n] * sv[:n, None].astype(np.float64))) / p.sum(axis=1, keepdims=True)
+            else:
+                s2 = np.where(visible, (qc @ k_codes[:n].T) * c[None, :n], -np.inf)
+                p256 = (np.exp2(s2 - stabilizer(s2)) * 256.0).astype(np.float32)
+                pu = e4m3.decode(e4m3.encode(p256))
+                pw = e4m3.decode(e4m3.encode((p256 * w[None, :n]).astype(np.float32)))
+                o = (pw * np.repeat(C, tile)[None, :n]) @ v_codes[:n] / pu.sum(axis=1, keepdims=True)
+            for i, (t, h) in enumerate(part):
+                out[t, h] = o[i]
+    return out
+
+
 def decode_reduced_accumulator(q, k_cache, v_cache, k_scale, v_scale, block_table,
                                seq_lens, sm_scale, mantissa_bits=14):
     """Planted-defect variant used only to show the long-context test is
