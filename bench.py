@@ -446,10 +446,11 @@ def prefill_flops(new=PF_NEW, cached=PF_CACHED, hq=HQ, d=D):
     return pairs * hq * 4 * d
 
 
-def prefill_leg(device, reps=10, accumulation=None, head_dim=D, cache_dtype="fp8_e4m3"):
+def prefill_leg(device, reps=10, accumulation=None, head_dim=D, cache_dtype="fp8_e4m3", per_token=False):
     """Chunked causal prefill of 4,096 new tokens on 28,672 cached FP8
-    tokens (32/8 heads, head_dim 128, or 256; E4M3 or E5M2 cache): TFLOP/s
-    of kvq_prefill_attention."""
+    tokens (32/8 heads, head_dim 128, or 256; E4M3 or E5M2 cache; per-head
+    or, with per_token, per-token scales): TFLOP/s of kvq_prefill_attention
+    (kvq_prefill_attention_per_token)."""
     import torch
     import fp8_kv_cache_reshape_gb300 as kvq
     import workloads as W
@@ -464,8 +465,12 @@ def prefill_leg(device, reps=10, accumulation=None, head_dim=D, cache_dtype="fp8
     fmt_max = W.E5M2_MAX if cache_dtype == "fp8_e5m2" else W.E4M3_MAX
     ks, vs = W.calibrate_amax(k, fmt_max), W.calibrate_amax(v, fmt_max)
     qs = (q.float().abs().amax() / 448.0).reshape(1).to(torch.float32)
-    kd, vd = kvq.alloc_kv_cache(nb, HKV, head_dim, cache_dtype=cache_dtype, device=device, fill=0)
-    kvq.kvq_reshape_and_cache(k, v, slots, kd, vd, ks, vs, cache_dtype=cache_dtype)
+    kd, vd = kvq.alloc_kv_cache(nb, HKV, head_dim, cache_dtype=cache_dtype, device=device, fill=0,
+                                per_token=per_token)
+    if per_token:
+        kvq.kvq_reshape_and_cache_per_token(k, v, slots, kd, vd, cache_dtype=cache_dtype)
+    else:
+        kvq.kvq_reshape_and_cache(k, v, slots, kd, vd, ks, vs, cache_dtype=cache_dtype)
     q8 = torch.empty(q.shape, dtype=torch.uint8, device=device)
     kvq.kvq_quantize_query(q, q8, qs)
     out = torch.empty(q.shape, dtype=torch.bfloat16, device=device)
@@ -475,6 +480,11 @@ def prefill_leg(device, reps=10, accumulation=None, head_dim=D, cache_dtype="fp8
     st = torch.zeros(1, dtype=torch.int32, device=device)
 
     def call():
+        if per_token:
+            kvq.kvq_prefill_attention_per_token(q8, qs, kd, vd, btd, cu, sl, out, max_q_tokens=PF_NEW,
+                                                sm_scale=1.0 / math.sqrt(head_dim), cache_dtype=cache_dtype,
+                                                dev_status=st)
+            return
         kvq.kvq_prefill_attention(q8, qs, kd, vd, ks, vs, btd, cu, sl, out, max_q_tokens=PF_NEW,
                                   sm_scale=1.0 / math.sqrt(head_dim), dev_status=st, accumulation=accumulation,
                                   cache_dtype=cache_dtype)
@@ -489,8 +499,9 @@ def prefill_leg(device, reps=10, accumulation=None, head_dim=D, cache_dtype="fp8
     flops = prefill_flops(d=head_dim)
     tf = flops / (ms * 1e-3) / 1e12
     name = ("llama31_8b_chunked_prefill_4k_on_28k" + ("" if head_dim == 128 else f"_head_dim_{head_dim}") +
-            ("" if cache_dtype == "fp8_e4m3" else "_" + cache_dtype))
+            ("" if cache_dtype == "fp8_e4m3" else "_" + cache_dtype) + ("_per_token_scales" if per_token else ""))
     return {"workload": name, "ms": round(ms, 4), "flops": flops, "head_dim": head_dim, "cache_dtype": cache_dtype,
+            "per_token_scales": per_token,
             "accumulation": accumulation or ("two_level" if head_dim == 128 else "single_level"),
             "bound": "tensor", "achieved": round(tf, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
             "frac": round(tf / fp8_peak, 4),
@@ -1005,6 +1016,7 @@ def ours_arm(args, rank, world, local_rank):
     pf = clocked(local_rank, prefill_leg, device) if legs and not args.no_prefill else None
     if pf is not None and not args.no_e5m2:
         pf["e5m2_cache"] = clocked(local_rank, prefill_leg, device, cache_dtype="fp8_e5m2")
+        pf["per_token_scales"] = clocked(local_rank, prefill_leg, device, per_token=True)
     no_cmp = not legs or args.no_sweep
     bf = None if (no_cmp or args.no_bf16) else clocked(local_rank, format_compare, sweep, device, "bf16")
     e5 = None if (no_cmp or args.no_e5m2) else clocked(local_rank, format_compare, sweep, device, "fp8_e5m2")

@@ -92,6 +92,9 @@ lib.kvq_prefill_attention_acc.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p
 lib.kvq_prefill_attention_dtype.restype = _i
 lib.kvq_prefill_attention_dtype.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
                                             _f, _i, _p, _p, _i]
+lib.kvq_prefill_attention_per_token.restype = _i
+lib.kvq_prefill_attention_per_token.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
+                                                _f, _i, _i, _p, _p]
 lib.kvq_prefill_attention.restype = _i
 lib.kvq_prefill_attention.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i64, _i,
                                       _f, _i, _p, _p]
@@ -332,4 +335,25 @@ def kvq_prefill_attention(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block
         _check(lib.kvq_prefill_attention(*args), "kvq_prefill_attention")
     else:
         _check(lib.kvq_prefill_attention_acc(*args, _acc_code(accumulation)), "kvq_prefill_attention_acc")
+    return out
+
+
+def kvq_prefill_attention_per_token(q8, q_scale, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, out,
+                                    max_q_tokens, num_blocks=None, sm_scale=None, causal=True,
+                                    cache_dtype="fp8_e4m3", dev_status=None, stream=None):
+    """Chunked causal prefill over a cache written by
+    kvq_reshape_and_cache_per_token; writes out (bf16 [Tq][Hq][D])."""
+    Tq, Hq, D = q8.shape
+    B = cu_seqlens_q.numel() - 1
+    Hkv = k_cache.shape[1]
+    if num_blocks is None:
+        num_blocks = k_cache.shape[0]
+    _check_per_token_cache(k_cache, v_cache, Hkv, D)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    _check(lib.kvq_prefill_attention_per_token(
+        _ptr(q8), _ptr(q_scale), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(cu_seqlens_q),
+        _ptr(seq_lens), _ptr(out), B, Hq, Hkv, D, PAGE, block_table.shape[1], num_blocks, int(max_q_tokens),
+        float(sm_scale), 1 if causal else 0, _dtype_code(cache_dtype), _ptr(dev_status), _stream(stream)),
+        "kvq_prefill_attention_per_token")
     return out

@@ -81,24 +81,33 @@ constexpr uint32_t TMEM_COLS = 512;
 // Shared-memory plan for one head dimension.  Q and the K tile are stored as
 // HD / 128 planes of 128-byte rows (dims 128h .. 128h + 127), each a canonical
 // SWIZZLE_128B K-major operand; V pages stay [d][16 slots].
-template <int HD_>
+// PT: per-token scales; each V page carries its scale tail (16 K scales, 16 V
+// scales) and lands with it, so V pages sit VPAGE_B = PAGE_B + 128 bytes
+// apart in the stage (the P.V operand's stride along the keys says so).
+template <int HD_, bool PT = false>
 struct Geo {
   static constexpr int HD = HD_;
   static constexpr int NKV = HD == 128 ? 4 : 2;  // K/V stages (2 x 64 KiB at head_dim 256)
   static_assert(NKV % NPROD == 0, "each stage belongs to one producer, which refills it in tile order");
-  static constexpr int PAGE_B = kPage * HD;      // bytes per page (K or V)
-  static constexpr int TILE_B = TK * HD;         // bytes per K tile (= V tile)
+  static constexpr int PAGE_B = kPage * HD;      // bytes per page (K or V codes)
+  static constexpr int VPAGE_B = PAGE_B + (PT ? kScaleTailBytes : 0);  // a V page in the stage
+  static constexpr int TILE_B = TK * HD;         // bytes per K tile
+  static constexpr int TILE_V = (TK / kPage) * VPAGE_B;  // bytes per V tile
   static constexpr int PLANE_Q = TQ * PLANE;     // one plane of Q
   static constexpr int PLANE_K = TK * PLANE;     // one plane of a K tile
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + TQ * HD;
-  static constexpr int STAGE_B = 2 * TILE_B;     // K tile + V tile
+  static constexpr int STAGE_B = TILE_B + TILE_V;  // K tile + V tile
   static constexpr int OFF_BAR = OFF_KV + NKV * STAGE_B;
   static constexpr int OFF_XCH = OFF_BAR + 512;  // row max exchange [2 tiles][NPART][TQ]
   static constexpr int OFF_ALPHA = OFF_XCH + 2 * NPART * TQ * 4;  // [4][TQ] rescale factors, softmax -> correction
-  static constexpr int OFF_ONES = OFF_ALPHA + 4 * TQ * 4;          // E4M3 ones: the B operand of the row-sum MMA
+  // PT: [4] the tiles' V-scale bounds C_t (softmax -> correction), then the
+  // largest V scale of each part's keys [2 tiles][NPART] (softmax exchange)
+  static constexpr int OFF_CT = OFF_ALPHA + 4 * TQ * 4;
+  static constexpr int OFF_ONES = OFF_CT + 64;                     // E4M3 ones: the B operand of the row-sum MMA
   static constexpr int SMEM_BYTES = OFF_ONES + 1024 + 1024;        // + alignment slack
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+  static_assert(VPAGE_B % 16 == 0 && OFF_ONES % 16 == 0, "16-byte aligned operands");
 };
 
 struct PrefillParams {
@@ -282,11 +291,19 @@ KVQ_DEVINL Job make_job(const PrefillParams& p) {
 // Head dim 256 needs it: two-level would need 2 x 256 TMEM columns for O.
 // E5: the caches hold E5M2 codes: K (the B operand of Q K^T) and V (the B
 // operand of P.V) are E5M2, Q and P stay E4M3.
-template <int HD, bool SL, bool E5 = false>
+// PT: per-token scales in the V pages' tails.  Scores are s2 = raw *
+// fl32(sk * b), b = fl32(fl32(q_scale * sm_scale) * log2 e); P.V runs on the
+// weighted codes e4m3(fl32(2^(s2 - M + 8) * (sv / C_t))), C_t = 2^ceil(log2
+// max sv) over the tile's cached keys, and the row sums on the unweighted
+// codes e4m3(2^(s2 - M + 8)); the correction warps carry O_run / C_t, so
+// every rescale stays a power of two.
+template <int HD, bool SL, bool E5 = false, bool PT = false>
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
-  using G = Geo<HD>;
+  using G = Geo<HD, PT>;
   static_assert(HD == 128 || (HD == 256 && SL), "head_dim 256 runs with single-level accumulation");
+  static_assert(!PT || (HD == 128 && !SL), "per-token scales: head_dim 128, two-level accumulation");
   constexpr int NKV = G::NKV, PAGE_B = G::PAGE_B, TILE_B = G::TILE_B, STAGE_B = G::STAGE_B;
+  constexpr int VPAGE_B = G::VPAGE_B;
   constexpr int OFF_Q = G::OFF_Q, OFF_KV = G::OFF_KV, OFF_XCH = G::OFF_XCH;
   using BarsN = Bars<NKV>;
   static_assert(sizeof(BarsN) <= 512, "barrier block");
@@ -387,20 +404,20 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         if (load_mask != 0xFFu) {
           for (int pg = 0; pg < TK / kPage; ++pg) {
             if (load_mask & (1u << pg)) continue;
-            uint4* vz = reinterpret_cast<uint4*>(vs + pg * PAGE_B);
+            uint4* vz = reinterpret_cast<uint4*>(vs + pg * VPAGE_B);
             for (int i = lane; i < PAGE_B / 16; i += 32) {
               // K: the page's kPage rows in each plane
               const int pl = i / (kPage * PLANE / 16), w = i % (kPage * PLANE / 16);
               reinterpret_cast<uint4*>(ks + pl * G::PLANE_K + pg * kPage * PLANE)[w] = make_uint4(0, 0, 0, 0);
-              vz[i] = make_uint4(0, 0, 0, 0);
             }
+            for (int i = lane; i < VPAGE_B / 16; i += 32) vz[i] = make_uint4(0, 0, 0, 0);  // codes (and scales)
           }
           fence_proxy_async_smem();  // the zeros, before the tensor cores read the stage
         }
         __syncwarp();
         if (lane == 0) {
           bars->stage_bad[st] = bad_mask & 0xFFu;
-          mbar_arrive_expect_tx(&bars->kv_full[st], 2u * PAGE_B * __popc(load_mask));
+          mbar_arrive_expect_tx(&bars->kv_full[st], static_cast<uint32_t>(PAGE_B + VPAGE_B) * __popc(load_mask));
         }
         __syncwarp();
         if (lane < TK / kPage && blk >= 0) {
@@ -410,7 +427,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
           for (int pl = 0; pl < HD / PLANE; ++pl)
             bulk_g2s(ks + pl * G::PLANE_K + lane * kPage * PLANE, p.k_cache + off + pl * kPage * PLANE, kPage * PLANE,
                      &bars->kv_full[st], policy_evict_last());
-          bulk_g2s(vs + lane * PAGE_B, p.v_cache + off, PAGE_B, &bars->kv_full[st], policy_evict_last());
+          const size_t voff = (static_cast<size_t>(blk) * p.Hkv + job.kvh) * VPAGE_B;  // PT: page + tail
+          bulk_g2s(vs + lane * VPAGE_B, p.v_cache + voff, VPAGE_B, &bars->kv_full[st], policy_evict_last());
         }
       }
       if (j < nkv && lane == 0) {  // abandoned: let this producer's issued copies land
@@ -472,18 +490,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
 #pragma unroll
           for (int kk = 0; kk < TK / 32; ++kk) {  // 32 keys = 2 V pages per MMA
             const uint32_t acc = (kk > 0 || (SL && j > 0)) ? 1u : 0u;
-            const uint64_t vdesc = desc_interleave(v_s + kk * 2 * PAGE_B, PAGE_B, 128);
+            const uint64_t vdesc = desc_interleave(v_s + kk * 2 * VPAGE_B, VPAGE_B, 128);
             // P for keys 32kk .. 32kk + 31: 8 columns at the start of part pt's slice of S_j
             const int pt = kk / KPP;
             umma_f8_ta(d, tmem + (j & 1) * TK + pt * (TK / NPART) + 8 * (kk - pt * KPP), vdesc, IDESC_O, acc);
           }
           // the tile's row sums of the same P8 codes, sum_k P8[row][k] in each of 16
-          // columns, into S_j's columns 32 .. 47 (already read by the softmax warps)
+          // columns, into S_j's columns 32 .. 47 (already read by the softmax warps);
+          // PT: of the unweighted codes, 16 columns after the weighted ones
+          constexpr int RS_SRC = PT ? 16 : 0;
 #pragma unroll
           for (int kk = 0; kk < TK / 32; ++kk) {
             const int pt = kk / KPP;
-            umma_f8_ta(tmem + (j & 1) * TK + 32, tmem + (j & 1) * TK + pt * (TK / NPART) + 8 * (kk - pt * KPP),
-                       ones_desc, IDESC_RS, kk > 0 ? 1u : 0u);
+            umma_f8_ta(tmem + (j & 1) * TK + 32,
+                       tmem + (j & 1) * TK + pt * (TK / NPART) + RS_SRC + 8 * (kk - pt * KPP), ones_desc, IDESC_RS,
+                       kk > 0 ? 1u : 0u);
           }
           umma_commit(&bars->o_full);
           umma_commit(&bars->kv_empty[st]);
@@ -514,6 +535,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
     const uint32_t o_tile = tmem + t_lane + 2 * TK;  // SL: O
     const uint32_t o_run = o_tile + HD;              // two-level only
     const float* alpha_s = reinterpret_cast<const float*>(smem + G::OFF_ALPHA);
+    const float* ct_s = reinterpret_cast<const float*>(smem + G::OFF_CT);  // PT: C_j of tile j in slot j % 4
+    float c_prev = 1.f;                                                     // PT: C of the last tile folded
     // the row sum of the rounded probabilities, in units of 2^8 p: the tensor
     // core's sums of each tile's P8 codes (S_j's columns 32 .. 47), rescaled
     // like the output
@@ -545,15 +568,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       }
       for (int j = 0; j < nkv && ok; ++j) {
         float alpha = 0.f;  // tile 0: O_run is zero
-        if (j > 0) {
+        float ratio = 1.f;  // PT: C_{j-1} / C_j, a power of two (O_run is kept in units of C_j)
+        if (j > 0 || PT) {
           if (!wait_all(&bars->a_full[j & 3], (j >> 2) & 1)) break;
-          alpha = alpha_s[(j & 3) * TQ + row];
+          if (j > 0) alpha = alpha_s[(j & 3) * TQ + row];
+          if constexpr (PT) {
+            const float c_j = ct_s[j & 3];
+            ratio = c_prev / c_j;
+            c_prev = c_j;
+          }
         }
         if (!wait_all(&bars->o_full, j & 1)) break;  // P.V of tile j is in O_tile
         tc_fence_after();
         l = fmaf(l, alpha, row_sum(j));
         tmem_wait_st();  // this thread's previous O_run update
-        const float2 a2 = make_float2(alpha, alpha);
+        const float am = PT ? alpha * ratio : alpha;
+        const float2 a2 = make_float2(am, am);
         // 32 columns of O_tile and of O_run per tensor-memory round trip (its
         // latency, not the arithmetic, sets the pace of this fold, and P.V of
         // the next tile waits for the last O_tile load)
@@ -612,11 +642,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       }
     }
     if (ok) {
-      // out = O * v_scale / l (both in units of 2^8 p)
+      // out = O * v_scale / l (both in units of 2^8 p); PT: O_run is in units
+      // of the last tile's C, and the V scales are inside it
       const float lt = l;
       const bool live_row = job.q0 + row < job.nq;
       const size_t out_row = (static_cast<size_t>(p.cu_seqlens_q[job.b]) + job.q0 + row) * p.Hq + job.h;
-      const float f = (lt > 0.f) ? p.v_scale[job.kvh] / lt : 0.f;
+      const float f = (lt > 0.f) ? (PT ? c_prev : p.v_scale[job.kvh]) / lt : 0.f;
       tmem_wait_st();
       const uint32_t o_out = SL ? o_tile : o_run;
       uint4* dst = reinterpret_cast<uint4*>(p.out + out_row * HD);
@@ -664,7 +695,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       fence_proxy_async_smem();
       mbar_arrive(&bars->q_full);
     }
-    const float coef = __fmul_rn(__fmul_rn(__fmul_rn(*p.q_scale, p.k_scale[job.kvh]), p.sm_scale), kLog2e);
+    // PT: the K scales multiply each score before the maximum (c_j = fl32(sk_j *
+    // bcoef)), and the exponent takes the scores as they are
+    const float bcoef = __fmul_rn(__fmul_rn(*p.q_scale, p.sm_scale), kLog2e);
+    const float coef =
+        PT ? 1.f : __fmul_rn(__fmul_rn(__fmul_rn(*p.q_scale, p.k_scale[job.kvh]), p.sm_scale), kLog2e);
+    float* ct_s = reinterpret_cast<float*>(smem + G::OFF_CT);  // PT: [4] C_j for the correction warps
+    float* xv = ct_s + 4;                                       // PT: [2 tiles][NPART] largest V scales
     const int tail = job.L % kPage;          // valid tokens in the last page (0 = full)
     const int last_page = (job.L - 1) / kPage;
 
@@ -700,6 +737,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       const bool tail_tile = tail != 0 && last_page / (TK / kPage) == j;  // holds the partial last page
       float sv[HC];
       float mx = -INFINITY;
+      float vmx = 0.f;  // PT: the largest V scale of this thread's cached keys
       uint32_t bad = 0;
       // S_j, then the stage's page flags and, for the last page, zeroing of its unused V slots
       if (wait_all(&bars->s_full[j & 1], (j >> 1) & 1) && wait_all(&bars->kv_full[st], (j / NKV) & 1)) {
@@ -708,7 +746,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         if (tail_tile) {
           // V rows (dims) row and row + 128 .. of the last page: slots past the sequence end
           for (int d = row + part * TQ; d < HD; d += NPART * TQ) {
-            uint8_t* vrow = smem + OFF_KV + st * STAGE_B + TILE_B + (last_page % (TK / kPage)) * PAGE_B + d * kPage;
+            uint8_t* vrow = smem + OFF_KV + st * STAGE_B + TILE_B + (last_page % (TK / kPage)) * VPAGE_B + d * kPage;
             for (int t = tail; t < kPage; ++t) vrow[fp8_v_slot(t)] = 0;
           }
         }
@@ -726,6 +764,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
 #pragma unroll
             for (int i = 0; i < 32; ++i) sv[32 * c + i] = __uint_as_float(v[c][i]);
           }
+        }
+        if constexpr (PT) {
+          // the scale tails of this thread's pages: K scales scale the scores; the
+          // largest V scale of the thread's cached keys goes to the exchange
+          float vm = 0.f;
+#pragma unroll
+          for (int pg = 0; pg < HC / kPage; ++pg) {
+            const float4* tl = reinterpret_cast<const float4*>(smem + OFF_KV + st * STAGE_B + TILE_B +
+                                                               (part * (HC / kPage) + pg) * VPAGE_B + PAGE_B);
+#pragma unroll
+            for (int i4 = 0; i4 < 4; ++i4) {
+              const float4 ks4 = tl[i4], vs4 = tl[4 + i4];
+              const float kk[4] = {ks4.x, ks4.y, ks4.z, ks4.w}, vv[4] = {vs4.x, vs4.y, vs4.z, vs4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int k = pg * 16 + 4 * i4 + e;
+                sv[k] = __fmul_rn(sv[k], __fmul_rn(kk[e], bcoef));
+                const bool cached = !tail_tile || key0 + k < job.L;  // slots past the end hold no scale
+                vm = fmaxf(vm, cached ? vv[e] : 0.f);
+              }
+            }
+          }
+          vmx = vm;
         }
         if (need_mask) {  // last tiles only; static indices keep sv in registers
           const int lim = kend - key0;  // columns k < lim are causally visible
@@ -757,6 +818,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         }
       }
       xmax[((j & 1) * NPART + part) * TQ + row] = mx;
+      if (PT && row == 0) xv[(j & 1) * NPART + part] = vmx;
       named_bar_sync(1, NSOFT * 32);
       if (ok) {
         // m and the maxima are raw scores; 2^(s - M) * 256 = 2^(raw * coef - (M - 8)),
@@ -767,12 +829,25 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         const float M_new = (m_new == -INFINITY) ? -INFINITY : ceilf(m_new * coef);
         const float nb = (m_new == -INFINITY) ? 0.f : 8.f - M_new;
         const float alpha = exp2_int(M - M_new);  // 0 on the first tile
+        // PT: C_j = 2^ceil(log2 max sv) over the tile's cached keys (1 if none)
+        float c_inv = 1.f;
+        if constexpr (PT) {
+          float vmax = 0.f;
+#pragma unroll
+          for (int pt = 0; pt < NPART; ++pt) vmax = fmaxf(vmax, xv[(j & 1) * NPART + pt]);
+          const uint32_t bits = __float_as_uint(vmax);
+          int e = static_cast<int>(bits >> 23) - 127 + ((bits & 0x7FFFFFu) != 0u ? 1 : 0);
+          e = vmax > 0.f ? (e < -126 ? -126 : e) : 0;
+          c_inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e, exact
+          if (row == 0 && part == 0) ct_s[j & 3] = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+        }
         if (part == 0) {  // for the correction warps
           alpha_s[(j & 3) * TQ + row] = alpha;
           mbar_arrive(&bars->a_full[j & 3]);
         }
         const float2 coef2 = make_float2(coef, coef), nb2 = make_float2(nb, nb);
-        uint32_t pw[4 * (HC / kPage)];  // this thread's P8 words (four keys each)
+        uint32_t pw[4 * (HC / kPage)];           // this thread's P8 words (four keys each); PT: weighted
+        uint32_t pu[PT ? 4 * (HC / kPage) : 1];  // PT: the unweighted words, for the row sums
 #pragma unroll
         for (int pg = 0; pg < HC / kPage; ++pg) {  // pages of 16 keys
           float q[16];
@@ -783,14 +858,38 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
             q[t + 1] = ex2(e.y);
           }
           // word w of a page holds keys 2w, 2w+1, 2w+8, 2w+9 (the V slot order)
+          auto words = [&](const float (&x)[16], uint32_t* out4) {
 #pragma unroll
-          for (int ww = 0; ww < 4; ++ww)
-            pw[4 * pg + ww] =
-                f32x2_to_e4m3x2(q[2 * ww], q[2 * ww + 1]) | (f32x2_to_e4m3x2(q[2 * ww + 8], q[2 * ww + 9]) << 16);
+            for (int ww = 0; ww < 4; ++ww)
+              out4[ww] =
+                  f32x2_to_e4m3x2(x[2 * ww], x[2 * ww + 1]) | (f32x2_to_e4m3x2(x[2 * ww + 8], x[2 * ww + 9]) << 16);
+          };
+          if constexpr (PT) {
+            words(q, &pu[4 * pg]);
+            const float4* tl = reinterpret_cast<const float4*>(smem + OFF_KV + st * STAGE_B + TILE_B +
+                                                               (part * (HC / kPage) + pg) * VPAGE_B + PAGE_B);
+            float qw[16];
+#pragma unroll
+            for (int i4 = 0; i4 < 4; ++i4) {
+              const float4 vs4 = tl[4 + i4];
+              const float vv[4] = {vs4.x, vs4.y, vs4.z, vs4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int t = 4 * i4 + e;
+                // sv / C_j is exact; slots past the sequence end hold no scale
+                const float w = (tail_tile && key0 + pg * 16 + t >= job.L) ? 0.f : vv[e] * c_inv;
+                qw[t] = __fmul_rn(q[t], w);
+              }
+            }
+            words(qw, &pw[4 * pg]);
+          } else {
+            words(q, &pw[4 * pg]);
+          }
         }
         m = m_new;
         M = M_new;
         tmem_st16(sbuf, pw);  // over the first 16 of this thread's 64 columns of S_j
+        if constexpr (PT) tmem_st16(sbuf + 16, pu);  // the unweighted codes next to them
         tmem_wait_st();
         if (tail_tile) fence_proxy_async_smem();  // the zeroed V slots, before the tensor cores read them
         tc_fence_before();
@@ -816,18 +915,19 @@ using namespace kvq;
 
 namespace {
 
-template <int HD, bool SL, bool E5 = false>
+template <int HD, bool SL, bool E5 = false, bool PT = false>
 kvq_status_t launch_prefill(const PrefillParams& prm, dim3 grid, cudaStream_t stream) {
-  constexpr int smem = Geo<HD>::SMEM_BYTES;
+  constexpr int smem = Geo<HD, PT>::SMEM_BYTES;
   static int configured_mask = 0;  // devices whose shared-memory attribute is set
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(configured_mask & (1 << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<HD, SL, E5>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel<HD, SL, E5, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_status(e, "prefill: set shared memory size");
     configured_mask |= 1 << (dev & 31);
   }
-  prefill_kernel<HD, SL, E5><<<grid, NTHREADS, smem, stream>>>(prm);
+  prefill_kernel<HD, SL, E5, PT><<<grid, NTHREADS, smem, stream>>>(prm);
   return cuda_status(cudaGetLastError(), "prefill launch");
 }
 
@@ -836,7 +936,7 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
                      const int32_t* cu_seqlens_q, const int32_t* seq_lens, void* out, int B, int Hq, int Hkv, int D,
                      int P, int max_blocks, int64_t num_blocks, int max_q_tokens, float sm_scale, int causal,
                      int* dev_status, kvq_stream_t stream, int accumulation,
-                     kvq_dtype_t cache_dtype = KVQ_DTYPE_FP8_E4M3) {
+                     kvq_dtype_t cache_dtype = KVQ_DTYPE_FP8_E4M3, bool per_token = false) {
   if (B < 1 || Hq < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1 || max_q_tokens < 0)
     return fail(KVQ_ERR_INVALID_ARG, "prefill: bad sizes");
   if (Hq % Hkv != 0) return fail(KVQ_ERR_INVALID_ARG, "prefill: Hq %% Hkv != 0");
@@ -850,9 +950,11 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
   const bool single_level = D == 256 || accumulation == KVQ_ACC_SINGLE_LEVEL;
   if (cache_dtype != KVQ_DTYPE_FP8_E4M3 && cache_dtype != KVQ_DTYPE_FP8_E5M2)
     return fail(KVQ_ERR_UNSUPPORTED, "prefill: FP8 (E4M3 or E5M2) caches only");
+  if (per_token && (D != 128 || single_level))
+    return fail(KVQ_ERR_UNSUPPORTED, "prefill: per-token scales at head_dim 128 with two-level accumulation");
   if (max_q_tokens == 0) return KVQ_OK;
-  if (!q8 || !q_scale || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !cu_seqlens_q ||
-      !seq_lens || !out)
+  if (!q8 || !q_scale || !k_cache || !v_cache || (!per_token && (!k_scale || !v_scale)) || !block_table ||
+      !cu_seqlens_q || !seq_lens || !out)
     return fail(KVQ_ERR_INVALID_ARG, "prefill: null pointer");
   if (!aligned(q8, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
     return fail(KVQ_ERR_INVALID_ARG, "prefill: pointers must be 16-byte aligned");
@@ -880,6 +982,9 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
   prm.stall_ns = stall_ns();
   dim3 grid(Hq, (max_q_tokens + TQ - 1) / TQ, B);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (per_token)
+    return cache_dtype == KVQ_DTYPE_FP8_E5M2 ? launch_prefill<128, false, true, true>(prm, grid, st)
+                                             : launch_prefill<128, false, false, true>(prm, grid, st);
   if (cache_dtype == KVQ_DTYPE_FP8_E5M2) {
     if (D == 256) return launch_prefill<256, true, true>(prm, grid, st);
     return single_level ? launch_prefill<128, true, true>(prm, grid, st)
@@ -928,4 +1033,17 @@ extern "C" kvq_status_t kvq_prefill_attention_acc(const uint8_t* q8, const float
   return prefill(q8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, cu_seqlens_q, seq_lens, out, B, Hq,
                  Hkv, D, P, max_blocks, num_blocks, max_q_tokens, sm_scale, causal, dev_status, stream,
                  static_cast<int>(accumulation));
+}
+
+extern "C" kvq_status_t kvq_prefill_attention_per_token(const uint8_t* q8, const float* q_scale, const void* k_cache,
+                                                        const void* v_cache, const int32_t* block_table,
+                                                        const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                                                        void* out, int B, int Hq, int Hkv, int D, int P,
+                                                        int max_blocks, int64_t num_blocks, int max_q_tokens,
+                                                        float sm_scale, int causal, kvq_dtype_t cache_dtype,
+                                                        int* dev_status, kvq_stream_t stream) {
+  clear_error();
+  return prefill(q8, q_scale, k_cache, v_cache, nullptr, nullptr, block_table, cu_seqlens_q, seq_lens, out, B, Hq,
+                 Hkv, D, P, max_blocks, num_blocks, max_q_tokens, sm_scale, causal, dev_status, stream,
+                 KVQ_ACC_TWO_LEVEL, cache_dtype, true);
 }

@@ -471,6 +471,35 @@ kvq_status_t kvq_prefill_attention_dtype(const uint8_t* q8, const float* q_scale
                                          kvq_dtype_t cache_dtype);
 
 /*
+ * kvq_prefill_attention_per_token -- kvq_prefill_attention over a cache
+ * written by kvq_reshape_and_cache_per_token (V pages of P*D + 8*P bytes
+ * with their scale tails).  [FP8KV] "Dynamic or static scale" (a scale per
+ * token); [GTNT] section 2.2 (per-token dynamic scales for new tokens).
+ *
+ *  Arguments as for kvq_prefill_attention without k_scale and v_scale;
+ *  cache_dtype KVQ_DTYPE_FP8_E4M3 or KVQ_DTYPE_FP8_E5M2; D = 128 (two-level
+ *  accumulation).
+ *  Declared rounding: per key, c_j = fl32(sk_j * b) with b = fl32(fl32(
+ *  q_scale * sm_scale) * log2(e)) and s2_j = fl32(raw_j * c_j) (raw the
+ *  FP32 dot product of the codes); M = ceil(max_j s2_j) as in
+ *  kvq_prefill_attention.  The V scales run along the P.V contraction, so
+ *  they enter the FP8 probabilities: per tile of 128 keys (aligned at key
+ *  0), C = 2^ceil(log2 max sv_j) over the tile's cached keys and the P.V
+ *  operand is e4m3(fl32(2^(s2_j - M + 8) * (sv_j / C))) (sv_j / C exact),
+ *  while the row sum adds the unweighted codes e4m3(2^(s2_j - M + 8)); the
+ *  tile's product is taken in units of C, and every rescale between tiles
+ *  is a power of two.
+ */
+kvq_status_t kvq_prefill_attention_per_token(const uint8_t* q8, const float* q_scale,
+                                             const void* k_cache, const void* v_cache,
+                                             const int32_t* block_table, const int32_t* cu_seqlens_q,
+                                             const int32_t* seq_lens, void* out,
+                                             int B, int Hq, int Hkv, int D, int P, int max_blocks,
+                                             int64_t num_blocks, int max_q_tokens, float sm_scale,
+                                             int causal, kvq_dtype_t cache_dtype, int* dev_status,
+                                             kvq_stream_t stream);
+
+/*
  * kvq_prefill_attention_acc -- kvq_prefill_attention with an explicit
  * accumulation mode.  Single-level: every tile's P8.V8 MMA accumulates into
  * one tensor-memory sum, which is multiplied by alpha in place before the

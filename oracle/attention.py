@@ -395,9 +395,15 @@ def prefill_per_token(q8, q_scale, k_cache, v_cache, kv_scale_cache, block_table
       o = sum_t C_t sum_{j in t} decode(Pw_j) v8_j / sum_j decode(Pu_j).
       With sv_j = C_t (all V scales of a group one power of two) Pw = Pu
       and this is prefill(mode="final") with the per-head scales.
+    * "mirror": the same walked group by group in key order with the running
+      integer stabilizer of the online softmax (the earlier numerator and row
+      sum multiplied by 2^(M_old - M_new)).  The weights sv_j / C_t move many
+      weighted probabilities into E4M3's subnormal range, where rounding does
+      not commute with powers of two, so unlike the per-head case this is not
+      "final": it is the reading of a one-pass kernel.
     Returns out float64 [Tq][Hq][D] (rows not in `rows` stay NaN).
     """
-    if mode not in ("pure", "final"):
+    if mode not in ("pure", "final", "mirror"):
         raise ValueError(f"unknown mode {mode!r}")
     q8 = np.asarray(q8, dtype=np.uint8)
     Tq, Hq, D = q8.shape
@@ -442,10 +448,28 @@ def prefill_per_token(q8, q_scale, k_cache, v_cache, kv_scale_cache, block_table
                 o = (p @ (v_codes[:n] * sv[:n, None].astype(np.float64))) / p.sum(axis=1, keepdims=True)
             else:
                 s2 = np.where(visible, (qc @ k_codes[:n].T) * c[None, :n], -np.inf)
-                p256 = (np.exp2(s2 - stabilizer(s2)) * 256.0).astype(np.float32)
-                pu = e4m3.decode(e4m3.encode(p256))
-                pw = e4m3.decode(e4m3.encode((p256 * w[None, :n]).astype(np.float32)))
-                o = (pw * np.repeat(C, tile)[None, :n]) @ v_codes[:n] / pu.sum(axis=1, keepdims=True)
+
+                def codes(seg, M, wseg):
+                    p256 = (np.exp2(seg - M) * 256.0).astype(np.float32)
+                    return (e4m3.decode(e4m3.encode(p256)),
+                            e4m3.decode(e4m3.encode((p256 * wseg[None, :]).astype(np.float32))))
+                if mode == "final":
+                    pu, pw = codes(s2, stabilizer(s2), w[:n])
+                    o = (pw * np.repeat(C, tile)[None, :n]) @ v_codes[:n] / pu.sum(axis=1, keepdims=True)
+                else:
+                    R = len(part)
+                    m_run = np.full(R, -np.inf)
+                    l = np.zeros(R)
+                    num = np.zeros((R, D))
+                    for gi, t0 in enumerate(range(0, n, tile)):
+                        seg = s2[:, t0:t0 + tile]
+                        m_new = np.maximum(m_run, stabilizer(seg)[:, 0])
+                        a = np.where(np.isfinite(m_run), np.exp2(m_run - m_new), 0.0)
+                        pu, pw = codes(seg, m_new[:, None], w[t0:t0 + seg.shape[1]])
+                        num = num * a[:, None] + C[gi] * (pw @ v_codes[t0:t0 + seg.shape[1]])
+                        l = l * a + pu.sum(axis=1)
+                        m_run = m_new
+                    o = num / l[:, None]
             for i, (t, h) in enumerate(part):
                 out[t, h] = o[i]
     return out

@@ -104,3 +104,23 @@ def test_append_entry_point_validates_without_gpu(lib):
     bad_d = list(sizes)
     bad_d[3] = 96
     assert d(fake, fake, fake, fake, *([fake] * 7), *bad_d, fake, 1 << 30, None, None) == 2  # head_dim 96
+
+
+def test_per_token_prefill_validates_without_gpu(lib):
+    """The per-token prefill refuses missing caches, a BF16 cache and head
+    dim 256 before any CUDA call; an empty batch of new tokens is a no-op."""
+    p = ctypes.c_void_p
+    i, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    f = lib.kvq_prefill_attention_per_token
+    f.restype = i
+    f.argtypes = [p, p, p, p, p, p, p, p, i, i, i, i, i, i, i64, i, f32, i, i, p, p]
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the calls return first
+    dims = [1, 8, 2, 128, 16, 4, 64, 16, 0.088, 1]  # B Hq Hkv D P max_blocks num_blocks max_q sm causal
+    assert f(fake, fake, fake, None, *[fake] * 4, *dims, 0, None, None) == 1  # no V cache
+    assert f(*[fake] * 8, *dims, 1, None, None) == 2  # BF16 cache
+    d256 = list(dims)
+    d256[3] = 256
+    assert f(*[fake] * 8, *d256, 0, None, None) == 2  # head dim 256
+    empty = list(dims)
+    empty[7] = 0
+    assert f(*[None] * 8, *empty, 0, None, None) == 0

@@ -1,16 +1,22 @@
 """GPU parity of kvq_prefill_attention (tcgen05 FP8 MMA, TMEM accumulators)
 against the float64 oracle on caches and query codes the oracle builds.
 
-Every check holds the kernel to max-abs 1e-2 and mean-abs 1e-3 against two
-oracle readings of the declared rounding (exact q8 / K8 products, the float32
-score coefficient, P8 = e4m3(2^(s - m) * 256), the row sum over unquantized
-p):
-* "final": m is the row's final maximum -- one rounding per probability,
-  independent of how any implementation tiles the keys;
-* "mirror": m is the running maximum of an online softmax over tiles of 128
-  keys, the order the kernel walks them in.
+Every check holds the kernel to max-abs 1e-2 (+ 2^-8 |ref| where |ref| > 1)
+and mean-abs 1e-3 against two oracle readings of the declared rounding
+(exact q8 / K8 products, the float32 score coefficient, the integer
+stabilizer M = ceil(max s2), P8 = e4m3(2^(s2 - M) * 256), the row sum over
+the same rounded P8):
+* "final": M of the whole row -- one rounding per probability, independent
+  of how any implementation tiles the keys;
+* "mirror": the running M of an online softmax over tiles of 128 keys, the
+  order the kernel walks them in (equal to "final": the rescales are powers
+  of two).
 The unquantized-P ("pure") result is checked too, within the bound that one
-E4M3 rounding of every probability allows."""
+E4M3 rounding of every probability allows.  Per-token-scaled caches
+(kvq_prefill_attention_per_token) are checked against
+attention.prefill_per_token's tile walk ("mirror": the V-scale weights move
+probabilities into E4M3's subnormal range, where the running and the final
+stabilizer round differently) and its exact softmax."""
 import numpy as np
 import pytest
 import torch
@@ -242,3 +248,73 @@ def test_prefill_over_an_e5m2_cache(D, nq, cached):
     if len(rows) > 2000:
         rows = [rows[i] for i in rng.choice(len(rows), 2000, replace=False)]
     check_all(got, c, rows, what=f"E5M2 cache head_dim {D} nq={nq}")
+
+
+def build_per_token(nq_list, cached_list, Hq=32, Hkv=8, seed=0, outliers=4, cache_dtype=kv_cache.FP8):
+    """Oracle per-token caches (NaN in unwritten scale slots) and q8 codes."""
+    gen = W.generator(9500 + seed)
+    lens = [a + b for a, b in zip(nq_list, cached_list)]
+    bt, nb = W.paged_layout(lens, 16, gen)
+    slots = torch.cat([W.slots_for(bt, b, torch.arange(L), 16) for b, L in enumerate(lens)])
+    T, D = int(slots.numel()), 128
+    k = W.randn_bf16((T, Hkv, D), gen)
+    v = W.randn_bf16((T, Hkv, D), gen)
+    if outliers:  # a few tokens x4 (their own scales absorb it; their tiles' other weights shrink)
+        idx = torch.randperm(T, generator=gen)[:outliers]
+        k[idx] = (k[idx].float() * 4).bfloat16()
+        v[idx] = (v[idx].float() * 4).bfloat16()
+    q = W.randn_bf16((sum(nq_list), Hq, D), gen)
+    qs = np.float32(q.float().abs().max().item() / 448)
+    kc = np.full((nb, Hkv, 16, D), 0xA5, np.uint8)
+    vc = np.full((nb, Hkv, D, 16), 0xA5, np.uint8)
+    sc = np.full((nb, Hkv, 2, 16), np.nan, np.float32)
+    kv_cache.reshape_and_cache_per_token(f32(k), f32(v), slots.numpy(), kc, vc, sc, cache_dtype)
+    q8 = kv_cache.quantize_query(f32(q), qs)
+    cu = np.concatenate([[0], np.cumsum(nq_list)]).astype(np.int32)
+    return dict(kc=kc, vc=vc, sc=sc, q8=q8, qs=qs, bt=bt.numpy(), nb=nb, cu=cu, lens=np.array(lens, np.int32),
+                Hq=Hq, Hkv=Hkv, sm=1 / np.sqrt(float(D)), dtype=cache_dtype)
+
+
+def gpu_prefill_per_token(c):
+    from oracle import layout
+    k = _k()
+    kd_np, vd_np = layout.to_device_format_per_token(c["kc"], c["vc"], c["sc"])
+    kd, vd = torch.from_numpy(kd_np).cuda(), torch.from_numpy(vd_np).cuda()
+    out = torch.full(c["q8"].shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k.kvq_prefill_attention_per_token(torch.from_numpy(c["q8"]).cuda(), torch.tensor([c["qs"]], device="cuda"), kd,
+                                      vd, torch.from_numpy(c["bt"]).cuda(), torch.from_numpy(c["cu"]).cuda(),
+                                      torch.from_numpy(c["lens"]).cuda(), out,
+                                      max_q_tokens=int(np.max(np.diff(c["cu"]))), num_blocks=c["nb"],
+                                      sm_scale=float(c["sm"]), cache_dtype=c["dtype"], dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, f"device status {int(st.item()):#x}"
+    return f32(out)
+
+
+def oracle_per_token(c, rows, mode="mirror"):
+    return attention.prefill_per_token(c["q8"], c["qs"], c["kc"], c["vc"], c["sc"], c["bt"], c["cu"], c["lens"],
+                                       float(np.float32(c["sm"])), mode=mode, rows=rows, cache_dtype=c["dtype"])
+
+
+@pytest.mark.parametrize("dtype", [kv_cache.FP8, kv_cache.FP8_E5M2])
+@pytest.mark.parametrize("nq,cached", [([256], [384]), ([1, 130, 300], [0, 17, 1000]), ([77], [3000])])
+def test_prefill_over_a_per_token_cache(nq, cached, dtype):
+    """Per-token K and V scales (a few tokens x4), ragged lengths, a partial
+    last page whose unwritten scale slots hold NaN; against the declared
+    reading (the tile walk, "mirror") and, within the probability rounding,
+    the exact softmax."""
+    c = build_per_token(nq, cached, seed=len(nq) + cached[0], cache_dtype=dtype)
+    got = gpu_prefill_per_token(c)
+    Tq = c["q8"].shape[0]
+    rng = np.random.default_rng(7)
+    rows = [(t, h) for t in range(Tq) for h in range(c["Hq"])]
+    if len(rows) > 2000:
+        rows = [rows[i] for i in rng.choice(len(rows), 2000, replace=False)]
+    check_rows(got, oracle_per_token(c, rows), rows, what=f"per-token nq={nq} cached={cached} {dtype}")
+    # against unquantized P: every weight within half an E4M3 ulp, numerator and row sum
+    pure = oracle_per_token(c, rows, mode="pure")
+    g = np.stack([got[t, h] for t, h in rows])
+    r = np.stack([pure[t, h] for t, h in rows])
+    vmax = np.max(np.abs(r))
+    assert np.all(np.abs(g - r) <= 2.0 ** -3 * vmax + 2.0 ** -8 * np.abs(r))

@@ -13,6 +13,9 @@
   the dequantized values), and a scale attached to the wrong token would
   not: the same check fails for a cache whose V scales are shifted by one
   token.
+* "mirror" (the tile walk with a running stabilizer) with power-of-two
+  scales per head is per-head prefill's mirror; with real per-token scales
+  it stays within the same rounding bound of pure.
 * The last causal row attends to every cached key: it equals per-token
   decode over the same keys (pure modes, up to decode's float32 query),
   and its "final" result is within the same bound of it.
@@ -112,3 +115,23 @@ def test_last_row_equals_per_token_decode_over_the_same_keys():
     assert np.allclose(pure, dec[0], rtol=1e-6, atol=1e-9)
     vmax = np.max(np.abs(dec))
     assert np.max(np.abs(fin - dec[0])) <= 2.0 ** -3 * vmax + 1e-12
+
+
+def test_mirror_with_power_of_two_scales_is_per_head_mirror_and_bounded_otherwise():
+    c = _case(nq=150, nc=300, seed=4)
+    Hkv = c["kc"].shape[1]
+    ks = np.array([2.0 ** -6, 2.0 ** -5], np.float32)[:Hkv]
+    vs = np.array([2.0 ** -7, 2.0 ** -4], np.float32)[:Hkv]
+    sc = np.zeros_like(c["sc"])
+    sc[:, :, 0, :] = ks[None, :, None]
+    sc[:, :, 1, :] = vs[None, :, None]
+    mir = _pt(c, sc=sc, mode="mirror")
+    ref = attention.prefill(c["q8"], c["qs"], c["kc"], c["vc"], ks, vs, c["bt"], c["cu"], c["sl"], 0.25,
+                            mode="mirror")
+    assert np.all(np.isfinite(mir))
+    assert np.allclose(mir, ref, rtol=1e-13, atol=0.0)  # float64 summation order only
+    c2 = _case(nq=100, nc=320, seed=2, outliers=6)
+    mir2 = _pt(c2, mode="mirror")
+    pure2 = _pt(c2, mode="pure")
+    assert np.all(np.isfinite(mir2))
+    assert np.max(np.abs(mir2 - pure2)) <= 2.0 ** -3 * np.max(np.abs(pure2))
