@@ -610,8 +610,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
 #pragma unroll
           for (int mt = 0; mt < G::MT; ++mt) va[mt][2] = va[mt][3] = 0u;
         }
-        // PT: V scales enter P as weights sv / c with c the stage's largest live
-        // V scale (so P stays in E4M3's range); the stage's P.V is scaled by c
+        // PT: V scales enter P as weights sv / c with c = 2^ceil(log2 m), m the
+        // stage's largest live V scale (so P stays in E4M3's range and 1 / c is
+        // exact); the stage's P.V is scaled by c
         float cst = 1.f, w00 = 1.f, w01 = 1.f, w10 = 1.f, w11 = 1.f;
         if constexpr (PT) {
           if (!two) sv10 = sv11 = 0.f;
@@ -621,10 +622,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
             if (!live(1, r)) sv10 = 0.f;
             if (!live(1, r + 8)) sv11 = 0.f;
           }
-          cst = fmaxf(fmaxf(sv00, sv01), fmaxf(sv10, sv11));
+          float mv = fmaxf(fmaxf(sv00, sv01), fmaxf(sv10, sv11));
 #pragma unroll
-          for (int o = 4; o < 32; o <<= 1) cst = fmaxf(cst, __shfl_xor_sync(0xffffffffu, cst, o));
-          const float rc = cst > 0.f ? 1.f / cst : 0.f;
+          for (int o = 4; o < 32; o <<= 1) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+          // exponent of 2^ceil(log2 mv), within the normal range
+          const uint32_t mb = __float_as_uint(mv);
+          int ec = static_cast<int>(mb >> 23) - 127 + ((mb & 0x7FFFFFu) != 0u ? 1 : 0);
+          ec = ec < -126 ? -126 : (ec > 126 ? 126 : ec);
+          cst = mv > 0.f ? __uint_as_float(static_cast<uint32_t>(127 + ec) << 23) : 0.f;
+          const float rc = mv > 0.f ? __uint_as_float(static_cast<uint32_t>(127 - ec) << 23) : 0.f;
           w00 = sv00 * rc;
           w01 = sv01 * rc;
           w10 = sv10 * rc;

@@ -349,8 +349,9 @@ kvq_status_t kvq_reshape_and_cache_per_token(const void* k, const void* v, const
  *  Declared rounding: the query terms and the per-head score coefficient as
  *  for kvq_paged_decode_attention with c = fl32(sm_scale * log2(e)); each
  *  score is then multiplied by its token's K scale.  V scales enter the
- *  probabilities: per stage of 32 tokens, with c the stage's largest V scale
- *  of a live token and f a power of two per query head that moves the
+ *  probabilities: per stage of 32 tokens, with c = 2^ceil(log2 m), m the
+ *  stage's largest V scale of a live token, and f a power of two per query
+ *  head that moves the
  *  stage's largest weighted probability into [128, 256), P.V runs on
  *  p_j * (sv_j / c) * f, rounded to float16 and split into three E4M3 terms
  *  (about 11 significant bits: the weights make even the largest
