@@ -76,6 +76,15 @@ CASES = {
                           FP8_E5M2, -1),
     "e5m2_window": (dict(batch=4, q_heads=64, kv_heads=8, head_dim=64, context=1000), [50, 128, 129, 1000],
                     FP8_E5M2, 128),
+    # more (sequence, KV head) pairs than resident CTAs (4 per SM at head dim
+    # 64, 3 at 128): one range each, several items per CTA, the ring reused
+    # across items, per-warp partials and the combine
+    "many_seqs_d64": (dict(batch=80, q_heads=16, kv_heads=8, head_dim=64, context=600),
+                      [17 + (37 * i) % 583 for i in range(80)], FP8, -1),
+    "many_seqs_d128": (dict(batch=60, q_heads=32, kv_heads=8, head_dim=128, context=400),
+                       [1 + (53 * i) % 400 for i in range(60)], FP8, -1),
+    "many_seqs_bf16_d64": (dict(batch=80, q_heads=16, kv_heads=8, head_dim=64, context=300),
+                           [3 + (29 * i) % 297 for i in range(80)], BF16, -1),
 }
 
 

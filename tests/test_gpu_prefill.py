@@ -318,3 +318,14 @@ def test_prefill_over_a_per_token_cache(nq, cached, dtype):
     r = np.stack([pure[t, h] for t, h in rows])
     vmax = np.max(np.abs(r))
     assert np.all(np.abs(g - r) <= 2.0 ** -3 * vmax + 2.0 ** -8 * np.abs(r))
+
+
+def test_prefill_over_a_per_token_cache_full_size():
+    """The prefill configuration (4,096 new tokens on 28,672 cached, 32/8
+    heads) over a per-token cache: rows of the first and the last query tile
+    (the causal diagonal and 32,768 keys) for every eighth head, against the
+    tile walk."""
+    c = build_per_token([4096], [28672], seed=21)
+    got = gpu_prefill_per_token(c)
+    rows = [(t, h) for t in list(range(0, 128, 9)) + list(range(3968, 4096, 9)) for h in range(0, 32, 8)]
+    check_rows(got, oracle_per_token(c, rows), rows, what="per-token prefill 4K on 28K")
