@@ -163,20 +163,36 @@ SCALE_TAIL_BYTES = 2 * PAGE * 4
 
 
 def alloc_kv_cache(num_blocks: int, kv_heads: int, head_dim: int, cache_dtype="fp8_e4m3",
-                   device="cuda", fill=None, per_token=False):
+                   device="cuda", fill=None, per_token=False, paired=False):
     """Allocate (k_cache, v_cache) as uint8 tensors in the library's paged
     format ([num_blocks][Hkv][P][D] and [num_blocks][Hkv][D][P] elements).
-    per_token: each V page also carries its scale tail (FP8 only)."""
+    per_token: each V page also carries its scale tail (FP8 only).
+    paired: one allocation [num_blocks][Hkv][K page | V page]; k_cache is it
+    and v_cache a flat view starting one K page in (the library recognizes
+    the layout from the pointers and moves each pair with one copy)."""
     esz = 2 if _dtype_code(cache_dtype) == KVQ_DTYPE_BF16 else 1
     if per_token and esz != 1:
         raise ValueError("per-token scales need an FP8 cache")
-    kshape = (num_blocks, kv_heads, PAGE * head_dim * esz)
-    vshape = (num_blocks, kv_heads, PAGE * head_dim * esz + (SCALE_TAIL_BYTES if per_token else 0))
-    if fill is None:
-        return (torch.empty(kshape, dtype=torch.uint8, device=device),
-                torch.empty(vshape, dtype=torch.uint8, device=device))
-    return (torch.full(kshape, fill, dtype=torch.uint8, device=device),
-            torch.full(vshape, fill, dtype=torch.uint8, device=device))
+    kpage = PAGE * head_dim * esz
+    vpage = kpage + (SCALE_TAIL_BYTES if per_token else 0)
+    make = (lambda shape: torch.empty(shape, dtype=torch.uint8, device=device)) if fill is None else \
+        (lambda shape: torch.full(shape, fill, dtype=torch.uint8, device=device))
+    if paired:
+        buf = make((num_blocks, kv_heads, kpage + vpage))
+        return buf, buf.view(-1)[kpage:]
+    return make((num_blocks, kv_heads, kpage)), make((num_blocks, kv_heads, vpage))
+
+
+def _is_paired(k_cache, v_cache, kpage):
+    return v_cache.data_ptr() == k_cache.data_ptr() + kpage
+
+
+def _num_blocks(k_cache, v_cache, Hkv, kpage):
+    """Blocks of a cache from its K tensor: [num_blocks][Hkv][...] (separate
+    or paired), or flat separate pages."""
+    if k_cache.dim() >= 2 or _is_paired(k_cache, v_cache, kpage):
+        return k_cache.shape[0]
+    return k_cache.numel() // (Hkv * kpage)
 
 
 def kvq_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None,
@@ -185,15 +201,21 @@ def kvq_reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_
     T, Hkv, D = k.shape
     dt = _dtype_code(cache_dtype)
     esz = 2 if dt == KVQ_DTYPE_BF16 else 1
-    num_blocks = k_cache.numel() // (Hkv * PAGE * D * esz)
+    num_blocks = _num_blocks(k_cache, v_cache, Hkv, PAGE * D * esz)
     _check(lib.kvq_reshape_and_cache(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
                                      _ptr(k_scale), _ptr(v_scale), T, Hkv, D, PAGE, num_blocks, dt,
                                      _ptr(dev_status), _stream(stream)), "kvq_reshape_and_cache")
 
 
 def _check_per_token_cache(k_cache, v_cache, Hkv, D):
-    nb = k_cache.numel() // (Hkv * PAGE * D)
-    if k_cache.numel() != nb * Hkv * PAGE * D or v_cache.numel() != nb * Hkv * (PAGE * D + SCALE_TAIL_BYTES):
+    kpage, vpage = PAGE * D, PAGE * D + SCALE_TAIL_BYTES
+    if _is_paired(k_cache, v_cache, kpage):
+        nb = k_cache.shape[0]
+        ok = k_cache.numel() == nb * Hkv * (kpage + vpage)
+    else:
+        nb = k_cache.numel() // (Hkv * kpage)
+        ok = k_cache.numel() == nb * Hkv * kpage and v_cache.numel() == nb * Hkv * vpage
+    if not ok:
         raise ValueError("per-token caches must be alloc_kv_cache(..., per_token=True) tensors")
     return nb
 

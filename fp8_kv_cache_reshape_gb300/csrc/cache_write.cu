@@ -56,10 +56,10 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
     const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
     const float* __restrict__ k_scale, const float* __restrict__ v_scale, int T, int Hkv, int64_t num_slots,
-    int* dev_status) {
+    int64_t kstr, int64_t vstr, int* dev_status) {
+  // kstr, vstr: bytes between consecutive (block, head) pages of each cache
   constexpr int CH = D / 16;          // 16-byte chunks per row
   constexpr int PAGE_BYTES = kPage * D;
-  constexpr int V_STRIDE = PAGE_BYTES + (PT ? kScaleTailBytes : 0);  // bytes per V page
   __shared__ __align__(16) uint8_t vt[D * kPage];  // transposed V page
   __shared__ int64_t slots[kPage];
   __shared__ int fast;
@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
       if (valid) {
         const int64_t blk = slot / kPage;
         const int off = static_cast<int>(slot % kPage);
-        const size_t page = (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
-        const size_t vpage = (static_cast<size_t>(blk) * Hkv + h) * V_STRIDE;
+        const size_t page = (static_cast<size_t>(blk) * Hkv + h) * kstr;
+        const size_t vpage = (static_cast<size_t>(blk) * Hkv + h) * vstr;
         if (j == 0) {  // the scale tail: K scales, then V scales, one per token slot
           float* tail = reinterpret_cast<float*>(v_cache + vpage + PAGE_BYTES);
           tail[off] = skt;
@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
     const int64_t blk = slot / kPage;
     const int off = static_cast<int>(slot % kPage);
     const size_t src = (static_cast<size_t>(g0 + t) * Hkv + h) * D + j * 16;
-    const size_t page = (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
+    const size_t page = (static_cast<size_t>(blk) * Hkv + h) * kstr;
+    const size_t vpage = (static_cast<size_t>(blk) * Hkv + h) * vstr;
     float x[16];
     load16_bf16(k + src, x);
     *reinterpret_cast<uint4*>(k_cache + page + fp8_k_offset(off, j, D)) = quant16<E5>(x, sk);
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
 #pragma unroll
       for (int i = 0; i < 16; ++i) vt[(j * 16 + i) * kPage + slot_in_row] = qb[i];
     } else {
-      uint8_t* vp = v_cache + page + slot_in_row;
+      uint8_t* vp = v_cache + vpage + slot_in_row;
 #pragma unroll
       for (int i = 0; i < 16; ++i) vp[(j * 16 + i) * kPage] = qb[i];
     }
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(128) reshape_and_cache_fp8_kernel(
   if (fast) {
     __syncthreads();
     const int64_t blk = slots[0] / kPage;
-    uint8_t* vp = v_cache + (static_cast<size_t>(blk) * Hkv + h) * V_STRIDE;
+    uint8_t* vp = v_cache + (static_cast<size_t>(blk) * Hkv + h) * vstr;
     for (int d = tid; d < D; d += blockDim.x)
       *reinterpret_cast<uint4*>(vp + d * kPage) = *reinterpret_cast<const uint4*>(vt + d * kPage);
   }
@@ -177,10 +178,9 @@ template <int D>
 __global__ void __launch_bounds__(128) reshape_and_cache_bf16_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int64_t* __restrict__ slot_mapping,
     uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, int T, int Hkv, int64_t num_slots,
-    int* dev_status) {
+    int64_t kstr, int64_t vstr, int* dev_status) {
   constexpr int ROWB = D * 2;
   constexpr int CH = ROWB / 16;  // 8 bf16 per chunk
-  constexpr int PAGE_BYTES = kPage * ROWB;
   const int g0 = blockIdx.x * kPage;
   const int h = blockIdx.y;
   for (int u = threadIdx.x; u < kPage * CH; u += blockDim.x) {
@@ -195,8 +195,8 @@ __global__ void __launch_bounds__(128) reshape_and_cache_bf16_kernel(
     const int64_t blk = slot / kPage;
     const int off = static_cast<int>(slot % kPage);
     const size_t src = (static_cast<size_t>(g0 + t) * Hkv + h) * D + j * 8;
-    uint8_t* page_k = k_cache + (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
-    uint8_t* page_v = v_cache + (static_cast<size_t>(blk) * Hkv + h) * PAGE_BYTES;
+    uint8_t* page_k = k_cache + (static_cast<size_t>(blk) * Hkv + h) * kstr;
+    uint8_t* page_v = v_cache + (static_cast<size_t>(blk) * Hkv + h) * vstr;
     *reinterpret_cast<uint4*>(page_k + k_chunk_offset(off, j, ROWB)) =
         __ldg(reinterpret_cast<const uint4*>(k + src));
     uint4 vv = __ldg(reinterpret_cast<const uint4*>(v + src));
@@ -258,13 +258,15 @@ extern "C" kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   dim3 grid((T + kPage - 1) / kPage, Hkv);
   const int64_t num_slots = num_blocks * kPage;
+  const int64_t page_b = static_cast<int64_t>(kPage) * D * (fp8 ? 1 : 2);
+  const PageStrides ps = page_strides(k_cache, v_cache, page_b, page_b);
   if (fp8) {
     auto kb = static_cast<const __nv_bfloat16*>(k);
     auto vb = static_cast<const __nv_bfloat16*>(v);
     auto kc = static_cast<uint8_t*>(k_cache);
     auto vc = static_cast<uint8_t*>(v_cache);
     auto launch = [&](auto kernel) {
-      kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, k_scale, v_scale, T, Hkv, num_slots,
+      kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, k_scale, v_scale, T, Hkv, num_slots, ps.k, ps.v,
                                   dev_status);
     };
     const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
@@ -283,10 +285,10 @@ extern "C" kvq_status_t kvq_reshape_and_cache(const void* k, const void* v, cons
     auto vc = static_cast<uint8_t*>(v_cache);
     if (D == 128)
       reshape_and_cache_bf16_kernel<128><<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, T, Hkv, num_slots,
-                                                              dev_status);
+                                                              ps.k, ps.v, dev_status);
     else
       reshape_and_cache_bf16_kernel<64><<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, T, Hkv, num_slots,
-                                                             dev_status);
+                                                             ps.k, ps.v, dev_status);
   }
   return cuda_status(cudaGetLastError(), "reshape_and_cache launch");
 }
@@ -315,8 +317,11 @@ extern "C" kvq_status_t kvq_reshape_and_cache_per_token(const void* k, const voi
   auto vb = static_cast<const __nv_bfloat16*>(v);
   auto kc = static_cast<uint8_t*>(k_cache);
   auto vc = static_cast<uint8_t*>(v_cache);
+  const int64_t page_b = static_cast<int64_t>(kPage) * D;
+  const PageStrides ps = page_strides(k_cache, v_cache, page_b, page_b + kScaleTailBytes);
   auto launch = [&](auto kernel) {
-    kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, nullptr, nullptr, T, Hkv, num_slots, dev_status);
+    kernel<<<grid, 128, 0, s>>>(kb, vb, slot_mapping, kc, vc, nullptr, nullptr, T, Hkv, num_slots, ps.k, ps.v,
+                                dev_status);
   };
   const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;
   if (D == 128)

@@ -58,6 +58,10 @@ struct DecodeParams {
   // bf16 output itself (no combine kernel)
   __nv_bfloat16* out;
   int direct;
+  // bytes between consecutive (block, KV head) pages of the K and V caches;
+  // paired: each pair's K page is followed by its V page (one copy moves both)
+  int64_t k_str, v_str;
+  int paired;
   int B, Hq, Hkv, g, max_blocks;
   int64_t num_blocks;
   float sm_scale;
@@ -286,9 +290,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
           return;
         }
         const int off = static_cast<int>(slot % kPage);
-        const size_t page = (static_cast<size_t>(slot / kPage) * p.Hkv + r.kvh) * G::PAGE;
-        uint8_t* kp = p.k_cache_w + page;
-        uint8_t* vp = p.v_cache_w + page;
+        const size_t pair = static_cast<size_t>(slot / kPage) * p.Hkv + r.kvh;
+        uint8_t* kp = p.k_cache_w + pair * p.k_str;
+        uint8_t* vp = p.v_cache_w + pair * p.v_str;
         const int d0 = lane * EPL;
         if constexpr (FP8) {
           const float sk = p.k_scale[r.kvh], sv = p.v_scale[r.kvh];
@@ -352,14 +356,19 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
             if (two) info |= kPresent1 | (d1 ? kBad1 : 0);
             stage_info[st] = info;
             mbar_arrive_expect_tx(&full[st], (two ? 2u : 1u) * static_cast<uint32_t>(G::PAGE + VS));
-            uint8_t* sk = stages + size_t(st) * STRIDE;  // [K0][K1][V0][V1]
+            uint8_t* sk = stages + size_t(st) * STRIDE;
             const size_t pg0 = static_cast<size_t>(b0) * p.Hkv + r.kvh;
-            bulk_g2s(sk, p.k_cache + pg0 * G::PAGE, G::PAGE, &full[st], pol);
-            bulk_g2s(sk + 2 * G::PAGE, p.v_cache + pg0 * VS, VS, &full[st], pol);
-            if (two) {
-              const size_t pg1 = static_cast<size_t>(b1) * p.Hkv + r.kvh;
-              bulk_g2s(sk + G::PAGE, p.k_cache + pg1 * G::PAGE, G::PAGE, &full[st], pol);
-              bulk_g2s(sk + 2 * G::PAGE + VS, p.v_cache + pg1 * VS, VS, &full[st], pol);
+            const size_t pg1 = static_cast<size_t>(b1) * p.Hkv + r.kvh;
+            if (p.paired) {  // [K0 V0][K1 V1]: one copy per page
+              bulk_g2s(sk, p.k_cache + pg0 * p.k_str, G::PAGE + VS, &full[st], pol);
+              if (two) bulk_g2s(sk + G::PAGE + VS, p.k_cache + pg1 * p.k_str, G::PAGE + VS, &full[st], pol);
+            } else {  // [K0][K1][V0][V1]
+              bulk_g2s(sk, p.k_cache + pg0 * p.k_str, G::PAGE, &full[st], pol);
+              bulk_g2s(sk + 2 * G::PAGE, p.v_cache + pg0 * p.v_str, VS, &full[st], pol);
+              if (two) {
+                bulk_g2s(sk + G::PAGE, p.k_cache + pg1 * p.k_str, G::PAGE, &full[st], pol);
+                bulk_g2s(sk + 2 * G::PAGE + VS, p.v_cache + pg1 * p.v_str, VS, &full[st], pol);
+              }
             }
           };
           int ok = 1;
@@ -402,7 +411,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
   }
   // V offsets.  FP8: matrix 0/1 = page 0 rows (16 mt + 0..7 / 8..15), matrix
   // 2/3 = the same rows of page 1.  BF16: one m-tile of one page per x4.
-  const int vofs = (lane >> 4) * v_stride<D, FP8, PT>() + (lane & 15) * kPage;  // FP8: + 256 per m-tile
+  // stage layout: K1 at k1off, V0 at v0off, V1 at v0off + v1d
+  constexpr int VSZ = v_stride<D, FP8, PT>();
+  const int k1off = p.paired ? G::PAGE + VSZ : G::PAGE;
+  const int v0off = p.paired ? G::PAGE : 2 * G::PAGE;
+  const int v1d = p.paired ? G::PAGE + VSZ : VSZ;
+  const int vofs = (lane >> 4) * v1d + (lane & 15) * kPage;  // FP8: + 256 per m-tile
   int voff[FP8 ? 1 : G::MT];
   if constexpr (FP8) {
     voff[0] = vofs;
@@ -501,7 +515,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
         break;
       }
       const uint32_t kb = smem_u32(stages + size_t(st) * STRIDE);
-      const uint32_t vb = kb + 2 * G::PAGE;
+      const uint32_t vb = kb + v0off;
       const int info = stage_info[st];
       const bool two = (info & kPresent1) != 0;
       const int tok0 = (rg.pg0 + i * PPS) * kPage;  // first token of page 0
@@ -545,9 +559,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
         // per-token scales (PT) of this lane's tokens r and r + 8 of both pages
         float sk00 = 1.f, sk01 = 1.f, sk10 = 1.f, sk11 = 1.f, sv00 = 0.f, sv01 = 0.f, sv10 = 0.f, sv11 = 0.f;
         if constexpr (PT) {  // the scale tails after each V page: 16 K scales, then 16 V scales
-          const uint8_t* v0 = stages + size_t(st) * STRIDE + 2 * G::PAGE;
+          const uint8_t* v0 = stages + size_t(st) * STRIDE + v0off;
           const float* t0 = reinterpret_cast<const float*>(v0 + G::PAGE);
-          const float* t1 = reinterpret_cast<const float*>(v0 + v_stride<D, FP8, PT>() + G::PAGE);
+          const float* t1 = reinterpret_cast<const float*>(v0 + v1d + G::PAGE);
           sk00 = t0[r];
           sk01 = t0[r + 8];
           sv00 = t0[kPage + r];
@@ -579,7 +593,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
           }
         };
         qk(kb, s0, sk00, sk01);
-        if (two) qk(kb + G::PAGE, s1, sk10, sk11);
+        if (two) qk(kb + k1off, s1, sk10, sk11);
         else s1[0] = s1[1] = s1[2] = s1[3] = NEG_INF;
         // ---- V fragments to registers, then release the ring slot ----
         uint32_t va[G::MT][4];
@@ -733,7 +747,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
           s[3] = (a[3] + b[3]) * coef1;
         };
         qk(kb, s0);
-        if (two) qk(kb + G::PAGE, s1);
+        if (two) qk(kb + k1off, s1);
         else s1[0] = s1[1] = s1[2] = s1[3] = NEG_INF;
         uint32_t vm0_lo = 0xFFFFFFFFu, vm0_hi = 0xFFFFFFFFu, vm1_lo = 0xFFFFFFFFu, vm1_hi = 0xFFFFFFFFu;
         if (edge) {
@@ -775,7 +789,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
           }
           if (two) {
             uint32_t y0, y1, y2, y3;
-            ldsm_x4(vb + G::PAGE + voff[mt], y0, y1, y2, y3);
+            ldsm_x4(vb + v1d + voff[mt], y0, y1, y2, y3);
             y0 &= vm1_lo;
             y1 &= vm1_lo;
             y2 &= vm1_hi;
@@ -1144,6 +1158,13 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
   prm.k_cache_w = app ? static_cast<uint8_t*>(const_cast<void*>(k_cache)) : nullptr;
   prm.v_cache_w = app ? static_cast<uint8_t*>(const_cast<void*>(v_cache)) : nullptr;
   prm.stall_ns = stall_ns();
+  {
+    const int64_t page_b = static_cast<int64_t>(kPage) * D * (fp8 ? 1 : 2);
+    const PageStrides ps = page_strides(k_cache, v_cache, page_b, page_b + (per_token ? kScaleTailBytes : 0));
+    prm.k_str = ps.k;
+    prm.v_str = ps.v;
+    prm.paired = ps.paired ? 1 : 0;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto o = static_cast<__nv_bfloat16*>(out);
   const bool e5 = cache_dtype == KVQ_DTYPE_FP8_E5M2;

@@ -20,4 +20,17 @@ inline bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintpt
 // The failure-path test hook of kvq_debug_set_stall_ns (0 = off).
 uint64_t stall_ns();
 
+// Bytes between the pages of consecutive (block, KV head) pairs in the K and
+// the V cache.  Separate caches: a K page and a V page (k_page, v_page bytes).
+// Paired layout (v_cache == k_cache + k_page: each pair's K page followed by
+// its V page in one allocation): both advance by k_page + v_page.
+struct PageStrides {
+  int64_t k, v;
+  bool paired;
+};
+inline PageStrides page_strides(const void* k_cache, const void* v_cache, int64_t k_page, int64_t v_page) {
+  const bool paired = static_cast<const uint8_t*>(v_cache) == static_cast<const uint8_t*>(k_cache) + k_page;
+  return paired ? PageStrides{k_page + v_page, k_page + v_page, true} : PageStrides{k_page, v_page, false};
+}
+
 }  // namespace kvq

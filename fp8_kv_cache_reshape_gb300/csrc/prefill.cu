@@ -126,6 +126,7 @@ struct PrefillParams {
   float sm_scale;
   int causal;
   int* dev_status;
+  int64_t k_str, v_str;  // bytes between consecutive (block, KV head) pages of each cache
   // failure-path test hook (kvq_debug_set_stall_ns): > 0 makes the softmax
   // warps wait up to this long on a barrier nothing arrives on before the
   // first key tile, which fails like a stuck pipeline wait
@@ -421,13 +422,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         }
         __syncwarp();
         if (lane < TK / kPage && blk >= 0) {
-          const size_t off = (static_cast<size_t>(blk) * p.Hkv + job.kvh) * PAGE_B;
+          const size_t off = (static_cast<size_t>(blk) * p.Hkv + job.kvh) * p.k_str;
           // K: one copy per plane (a K page of head dim 256 is stored as two half-pages)
 #pragma unroll
           for (int pl = 0; pl < HD / PLANE; ++pl)
             bulk_g2s(ks + pl * G::PLANE_K + lane * kPage * PLANE, p.k_cache + off + pl * kPage * PLANE, kPage * PLANE,
                      &bars->kv_full[st], policy_evict_last());
-          const size_t voff = (static_cast<size_t>(blk) * p.Hkv + job.kvh) * VPAGE_B;  // PT: page + tail
+          const size_t voff = (static_cast<size_t>(blk) * p.Hkv + job.kvh) * p.v_str;  // PT: page + tail
           bulk_g2s(vs + lane * VPAGE_B, p.v_cache + voff, VPAGE_B, &bars->kv_full[st], policy_evict_last());
         }
       }
@@ -980,6 +981,12 @@ kvq_status_t prefill(const uint8_t* q8, const float* q_scale, const void* k_cach
   prm.causal = causal ? 1 : 0;
   prm.dev_status = dev_status;
   prm.stall_ns = stall_ns();
+  {
+    const int64_t page_b = static_cast<int64_t>(kPage) * D;
+    const PageStrides ps = page_strides(k_cache, v_cache, page_b, page_b + (per_token ? kScaleTailBytes : 0));
+    prm.k_str = ps.k;
+    prm.v_str = ps.v;
+  }
   dim3 grid(Hq, (max_q_tokens + TQ - 1) / TQ, B);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (per_token)

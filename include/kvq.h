@@ -52,6 +52,16 @@
  *  - FP8 elements are E4M3 ("OCP FN": bias 7, max 448, min subnormal 2^-9,
  *    0x7F/0xFF NaN, no infinity) or E5M2 (KVQ_DTYPE_FP8_E5M2).  Page bytes =
  *    P * D * esize.
+ *  - Separate or paired.  Two separate allocations [num_blocks][Hkv][K page]
+ *    and [num_blocks][Hkv][V page], or one paired allocation
+ *    [num_blocks][Hkv][K page | V page]: each (block, KV head) pair's K page
+ *    directly followed by its V page (with per-token scales, the V page with
+ *    its scale tail).  Every entry point takes a paired cache as k_cache =
+ *    the allocation and v_cache = k_cache + K page bytes, and recognizes the
+ *    layout from exactly that pointer relation (both caches then advance by
+ *    K page + V page bytes per pair).  Results are bit-identical between the
+ *    two layouts; decode moves a paired page pair with one bulk copy instead
+ *    of two.
  *
  * Quantization (kvq_reshape_and_cache, kvq_quantize_query):
  *    code = e4m3_rne_satfinite( fl32(x / scale) )

@@ -113,3 +113,13 @@ def from_device_format_per_token(kd, vd, D: int):
     tail = np.ascontiguousarray(vd[:, :, P * D:]).view(np.float32).reshape(nb, H, 2, P)
     kl, vl = from_device_format(kd, codes, D, 1)
     return kl, vl, tail
+
+
+def to_device_format_paired(k_cache, v_cache, kv_scale_cache=None):
+    """The paired layout: [num_blocks][Hkv][K page | V page] bytes (with
+    per-token scales, the V page carries its scale tail)."""
+    if kv_scale_cache is None:
+        kd, vd = to_device_format(k_cache, v_cache)
+    else:
+        kd, vd = to_device_format_per_token(k_cache, v_cache, kv_scale_cache)
+    return np.concatenate([kd, vd], axis=2)

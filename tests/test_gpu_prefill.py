@@ -275,11 +275,15 @@ def build_per_token(nq_list, cached_list, Hq=32, Hkv=8, seed=0, outliers=4, cach
                 Hq=Hq, Hkv=Hkv, sm=1 / np.sqrt(float(D)), dtype=cache_dtype)
 
 
-def gpu_prefill_per_token(c):
+def gpu_prefill_per_token(c, caches=None):
+    """caches: device (k_cache, v_cache) to read instead of separate ones."""
     from oracle import layout
     k = _k()
-    kd_np, vd_np = layout.to_device_format_per_token(c["kc"], c["vc"], c["sc"])
-    kd, vd = torch.from_numpy(kd_np).cuda(), torch.from_numpy(vd_np).cuda()
+    if caches is None:
+        kd_np, vd_np = layout.to_device_format_per_token(c["kc"], c["vc"], c["sc"])
+        kd, vd = torch.from_numpy(kd_np).cuda(), torch.from_numpy(vd_np).cuda()
+    else:
+        kd, vd = caches
     out = torch.full(c["q8"].shape, float("nan"), dtype=torch.bfloat16, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     k.kvq_prefill_attention_per_token(torch.from_numpy(c["q8"]).cuda(), torch.tensor([c["qs"]], device="cuda"), kd,
