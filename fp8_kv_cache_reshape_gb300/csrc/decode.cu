@@ -348,8 +348,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
               __syncwarp();
             }
           }
-          // one stage = pages j, j + 1: a bulk copy per K page and per V page
-          // (per-token scales: the V page with its scale tail)
+          // one stage = pages j, j + 1 laid out [K0][V0][K1][V1] (per-token
+          // scales: each V page with its scale tail): a bulk copy per K page
+          // and per V page, or over a paired cache one per page pair
           auto issue_pages = [&](int st) {
             constexpr int VS = v_stride<D, FP8, PT>();
             int info = kPresent0 | (d0 ? kBad0 : 0);
@@ -359,14 +360,14 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
             uint8_t* sk = stages + size_t(st) * STRIDE;
             const size_t pg0 = static_cast<size_t>(b0) * p.Hkv + r.kvh;
             const size_t pg1 = static_cast<size_t>(b1) * p.Hkv + r.kvh;
-            if (p.paired) {  // [K0 V0][K1 V1]: one copy per page
+            if (p.paired) {
               bulk_g2s(sk, p.k_cache + pg0 * p.k_str, G::PAGE + VS, &full[st], pol);
               if (two) bulk_g2s(sk + G::PAGE + VS, p.k_cache + pg1 * p.k_str, G::PAGE + VS, &full[st], pol);
-            } else {  // [K0][K1][V0][V1]
+            } else {
               bulk_g2s(sk, p.k_cache + pg0 * p.k_str, G::PAGE, &full[st], pol);
-              bulk_g2s(sk + 2 * G::PAGE, p.v_cache + pg0 * p.v_str, VS, &full[st], pol);
+              bulk_g2s(sk + G::PAGE, p.v_cache + pg0 * p.v_str, VS, &full[st], pol);
               if (two) {
-                bulk_g2s(sk + G::PAGE, p.k_cache + pg1 * p.k_str, G::PAGE, &full[st], pol);
+                bulk_g2s(sk + G::PAGE + VS, p.k_cache + pg1 * p.k_str, G::PAGE, &full[st], pol);
                 bulk_g2s(sk + 2 * G::PAGE + VS, p.v_cache + pg1 * p.v_str, VS, &full[st], pol);
               }
             }
@@ -411,11 +412,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
   }
   // V offsets.  FP8: matrix 0/1 = page 0 rows (16 mt + 0..7 / 8..15), matrix
   // 2/3 = the same rows of page 1.  BF16: one m-tile of one page per x4.
-  // stage layout: K1 at k1off, V0 at v0off, V1 at v0off + v1d
+  // stage layout [K0][V0][K1][V1]: K1 at k1off, V0 at v0off, V1 at v0off + v1d
   constexpr int VSZ = v_stride<D, FP8, PT>();
-  const int k1off = p.paired ? G::PAGE + VSZ : G::PAGE;
-  const int v0off = p.paired ? G::PAGE : 2 * G::PAGE;
-  const int v1d = p.paired ? G::PAGE + VSZ : VSZ;
+  constexpr int k1off = G::PAGE + VSZ;
+  constexpr int v0off = G::PAGE;
+  constexpr int v1d = G::PAGE + VSZ;
   const int vofs = (lane >> 4) * v1d + (lane & 15) * kPage;  // FP8: + 256 per m-tile
   int voff[FP8 ? 1 : G::MT];
   if constexpr (FP8) {
