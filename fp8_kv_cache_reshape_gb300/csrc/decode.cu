@@ -207,6 +207,38 @@ KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
   return r;
 }
 
+// Before the preceding kernel has completed: bring the first pages of this
+// CTA's first item into L2, so that its first stages arrive at L2 rather
+// than HBM latency once it may start.  The sequence length and block ids are
+// read only for this hint (they may still change and are read again after
+// the wait; loads cached in L2 only leave no stale L1 line), clamped so that
+// every address stays inside the block table and the caches.  A page the
+// preceding kernel writes after the hint is updated in L2 like any other.
+template <int D, bool FP8, bool PT>
+KVQ_DEVINL void prefetch_first_pages(const DecodeParams& p, int lane, int max_pages) {
+  using G = Geo<D, FP8>;
+  constexpr int VS = v_stride<D, FP8, PT>();
+  const int NG = p.B * p.Hkv;
+  const int item = blockIdx.x;
+  const int bh = item % NG;
+  const int b = bh / p.Hkv, kvh = bh - b * p.Hkv;
+  int L = ld_l2only_s32(p.seq_lens + b);
+  L = min(max(L, 0), p.max_blocks * kPage);
+  const SplitPages sp = split_pages(L, p.window, p.num_splits);
+  const int pg0 = sp.first + (item / NG) * sp.pps;
+  const int n = min(min(sp.pps, sp.last - pg0), max_pages);
+  if (lane >= n) return;
+  const int blk = ld_l2only_s32(p.block_table + static_cast<size_t>(b) * p.max_blocks + pg0 + lane);
+  if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) return;
+  const size_t pair = static_cast<size_t>(blk) * p.Hkv + kvh;
+  if (p.paired) {
+    prefetch_l2(p.k_cache + pair * p.k_str, G::PAGE + VS);
+  } else {
+    prefetch_l2(p.k_cache + pair * p.k_str, G::PAGE);
+    prefetch_l2(p.v_cache + pair * p.v_str, VS);
+  }
+}
+
 // Stage info word written by the producer: bit 0/1 = page 0/1 present,
 // bit 2/3 = page 0/1 had an invalid block id (fully masked).
 constexpr int kPresent0 = 1, kPresent1 = 2, kBad0 = 4, kBad1 = 8;
@@ -252,6 +284,12 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
   // point, so it too sees the preceding kernel's writes.  Without a combine
   // (direct output) the next kernel launches as the CTAs exit: its CTAs
   // waiting beside this grid's slowest ones would slow them.
+  // the last consumer warp issues the hint: its first stage comes last, and
+  // the producer's own chain is not lengthened where nothing runs before.
+  // Direct-output calls (one short range per pair) gain nothing from it.
+  if (warp == NW - 1 && !p.direct && blockIdx.x < p.num_items) {
+    prefetch_first_pages<D, FP8, PT>(p, lane, PPS * NW);
+  }
   grid_dependency_wait();
   if (!p.direct) grid_launch_dependents();
 

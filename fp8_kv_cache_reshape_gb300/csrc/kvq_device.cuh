@@ -139,6 +139,18 @@ KVQ_DEVINL uint64_t policy_evict_last() {
   return p;
 }
 
+// A 32-bit load cached in L2 only (no L1 line is left behind).
+KVQ_DEVINL int ld_l2only_s32(const int32_t* src) {
+  int v;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(src) : "memory");
+  return v;
+}
+// Hint: bring `bytes` at src into L2 (no data returned, no completion to wait
+// for).  src 16-byte aligned; bytes % 16 == 0.
+KVQ_DEVINL void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch: wait until the preceding grid's memory is visible.
 KVQ_DEVINL void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Allow the programmatic dependent grid to be scheduled (it still waits for
