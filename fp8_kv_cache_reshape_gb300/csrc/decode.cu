@@ -68,6 +68,13 @@ struct DecodeParams {
   int window;
   int num_splits;
   int num_items;
+  // balanced plan (ragged batches): per KV head, the batch's attended pages
+  // laid end to end are cut into num_slots = B * S equal slots; a slot's part
+  // inside one sequence is a segment, whose partials sit at segment id
+  // slot + b of [Hq][kseg][NW] (kseg = num_slots + B - 1)
+  int balanced;
+  int num_slots;
+  int kseg;
   int* dev_status;
   // Append (optional, k_new != nullptr): the new token of each sequence,
   // bf16 [B][Hkv][D], is written into its cache slot slot_new[b] (-1: none)
@@ -156,7 +163,8 @@ static_assert(ctas_per_sm<64>() * (decode_smem_bytes<64, true, stages_for<64, tr
 struct ItemRange {
   int b, kvh, split;
   int lo, hi;     // attended token positions [lo, hi)
-  int pg0, n;     // first page and page count of this split
+  int pg0, n;     // first page and page count of this split (balanced plan:
+                  // of this segment of slot `split`)
 };
 
 // The pages [first, last) that a sequence of L cached tokens attends to, cut
@@ -207,6 +215,147 @@ KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
   return r;
 }
 
+// Balanced plan: lane b (< B <= 32) of a warp holds sequence b's length,
+// first attended page, attended page count and the inclusive prefix of the
+// page counts over the batch.  spec: a hint read before the preceding kernel
+// has completed (L2-only loads, nothing reported).
+struct BatchScan {
+  int L, first, pages, incl, total;
+};
+KVQ_DEVINL BatchScan batch_scan_of(const int32_t* seq_lens, int B, int max_blocks, int window, int lane, bool spec,
+                                    int* report_to) {
+  BatchScan bs;
+  int L = 0;
+  if (lane < B) {
+    L = spec ? ld_l2only_s32(seq_lens + lane) : seq_lens[lane];
+    const int cap = max_blocks * kPage;
+    if (L < 0 || L > cap) {
+      if (report_to) set_status(report_to, KVQ_DEV_BAD_SEQLEN);
+      L = L < 0 ? 0 : cap;
+    }
+  }
+  const SplitPages sp = split_pages(L, window, 1);
+  bs.L = L;
+  bs.first = sp.first;
+  bs.pages = lane < B ? sp.last - sp.first : 0;
+  int x = bs.pages;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  bs.incl = x;
+  bs.total = __shfl_sync(0xffffffffu, x, 31);
+  return bs;
+}
+KVQ_DEVINL BatchScan batch_scan(const DecodeParams& p, int lane, bool spec, bool report) {
+  return batch_scan_of(p.seq_lens, p.B, p.max_blocks, p.window, lane, spec, report ? p.dev_status : nullptr);
+}
+// Slots that hold pages: all num_slots, or one per page when the batch has
+// fewer pages (every used slot then holds at least one page, so the segment
+// ids of a sequence's slots are all written).
+KVQ_DEVINL int used_slots(int num_slots, int total) { return total < num_slots ? total : num_slots; }
+// The slot holding stream page x (0 <= x < T, N = used slots): the largest s
+// with floor(s * T / N) <= x.
+KVQ_DEVINL int slot_of(int64_t x, int64_t T, int64_t N) { return static_cast<int>(((x + 1) * N + T - 1) / T) - 1; }
+
+// The segments of one item, in stream order: one ItemRange per item in the
+// per-sequence plan; in the balanced plan the parts of the item's slot inside
+// each sequence it covers (none for an empty slot).  Warp-uniform.  The
+// batch scan is taken again at each step rather than kept (registers).
+struct SegCursor {
+  int item;
+  int pos, end;  // balanced: the slot's remaining stream pages [pos, end)
+  int b;         // balanced: the next sequence to look at; per-sequence: 1 once returned
+};
+template <bool BAL>
+KVQ_DEVINL SegCursor seg_begin(const DecodeParams& p, int item, int lane, bool spec) {
+  SegCursor c;
+  c.item = item;
+  c.pos = c.end = c.b = 0;
+  if constexpr (BAL) {
+    const BatchScan bs = batch_scan(p, lane, spec, false);
+    const int64_t T = bs.total;
+    const int64_t N = used_slots(p.num_slots, bs.total);
+    const int slot = item / p.Hkv;
+    if (slot < N) {
+      c.pos = static_cast<int>(slot * T / N);
+      c.end = static_cast<int>((slot + 1) * T / N);
+    }
+    // first sequence whose pages reach past pos
+    c.b = __popc(__ballot_sync(0xffffffffu, lane < p.B && bs.incl <= c.pos));
+  }
+  return c;
+}
+template <bool BAL>
+KVQ_DEVINL bool seg_next(const DecodeParams& p, SegCursor& c, ItemRange& r, int lane, bool spec, bool report) {
+  if constexpr (!BAL) {
+    if (c.b) return false;
+    r = item_range(p, c.item, report);
+    c.b = 1;
+    return true;
+  }
+  if (c.pos >= c.end) return false;
+  const BatchScan bs = batch_scan(p, lane, spec, report);
+  while (c.pos < c.end && c.b < p.B) {
+    const int incl = __shfl_sync(0xffffffffu, bs.incl, c.b);
+    const int pages = __shfl_sync(0xffffffffu, bs.pages, c.b);
+    if (incl <= c.pos) {  // sequence b ends before pos (or is empty)
+      ++c.b;
+      continue;
+    }
+    const int start = incl - pages;  // sequence b's first stream page
+    const int stop = min(c.end, incl);
+    const int L = __shfl_sync(0xffffffffu, bs.L, c.b);
+    const int kvh = c.item % p.Hkv, slot = c.item / p.Hkv;
+    r.b = c.b;
+    r.kvh = kvh;
+    r.split = slot;
+    r.hi = L;
+    r.lo = (p.window > 0 && L > p.window) ? L - p.window : 0;
+    r.pg0 = __shfl_sync(0xffffffffu, bs.first, c.b) + (c.pos - start);
+    r.n = stop - c.pos;
+    c.pos = stop;
+    if (stop == incl) ++c.b;
+    return true;
+  }
+  return false;
+}
+
+// Every segment of this CTA's items (item = blockIdx.x, + gridDim.x, ...).
+template <bool BAL>
+struct SegWalk {
+  SegCursor c;
+  KVQ_DEVINL SegWalk(const DecodeParams& p, int lane) {
+    c.item = blockIdx.x;
+    c.pos = c.end = c.b = 0;
+    if (c.item < p.num_items) c = seg_begin<BAL>(p, c.item, lane, false);
+  }
+  KVQ_DEVINL bool next(const DecodeParams& p, int lane, ItemRange& r, bool report) {
+    while (c.item < p.num_items) {
+      if (seg_next<BAL>(p, c, r, lane, false, report)) return true;
+      const int item = c.item + gridDim.x;
+      c.item = item;
+      if (item < p.num_items) c = seg_begin<BAL>(p, item, lane, false);
+    }
+    return false;
+  }
+};
+// The per-sequence plan: one segment per item.
+template <>
+struct SegWalk<false> {
+  int item;
+  bool started;
+  KVQ_DEVINL SegWalk(const DecodeParams&, int) : item(blockIdx.x), started(false) {}
+  KVQ_DEVINL bool next(const DecodeParams& p, int, ItemRange& r, bool report) {
+    if (started) item += gridDim.x;
+    started = true;
+    if (item >= p.num_items) return false;
+    r = item_range(p, item, report);
+    return true;
+  }
+};
+
 // Before the preceding kernel has completed: bring the first pages of this
 // CTA's first item into L2, so that its first stages arrive at L2 rather
 // than HBM latency once it may start.  The sequence length and block ids are
@@ -214,19 +363,32 @@ KVQ_DEVINL ItemRange item_range(const DecodeParams& p, int item, bool report) {
 // the wait; loads cached in L2 only leave no stale L1 line), clamped so that
 // every address stays inside the block table and the caches.  A page the
 // preceding kernel writes after the hint is updated in L2 like any other.
-template <int D, bool FP8, bool PT>
+template <int D, bool FP8, bool PT, bool BAL>
 KVQ_DEVINL void prefetch_first_pages(const DecodeParams& p, int lane, int max_pages) {
   using G = Geo<D, FP8>;
   constexpr int VS = v_stride<D, FP8, PT>();
-  const int NG = p.B * p.Hkv;
-  const int item = blockIdx.x;
-  const int bh = item % NG;
-  const int b = bh / p.Hkv, kvh = bh - b * p.Hkv;
-  int L = ld_l2only_s32(p.seq_lens + b);
-  L = min(max(L, 0), p.max_blocks * kPage);
-  const SplitPages sp = split_pages(L, p.window, p.num_splits);
-  const int pg0 = sp.first + (item / NG) * sp.pps;
-  const int n = min(min(sp.pps, sp.last - pg0), max_pages);
+  int b, kvh, pg0, n;
+  if constexpr (BAL) {
+    SegCursor cur = seg_begin<true>(p, blockIdx.x, lane, true);
+    ItemRange r;
+    if (!seg_next<true>(p, cur, r, lane, true, false)) return;
+    b = r.b;
+    kvh = r.kvh;
+    pg0 = r.pg0;
+    n = r.n;
+  } else {
+    const int NG = p.B * p.Hkv;
+    const int item = blockIdx.x;
+    const int bh = item % NG;
+    b = bh / p.Hkv;
+    kvh = bh - b * p.Hkv;
+    int L = ld_l2only_s32(p.seq_lens + b);
+    L = min(max(L, 0), p.max_blocks * kPage);
+    const SplitPages sp = split_pages(L, p.window, p.num_splits);
+    pg0 = sp.first + (item / NG) * sp.pps;
+    n = min(sp.pps, sp.last - pg0);
+  }
+  n = min(n, max_pages);
   if (lane >= n) return;
   const int blk = ld_l2only_s32(p.block_table + static_cast<size_t>(b) * p.max_blocks + pg0 + lane);
   if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) return;
@@ -251,12 +413,13 @@ constexpr int kPresent0 = 1, kPresent1 = 2, kBad0 = 4, kBad1 = 8;
 // fresh FP32 tile per stage (FP8, per-head scales only).
 // AP: the append entry point's instantiation (the new token's cache write);
 // the plain decode is compiled without it.
-template <int D, bool FP8, int NW, int NST, bool E5, bool PT, bool SL, bool AP = false>
+template <int D, bool FP8, int NW, int NST, bool E5, bool PT, bool SL, bool AP = false, bool BAL = false>
 __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partial_kernel(const __grid_constant__ DecodeParams p) {
   using G = Geo<D, FP8>;
   static_assert(NST % NW == 0 && NST >= NW, "each ring slot must belong to one consumer warp");
   static_assert(FP8 || !PT, "per-token scales apply to FP8 caches");
   static_assert(!SL || (FP8 && !PT), "the single-level ablation covers the per-head FP8 path");
+  static_assert(!BAL || (D == 128 && FP8 && !E5 && !PT && !SL), "the balanced plan covers the E4M3 per-head path");
   constexpr int STRIDE = stage_stride<D, FP8, PT>();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
@@ -288,7 +451,7 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
   // the producer's own chain is not lengthened where nothing runs before.
   // Direct-output calls (one short range per pair) gain nothing from it.
   if (warp == NW - 1 && !p.direct && blockIdx.x < p.num_items) {
-    prefetch_first_pages<D, FP8, PT>(p, lane, PPS * NW);
+    prefetch_first_pages<D, FP8, PT, BAL>(p, lane, PPS * NW);
   }
   grid_dependency_wait();
   if (!p.direct) grid_launch_dependents();
@@ -298,8 +461,11 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
     const uint64_t pol = policy_evict_first();
     uint32_t it = 0;  // stage counter
     bool aborted = false;
-    for (int item = blockIdx.x; item < p.num_items && !aborted; item += gridDim.x) {
-      const ItemRange r = item_range(p, item, lane == 0);
+    SegWalk<BAL> walk(p, lane);
+    // faults in the lengths: reported by lane 0 per item, or (balanced) by the
+    // lane of each sequence in CTA 0
+    const bool report = BAL ? blockIdx.x == 0 : lane == 0;
+    for (ItemRange r; !aborted && walk.next(p, lane, r, report);) {
       const int32_t* bt = p.block_table + static_cast<size_t>(r.b) * p.max_blocks + r.pg0;
       // append: this item holds the page of the sequence's last token
       const int last_pg = (r.hi - 1) / kPage;
@@ -474,8 +640,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
     }
   }
   uint32_t it0 = 0;
-  for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
-    const ItemRange rg = item_range(p, item, false);
+  SegWalk<BAL> walk(p, lane);
+  for (ItemRange rg; walk.next(p, lane, rg, false);) {
     // ---- query fragments of head (kvh * g + r); heads >= g are zero padding ----
     // FP8: q * sigma = hi + lo, two E4M3 terms (sigma = 2^(7 - floor(log2 max|q|))
     // per head) feed the E4M3 MMA; lanes c hold dims 32kk + 4c..4c+3 (b0) and
@@ -847,9 +1013,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
     }
     it0 += nst_item;
 
-    // ---- this warp's partial result for the item (no cross-warp merge) ----
-    // partial row ((b * Hq + head) * S + split) * NW + warp; l and O are in
-    // units of 2^8 p, the log-sum-exp in units of p
+    // ---- this warp's partial result for the segment (no cross-warp merge) ----
+    // partial ((b * Hq + head) * S + split) * NW + warp, or in the balanced
+    // plan (head * kseg + slot + b) * NW + warp; l and O are in units of 2^8 p,
+    // the log-sum-exp in units of p
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       l[0] += __shfl_xor_sync(0xffffffffu, l[0], o);
@@ -904,14 +1071,15 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
     }
     {
       const float vs = (FP8 && !PT) ? p.v_scale[rg.kvh] : 1.f;  // PT: V scales are inside O
-      const size_t row0 = static_cast<size_t>(rg.b) * p.Hq + rg.kvh * p.g;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int h = 2 * c + hh;
         if (h < p.g) {
           const bool any = l[hh] > 0.f;
           const float f = any ? vs / l[hh] : 0.f;
-          const size_t idx = ((row0 + h) * p.num_splits + rg.split) * NW + warp;
+          const size_t hq = static_cast<size_t>(rg.kvh) * p.g + h;
+          const size_t idx = BAL ? ((hq * p.kseg + rg.split + rg.b) * NW + warp)
+                                 : (((static_cast<size_t>(rg.b) * p.Hq + hq) * p.num_splits + rg.split) * NW + warp);
           float* dst = p.o_part + idx * D;
 #pragma unroll
           for (int mt = 0; mt < G::MT; ++mt) {
@@ -932,24 +1100,51 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
 // together (one round trip), merges them against its own maximum, and the
 // warps' results are merged through shared memory.
 constexpr int kCombinePer = 8;  // partials per warp and pass
+// Where a row's partials sit: per-sequence plan, S consecutive partials per
+// row (row * S); balanced plan, the row's segments in its query head's block.
+struct CombinePlan {
+  int S;  // partials per row (per-sequence plan)
+  int balanced;
+  const int32_t* seq_lens;
+  int B, Hq, max_blocks, window, num_slots, kseg;
+};
 template <int NW>
 __global__ void __launch_bounds__(NW * 32) decode_combine_kernel(const float* __restrict__ o_part,
                                                                  const float* __restrict__ lse_part,
-                                                                 __nv_bfloat16* __restrict__ out, int S, int D) {
+                                                                 __nv_bfloat16* __restrict__ out,
+                                                                 const CombinePlan cp, int D) {
   static_assert(NW >= 1 && NW <= 32, "one lane per warp in the final merge");
   __shared__ float m_s[NW];
   __shared__ float den_s[NW];
   __shared__ float acc_s[NW][33];
+  const int row = blockIdx.x;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  size_t first = static_cast<size_t>(row) * cp.S;
+  int S = cp.S;
+  if (cp.balanced) {
+    // the sequence lengths were final before any partial CTA passed its wait,
+    // and this grid launches only after that; L2-only loads see them
+    const BatchScan bs = batch_scan_of(cp.seq_lens, cp.B, cp.max_blocks, cp.window, lane, true, nullptr);
+    const int b = row / cp.Hq, hq = row - b * cp.Hq;
+    const int incl = __shfl_sync(0xffffffffu, bs.incl, b);
+    const int pages = __shfl_sync(0xffffffffu, bs.pages, b);
+    int k0 = 0, cnt = 0;
+    if (pages > 0) {
+      const int N = used_slots(cp.num_slots, bs.total);
+      k0 = slot_of(incl - pages, bs.total, N) + b;
+      cnt = slot_of(incl - 1, bs.total, N) + b - k0 + 1;
+    }
+    first = (static_cast<size_t>(hq) * cp.kseg + k0) * kNW;
+    S = cnt * kNW;
+  }
   grid_dependency_wait();  // the partial kernel's writes are visible past this point
   // the next call's partial kernel may now start its setup (not earlier: its
   // CTAs would wait beside this call's partial CTAs, the slowest of which
   // set the call's time)
   grid_launch_dependents();
-  const int row = blockIdx.x;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int d = blockIdx.y * 32 + lane;
-  const float* lp = lse_part + static_cast<size_t>(row) * S;
-  const float* op = o_part + static_cast<size_t>(row) * S * D + d;
+  const float* lp = lse_part + first;
+  const float* op = o_part + first * D + d;
   float m = -INFINITY, den = 0.f, acc = 0.f;
   for (int s0 = wid; s0 < S; s0 += NW * kCombinePer) {
     float l[kCombinePer], o[kCombinePer];
@@ -1031,11 +1226,22 @@ void split_plan(int B, int Hkv, int D, int P, int max_blocks, int window, int nu
   *pps_out = pps;
 }
 
-template <int D, bool FP8, bool E5 = false, bool PT = false, bool SL = false, bool AP = false>
+// The balanced plan (pages of the batch cut into equal slots) applies to
+// ragged-capable batches that are split at all and fit one warp's scan.
+bool balanced_plan(int B, int S) { return B > 1 && B <= 32 && S > 1; }
+
+// Partials (one per consumer warp) a call writes: per-sequence plan B * Hq
+// * S; balanced plan Hq * (B * S + B - 1) (segment ids slot + b).
+size_t partial_count(int B, int Hq, int S) {
+  if (balanced_plan(B, S)) return static_cast<size_t>(Hq) * (static_cast<size_t>(B) * S + B - 1) * kNW;
+  return static_cast<size_t>(B) * Hq * S * kNW;
+}
+
+template <int D, bool FP8, bool E5 = false, bool PT = false, bool SL = false, bool AP = false, bool BAL = false>
 kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream_t s) {
   constexpr int NST = stages_for<D, FP8, PT>();
   constexpr size_t smem = decode_smem_bytes<D, FP8, NST, PT>();
-  auto kern = decode_partial_kernel<D, FP8, kNW, NST, E5, PT, SL, AP>;
+  auto kern = decode_partial_kernel<D, FP8, kNW, NST, E5, PT, SL, AP, BAL>;
   static int configured_mask = 0;  // devices whose attribute is set
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1077,22 +1283,33 @@ kvq_status_t launch_decode(const DecodeParams& p, __nv_bfloat16* out, cudaStream
   if (q.direct) return KVQ_OK;
   cfg.gridDim = dim3(p.B * p.Hq, D / 32);
   cfg.dynamicSmemBytes = 0;
-  // warps per combine CTA: enough for the row's partials in one pass
-  const int parts = p.num_splits * kNW;
+  CombinePlan cp;
+  cp.S = p.num_splits * kNW;
+  cp.balanced = p.balanced;
+  cp.seq_lens = p.seq_lens;
+  cp.B = p.B;
+  cp.Hq = p.Hq;
+  cp.max_blocks = p.max_blocks;
+  cp.window = p.window;
+  cp.num_slots = p.num_slots;
+  cp.kseg = p.kseg;
+  // warps per combine CTA: enough for a row's partials in one pass (balanced:
+  // a sequence of average length spans about S + 1 segments)
+  const int parts = (p.num_splits + (p.balanced ? 2 : 0)) * kNW;
   const float* op = p.o_part;
   const float* lp = p.lse_part;
   if (parts <= 4 * kCombinePer) {
     cfg.blockDim = dim3(4 * 32);
-    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<4>, op, lp, out, parts, D);
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<4>, op, lp, out, cp, D);
   } else if (parts <= 8 * kCombinePer) {
     cfg.blockDim = dim3(8 * 32);
-    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<8>, op, lp, out, parts, D);
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<8>, op, lp, out, cp, D);
   } else if (parts <= 16 * kCombinePer) {
     cfg.blockDim = dim3(16 * 32);
-    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<16>, op, lp, out, parts, D);
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<16>, op, lp, out, cp, D);
   } else {
     cfg.blockDim = dim3(32 * 32);
-    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<32>, op, lp, out, parts, D);
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<32>, op, lp, out, cp, D);
   }
   return cuda_status(e, "decode combine launch");
 }
@@ -1115,7 +1332,7 @@ extern "C" size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P
   if (B < 1 || Hq < 1 || Hkv < 1 || D < 1 || P < 1 || max_blocks < 1 || num_splits < 0) return 0;
   int S, pps;
   split_plan(B, Hkv, D, P, max_blocks, window, num_splits, &S, &pps);
-  const size_t rows = static_cast<size_t>(B) * Hq * S * kNW;  // one partial per consumer warp
+  const size_t rows = partial_count(B, Hq, S);  // one partial per consumer warp
   const size_t o_bytes = rows * D * sizeof(float);
   return o_bytes + ((rows * sizeof(float) + 15) / 16) * 16;
 }
@@ -1178,8 +1395,7 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
   prm.o_part = static_cast<float*>(workspace);
-  prm.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                          static_cast<size_t>(B) * Hq * S * kNW * D * sizeof(float));
+  prm.lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + partial_count(B, Hq, S) * D * sizeof(float));
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
@@ -1190,6 +1406,12 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
   prm.window = window;
   prm.num_splits = S;
   prm.num_items = static_cast<int>(items);
+  // the balanced plan is compiled for the E4M3 per-head two-level path at
+  // head_dim 128; other paths keep one range per (sequence, KV head, split)
+  prm.balanced = (balanced_plan(B, S) && D == 128 && cache_dtype == KVQ_DTYPE_FP8_E4M3 && !per_token &&
+                  !single_level) ? 1 : 0;
+  prm.num_slots = B * S;
+  prm.kseg = B * S + B - 1;
   prm.dev_status = dev_status;
   prm.k_new = app ? static_cast<const uint16_t*>(app->k_new) : nullptr;
   prm.v_new = app ? static_cast<const uint16_t*>(app->v_new) : nullptr;
@@ -1222,14 +1444,19 @@ kvq_status_t paged_decode(const void* q, const void* k_cache, const void* v_cach
     if (e5)
       return D == 128 ? launch_decode<128, true, true, false, false, true>(prm, o, s)
                       : launch_decode<64, true, true, false, false, true>(prm, o, s);
-    if (D == 128)
+    if (D == 128) {
+      if (prm.balanced) return launch_decode<128, true, false, false, false, true, true>(prm, o, s);
       return fp8 ? launch_decode<128, true, false, false, false, true>(prm, o, s)
                  : launch_decode<128, false, false, false, false, true>(prm, o, s);
+    }
     return fp8 ? launch_decode<64, true, false, false, false, true>(prm, o, s)
                : launch_decode<64, false, false, false, false, true>(prm, o, s);
   }
   if (e5) return D == 128 ? launch_decode<128, true, true>(prm, o, s) : launch_decode<64, true, true>(prm, o, s);
-  if (D == 128) return fp8 ? launch_decode<128, true>(prm, o, s) : launch_decode<128, false>(prm, o, s);
+  if (D == 128) {
+    if (prm.balanced) return launch_decode<128, true, false, false, false, false, true>(prm, o, s);
+    return fp8 ? launch_decode<128, true>(prm, o, s) : launch_decode<128, false>(prm, o, s);
+  }
   return fp8 ? launch_decode<64, true>(prm, o, s) : launch_decode<64, false>(prm, o, s);
 }
 

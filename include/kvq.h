@@ -200,7 +200,8 @@ int kvq_decode_num_splits(int B, int Hkv, int D, int P, int max_blocks, int wind
 
 /* Workspace bytes a decode call with these arguments needs (float32
  * partial outputs [B][Hq][S][4][D] and log-sum-exps [B][Hq][S][4]: one per
- * consumer warp of each of the S page ranges). */
+ * consumer warp of each of the S page ranges; for 2 to 32 sequences and
+ * S > 1, [Hq][B * S + B - 1][4] partials, the ragged-batch plan's). */
 size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P, int max_blocks,
                                  int window, int num_splits);
 
@@ -221,9 +222,16 @@ size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P, int max_b
  * partial kernel merges its warps in shared memory and writes the output
  * itself):
  *   lse = log sum_i exp(lse_i),  out = sum_i exp(lse_i - lse) out_i.
+ * Ragged batches (E4M3 cache, per-head scales, D = 128, 2 to 32 sequences,
+ * S = num_splits > 1): per KV head the batch's attended pages are laid end
+ * to end and cut into min(B * S, pages) equal slots instead, so that a long
+ * sequence gets more ranges than a short one; a slot's part inside each
+ * sequence it covers is merged like a range.  The plan is a function of
+ * seq_lens alone: results are deterministic.
  * Both kernels are programmatic dependent launches: their launch and setup
- * overlap the preceding kernel on the stream, and neither touches global
- * memory before that kernel has completed.  A grid smaller than the GPU's
+ * overlap the preceding kernel on the stream, and neither reads anything it
+ * uses from global memory before that kernel has completed (before it, the
+ * partial kernel only hints L2 with its first pages).  A grid smaller than the GPU's
  * resident capacity asks for more shared memory per CTA than it uses, so
  * that its CTAs spread over the SMs; the combine's CTAs have as many warps
  * as the partials of a row need.
