@@ -136,8 +136,13 @@ struct PrefillParams {
 template <int NKV>
 struct Bars {
   uint64_t q_full;
-  uint64_t kv_full[NKV];
-  uint64_t kv_empty[NKV];
+  // K and V of a stage land and are released separately: K once S = Q K^T
+  // has been computed, V once P.V has, so the next K tile is copied while
+  // this tile's softmax and P.V still run
+  uint64_t k_full[NKV];
+  uint64_t v_full[NKV];
+  uint64_t k_empty[NKV];
+  uint64_t v_empty[NKV];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full;  // P.V of the current tile is in O_tile
@@ -148,7 +153,7 @@ struct Bars {
   uint64_t stall;  // nothing arrives on it (test hook)
   uint32_t tmem_base;
   int abort;
-  uint32_t stage_bad[NKV];  // bit i: page i of the stage was zero-filled (bad block id)
+  uint32_t tile_bad[8];  // bit i: page i of tile j (slot j % 8) had a bad block id
 };
 
 // ------------------------------------------------------------ tcgen05 PTX ---
@@ -302,6 +307,14 @@ template <int HD, bool SL, bool E5 = false, bool PT = false>
 __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
   using G = Geo<HD, PT>;
   static_assert(HD == 128 || (HD == 256 && SL), "head_dim 256 runs with single-level accumulation");
+  // K/V stage protocol.  Split: K and V of a stage land and are released
+  // separately (K once S = Q K^T is computed and the softmax has read the
+  // tile's page flags, V after P.V), so the next K tile is copied while this
+  // tile's softmax and P.V run; the ring holds only two 64 KiB stages at head
+  // dim 256, where this took 5.19 ms to 1.88 ms.  Combined: one barrier pair
+  // per stage, both halves released after P.V -- per-token scales, whose
+  // softmax reads the K scales from the V pages' tails (measured faster).
+  constexpr bool SPLIT = !PT;
   static_assert(!PT || (HD == 128 && !SL), "per-token scales: head_dim 128, two-level accumulation");
   constexpr int NKV = G::NKV, PAGE_B = G::PAGE_B, TILE_B = G::TILE_B, STAGE_B = G::STAGE_B;
   constexpr int VPAGE_B = G::VPAGE_B;
@@ -323,9 +336,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, NSOFT * 32);
     for (int i = 0; i < NKV; ++i) {
-      mbar_init(&bars->kv_full[i], 1);
-      mbar_init(&bars->kv_empty[i], 1);
-      bars->stage_bad[i] = 0;
+      mbar_init(&bars->k_full[i], 1);
+      mbar_init(&bars->v_full[i], 1);
+      // split: released by the QK^T commit and by the softmax once every
+      // softmax thread is past its wait on k_full (which then cannot move on)
+      mbar_init(&bars->k_empty[i], SPLIT ? 2 : 1);
+      mbar_init(&bars->v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -374,6 +390,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       int ids = load_ids(0);
       int ids_next = load_ids(1);
       int cur_grp = 0;
+      bool k_only = false;  // stopped between a tile's K and V copies
       int j = (warp == W_PROD0) ? 0 : 1;  // this producer's first tile
       for (; j < nkv; j += NPROD) {
         if ((j >> 2) != cur_grp) {  // steps of NPROD < 4 tiles: at most one group ahead
@@ -382,60 +399,94 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
           ids_next = load_ids(cur_grp + 1);
         }
         const int st = j % NKV;
+        const uint32_t free_parity = ((j / NKV) & 1) ^ 1;
+        // split: K on k_full after k_empty, V below; combined: both halves on
+        // v_full after v_empty
+        uint64_t* k_bar = SPLIT ? &bars->k_full[st] : &bars->v_full[st];
+        uint64_t* k_free = SPLIT ? &bars->k_empty[st] : &bars->v_empty[st];
         int ok = 1;
-        if (lane == 0) ok = (!*abort_flag && mbar_wait(&bars->kv_empty[st], ((j / NKV) & 1) ^ 1, abort_flag)) ? 1 : 0;
+        if (lane == 0) ok = (!*abort_flag && mbar_wait(k_free, free_parity, abort_flag)) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         uint8_t* ks = smem + OFF_KV + st * STAGE_B;
         uint8_t* vs = ks + TILE_B;
         // lanes 0..7: one page each
         int blk = __shfl_sync(0xffffffffu, ids, ((j & 3) << 3) | (lane & 7));
-        uint32_t bad = 0;
         const int page = j * (TK / kPage) + lane;
         if (lane >= TK / kPage || page >= n_pages) {
           blk = -1;
         } else if (blk < 0 || static_cast<int64_t>(blk) >= p.num_blocks) {
           set_status(p.dev_status, KVQ_DEV_BAD_BLOCK);
           blk = -1;
-          bad = 1;
         }
-        const uint32_t bad_mask = __ballot_sync(0xffffffffu, bad != 0);
         const uint32_t load_mask = __ballot_sync(0xffffffffu, blk >= 0) & 0xFFu;
-        // zero-fill pages that are not loaded (past the end, or bad block ids)
-        if (load_mask != 0xFFu) {
+        const uint32_t bad_mask = __ballot_sync(0xffffffffu, lane < TK / kPage && page < n_pages && blk < 0) & 0xFFu;
+        // zero-fill pages that are not loaded (past the end, or bad block ids):
+        // K here, V once its half of the stage is free
+        auto zero_v = [&]() {
           for (int pg = 0; pg < TK / kPage; ++pg) {
             if (load_mask & (1u << pg)) continue;
             uint4* vz = reinterpret_cast<uint4*>(vs + pg * VPAGE_B);
+            for (int i = lane; i < VPAGE_B / 16; i += 32) vz[i] = make_uint4(0, 0, 0, 0);  // codes (and scales)
+          }
+        };
+        if (load_mask != 0xFFu) {
+          for (int pg = 0; pg < TK / kPage; ++pg) {
+            if (load_mask & (1u << pg)) continue;
             for (int i = lane; i < PAGE_B / 16; i += 32) {
               // K: the page's kPage rows in each plane
               const int pl = i / (kPage * PLANE / 16), w = i % (kPage * PLANE / 16);
               reinterpret_cast<uint4*>(ks + pl * G::PLANE_K + pg * kPage * PLANE)[w] = make_uint4(0, 0, 0, 0);
             }
-            for (int i = lane; i < VPAGE_B / 16; i += 32) vz[i] = make_uint4(0, 0, 0, 0);  // codes (and scales)
           }
+          if constexpr (!SPLIT) zero_v();
           fence_proxy_async_smem();  // the zeros, before the tensor cores read the stage
         }
         __syncwarp();
         if (lane == 0) {
-          bars->stage_bad[st] = bad_mask & 0xFFu;
-          mbar_arrive_expect_tx(&bars->kv_full[st], static_cast<uint32_t>(PAGE_B + VPAGE_B) * __popc(load_mask));
+          bars->tile_bad[j & 7] = bad_mask;
+          mbar_arrive_expect_tx(k_bar, static_cast<uint32_t>(SPLIT ? PAGE_B : PAGE_B + VPAGE_B) * __popc(load_mask));
         }
         __syncwarp();
+        size_t pair_off = 0;
         if (lane < TK / kPage && blk >= 0) {
-          const size_t off = (static_cast<size_t>(blk) * p.Hkv + job.kvh) * p.k_str;
-          // K: one copy per plane (a K page of head dim 256 is stored as two half-pages)
+          pair_off = static_cast<size_t>(blk) * p.Hkv + job.kvh;
+          const size_t off = pair_off * p.k_str;
+          // one copy per plane (a K page of head dim 256 is stored as two half-pages)
 #pragma unroll
           for (int pl = 0; pl < HD / PLANE; ++pl)
             bulk_g2s(ks + pl * G::PLANE_K + lane * kPage * PLANE, p.k_cache + off + pl * kPage * PLANE, kPage * PLANE,
-                     &bars->kv_full[st], policy_evict_last());
-          const size_t voff = (static_cast<size_t>(blk) * p.Hkv + job.kvh) * p.v_str;  // PT: page + tail
-          bulk_g2s(vs + lane * VPAGE_B, p.v_cache + voff, VPAGE_B, &bars->kv_full[st], policy_evict_last());
+                     k_bar, policy_evict_last());
+          // combined: the V page (PT: with its scale tail) on the same barrier
+          if constexpr (!SPLIT)
+            bulk_g2s(vs + lane * VPAGE_B, p.v_cache + pair_off * p.v_str, VPAGE_B, k_bar, policy_evict_last());
+        }
+        if constexpr (SPLIT) {
+          if (lane == 0) ok = (!*abort_flag && mbar_wait(&bars->v_empty[st], free_parity, abort_flag)) ? 1 : 0;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) {
+            k_only = true;
+            break;
+          }
+          if (load_mask != 0xFFu) {
+            zero_v();
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], static_cast<uint32_t>(VPAGE_B) * __popc(load_mask));
+          __syncwarp();
+          if (lane < TK / kPage && blk >= 0)
+            bulk_g2s(vs + lane * VPAGE_B, p.v_cache + pair_off * p.v_str, VPAGE_B, &bars->v_full[st], policy_evict_last());
         }
       }
       if (j < nkv && lane == 0) {  // abandoned: let this producer's issued copies land
         set_status(p.dev_status, KVQ_DEV_TIMEOUT);
         *abort_flag = 1;
-        for (int k = j - NPROD; k >= 0 && k >= j - NKV; k -= NPROD) mbar_wait(&bars->kv_full[k % NKV], (k / NKV) & 1);
+        for (int k = j - NPROD; k >= 0 && k >= j - NKV; k -= NPROD) {
+          if constexpr (SPLIT) mbar_wait(&bars->k_full[k % NKV], (k / NKV) & 1);
+          mbar_wait(&bars->v_full[k % NKV], (k / NKV) & 1);
+        }
+        if (k_only) mbar_wait(&bars->k_full[j % NKV], (j / NKV) & 1);
       }
     } else if (warp == W_MMA) {
       // ------------------------------------------------------------ MMA issuer --
@@ -455,7 +506,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       };
       auto issue_s = [&](int j) {  // S[j%2] = Q K_j^T
         const int st = j % NKV;
-        if (!wait(&bars->kv_full[st], (j / NKV) & 1)) return;
+        if (!wait(SPLIT ? &bars->k_full[st] : &bars->v_full[st], (j / NKV) & 1)) return;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t k_s = sbase + OFF_KV + st * STAGE_B;
@@ -465,6 +516,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
             umma_f8(d, desc_sw128(q_s + (kk >> 2) * G::PLANE_Q + (kk & 3) * 32),
                     desc_sw128(k_s + (kk >> 2) * G::PLANE_K + (kk & 3) * 32), IDESC_S, kk > 0 ? 1u : 0u);
           umma_commit(&bars->s_full[j & 1]);
+          if constexpr (SPLIT) umma_commit(&bars->k_empty[st]);  // the K half may be refilled
         }
         __syncwarp();
       };
@@ -482,6 +534,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
         if (!wait(&bars->p_full[j & 1], (j >> 1) & 1)) break;
         // two-level: O_tile of tile j - 1 has been read; SL: O has been rescaled for tile j
         if (j >= 1 && !wait(&bars->o_free, (j - 1) & 1)) break;
+        // split: V_j (combined: it landed with K_j, before S_j)
+        if (SPLIT && !wait(&bars->v_full[j % NKV], (j / NKV) & 1)) break;
         tc_fence_after();
         if (lane == 0) {
           const int st = j % NKV;
@@ -508,7 +562,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
                        kk > 0 ? 1u : 0u);
           }
           umma_commit(&bars->o_full);
-          umma_commit(&bars->kv_empty[st]);
+          umma_commit(&bars->v_empty[st]);
         }
         __syncwarp();
       }
@@ -739,11 +793,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       float sv[HC];
       float mx = -INFINITY;
       float vmx = 0.f;  // PT: the largest V scale of this thread's cached keys
-      uint32_t bad = 0;
-      // S_j, then the stage's page flags and, for the last page, zeroing of its unused V slots
-      if (wait_all(&bars->s_full[j & 1], (j >> 1) & 1) && wait_all(&bars->kv_full[st], (j / NKV) & 1)) {
+      uint32_t bad = 0;  // pages of the tile with an invalid block id (zero-filled)
+      // S_j; then the stage's barrier for the tile's page flags -- split: k_full,
+      // which cannot move on before every softmax thread has passed this wait
+      // (the softmax's arrive on k_empty below); combined: v_full -- and, split,
+      // V_j where the last page's unused V slots are zeroed here
+      if (wait_all(&bars->s_full[j & 1], (j >> 1) & 1) &&
+          wait_all(SPLIT ? &bars->k_full[st] : &bars->v_full[st], (j / NKV) & 1) &&
+          (!SPLIT || !tail_tile || wait_all(&bars->v_full[st], (j / NKV) & 1))) {
         tc_fence_after();
-        bad = bars->stage_bad[st];
+        bad = bars->tile_bad[j & 7];
         if (tail_tile) {
           // V rows (dims) row and row + 128 .. of the last page: slots past the sequence end
           for (int d = row + part * TQ; d < HD; d += NPART * TQ) {
@@ -821,6 +880,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) prefill_kernel(const __grid_const
       xmax[((j & 1) * NPART + part) * TQ + row] = mx;
       if (PT && row == 0) xv[(j & 1) * NPART + part] = vmx;
       named_bar_sync(1, NSOFT * 32);
+      // split: every softmax thread has read the tile's page flags and passed
+      // k_full: the K half of the stage may be refilled once S_j is computed
+      if (SPLIT && threadIdx.x == 0) mbar_arrive(&bars->k_empty[st]);
       if (ok) {
         // m and the maxima are raw scores; 2^(s - M) * 256 = 2^(raw * coef - (M - 8)),
         // the largest in (128, 256]
