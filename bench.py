@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--no-per-token", action="store_true")
     ap.add_argument("--no-ablation", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the tiny, concurrency-8 and hybrid legs")
+    ap.add_argument("--prefill-head-dim", type=int, choices=[128, 256], default=128,
+                    help="head dim of the prefill leg (256 runs single-level accumulation)")
     ap.add_argument("--separate-caches", action="store_true",
                     help="separate K and V allocations instead of the paired layout")
     ap.add_argument("--layers", type=int, default=32,
@@ -1050,7 +1052,12 @@ def ours_arm(args, rank, world, local_rank):
         configs = {"tiny_decode_512": clocked(local_rank, tiny_leg, device),
                    "llama31_8b_decode_conc8_20k": clocked(local_rank, conc8_leg, device),
                    "gpt_oss_20b_hybrid_decode_32k": clocked(local_rank, hybrid_leg, device)}
-    pf = clocked(local_rank, prefill_leg, device) if legs and not args.no_prefill else None
+    pf = None
+    if legs and not args.no_prefill:
+        if args.prefill_head_dim == 256:
+            pf = clocked(local_rank, prefill_leg, device, head_dim=256)
+        else:
+            pf = clocked(local_rank, prefill_leg, device)
     if pf is not None and not args.no_e5m2:
         pf["e5m2_cache"] = clocked(local_rank, prefill_leg, device, cache_dtype="fp8_e5m2")
         pf["per_token_scales"] = clocked(local_rank, prefill_leg, device, per_token=True)
