@@ -193,8 +193,10 @@ kvq_status_t kvq_quantize_query(const void* q, uint8_t* q8, const float* q_scale
 /*
  * Split-KV plan for kvq_paged_decode_attention.  num_splits = 0 asks for the
  * library's choice for this GPU (one wave of resident CTAs: 3 per SM, 4 at
- * head dim D = 64); the function returns the number of splits that a call
- * with the same arguments will use (>= 1), or 0 on bad input.
+ * head dim D = 64; at least 4 pages per split; 1 split for at most 8 pages,
+ * or at most 16 pages over 32 or more (sequence, KV head) pairs); the
+ * function returns the number of splits that a call with the same arguments
+ * will use (>= 1), or 0 on bad input.
  */
 int kvq_decode_num_splits(int B, int Hkv, int D, int P, int max_blocks, int window, int num_splits);
 
