@@ -17,13 +17,16 @@
 // ring of NST shared-memory stages guarded by mbarriers.  Warps 0..NW-1
 // consume stages round-robin; each ring slot belongs to one warp.  FP8
 // cache: a consumer copies its whole stage into registers with ldmatrix and
-// releases the slot at once; S^T = K Q^T (16 tokens x 8 query heads, M =
-// tokens) runs on mma.m16n8k32 with E4M3 operands straight from the cache
-// bytes, q entering as two exact E4M3 terms; one online-softmax update (base
-// 2) covers the stage's 32 tokens; P is transposed in registers (movmatrix)
-// and split into two E4M3 terms, and O^T = V^T P^T (M = dims, K = the 32
-// token slots of both pages) goes into fresh FP32 fragments that are then
-// added into the running output.  BF16 cache: the same flow on bf16 MMAs.
+// releases the slot at once; the FP8 codes are converted to f16 in registers
+// (exact) and S^T = K Q^T (16 tokens x 8 query heads, M = tokens) runs on
+// mma.m16n8k16 f16 with q as f16(q * 2^k); one online-softmax update (base 2)
+// covers the stage's 32 tokens; P is rounded to f16 and transposed in
+// registers (movmatrix), and O^T = V^T P^T (M = dims, K = the tokens of each
+// page) goes into fresh FP32 fragments that are then added into the running
+// output.  (On this GPU an E4M3 mma.sync costs about as many issue slots per
+// instruction as an f16 one plus the operand conversion, and its latency is
+// higher: the conversion done once per fragment here is cheaper.)  BF16
+// cache: the same flow on bf16 MMAs.
 // At the end of an item each consumer warp writes its own normalized partial
 // output and log2-sum-exp per query head (no cross-warp merge).  Items are
 // ordered so that consecutive CTAs serve different (sequence, KV head)
@@ -643,21 +646,24 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
   SegWalk<BAL> walk(p, lane);
   for (ItemRange rg; walk.next(p, lane, rg, false);) {
     // ---- query fragments of head (kvh * g + r); heads >= g are zero padding ----
-    // FP8: q * sigma = hi + lo, two E4M3 terms (sigma = 2^(7 - floor(log2 max|q|))
-    // per head) feed the E4M3 MMA; lanes c hold dims 32kk + 4c..4c+3 (b0) and
-    // 32kk + 16 + 4c..4c+3 (b1).  BF16: q as stored.
-    constexpr int QW = FP8 ? (D / 32) * 2 : G::KS * 2;  // 32-bit words per term
-    uint32_t qh[QW], ql[FP8 ? QW : 1];
+    // FP8 cache: f16(q * sigma), sigma = 2^(7 - floor(log2 max|q|)) per head (a
+    // bf16 value times a power of two: exact unless it falls below f16's
+    // normal range), for the f16 MMAs; word 2w holds dims d, d + 1 and word
+    // 2w + 1 dims d + 2, d + 3 for d = 32 (w / 2) + 16 (w % 2) + 4c.  BF16: q
+    // as stored.
+    constexpr int QW = D / 8;  // 32-bit words of q per lane
+    uint32_t qh[QW];
     float coef0, coef1;  // score coefficient of heads 2c and 2c + 1
     {
       const bool live = r < p.g;
       const uint16_t* qrow = static_cast<const uint16_t*>(p.q) +
                              (static_cast<size_t>(rg.b) * p.Hq + rg.kvh * p.g + (live ? r : 0)) * D;
       if constexpr (FP8) {
-        float x[QW][4];
+        constexpr int NL = D / 16;  // loads of four dims per lane
+        float x[NL][4];
         float mx = 0.f;
 #pragma unroll
-        for (int w = 0; w < QW; ++w) {
+        for (int w = 0; w < NL; ++w) {
           const int dim = (w >> 1) * 32 + (w & 1) * 16 + 4 * c;
           const uint2 u = live ? __ldg(reinterpret_cast<const uint2*>(qrow + dim)) : make_uint2(0, 0);
           x[w][0] = __uint_as_float(u.x << 16);
@@ -674,15 +680,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
         const float sigma = __uint_as_float(static_cast<uint32_t>(127 + 7 - e2) << 23);   // 2^(7 - e2)
         const float inv_sigma = __uint_as_float(static_cast<uint32_t>(127 - 7 + e2) << 23);
 #pragma unroll
-        for (int w = 0; w < QW; ++w) {
-          const float y0 = x[w][0] * sigma, y1 = x[w][1] * sigma, y2 = x[w][2] * sigma, y3 = x[w][3] * sigma;
-          const uint32_t h01 = f32x2_to_e4m3x2(y0, y1), h23 = f32x2_to_e4m3x2(y2, y3);
-          const uint32_t f01 = e4m3x2_to_f16x2(static_cast<uint16_t>(h01));
-          const uint32_t f23 = e4m3x2_to_f16x2(static_cast<uint16_t>(h23));
-          const float2 d01 = __half22float2(*reinterpret_cast<const __half2*>(&f01));
-          const float2 d23 = __half22float2(*reinterpret_cast<const __half2*>(&f23));
-          qh[w] = h01 | (h23 << 16);
-          ql[w] = f32x2_to_e4m3x2(y0 - d01.x, y1 - d01.y) | (f32x2_to_e4m3x2(y2 - d23.x, y3 - d23.y) << 16);
+        for (int w = 0; w < NL; ++w) {
+          qh[2 * w] = pack_f16x2(x[w][0] * sigma, x[w][1] * sigma);
+          qh[2 * w + 1] = pack_f16x2(x[w][2] * sigma, x[w][3] * sigma);
         }
         // per-head K scale folded in here; per-token K scales multiply each score later
         const float cf = PT ? __fmul_rn(p.sm_scale, kLog2e) : __fmul_rn(__fmul_rn(p.k_scale[rg.kvh], p.sm_scale), kLog2e);
@@ -695,7 +695,6 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
           qh[2 * kk] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * c)) : 0u;
           qh[2 * kk + 1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * c)) : 0u;
         }
-        ql[0] = 0u;
         coef0 = coef1 = __fmul_rn(p.sm_scale, kLog2e);
       }
     }
@@ -776,15 +775,25 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
           sv10 = t1[kPage + r];
           sv11 = t1[kPage + r + 8];
         }
-        // ---- S^T = K Q^T, E4M3 MMA, q as hi + lo (two independent chains) ----
+        // ---- S^T = K Q^T on f16 MMAs: the K codes converted in registers (exact).
+        // An ldmatrix of 32 dims holds, per lane, dims 4c..4c+3 (x0: row r, x1:
+        // row r + 8) and 16 + 4c..16 + 4c + 3 (x2, x3) of the chunk; each half
+        // is one m16n8k16 with its k order permuted (k 2c, 2c + 1 <- dims 4c,
+        // 4c + 1; k 2c + 8, 2c + 9 <- dims 4c + 2, 4c + 3), q permuted alike.
+        // Two independent accumulation chains, one per half ----
         auto qk = [&](uint32_t kp, float (&s)[4], float ska, float skb) {  // ska, skb: tokens r, r + 8
           float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < D / 32; ++kk) {
             uint32_t x0, x1, x2, x3;
             ldsm_x4(kp + koff[kk], x0, x1, x2, x3);
-            mma_fp8<E5>(a, x0, x1, x2, x3, qh[2 * kk], qh[2 * kk + 1], a);
-            mma_fp8<E5>(b, x0, x1, x2, x3, ql[2 * kk], ql[2 * kk + 1], b);
+            uint32_t l0, h0, l1, h1, l2, h2, l3, h3;
+            fp8x4_to_f16x2x2<E5>(x0, l0, h0);
+            fp8x4_to_f16x2x2<E5>(x1, l1, h1);
+            fp8x4_to_f16x2x2<E5>(x2, l2, h2);
+            fp8x4_to_f16x2x2<E5>(x3, l3, h3);
+            mma_f16(a, l0, l1, h0, h1, qh[4 * kk], qh[4 * kk + 1], a);
+            mma_f16(b, l2, l3, h2, h3, qh[4 * kk + 2], qh[4 * kk + 3], b);
           }
           s[0] = (a[0] + b[0]) * coef0;
           s[1] = (a[1] + b[1]) * coef1;
@@ -860,8 +869,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
         if constexpr (PT) {  // l above summed the unweighted p
           p00 *= w00; p01 *= w00; p02 *= w01; p03 *= w01;
           p10 *= w10; p11 *= w10; p12 *= w11; p13 *= w11;
-          // Weights below 1 push probabilities toward E4M3's lower end, where the
-          // two-term split loses them.  Per head, a power of two f moves the stage's
+          // Weights below 1 push probabilities toward f16's lower end, where they
+          // lose bits.  Per head, a power of two f moves the stage's
           // largest weighted probability into [128, 256); P.V is then scaled by c / f.
           float pm0 = fmaxf(fmaxf(p00, p02), fmaxf(p10, p12));
           float pm1 = fmaxf(fmaxf(p01, p03), fmaxf(p11, p13));
@@ -882,46 +891,29 @@ __global__ void __launch_bounds__((NW + 1) * 32, ctas_per_sm<D>()) decode_partia
           p00 *= f0; p01 *= f1; p02 *= f0; p03 *= f1;
           p10 *= f0; p11 *= f1; p12 *= f0; p13 *= f1;
         }
-        // ---- P^T fragments: transpose f16 pairs, then two E4M3 terms (three with
-        // per-token weights, which make even the largest probability inexact in
-        // E4M3); each residual is an exact f16 difference of nearby values ----
-        auto pterms = [&](float x0, float x1, float x2, float x3, uint32_t& hi, uint32_t& lo, uint32_t& lo2) {
-          const uint32_t t0 = movmatrix_t(pack_f16x2(x0, x1));  // tokens 2c, 2c+1 of head r
-          const uint32_t t1 = movmatrix_t(pack_f16x2(x2, x3));  // tokens 2c+8, 2c+9
-          const uint32_t h0 = f16x2_to_e4m3x2(t0), h1 = f16x2_to_e4m3x2(t1);
-          hi = h0 | (h1 << 16);
-          const uint32_t d0 = e4m3x2_to_f16x2(static_cast<uint16_t>(h0));
-          const uint32_t d1 = e4m3x2_to_f16x2(static_cast<uint16_t>(h1));
-          const __half2 r0 = __hsub2(*reinterpret_cast<const __half2*>(&t0), *reinterpret_cast<const __half2*>(&d0));
-          const __half2 r1 = __hsub2(*reinterpret_cast<const __half2*>(&t1), *reinterpret_cast<const __half2*>(&d1));
-          const uint32_t l0 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&r0));
-          const uint32_t l1 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&r1));
-          lo = l0 | (l1 << 16);
-          if constexpr (PT) {
-            const uint32_t e0 = e4m3x2_to_f16x2(static_cast<uint16_t>(l0));
-            const uint32_t e1 = e4m3x2_to_f16x2(static_cast<uint16_t>(l1));
-            const __half2 u0 = __hsub2(r0, *reinterpret_cast<const __half2*>(&e0));
-            const __half2 u1 = __hsub2(r1, *reinterpret_cast<const __half2*>(&e1));
-            lo2 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&u0)) |
-                  (f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&u1)) << 16);
-          }
-        };
-        uint32_t ph0, pl0, pt0 = 0u, ph1 = 0u, pl1 = 0u, pt1 = 0u;
-        pterms(p00, p01, p02, p03, ph0, pl0, pt0);
-        pterms(p10, p11, p12, p13, ph1, pl1, pt1);
-        // ---- O^T += V^T P^T (32 token slots per MMA), fresh FP32 per stage ----
+        // ---- P^T fragments: f16 pairs transposed, tokens 2c, 2c + 1 (pa0) and
+        // 2c + 8, 2c + 9 (pa1) of head r: the B operand of the f16 P.V MMAs ----
+        const uint32_t pa0 = movmatrix_t(pack_f16x2(p00, p01)), pa1 = movmatrix_t(pack_f16x2(p02, p03));  // page 0
+        const uint32_t pb0 = movmatrix_t(pack_f16x2(p10, p11)), pb1 = movmatrix_t(pack_f16x2(p12, p13));  // page 1
+        // ---- O^T += V^T P^T: per m-tile one m16n8k16 per page on the V codes
+        // converted in registers (a lane's word holds tokens 2c, 2c + 1, 2c + 8,
+        // 2c + 9 of its dimension: the A operand's k order), fresh FP32 per stage ----
 #pragma unroll
         for (int mt = 0; mt < G::MT; ++mt) {
+          uint32_t v0l, v0h, v1l, v1h, v2l, v2h, v3l, v3h;
+          fp8x4_to_f16x2x2<E5>(va[mt][0], v0l, v0h);
+          fp8x4_to_f16x2x2<E5>(va[mt][1], v1l, v1h);
+          fp8x4_to_f16x2x2<E5>(va[mt][2], v2l, v2h);
+          fp8x4_to_f16x2x2<E5>(va[mt][3], v3l, v3h);
           if constexpr (SL) {  // the MMAs add this stage into O * alpha themselves
             float c4[4] = {O[mt][0] * al0, O[mt][1] * al1, O[mt][2] * al0, O[mt][3] * al1};
-            mma_fp8<E5>(c4, va[mt][0], va[mt][1], va[mt][2], va[mt][3], ph0, ph1, c4);
-            mma_fp8<E5>(O[mt], va[mt][0], va[mt][1], va[mt][2], va[mt][3], pl0, pl1, c4);
+            mma_f16(c4, v0l, v1l, v0h, v1h, pa0, pa1, c4);
+            mma_f16(O[mt], v2l, v3l, v2h, v3h, pb0, pb1, c4);
             continue;
           }
           float t[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_fp8<E5>(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], ph0, ph1, t);
-          mma_fp8<E5>(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], pl0, pl1, t);
-          if constexpr (PT) mma_fp8<E5>(t, va[mt][0], va[mt][1], va[mt][2], va[mt][3], pt0, pt1, t);
+          mma_f16(t, v0l, v1l, v0h, v1h, pa0, pa1, t);
+          mma_f16(t, v2l, v3l, v2h, v3h, pb0, pb1, t);
           if constexpr (PT) {
             O[mt][0] = fmaf(t[0], g0, O[mt][0] * al0);
             O[mt][1] = fmaf(t[1], g1, O[mt][1] * al1);

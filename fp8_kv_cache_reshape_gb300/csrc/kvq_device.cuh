@@ -260,6 +260,21 @@ KVQ_DEVINL void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
       : "=r"(lo), "=r"(hi)
       : "r"(x));
 }
+// Four E5M2 codes in one register -> two f16x2 registers, as above; exact.
+KVQ_DEVINL void e5m2x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e5m2x2 %0, a;\n\tcvt.rn.f16x2.e5m2x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+template <bool E5>
+KVQ_DEVINL void fp8x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  if constexpr (E5) {
+    e5m2x4_to_f16x2x2(x, lo, hi);
+  } else {
+    e4m3x4_to_f16x2x2(x, lo, hi);
+  }
+}
 KVQ_DEVINL uint32_t pack_f16x2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

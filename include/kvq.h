@@ -257,16 +257,15 @@ size_t kvq_decode_workspace_size(int B, int Hq, int Hkv, int D, int P, int max_b
  *               16-byte aligned, owned by the caller; contents on entry are
  *               ignored; calls sharing a workspace must not overlap.
  *  Supported: D in {64, 128}, P == 16, Hq % Hkv == 0, Hq / Hkv <= 8.
- *  Declared rounding: FP8 -- per query head, sigma = 2^(7 - floor(log2
- *  max_d |q_d|)) and q * sigma = hi + lo with hi = e4m3(q * sigma), lo =
- *  e4m3(q * sigma - hi) (float32, RNE, saturating): exact except for
- *  elements below 2^-9 of the head's maximum; K and V codes are used
- *  exactly (E4M3 or E5M2: the MMA takes either as its cache operand, with
- *  the query / probability operand in E4M3); scores s2 = fl32(sum_d
- *  (hi + lo)_d k8_d) * c / sigma with c =
- *  fl32(fl32(k_scale * sm_scale) * log2(e)); probabilities 2^(s2 - m) * 2^8
- *  are rounded to float16 and fed to the P.V MMA as two E4M3 terms (hi + lo,
- *  about 8 significant bits); the result is multiplied by v_scale.  BF16 -- scores use
+ *  Declared rounding: FP8 -- the K and V codes (E4M3 or E5M2) are converted
+ *  to float16 in registers (exact) and both contractions run on float16
+ *  MMAs with FP32 accumulation; per query head, sigma = 2^(7 - floor(log2
+ *  max_d |q_d|)) and the query enters as qf = f16(fl32(q * sigma)) (RNE:
+ *  exact for bf16 queries except elements that fall below float16's normal
+ *  range, under 2^-21 of the head's maximum); scores s2 = fl32(sum_d qf_d
+ *  k8_d) * c / sigma with c = fl32(fl32(k_scale * sm_scale) * log2(e));
+ *  probabilities 2^(s2 - m) * 2^8 are rounded to float16 (11 significant
+ *  bits) for the P.V MMA; the result is multiplied by v_scale.  BF16 -- scores use
  *  q and k exactly, c = fl32(sm_scale * log2(e)); probabilities are fed to
  *  the P.V MMA as the sum of two bfloat16 terms.  The output is rounded to
  *  bf16 once, at the end.
@@ -373,10 +372,8 @@ kvq_status_t kvq_reshape_and_cache_per_token(const void* k, const void* v, const
  *  stage's largest V scale of a live token, and f a power of two per query
  *  head that moves the
  *  stage's largest weighted probability into [128, 256), P.V runs on
- *  p_j * (sv_j / c) * f, rounded to float16 and split into three E4M3 terms
- *  (about 11 significant bits: the weights make even the largest
- *  probability inexact in E4M3), and the stage's result is multiplied by
- *  c / f before it is added to the running FP32 sum.  The row sum uses the
+ *  p_j * (sv_j / c) * f, rounded to float16, and the stage's result is
+ *  multiplied by c / f before it is added to the running FP32 sum.  The row sum uses the
  *  unweighted p_j.
  *  Workspace: kvq_decode_workspace_size() of the same arguments.
  */

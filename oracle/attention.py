@@ -49,17 +49,16 @@ Mirrored quantization points
 ----------------------------
 ``mode="mirror"`` rounds exactly where the CUDA path declares it rounds:
 * decode: per query head, sigma = 2^(7 - floor(log2 max_d |q_d|)) (a power
-  of two) and q * sigma = hi + lo, hi = e4m3(q * sigma), lo = e4m3(q * sigma
-  - hi) -- two E4M3 terms that feed an FP8 MMA; scores are taken in base-2
-  units, s2 = (sum_d (hi + lo)[d] * k8[d]) / sigma * c with
-  c = fl32(fl32(k_scale * sm_scale) * log2(e));
+  of two) and the query enters the MMA as qf = f16(fl32(q * sigma)) (RNE;
+  exact for a bf16 q unless q * sigma falls below float16's normal range);
+  scores are taken in base-2 units, s2 = (sum_d qf[d] * k8[d]) / sigma * c
+  with c = fl32(fl32(k_scale * sm_scale) * log2(e));
   o = s_v * sum_j 2^(s2_j - m) v8_j / sum_j 2^(s2_j - m).  The kernel's
-  rounding of P for the P.V MMA (two E4M3 terms of 2^(s2 - m) * 256 taken
-  against the running maximum, about 8 significant bits, the maximum itself
-  exact) is not mirrored: it depends on how the context is cut into stages
-  and splits; the tolerance carries it (2^-8 of |o| where |o| > 1).
-  An E5M2 cache is mirrored the same way: its codes are decoded as E5M2,
-  the query and probability terms stay E4M3.
+  rounding of P for the P.V MMA (2^(s2 - m) * 256 to float16, 11
+  significant bits, taken against the running maximum) is not mirrored: it
+  depends on how the context is cut into stages and splits; the tolerance
+  carries it.  An E5M2 cache is mirrored the same way: its codes are
+  decoded as E5M2.
 * prefill: s2 = (sum_d q8[d] * k8[d]) * c with
   c = fl32(fl32(fl32(q_scale * k_scale) * sm_scale) * log2(e)), and P8 as
   above.
@@ -101,11 +100,11 @@ def _softmax_row(scores_base_e):
     return p, m, p.sum()
 
 
-def split_query_e4m3(q_row):
+def query_f16(q_row):
     """The decode kernels' declared rounding of one query head: returns
-    (hi + lo) / sigma in float64, with sigma = 2^(7 - floor(log2 max|q|))
-    (exponent clamped at -100), hi = e4m3(fl32(q * sigma)) and
-    lo = e4m3(fl32(q * sigma - hi))."""
+    f16(fl32(q * sigma)) / sigma in float64, with sigma = 2^(7 -
+    floor(log2 max|q|)) (exponent clamped at -100) and float16
+    round-to-nearest-even (subnormals kept)."""
     q = np.asarray(q_row, dtype=np.float32)
     mx = float(np.max(np.abs(q))) if q.size else 0.0
     if mx == 0.0:
@@ -113,10 +112,7 @@ def split_query_e4m3(q_row):
     e = max(int(np.frexp(np.float32(mx))[1]) - 1, -100)
     sigma = np.float32(2.0 ** (7 - e))
     y = (q * sigma).astype(np.float32)
-    hi = e4m3.decode(e4m3.encode(y))
-    res = (y.astype(np.float64) - hi).astype(np.float32)
-    lo = e4m3.decode(e4m3.encode(res))
-    return (hi + lo) / float(sigma)
+    return y.astype(np.float16).astype(np.float64) / float(sigma)
 
 
 def stabilizer(s2):
@@ -166,8 +162,8 @@ def paged_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
             for h in range(kv * g, (kv + 1) * g):
                 qh = q[b, h].astype(np.float64)
                 if mode == "mirror":
-                    if cache_dtype in FP8_TYPES:  # q terms are E4M3 for either cache format
-                        qe = split_query_e4m3(q[b, h])
+                    if cache_dtype in FP8_TYPES:  # f16 query for either cache format
+                        qe = query_f16(q[b, h])
                         c = float(decode_score_coef(k_scale[kv], sm_scale))
                     else:
                         qe = qh
@@ -192,8 +188,8 @@ def paged_decode_per_token(q, k_cache, v_cache, kv_scale_cache, block_table, seq
     (kv_cache.reshape_and_cache_per_token; kv_scale_cache [nb][Hkv][2][P]):
     token j dequantizes as decode(k8_j) * sk_j and decode(v8_j) * sv_j.
 
-    mirror: the query terms as in paged_decode; s2_j = (sum_d (hi + lo)_d
-    k8_jd) / sigma * c_j with c_j = fl32(fl32(sm_scale * log2(e)) * sk_j);
+    mirror: the query as in paged_decode; s2_j = (sum_d qf_d k8_jd) / sigma
+    * c_j with c_j = fl32(fl32(sm_scale * log2(e)) * sk_j);
     o = sum_j 2^(s2_j - m) sv_j v8_j / sum_j 2^(s2_j - m).
     pure: exact dequantized values, natural exponentials.
     Returns (out float64 [B][Hq][D], lse float64 [B][Hq])."""
@@ -217,7 +213,7 @@ def paged_decode_per_token(q, k_cache, v_cache, kv_scale_cache, block_table, seq
             for h in range(kv * g, (kv + 1) * g):
                 if mode == "mirror":
                     c = (c0 * sk).astype(np.float32).astype(np.float64)
-                    s2 = (k_codes @ split_query_e4m3(q[b, h])) * c
+                    s2 = (k_codes @ query_f16(q[b, h])) * c
                     m2 = np.max(s2)
                     p = np.exp2(s2 - m2)
                     l = p.sum()

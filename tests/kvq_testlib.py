@@ -15,12 +15,11 @@ SENTINEL = 0xA5
 # 1e-3, flat, for every element with |o| <= 1.  An element with |o| > 1 (in
 # these workloads the x20 outlier channels, |o| up to ~60) gets 2^-8 |o| on
 # top: the output is bfloat16 (8 significant bits), whose nearest value can
-# be half an ulp, up to 2^-8 |o|, from the exact one, and the decode kernels'
-# declared rounding of P for the P.V MMA (two E4M3 terms, about 8
-# significant bits per probability, taken against a running maximum that
-# depends on how the context is cut into stages and splits) is a 2^-8
-# relative effect the oracle does not mirror.  Below |o| = 1 both stay
-# inside the flat 1e-2.
+# be half an ulp, up to 2^-8 |o|, from the exact one; the decode kernels'
+# declared rounding of P for the P.V MMA (float16, taken against a running
+# maximum that depends on how the context is cut into stages and splits) is
+# a smaller relative effect the oracle does not mirror.  Below |o| = 1 both
+# stay inside the flat 1e-2.
 MAX_ABS = 1e-2
 MEAN_ABS = 1e-3
 REL_ABOVE_ONE = 2.0 ** -8

@@ -249,19 +249,23 @@ def test_long_context_sensitivity_to_reduced_accumulator():
     assert errs[65536] > 1e-2 and errs[65536] > 2 * errs[1024]
 
 
-def test_split_query_e4m3_is_exact_for_elements_near_the_head_maximum():
-    """hi + lo reproduces a bf16 query exactly wherever |q| >= 2^-9 max|q|
-    (a bf16 value has 8 significant bits, two E4M3 terms carry 4 + 4), and
-    within 2^-10 / sigma below that."""
+def test_query_f16_is_exact_in_float16_normal_range():
+    """A bf16 query (8 significant bits) scaled by a power of two is exact in
+    float16 (11 bits) wherever it lands in float16's normal range
+    (|q sigma| >= 2^-14); below that, float16 subnormals are spaced 2^-24
+    apart, so the rounding is within 2^-25 / sigma; the scaled maximum lies
+    in [128, 256)."""
     rng = np.random.default_rng(12)
-    for scale in (1.0, 1e-3, 37.0):
+    for scale in (1.0, 1e-3, 37.0, 3e4):
         q = _bf16(rng.standard_normal(128) * scale)
-        q[5] = _bf16(np.float32(q[5] * 1e-4))  # a tiny element
-        got = attention.split_query_e4m3(q)
+        q[5] = _bf16(np.float32(q[5] * 2.0 ** -22))  # far below the maximum: subnormal after scaling
+        got = attention.query_f16(q)
         mx = np.max(np.abs(q))
-        big = np.abs(q) >= mx * 2.0 ** -9
-        assert np.array_equal(got[big], q[big].astype(np.float64))
         sigma = 2.0 ** (7 - (np.frexp(np.float32(mx))[1] - 1))
-        assert np.all(np.abs(got - q) <= 2.0 ** -10 / sigma)
-    assert np.all(attention.split_query_e4m3(np.zeros(8, np.float32)) == 0)
+        assert 128 <= mx * sigma < 256
+        normal = np.abs(q) * sigma >= 2.0 ** -14
+        assert np.array_equal(got[normal], q[normal].astype(np.float64))
+        assert np.all(np.abs(got - q) <= 2.0 ** -25 / sigma)
+        assert not np.all(normal)  # the planted element exercises the subnormal bound
+    assert np.all(attention.query_f16(np.zeros(8, np.float32)) == 0)
 
