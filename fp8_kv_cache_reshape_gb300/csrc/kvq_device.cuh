@@ -208,49 +208,9 @@ KVQ_DEVINL void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, u
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
 
-// D = A(16x32, row) * B(32x8, col) + C with E4M3 inputs (products exact), f32 accumulators.
-KVQ_DEVINL void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                         uint32_t b1, const float (&c)[4]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%11,%12,%13};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
-}
-// As mma_e4m3, with A holding E5M2 codes (an E5M2 cache) and B E4M3.
-KVQ_DEVINL void mma_e5m2_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                              uint32_t b1, const float (&c)[4]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e5m2.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%10,%11,%12,%13};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
-}
-// A operand in the cache's 8-bit format (E4M3, or E5M2 when A5 is set), B E4M3.
-template <bool A5>
-KVQ_DEVINL void mma_fp8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1,
-                        const float (&c)[4]) {
-  if constexpr (A5)
-    mma_e5m2_e4m3(d, a0, a1, a2, a3, b0, b1, c);
-  else
-    mma_e4m3(d, a0, a1, a2, a3, b0, b1, c);
-}
 // Two float32 -> two E4M3 codes (lo -> low byte), RNE, saturating.
 KVQ_DEVINL uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
-}
-// f16x2 -> two E4M3 codes (low half -> low byte), RNE, saturating.
-KVQ_DEVINL uint32_t f16x2_to_e4m3x2(uint32_t h) {
-  __half2_raw r;
-  r.x = static_cast<unsigned short>(h & 0xFFFF);
-  r.y = static_cast<unsigned short>(h >> 16);
-  return static_cast<uint32_t>(__nv_cvt_halfraw2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3));
-}
-
-// Two E4M3 codes (low byte -> low half) to an f16x2 register; exact.
-KVQ_DEVINL uint32_t e4m3x2_to_f16x2(uint16_t two) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 // Four E4M3 codes in one register -> two f16x2 registers (bytes 0,1 -> lo;
 // bytes 2,3 -> hi); exact.
